@@ -1,0 +1,317 @@
+"""Oracle for the TSP layer forward. TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, float64 NumPy restatement of what one transformer layer computes
+under Folding Tensor and Sequence Parallelism (TSP). Only the test suite, the
+package smoke check and the benchmark's CPU-baseline / reference legs may import
+this module; the library never does. It shares no code with the CUDA path: the
+only thing both sides take from elsewhere is the seeded input generator, which
+holds none of the method's arithmetic.
+
+Source, cited below as [TSP]: the summary page "Folding Tensor and Sequence
+Parallelism for Memory-Efficient Transformer Training & Inference"
+(gist.science, paper 2604.26294), sections 1 (Problem statement),
+2 (Methodology) and 3 (Contributions).
+
+What the page fixes, and what this module writes out:
+  * each of D ranks holds 1/D of the parameters and 1/D of the sequence tokens
+    ([TSP] s2, "Unified sharding");
+  * attention runs a broadcast schedule over packed W_Q/W_K/W_V/W_O shards:
+    local projections on each rank's own tokens, an all-gather of K/V along the
+    sequence, then FlashAttention ([TSP] s2, "Attention layers");
+  * zigzag partitioning balances causal attention work ([TSP] s2, same bullet list);
+  * the gated MLP runs a ring schedule over W1/W2/W3 shards and each rank
+    accumulates its partial outputs locally, with no all-reduce
+    ([TSP] s2, "Gated MLP layers");
+  * per-device FLOPs equal those of tensor/sequence parallelism ([TSP] s3,
+    "Theoretical analysis" - FLOPs), i.e. the sharded layer computes the plain
+    layer's result.
+
+Readings taken where the page is silent (each is listed in the design notes):
+  * no normalisation, no positional encoding, no dropout, batch 1;
+  * softmax scale 1/sqrt(head_dim); causal mask j <= i over global positions,
+    diagonal included;
+  * W1 = gate (through SiLU), W3 = up, W2 = down; silu(z) = z / (1 + e^-z);
+  * a layer is  h = x + Attn(x),  out = h + MLP(h); the block functions return
+    the block outputs without the residual;
+  * zigzag: the sequence is cut into 2D equal chunks of C = S/(2D) tokens and
+    rank r owns chunks r and 2D-1-r, in that local order;
+  * attention weight shard k = heads [k*h/D, (k+1)*h/D): the matching rows of
+    W_Q, W_K, W_V and columns of W_O; MLP shard k = ffn slice [k*F/D, (k+1)*F/D):
+    rows of W1, W3 and columns of W2;
+  * broadcast iteration k uses shard k; at ring step t rank r holds shard
+    (r + t) mod D;
+  * the O projection is reduced like the MLP: each rank accumulates its partial
+    products over k locally.
+
+Everything is computed in float64 from the bfloat16 bit patterns of the inputs.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "widen_bf16",
+    "zigzag_owner",
+    "zigzag_forward_index",
+    "zigzag_inverse_index",
+    "shard_tokens",
+    "unshard_tokens",
+    "rank_positions",
+    "causal_attention_head",
+    "multihead_causal_attention",
+    "attention_block",
+    "silu",
+    "swiglu_mlp",
+    "layer_forward",
+    "tsp_layer_forward",
+    "causal_pairs_per_rank",
+    "layer_flops",
+    "rank_parameter_count",
+    "rank_activation_count",
+]
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64 values (exact widening)."""
+    b = np.ascontiguousarray(bits).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Zigzag sequence partitioning  ([TSP] s2, "Attention layers", last bullet)
+# --------------------------------------------------------------------------
+
+def zigzag_owner(S: int, D: int):
+    """Rank and rank-local index of every global token position.
+
+    The sequence is cut into 2D chunks of C = S/(2D) tokens. Chunk c < D goes to
+    rank c (local rows 0..C-1); chunk c >= D goes to rank 2D-1-c (local rows
+    C..2C-1). Returns (rank[S], local[S]) as int64 arrays.
+    """
+    if S % (2 * D):
+        raise ValueError("S must be a multiple of 2D")
+    C = S // (2 * D)
+    t = np.arange(S, dtype=np.int64)
+    chunk, off = t // C, t % C
+    first = chunk < D
+    rank = np.where(first, chunk, 2 * D - 1 - chunk)
+    local = np.where(first, off, C + off)
+    return rank, local
+
+
+def zigzag_forward_index(S: int, D: int) -> np.ndarray:
+    """fwd[t] = row of global token t in the rank-major [D, S/D] layout."""
+    rank, local = zigzag_owner(S, D)
+    return rank * (S // D) + local
+
+
+def zigzag_inverse_index(S: int, D: int) -> np.ndarray:
+    """inv[row] = global position of row `row` of the rank-major layout."""
+    fwd = zigzag_forward_index(S, D)
+    inv = np.empty_like(fwd)
+    inv[fwd] = np.arange(S, dtype=np.int64)
+    return inv
+
+
+def shard_tokens(x: np.ndarray, D: int) -> np.ndarray:
+    """[S, ...] natural order -> [D, S/D, ...]: rank r's tokens in local order."""
+    S = x.shape[0]
+    out = np.empty_like(x)
+    out[zigzag_forward_index(S, D)] = x
+    return out.reshape((D, S // D) + x.shape[1:])
+
+
+def unshard_tokens(xs: np.ndarray, D: int) -> np.ndarray:
+    """Inverse of shard_tokens: [D, S/D, ...] -> [S, ...] in natural order."""
+    S = xs.shape[0] * xs.shape[1]
+    flat = xs.reshape((S,) + xs.shape[2:])
+    return flat[zigzag_forward_index(S, D)]
+
+
+def rank_positions(S: int, D: int) -> np.ndarray:
+    """[D, S/D]: global position of each rank's local token."""
+    return zigzag_inverse_index(S, D).reshape(D, S // D)
+
+
+# --------------------------------------------------------------------------
+# Causal attention  ([TSP] s2, "Attention layers": FlashAttention over the
+# gathered K/V; FlashAttention computes exact softmax attention)
+# --------------------------------------------------------------------------
+
+def causal_attention_head(q, k, v, q_pos, k_pos) -> np.ndarray:
+    """One head: out_i = sum_j p_ij v_j / sum_j p_ij over keys with k_pos[j] <= q_pos[i].
+
+    p_ij = exp(s_ij - max_j s_ij), s_ij = q_i . k_j / sqrt(d). q: [nq, d],
+    k, v: [nk, d], positions int arrays. float64 throughout.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    d = q.shape[1]
+    s = (q @ k.T) / math.sqrt(d)
+    visible = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]
+    s = np.where(visible, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    return (p @ v) / p.sum(axis=1, keepdims=True)
+
+
+def multihead_causal_attention(q, k, v, heads: int, q_pos=None, k_pos=None,
+                               q_block: int = 1024) -> np.ndarray:
+    """Split the H columns into `heads` heads of d = H/heads and attend per head.
+
+    q: [nq, H], k, v: [nk, H]; positions default to 0..n-1. Queries are taken in
+    blocks of `q_block` rows only to bound the score matrix's memory.
+    """
+    nq, H = q.shape
+    nk = k.shape[0]
+    d = H // heads
+    q_pos = np.arange(nq) if q_pos is None else np.asarray(q_pos)
+    k_pos = np.arange(nk) if k_pos is None else np.asarray(k_pos)
+    out = np.empty((nq, H), dtype=np.float64)
+    for j in range(heads):
+        c = slice(j * d, (j + 1) * d)
+        for lo in range(0, nq, q_block):
+            r = slice(lo, min(nq, lo + q_block))
+            out[r, c] = causal_attention_head(q[r, c], k[:, c], v[:, c], q_pos[r], k_pos)
+    return out
+
+
+def attention_block(x, Wq, Wk, Wv, Wo, heads: int, rows=None) -> np.ndarray:
+    """Causal multi-head self-attention of a plain (unsharded) layer, no residual.
+
+    Attn(x) = concat_j softmax(Q_j K_j^T / sqrt(d) + causal) V_j  W_O^T with
+    Q = x W_Q^T, K = x W_K^T, V = x W_V^T. All inputs float64 arrays.
+    With `rows` (sorted positions) only those output rows are computed; K/V are
+    projected for positions 0..max(rows), one head at a time.
+    """
+    S, H = x.shape
+    d = H // heads
+    if rows is None:
+        rows = np.arange(S)
+    rows = np.asarray(rows, dtype=np.int64)
+    kmax = int(rows.max()) + 1
+    xk = x[:kmax]
+    xq = x[rows]
+    o = np.empty((rows.size, H), dtype=np.float64)
+    for j in range(heads):
+        c = slice(j * d, (j + 1) * d)
+        qh = xq @ Wq[c].T
+        kh = xk @ Wk[c].T
+        vh = xk @ Wv[c].T
+        for lo in range(0, rows.size, 1024):
+            r = slice(lo, min(rows.size, lo + 1024))
+            o[r, c] = causal_attention_head(qh[r], kh, vh, rows[r], np.arange(kmax))
+    return o @ Wo.T
+
+
+# --------------------------------------------------------------------------
+# Gated MLP  ([TSP] s2, "Gated MLP layers": weights W1, W2, W3)
+# --------------------------------------------------------------------------
+
+def silu(z):
+    """SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_mlp(h, W1, W3, W2) -> np.ndarray:
+    """MLP(h) = (silu(h W1^T) * (h W3^T)) W2^T, no residual."""
+    return (silu(h @ W1.T) * (h @ W3.T)) @ W2.T
+
+
+# --------------------------------------------------------------------------
+# Whole layer, plain and TSP-sharded
+# --------------------------------------------------------------------------
+
+def layer_forward(x, W: dict, heads: int, rows=None) -> dict:
+    """Plain layer: h = x + Attn(x); out = h + MLP(h). float64 arrays in and out.
+
+    W holds Wq, Wk, Wv, Wo, W1, W3, W2 (float64, [out, in]). With `rows` only those
+    token rows are returned (attention still sees every earlier token).
+    Returns {"attn", "h", "mlp", "out"} for the requested rows.
+    """
+    attn = attention_block(x, W["Wq"], W["Wk"], W["Wv"], W["Wo"], heads, rows=rows)
+    xr = x if rows is None else x[np.asarray(rows)]
+    h = xr + attn
+    mlp = swiglu_mlp(h, W["W1"], W["W3"], W["W2"])
+    return {"attn": attn, "h": h, "mlp": mlp, "out": h + mlp}
+
+
+def tsp_layer_forward(x, W: dict, heads: int, D: int) -> dict:
+    """The same layer computed rank by rank under TSP's schedules ([TSP] s2).
+
+    Rank r holds its zigzag token shard xs[r] ([S/D, H]). Attention: for each
+    broadcast iteration k, every rank projects its own tokens with shard k's
+    W_Q/W_K/W_V rows, K/V of all ranks are gathered along the sequence into
+    natural order, each rank attends its queries (by global position) to the full
+    K/V, and accumulates O_rk W_O,k^T locally. MLP: at ring step t rank r holds
+    shard k = (r + t) mod D and adds silu(h_r W1_k^T) * (h_r W3_k^T) W2_k^T to its
+    local accumulator; there is no all-reduce. Results are unsharded at the end
+    and returned like layer_forward's (natural order).
+    """
+    S, H = x.shape
+    F = W["W1"].shape[0]
+    if heads % D or F % D or S % (2 * D):
+        raise ValueError("TSP needs heads % D == 0, ffn % D == 0 and S % 2D == 0")
+    hpr, Hd, Fd, T = heads // D, H // D, F // D, S // D
+    xs = shard_tokens(x, D)
+    pos = rank_positions(S, D)
+    every = np.arange(S)
+
+    acc = np.zeros((D, T, H))
+    for k in range(D):                      # broadcast iteration: shard k goes to all
+        c = slice(k * Hd, (k + 1) * Hd)
+        Wq_k, Wk_k, Wv_k, Wo_k = W["Wq"][c], W["Wk"][c], W["Wv"][c], W["Wo"][:, c]
+        q = [xs[r] @ Wq_k.T for r in range(D)]          # local projections
+        k_all = unshard_tokens(np.stack([xs[r] @ Wk_k.T for r in range(D)]), D)
+        v_all = unshard_tokens(np.stack([xs[r] @ Wv_k.T for r in range(D)]), D)
+        for r in range(D):
+            o = multihead_causal_attention(q[r], k_all, v_all, hpr, pos[r], every)
+            acc[r] += o @ Wo_k.T                         # local accumulation over k
+    hs = xs + acc
+
+    acc2 = np.zeros((D, T, H))
+    for t in range(D):                      # ring step
+        for r in range(D):
+            k = (r + t) % D
+            f = slice(k * Fd, (k + 1) * Fd)
+            g = silu(hs[r] @ W["W1"][f].T) * (hs[r] @ W["W3"][f].T)
+            acc2[r] += g @ W["W2"][:, f].T
+    outs = hs + acc2
+    return {"attn": unshard_tokens(acc, D), "h": unshard_tokens(hs, D),
+            "mlp": unshard_tokens(acc2, D), "out": unshard_tokens(outs, D)}
+
+
+# --------------------------------------------------------------------------
+# Counting  ([TSP] s2 "Unified sharding"; s3 memory and FLOPs analysis)
+# --------------------------------------------------------------------------
+
+def causal_pairs_per_rank(S: int, D: int) -> np.ndarray:
+    """Number of visible (query, key) pairs of each rank's queries, by brute count."""
+    rank, _ = zigzag_owner(S, D)
+    keys_seen = np.arange(S, dtype=np.int64) + 1   # query at position p sees p+1 keys
+    return np.bincount(rank, weights=keys_seen, minlength=D).astype(np.int64)
+
+
+def layer_flops(S: int, H: int, F: int) -> int:
+    """Algorithmic FLOPs of one layer forward (multiply-add = 2 FLOPs).
+
+    Q/K/V/O projections 4 * 2SH^2, SwiGLU 3 * 2SHF, causal attention
+    2 * (QK^T and PV) * d * (S(S+1)/2 pairs) * heads = 2HS(S+1).
+    """
+    return 8 * S * H * H + 6 * S * H * F + 2 * H * S * (S + 1)
+
+
+def rank_parameter_count(H: int, F: int, D: int) -> int:
+    """Parameters one rank holds: 1/D of W_Q, W_K, W_V, W_O, W1, W2, W3."""
+    total = 4 * H * H + 3 * H * F
+    if total % D:
+        raise ValueError("parameters do not split evenly")
+    return total // D
+
+
+def rank_activation_count(S: int, H: int, D: int) -> int:
+    """Layer-input activations one rank holds: its S/D tokens times H."""
+    return (S // D) * H
