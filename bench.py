@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark of the TSP layer forward on GB300: prints ONE JSON line.
+
+Workload (default): the 7B-shaped layer at 64K tokens - D=8 logical ranks,
+S=65536, hidden 4096, 32 heads x 128, SwiGLU ffn 11008, batch 1, bf16, seeded
+synthetic inputs (x ~ N(0,1), weights ~ N(0,0.02)). A step is one whole layer
+forward (tsp_layer_fwd) over all D ranks. Inputs stay resident in HBM; every
+input (x: 512 MiB, weights: 400 MiB) is larger than the 129 MB L2, so no flush
+is needed between steps.
+
+Reported:
+  value       tokens/s of the whole job (N replicas x S tokens / max step time)
+  tflops      algorithmic TFLOP/s (8SH^2 + 6SHF + 2HS(S+1) per layer)
+  roofline    the dominant kernel: algorithmic FLOPs (or bytes) per launch over
+              its CUDA-event duration, measured in a second timed pass that issues
+              the same kernels through the single-step entry points
+  e2e         the same metric through tsp_layer_fwd_host with pinned host buffers
+              (host->device copy of x and device->host copy of out every step)
+  cpu_baseline the float64 oracle on the host cores, timed on a causal prefix of
+              the same workload and scaled by FLOPs to the full workload
+  --impl reference  times that oracle alone (the slow reference arm).
+Multi-GPU (torchrun): independent replicas, one per GPU; no collective on the
+data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import tsp_inputs  # noqa: E402
+
+METRIC = "TSP layer fwd tokens/s and TFLOP/s (frac of bf16 TC peak) on 1 GB300"
+DEFAULT_WORKLOAD = "7b-64k"
+
+# DRAM bytes (read + write) per launch from an ncu capture of the kernel as it is
+# now, keyed by kernel; None until a capture of the current kernel exists.
+NCU_TRAFFIC_BYTES = {}
+
+
+def algorithmic_flops(S, H, F):
+    return 8 * S * H * H + 6 * S * H * F + 2 * H * S * (S + 1)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        power = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def gpu_smi_id(local_rank):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else f"GPU-{s}"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[local_rank]
+        return local_rank
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cfg, bits, n_tokens, repeats=1):
+    """Time the float64 oracle on the first n_tokens of the workload (a causal prefix).
+
+    Returns (seconds per repeat, tokens/s extrapolated to the full workload by
+    algorithmic FLOPs, description).
+    """
+    import oracle  # the oracle is timed here only as the CPU baseline / reference arm
+    n = int(min(n_tokens, cfg.S))
+    x = oracle.widen_bf16(bits["x"][:n])
+    W = {k: oracle.widen_bf16(bits[k]) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")}
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.layer_forward(x, W, cfg.heads)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    f_sample = algorithmic_flops(n, cfg.hidden, cfg.ffn)
+    f_full = algorithmic_flops(cfg.S, cfg.hidden, cfg.ffn)
+    rate = f_sample / t
+    tokens_per_s = cfg.S * rate / f_full
+    desc = (f"float64 NumPy oracle, full layer on the causal prefix of {n} tokens of {cfg.name} "
+            f"({t:.2f} s, {rate / 1e9:.1f} GFLOP/s), scaled by algorithmic FLOPs to the "
+            f"{cfg.S}-token workload")
+    return t, tokens_per_s, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------- ours
+
+def run_ours(args, world, rank, local):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import folded_tensor_sequence_tsp_gb300 as tsp
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = tsp_inputs.config_by_name(args.workload)
+    S, H, F, D = cfg.S, cfg.hidden, cfg.ffn, cfg.D
+    bits = tsp_inputs.layer_inputs(cfg)
+    to_dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+    dev = {k: to_dev(v) for k, v in bits.items()}
+    layer = tsp.TSPLayer(D, S, H, cfg.heads, F, dev)
+    plan, i = layer.plan, layer.plan.info
+    xs = torch.empty_like(dev["x"])
+    tsp.tsp_shard(plan, dev["x"], xs)
+    out = torch.empty_like(xs)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline: K whole-layer steps
+    for _ in range(args.warmup):
+        layer.forward(xs, out)
+    layer.check()
+    barrier()
+    clocks = ClockSampler(gpu_smi_id(local))
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward(xs, out)
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    layer.check()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    launches_per_step = 3 * D + 3
+
+    # ---- per-kernel pass: the same kernels through the single-step entry points
+    qkv = torch.empty((S, 3 * i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    kn = torch.empty((S, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    o = torch.empty_like(xs)
+    h = torch.empty_like(xs)
+    h32 = torch.empty(xs.shape, dtype=torch.float32, device="cuda")
+    g = torch.empty((S, i.ffn_padded), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty_like(xs)
+    ws, wp = layer.ws, layer.wpack
+    names = ["gemm_qkv", "kv_gather", "attention", "gemm_o", "gemm_gate_up", "gemm_down"]
+    spans = {n: [] for n in names}
+
+    def composed_step(record):
+        evs = []
+
+        def mark(name):
+            if record:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(stream)
+                evs.append((name, ev))
+
+        mark(None)
+        for k in range(D):
+            tsp.tsp_qkv_projection(plan, k, xs, wp, qkv, ws)
+            mark("gemm_qkv")
+            tsp.tsp_kv_allgather(plan, qkv, kn, vn)
+            mark("kv_gather")
+            tsp.tsp_causal_attention(plan, k, qkv, kn, vn, o, ws)
+            mark("attention")
+        tsp.tsp_o_projection(plan, o, wp, xs, h, ws, out32=h32)
+        mark("gemm_o")
+        tsp.tsp_swiglu_gate_up(plan, h, wp, g, ws)
+        mark("gemm_gate_up")
+        tsp.tsp_swiglu_down(plan, g, wp, None, out2, ws, residual32=h32)
+        mark("gemm_down")
+        return evs
+
+    for _ in range(max(1, args.warmup)):
+        composed_step(False)
+    barrier()
+    all_evs = [composed_step(True) for _ in range(args.steps)]
+    barrier()
+    layer.check()
+    same = torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    for evs in all_evs:
+        for (_, a), (n, b) in zip(evs[:-1], evs[1:]):
+            spans[n].append(a.elapsed_time(b))
+    per_launch_work = {
+        "gemm_qkv": ("tensor", 2.0 * S * H * 3 * i.shard_hidden),
+        "kv_gather": ("hbm", 8.0 * S * i.shard_hidden),
+        "attention": ("tensor", 2.0 * i.shard_hidden * S * (S + 1)),
+        "gemm_o": ("tensor", 2.0 * S * H * H),
+        "gemm_gate_up": ("tensor", 4.0 * S * H * F),
+        "gemm_down": ("tensor", 2.0 * S * F * H),
+    }
+    peaks, peak_src = measured_peaks()
+    kernels = {}
+    for n in names:
+        avg = statistics.mean(spans[n])
+        bound, work = per_launch_work[n]
+        if bound == "tensor":
+            ach = work / (avg * 1e-3) / 1e12
+            pk = peaks["bf16_tflops_sustained"]
+        else:
+            ach = work / (avg * 1e-3) / 1e9
+            pk = peaks["hbm_gbs"]
+        kernels[n] = {"bound": bound, "avg_ms": round(avg, 4),
+                      "launches_per_step": D if n in ("gemm_qkv", "kv_gather", "attention") else 1,
+                      "share": None, "achieved": round(ach, 1), "frac": round(ach / pk, 4)}
+    total_ms = sum(kernels[n]["avg_ms"] * kernels[n]["launches_per_step"] for n in names)
+    for n in names:
+        kernels[n]["share"] = round(kernels[n]["avg_ms"] * kernels[n]["launches_per_step"] / total_ms, 4)
+    dom = max(names, key=lambda n: kernels[n]["avg_ms"] * kernels[n]["launches_per_step"])
+    kd = kernels[dom]
+    roofline = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved"],
+                "peak": peaks["bf16_tflops_sustained"] if kd["bound"] == "tensor" else peaks["hbm_gbs"],
+                "unit": "TFLOP/s" if kd["bound"] == "tensor" else "GB/s",
+                "frac": kd["frac"], "traffic": NCU_TRAFFIC_BYTES.get(dom),
+                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kd['bound'] == 'tensor' else 'hbm_gbs'})"}
+    del qkv, kn, vn, o, h, h32, g, out2
+
+    # ---- end to end through the host entry point (pinned buffers)
+    x_host = torch.from_numpy(bits["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        layer.forward_host(x_host, out_host)
+    barrier()
+    e_ms = []
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.forward_host(x_host, out_host)
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    layer.check()
+    e2e_ms = max_over_ranks(statistics.mean(e_ms))
+
+    tflops = algorithmic_flops(S, H, F) / (ms * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(world * S / (ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "tflops": round(world * tflops, 1),
+        "frac_of_peak": round(tflops / peaks["bf16_tflops"], 4),
+        "frac_of_peak_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
+        "config": {"workload": cfg.name, "D": D, "S": S, "hidden": H, "heads": cfg.heads,
+                   "head_dim": cfg.head_dim, "ffn": F, "batch": 1,
+                   "parallelism": f"tsp{D} on one GPU" + (f", {world} replicas" if world > 1 else ""),
+                   "l2": "no flush: x (512 MiB at 64K) and weights exceed the 129 MB L2"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "composed_equals_layer_fwd": bool(same),
+        "e2e": {"value": round(world * S / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 3),
+                "h2d_bytes_per_step": S * H * 2, "d2h_bytes_per_step": S * H * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, v, desc = oracle_sample(cfg, bits, args.cpu_sample_tokens)
+        result["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),
+                                  "kind": "oracle", "sample": desc}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# --------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    cfg = tsp_inputs.config_by_name(args.workload)
+    bits = tsp_inputs.layer_inputs(cfg)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, bits, args.ref_sample_tokens)
+    times, vals = [], []
+    desc = ""
+    for _ in range(args.steps):
+        t, v, desc = oracle_sample(cfg, bits, args.ref_sample_tokens)
+        times.append(t)
+        vals.append(v)
+    v = statistics.mean(vals)
+    result = {
+        "metric": METRIC, "impl": "reference", "value": round(v, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(times), 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "D": cfg.D, "S": cfg.S, "hidden": cfg.hidden,
+                   "heads": cfg.heads, "head_dim": cfg.head_dim, "ffn": cfg.ffn, "batch": 1},
+        "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[c.name for c in tsp_inputs.CONFIGS])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--ref-sample-tokens", type=int, default=1024)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps do not meet the timing rules", file=sys.stderr)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,326 @@
+"""Thin ctypes binding of libtsp.so (declared in include/tsp.h).
+
+Argument marshalling only: each function checks the tensors it is given (device,
+dtype, contiguity, size - the C ABI takes raw pointers and cannot check sizes),
+passes their pointers and the current CUDA stream, and raises TSPError on a
+non-OK status. Every step of the computation runs in the library's kernels; if
+the library is not built, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "TSPError", "PlanInfo", "Plan", "load_library", "library_path", "declared_functions",
+    "TSP_OK", "TSP_ERR_INVALID_ARG", "TSP_ERR_UNSUPPORTED", "TSP_ERR_CUDA", "TSP_ERR_TIMEOUT",
+    "tsp_plan", "tsp_get_plan_info", "tsp_workspace_bytes", "tsp_packed_weight_bytes",
+    "tsp_workspace_init", "tsp_pack_weights", "tsp_shard_index", "tsp_shard", "tsp_unshard",
+    "tsp_attention_fwd", "tsp_mlp_fwd", "tsp_layer_fwd", "tsp_layer_fwd_host",
+    "tsp_qkv_projection", "tsp_kv_allgather", "tsp_causal_attention", "tsp_o_projection",
+    "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
+    "tsp_last_error",
+]
+
+TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
+_NAMES = {0: "TSP_OK", 1: "TSP_ERR_INVALID_ARG", 2: "TSP_ERR_UNSUPPORTED", 3: "TSP_ERR_CUDA",
+          4: "TSP_ERR_TIMEOUT"}
+
+HEADER = os.path.join(_build.ROOT, "include", "tsp.h")
+
+
+class TSPError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("D", ctypes.c_int), ("S", ctypes.c_int64), ("hidden", ctypes.c_int),
+        ("heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+        ("T", ctypes.c_int64), ("C", ctypes.c_int64), ("shard_hidden", ctypes.c_int),
+        ("shard_ffn", ctypes.c_int), ("shard_ffn_padded", ctypes.c_int),
+        ("ffn_padded", ctypes.c_int), ("wpack_qkv", ctypes.c_size_t),
+        ("wpack_o", ctypes.c_size_t), ("wpack_w13", ctypes.c_size_t),
+        ("wpack_w2", ctypes.c_size_t), ("wpack_elems", ctypes.c_size_t),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "tsp_plan": (_I, [_I, ctypes.c_int64, _I, _I, _I, ctypes.POINTER(_P)]),
+    "tsp_plan_destroy": (None, [_P]),
+    "tsp_get_plan_info": (_I, [_P, ctypes.POINTER(PlanInfo)]),
+    "tsp_workspace_bytes": (ctypes.c_size_t, [_P]),
+    "tsp_packed_weight_bytes": (ctypes.c_size_t, [_P]),
+    "tsp_workspace_init": (_I, [_P, _P, _P]),
+    "tsp_pack_weights": (_I, [_P] * 9 + [_P]),
+    "tsp_shard_index": (_I, [_P, _P, _P, _P]),
+    "tsp_shard": (_I, [_P, _P, _P, _P]),
+    "tsp_unshard": (_I, [_P, _P, _P, _P]),
+    "tsp_attention_fwd": (_I, [_P] * 6),
+    "tsp_mlp_fwd": (_I, [_P] * 6),
+    "tsp_layer_fwd": (_I, [_P] * 6),
+    "tsp_layer_fwd_host": (_I, [_P] * 6),
+    "tsp_qkv_projection": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "tsp_kv_allgather": (_I, [_P] * 5),
+    "tsp_causal_attention": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "tsp_o_projection": (_I, [_P] * 8),
+    "tsp_swiglu_gate_up": (_I, [_P] * 6),
+    "tsp_swiglu_down": (_I, [_P] * 8),
+    "tsp_device_status": (_I, [_P, _P]),
+    "tsp_wait_selftest": (_I, [_P, ctypes.c_uint64, _P]),
+    "tsp_last_error": (ctypes.c_char_p, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def declared_functions() -> list:
+    """Names of the functions include/tsp.h declares."""
+    with open(HEADER) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsp_[a-z0-9_]+)\s*\(", text)))
+
+
+def load_library():
+    """Load libtsp.so (built by __graft_entry__.build()); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libtsp.so is not built ({path}); run __graft_entry__.build() "
+                           "or python -m folded_tensor_sequence_tsp_gb300.build")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def tsp_last_error() -> str:
+    return load_library().tsp_last_error().decode()
+
+
+def _check(status: int, name: str):
+    if status != TSP_OK:
+        raise TSPError(status, f"{name}: {tsp_last_error()}")
+
+
+def _stream(stream):
+    if stream is None:
+        return _P(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return _P(stream.cuda_stream)
+    return _P(int(stream))
+
+
+def _dev(t, name, numel=None, dtype=torch.bfloat16, optional=False):
+    """Pointer of a contiguous CUDA tensor of `dtype` with at least `numel` elements."""
+    if t is None:
+        if optional:
+            return _P(None)
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+    return _P(t.data_ptr())
+
+
+def _host(t, name, numel):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be a bfloat16 CPU tensor")
+    if not t.is_contiguous() or t.numel() < numel:
+        raise ValueError(f"{name} must be contiguous with {numel} elements")
+    return _P(t.data_ptr())
+
+
+class Plan:
+    """Owns a tsp_plan_t handle."""
+
+    def __init__(self, handle, lib):
+        self._h = handle
+        self._lib = lib
+        info = PlanInfo()
+        _check(lib.tsp_get_plan_info(handle, ctypes.byref(info)), "tsp_get_plan_info")
+        self.info = info
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._lib is not None:
+            self._lib.tsp_plan_destroy(self._h)
+            self._h = None
+
+    # shapes used by the checks below
+    @property
+    def act_elems(self):
+        return self.info.S * self.info.hidden
+
+
+def tsp_plan(D: int, S: int, hidden: int, heads: int, ffn: int) -> Plan:
+    lib = load_library()
+    h = _P()
+    _check(lib.tsp_plan(D, S, hidden, heads, ffn, ctypes.byref(h)), "tsp_plan")
+    return Plan(h, lib)
+
+
+def tsp_get_plan_info(plan: Plan) -> dict:
+    return plan.info.as_dict()
+
+
+def tsp_workspace_bytes(plan: Plan) -> int:
+    return load_library().tsp_workspace_bytes(plan.handle)
+
+
+def tsp_packed_weight_bytes(plan: Plan) -> int:
+    return load_library().tsp_packed_weight_bytes(plan.handle)
+
+
+def _ws(plan, ws):
+    return _dev(ws, "ws", tsp_workspace_bytes(plan), dtype=torch.uint8)
+
+
+def tsp_workspace_init(plan, ws, stream=None):
+    _check(load_library().tsp_workspace_init(plan.handle, _ws(plan, ws), _stream(stream)),
+           "tsp_workspace_init")
+
+
+def tsp_pack_weights(plan, Wq, Wk, Wv, Wo, W1, W3, W2, wpack, stream=None):
+    i = plan.info
+    H, F = i.hidden, i.ffn
+    args = [_dev(Wq, "Wq", H * H), _dev(Wk, "Wk", H * H), _dev(Wv, "Wv", H * H),
+            _dev(Wo, "Wo", H * H), _dev(W1, "W1", F * H), _dev(W3, "W3", F * H),
+            _dev(W2, "W2", H * F), _dev(wpack, "wpack", i.wpack_elems)]
+    _check(load_library().tsp_pack_weights(plan.handle, *args, _stream(stream)), "tsp_pack_weights")
+
+
+def tsp_shard_index(plan, fwd, inv, stream=None):
+    S = plan.info.S
+    _check(load_library().tsp_shard_index(
+        plan.handle, _dev(fwd, "fwd", S, torch.int32, optional=True),
+        _dev(inv, "inv", S, torch.int32, optional=True), _stream(stream)), "tsp_shard_index")
+
+
+def tsp_shard(plan, x, xs, stream=None):
+    n = plan.act_elems
+    _check(load_library().tsp_shard(plan.handle, _dev(x, "x", n), _dev(xs, "xs", n),
+                                    _stream(stream)), "tsp_shard")
+
+
+def tsp_unshard(plan, xs, x, stream=None):
+    n = plan.act_elems
+    _check(load_library().tsp_unshard(plan.handle, _dev(xs, "xs", n), _dev(x, "x", n),
+                                      _stream(stream)), "tsp_unshard")
+
+
+def _block(fn_name, plan, a, wpack, out, ws, stream):
+    n = plan.act_elems
+    fn = getattr(load_library(), fn_name)
+    _check(fn(plan.handle, _dev(a, "input", n), _dev(wpack, "wpack", plan.info.wpack_elems),
+              _dev(out, "out", n), _ws(plan, ws), _stream(stream)), fn_name)
+
+
+def tsp_attention_fwd(plan, xs, wpack, attn, ws, stream=None):
+    _block("tsp_attention_fwd", plan, xs, wpack, attn, ws, stream)
+
+
+def tsp_mlp_fwd(plan, hs, wpack, mlp, ws, stream=None):
+    _block("tsp_mlp_fwd", plan, hs, wpack, mlp, ws, stream)
+
+
+def tsp_layer_fwd(plan, xs, wpack, out, ws, stream=None):
+    _block("tsp_layer_fwd", plan, xs, wpack, out, ws, stream)
+
+
+def tsp_layer_fwd_host(plan, x_host, wpack, out_host, ws, stream=None):
+    n = plan.act_elems
+    _check(load_library().tsp_layer_fwd_host(
+        plan.handle, _host(x_host, "x_host", n), _dev(wpack, "wpack", plan.info.wpack_elems),
+        _host(out_host, "out_host", n), _ws(plan, ws), _stream(stream)), "tsp_layer_fwd_host")
+
+
+def tsp_qkv_projection(plan, shard, xs, wpack, qkv, ws, stream=None):
+    i = plan.info
+    _check(load_library().tsp_qkv_projection(
+        plan.handle, int(shard), _dev(xs, "xs", plan.act_elems),
+        _dev(wpack, "wpack", i.wpack_elems), _dev(qkv, "qkv", i.S * 3 * i.shard_hidden),
+        _ws(plan, ws), _stream(stream)), "tsp_qkv_projection")
+
+
+def tsp_kv_allgather(plan, qkv, kn, vn, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    _check(load_library().tsp_kv_allgather(
+        plan.handle, _dev(qkv, "qkv", 3 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _stream(stream)), "tsp_kv_allgather")
+
+
+def tsp_causal_attention(plan, shard, qkv, kn, vn, o, ws, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    _check(load_library().tsp_causal_attention(
+        plan.handle, int(shard), _dev(qkv, "qkv", 3 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _dev(o, "o", plan.act_elems), _ws(plan, ws), _stream(stream)), "tsp_causal_attention")
+
+
+def tsp_o_projection(plan, o, wpack, residual, out, ws, stream=None, out32=None):
+    n = plan.act_elems
+    _check(load_library().tsp_o_projection(
+        plan.handle, _dev(o, "o", n), _dev(wpack, "wpack", plan.info.wpack_elems),
+        _dev(residual, "residual", n, optional=True), _dev(out, "out", n),
+        _dev(out32, "out32", n, torch.float32, optional=True), _ws(plan, ws),
+        _stream(stream)), "tsp_o_projection")
+
+
+def tsp_swiglu_gate_up(plan, hs, wpack, g, ws, stream=None):
+    i = plan.info
+    _check(load_library().tsp_swiglu_gate_up(
+        plan.handle, _dev(hs, "hs", plan.act_elems), _dev(wpack, "wpack", i.wpack_elems),
+        _dev(g, "g", i.S * i.ffn_padded), _ws(plan, ws), _stream(stream)), "tsp_swiglu_gate_up")
+
+
+def tsp_swiglu_down(plan, g, wpack, residual, out, ws, stream=None, residual32=None):
+    i = plan.info
+    n = plan.act_elems
+    _check(load_library().tsp_swiglu_down(
+        plan.handle, _dev(g, "g", i.S * i.ffn_padded), _dev(wpack, "wpack", i.wpack_elems),
+        _dev(residual, "residual", n, optional=True),
+        _dev(residual32, "residual32", n, torch.float32, optional=True), _dev(out, "out", n),
+        _ws(plan, ws), _stream(stream)), "tsp_swiglu_down")
+
+
+def tsp_device_status(ws, stream=None) -> int:
+    """Synchronise the stream; return (and clear) the workspace status code."""
+    return load_library().tsp_device_status(_dev(ws, "ws", 256, dtype=torch.uint8),
+                                            _stream(stream))
+
+
+def tsp_wait_selftest(ws, limit_ns: int, stream=None):
+    _check(load_library().tsp_wait_selftest(_dev(ws, "ws", 256, dtype=torch.uint8),
+                                            int(limit_ns), _stream(stream)), "tsp_wait_selftest")

@@ -1,0 +1,571 @@
+// api.cu - the C ABI of the TSP layer forward (declared in include/tsp.h).
+//
+// Host orchestration of the schedules of "Folding Tensor and Sequence Parallelism
+// for Memory-Efficient Transformer Training & Inference", section 2:
+//   attention  broadcast schedule: for shard k = 0..D-1 every rank projects its own
+//              tokens with shard k's W_Q/W_K/W_V (one GEMM over all ranks' rows),
+//              K/V are gathered along the sequence into natural order, causal
+//              attention runs for the h/D heads of the shard; the O projection then
+//              accumulates the shards' partial products on chip (its K loop walks
+//              the shards in broadcast order).
+//   MLP        ring schedule: the gate/up GEMM produces every shard's gated
+//              activation; the down GEMM accumulates, for rank r's rows, shard
+//              (r + t) mod D at step t in the on-chip accumulator (no all-reduce).
+// On one GPU the broadcast and the ring hand-off are reads of a shard in place.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "tsp_device.cuh"
+#include "tsp_internal.h"
+
+struct tsp_plan_s {
+  tsp::Plan p;
+};
+
+namespace tsp {
+
+namespace {
+thread_local std::string g_last_error;
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+DevStatus* status_of(void* ws) { return static_cast<DevStatus*>(ws); }
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+}  // namespace
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+tsp_status fail(tsp_status code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+tsp_status cuda_fail(cudaError_t err, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(err);
+  return TSP_ERR_CUDA;
+}
+
+tsp_status make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                             uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(TSP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for %llux%llu stride %llu",
+             (int)r, (unsigned long long)inner, (unsigned long long)outer,
+             (unsigned long long)row_stride_bytes);
+    return fail(TSP_ERR_CUDA, buf);
+  }
+  return TSP_OK;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* e = getenv("TSP_WAIT_LIMIT_NS");
+    unsigned long long x = e ? strtoull(e, nullptr, 10) : 0ull;
+    return x ? x : 4000000000ull;  // 4 s: far above any legitimate wait
+  }();
+  return v;
+}
+
+// ------------------------------------------------------------------ steps
+
+namespace {
+
+tsp_status qkv_projection(const Plan& p, int k, const void* xs, const void* wpack, void* qkv,
+                          void* ws, cudaStream_t s) {
+  GemmCall c{};
+  c.epi = EPI_STORE;
+  c.A = xs;
+  c.lda = p.H;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;
+  c.ldb = p.H;
+  c.b_rows = 3LL * p.H;
+  c.b_row0 = (int64_t)k * 3 * p.Hd;
+  c.N = 3LL * p.Hd;
+  c.K = p.H;
+  c.C = qkv;
+  c.ldc = 3LL * p.Hd;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+tsp_status causal_attention(const Plan& p, int k, const void* qkv, const void* kn, const void* vn,
+                            void* o, void* ws, cudaStream_t s) {
+  AttentionCall a{};
+  a.qkv = qkv;
+  a.ld_qkv = 3LL * p.Hd;
+  a.kn = kn;
+  a.vn = vn;
+  a.ld_kv = p.Hd;
+  a.o = o;
+  a.ld_o = p.H;
+  a.o_col0 = (int64_t)k * p.Hd;
+  a.S = p.S;
+  a.T = p.T;
+  a.C = p.C;
+  a.D = p.D;
+  a.heads = p.hpr;
+  a.d = p.d;
+  a.status = status_of(ws);
+  return launch_attention(a, s);
+}
+
+// out = o W_O^T (+ residual, bf16); with out32 also the fp32 value of out.
+tsp_status o_projection(const Plan& p, const void* o, const void* wpack, const void* residual,
+                        void* out, void* out32, void* ws, cudaStream_t s) {
+  GemmCall c{};
+  c.epi = residual ? EPI_RESIDUAL : EPI_STORE;
+  c.A = o;
+  c.lda = p.H;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_o;
+  c.ldb = p.H;
+  c.b_rows = p.H;
+  c.b_row0 = 0;
+  c.N = p.H;
+  c.K = p.H;
+  c.C = out;
+  c.ldc = p.H;
+  c.R = residual;
+  c.ldr = p.H;
+  c.C32 = out32;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+tsp_status swiglu_gate_up(const Plan& p, const void* hs, const void* wpack, void* g, void* ws,
+                          cudaStream_t s) {
+  GemmCall c{};
+  c.epi = EPI_SWIGLU;
+  c.A = hs;
+  c.lda = p.H;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_w13;
+  c.ldb = p.H;
+  c.b_rows = 2LL * p.NF;
+  c.b_row0 = 0;
+  c.N = 2LL * p.NF;
+  c.K = p.H;
+  c.C = g;
+  c.ldc = p.NF;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+// out = G W2^T (+ residual: bf16, or fp32 when residual_f32) in ring order.
+tsp_status swiglu_down(const Plan& p, const void* g, const void* wpack, const void* residual,
+                       int residual_f32, void* out, void* ws, cudaStream_t s) {
+  GemmCall c{};
+  c.epi = residual ? EPI_RESIDUAL : EPI_STORE;
+  c.A = g;
+  c.lda = p.NF;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_w2;
+  c.ldb = p.NF;
+  c.b_rows = p.H;
+  c.b_row0 = 0;
+  c.N = p.H;
+  c.K = p.NF;
+  c.C = out;
+  c.ldc = p.H;
+  c.R = residual;
+  c.ldr = p.H;
+  c.residual_f32 = residual_f32;
+  c.ring_rows = p.T;
+  c.ring_kblocks = p.Fp / 64;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+#define TSP_TRY(expr)              \
+  do {                             \
+    tsp_status st_ = (expr);       \
+    if (st_ != TSP_OK) return st_; \
+  } while (0)
+
+tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,
+                           void* out, void* out32, void* ws, cudaStream_t s) {
+  void* qkv = at<void>(ws, p.ws.qkv);
+  void* kn = at<void>(ws, p.ws.kn);
+  void* vn = at<void>(ws, p.ws.vn);
+  void* o = at<void>(ws, p.ws.o);
+  for (int k = 0; k < p.D; ++k) {  // broadcast iteration k: every rank reads shard k
+    TSP_TRY(qkv_projection(p, k, xs, wpack, qkv, ws, s));
+    TSP_TRY(launch_kv_gather(p, qkv, kn, vn, s));
+    TSP_TRY(causal_attention(p, k, qkv, kn, vn, o, ws, s));
+  }
+  return o_projection(p, o, wpack, residual, out, out32, ws, s);
+}
+
+tsp_status mlp_block(const Plan& p, const void* hs, const void* wpack, const void* residual,
+                     int residual_f32, void* out, void* ws, cudaStream_t s) {
+  void* g = at<void>(ws, p.ws.g);
+  TSP_TRY(swiglu_gate_up(p, hs, wpack, g, ws, s));
+  return swiglu_down(p, g, wpack, residual, residual_f32, out, ws, s);
+}
+
+tsp_status check_plan(tsp_plan_t plan) {
+  return plan ? TSP_OK : fail(TSP_ERR_INVALID_ARG, "null plan");
+}
+
+tsp_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+  for (const void* q : ptrs) {
+    if (!q) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": null pointer");
+    if (!al16(q)) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": pointer not 16-byte aligned");
+  }
+  return TSP_OK;
+}
+
+tsp_status check_ws(void* ws, const char* what) {
+  if (!ws) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": null workspace");
+  if (!al256(ws)) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": workspace not 256-byte aligned");
+  return TSP_OK;
+}
+
+}  // namespace
+}  // namespace tsp
+
+using namespace tsp;
+
+#define TSP_GUARD_BEGIN try {
+#define TSP_GUARD_END                                                   \
+  }                                                                     \
+  catch (const std::bad_alloc&) {                                       \
+    return fail(TSP_ERR_INVALID_ARG, "host allocation failed");         \
+  }                                                                     \
+  catch (...) {                                                         \
+    return fail(TSP_ERR_INVALID_ARG, "unexpected host exception");      \
+  }
+
+extern "C" {
+
+tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t* out) {
+  TSP_GUARD_BEGIN
+  if (!out) return fail(TSP_ERR_INVALID_ARG, "tsp_plan: null output");
+  *out = nullptr;
+  if (D < 1 || D > 64) return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: D must be in [1, 64]");
+  if (S < 2LL * D || S > (1LL << 26) || S % (2LL * D))
+    return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: S must be a multiple of 2D in [2D, 2^26]");
+  if (heads < 1 || hidden < 1 || hidden % heads)
+    return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: hidden must be a multiple of heads");
+  const int d = hidden / heads;
+  if (d != 64 && d != 128) return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: head_dim must be 64 or 128");
+  if (heads % D) return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: heads must be a multiple of D");
+  if (hidden % 64 || hidden > 32768) return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: hidden must be a multiple of 64, <= 32768");
+  if (ffn < D || ffn % D || ffn > (1 << 20)) return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: ffn must be a positive multiple of D");
+
+  Plan p{};
+  p.D = D;
+  p.S = S;
+  p.H = hidden;
+  p.heads = heads;
+  p.d = d;
+  p.F = ffn;
+  p.T = S / D;
+  p.C = S / (2LL * D);
+  p.Hd = hidden / D;
+  p.hpr = heads / D;
+  p.Fd = ffn / D;
+  p.Fp = (p.Fd + 63) / 64 * 64;
+  if ((long long)D * p.Fp % 128) p.Fp = (p.Fd + 127) / 128 * 128;
+  p.NF = D * p.Fp;
+
+  const size_t H = hidden;
+  p.wp_qkv = 0;
+  p.wp_o = 3 * H * H;
+  p.wp_w13 = p.wp_o + H * H;
+  p.wp_w2 = p.wp_w13 + 2 * (size_t)p.NF * H;
+  p.wp_elems = p.wp_w2 + H * (size_t)p.NF;
+
+  const size_t Sz = (size_t)S;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  p.ws.status = take(256);
+  p.ws.qkv = take(Sz * 3 * p.Hd * 2);
+  p.ws.kn = take(Sz * p.Hd * 2);
+  p.ws.vn = take(Sz * p.Hd * 2);
+  p.ws.o = take(Sz * H * 2);
+  p.ws.h = take(Sz * H * 2);
+  p.ws.h32 = take(Sz * H * 4);
+  p.ws.g = take(Sz * p.NF * 2);
+  p.ws.stage_in = take(Sz * H * 2);
+  p.ws.stage_out = take(Sz * H * 2);
+  p.ws.total = off;
+
+  tsp_plan_s* obj = new tsp_plan_s;
+  obj->p = p;
+  *out = obj;
+  return TSP_OK;
+  TSP_GUARD_END
+}
+
+void tsp_plan_destroy(tsp_plan_t plan) { delete plan; }
+
+tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info) {
+  TSP_TRY(check_plan(plan));
+  if (!info) return fail(TSP_ERR_INVALID_ARG, "tsp_get_plan_info: null info");
+  const Plan& p = plan->p;
+  info->D = p.D;
+  info->S = p.S;
+  info->hidden = p.H;
+  info->heads = p.heads;
+  info->head_dim = p.d;
+  info->ffn = p.F;
+  info->T = p.T;
+  info->C = p.C;
+  info->shard_hidden = p.Hd;
+  info->shard_ffn = p.Fd;
+  info->shard_ffn_padded = p.Fp;
+  info->ffn_padded = p.NF;
+  info->wpack_qkv = p.wp_qkv;
+  info->wpack_o = p.wp_o;
+  info->wpack_w13 = p.wp_w13;
+  info->wpack_w2 = p.wp_w2;
+  info->wpack_elems = p.wp_elems;
+  info->workspace_bytes = p.ws.total;
+  return TSP_OK;
+}
+
+size_t tsp_workspace_bytes(tsp_plan_t plan) { return plan ? plan->p.ws.total : 0; }
+
+size_t tsp_packed_weight_bytes(tsp_plan_t plan) { return plan ? plan->p.wp_elems * 2 : 0; }
+
+tsp_status tsp_workspace_init(tsp_plan_t plan, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ws(ws, "tsp_workspace_init"));
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TSP_OK : cuda_fail(e, "tsp_workspace_init");
+}
+
+tsp_status tsp_pack_weights(tsp_plan_t plan, const tsp_bf16* Wq, const tsp_bf16* Wk,
+                            const tsp_bf16* Wv, const tsp_bf16* Wo, const tsp_bf16* W1,
+                            const tsp_bf16* W3, const tsp_bf16* W2, tsp_bf16* wpack,
+                            void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({Wq, Wk, Wv, Wo, W1, W3, W2, wpack}, "tsp_pack_weights"));
+  return launch_pack_weights(plan->p, Wq, Wk, Wv, Wo, W1, W3, W2, wpack,
+                             static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_shard_index(tsp_plan_t plan, int32_t* fwd, int32_t* inv, void* stream) {
+  TSP_TRY(check_plan(plan));
+  if (!fwd && !inv) return TSP_OK;
+  return launch_zigzag_index(plan->p, fwd, inv, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_shard(tsp_plan_t plan, const tsp_bf16* x, tsp_bf16* xs, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({x, xs}, "tsp_shard"));
+  if (x == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_shard: buffers overlap");
+  return launch_zigzag_rows(plan->p, x, xs, plan->p.H, true, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_unshard(tsp_plan_t plan, const tsp_bf16* xs, tsp_bf16* x, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({x, xs}, "tsp_unshard"));
+  if (x == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_unshard: buffers overlap");
+  return launch_zigzag_rows(plan->p, xs, x, plan->p.H, false, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_attention_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                             tsp_bf16* attn, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, attn}, "tsp_attention_fwd"));
+  TSP_TRY(check_ws(ws, "tsp_attention_fwd"));
+  if (attn == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_attention_fwd: attn aliases xs");
+  return attention_block(plan->p, xs, wpack, nullptr, attn, nullptr, ws,
+                         static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_mlp_fwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack, tsp_bf16* mlp,
+                       void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({hs, wpack, mlp}, "tsp_mlp_fwd"));
+  TSP_TRY(check_ws(ws, "tsp_mlp_fwd"));
+  if (mlp == hs) return fail(TSP_ERR_INVALID_ARG, "tsp_mlp_fwd: mlp aliases hs");
+  return mlp_block(plan->p, hs, wpack, nullptr, 0, mlp, ws, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                         tsp_bf16* out, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, out}, "tsp_layer_fwd"));
+  TSP_TRY(check_ws(ws, "tsp_layer_fwd"));
+  if (out == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd: out aliases xs");
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* h = at<void>(ws, p.ws.h);
+  void* h32 = at<void>(ws, p.ws.h32);
+  // h = x + Attn(x), kept in bf16 (the MLP's input) and in fp32 (its residual), so
+  // that out = h + MLP(h) is rounded to bf16 once
+  TSP_TRY(attention_block(p, xs, wpack, xs, h, h32, ws, s));
+  return mlp_block(p, h, wpack, h32, 1, out, ws, s);
+}
+
+tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
+                              tsp_bf16* out_host, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  if (!x_host || !out_host) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd_host: null host buffer");
+  TSP_TRY(check_ptrs({wpack}, "tsp_layer_fwd_host"));
+  TSP_TRY(check_ws(ws, "tsp_layer_fwd_host"));
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)p.S * p.H * 2;
+  void* a = at<void>(ws, p.ws.stage_in);
+  void* b = at<void>(ws, p.ws.stage_out);
+  cudaError_t e = cudaMemcpyAsync(a, x_host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy in");
+  TSP_TRY(launch_zigzag_rows(p, a, b, p.H, true, s));  // b = shard(x)
+  TSP_TRY(tsp_layer_fwd(plan, static_cast<const tsp_bf16*>(b), wpack, static_cast<tsp_bf16*>(a),
+                        ws, stream));                   // a = layer(b)
+  TSP_TRY(launch_zigzag_rows(p, a, b, p.H, false, s));  // b = unshard(a)
+  e = cudaMemcpyAsync(out_host, b, bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy out");
+  return TSP_OK;
+}
+
+tsp_status tsp_qkv_projection(tsp_plan_t plan, int shard, const tsp_bf16* xs,
+                              const tsp_bf16* wpack, tsp_bf16* qkv, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, qkv}, "tsp_qkv_projection"));
+  TSP_TRY(check_ws(ws, "tsp_qkv_projection"));
+  if (shard < 0 || shard >= plan->p.D) return fail(TSP_ERR_INVALID_ARG, "tsp_qkv_projection: shard out of range");
+  return qkv_projection(plan->p, shard, xs, wpack, qkv, ws, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, tsp_bf16* vn,
+                            void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({qkv, kn, vn}, "tsp_kv_allgather"));
+  return launch_kv_gather(plan->p, qkv, kn, vn, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_causal_attention(tsp_plan_t plan, int shard, const tsp_bf16* qkv,
+                                const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o, void* ws,
+                                void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({qkv, kn, vn, o}, "tsp_causal_attention"));
+  TSP_TRY(check_ws(ws, "tsp_causal_attention"));
+  if (shard < 0 || shard >= plan->p.D) return fail(TSP_ERR_INVALID_ARG, "tsp_causal_attention: shard out of range");
+  return causal_attention(plan->p, shard, qkv, kn, vn, o, ws, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_o_projection(tsp_plan_t plan, const tsp_bf16* o, const tsp_bf16* wpack,
+                            const tsp_bf16* residual, tsp_bf16* out, float* out32, void* ws,
+                            void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({o, wpack, out}, "tsp_o_projection"));
+  TSP_TRY(check_ws(ws, "tsp_o_projection"));
+  if (residual && !al16(residual)) return fail(TSP_ERR_INVALID_ARG, "tsp_o_projection: residual not 16-byte aligned");
+  if (out32 && !residual) return fail(TSP_ERR_INVALID_ARG, "tsp_o_projection: out32 needs a residual");
+  if (out32 && !al16(out32)) return fail(TSP_ERR_INVALID_ARG, "tsp_o_projection: out32 not 16-byte aligned");
+  return o_projection(plan->p, o, wpack, residual, out, out32, ws,
+                      static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_swiglu_gate_up(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
+                              tsp_bf16* g, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({hs, wpack, g}, "tsp_swiglu_gate_up"));
+  TSP_TRY(check_ws(ws, "tsp_swiglu_gate_up"));
+  return swiglu_gate_up(plan->p, hs, wpack, g, ws, static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_swiglu_down(tsp_plan_t plan, const tsp_bf16* g, const tsp_bf16* wpack,
+                           const tsp_bf16* residual, const float* residual32, tsp_bf16* out,
+                           void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({g, wpack, out}, "tsp_swiglu_down"));
+  TSP_TRY(check_ws(ws, "tsp_swiglu_down"));
+  if (residual && !al16(residual)) return fail(TSP_ERR_INVALID_ARG, "tsp_swiglu_down: residual not 16-byte aligned");
+  if (residual32 && !al16(residual32)) return fail(TSP_ERR_INVALID_ARG, "tsp_swiglu_down: residual32 not 16-byte aligned");
+  const void* r = residual32 ? static_cast<const void*>(residual32) : residual;
+  return swiglu_down(plan->p, g, wpack, r, residual32 ? 1 : 0, out, ws,
+                     static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_device_status(void* ws, void* stream) {
+  TSP_TRY(check_ws(ws, "tsp_device_status"));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus st{};
+  cudaError_t e = cudaMemcpyAsync(&st, ws, sizeof st, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "tsp_device_status");
+  if (st.code == 0) return TSP_OK;
+  e = cudaMemsetAsync(ws, 0, sizeof st, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "tsp_device_status: clear");
+  char buf[160];
+  snprintf(buf, sizeof buf, "device wait gave up (site %u, block %u, thread %u)", st.site, st.block,
+           st.thread);
+  return fail(st.code == TSP_ERR_TIMEOUT ? TSP_ERR_TIMEOUT : TSP_ERR_CUDA, buf);
+}
+
+tsp_status tsp_wait_selftest(void* ws, uint64_t limit_ns, void* stream) {
+  TSP_TRY(check_ws(ws, "tsp_wait_selftest"));
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(TSP_ERR_INVALID_ARG, "tsp_wait_selftest: limit must be in (0, 10 s]");
+  return launch_wait_selftest(status_of(ws), limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+const char* tsp_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,380 @@
+// gemm_tcgen05.cu - the dense bf16 contractions of the TSP layer on sm_103a:
+//   * Q/K/V projection of one attention shard   (local projections of a broadcast
+//     iteration, "Folding Tensor and Sequence Parallelism for Memory-Efficient
+//     Transformer Training & Inference", section 2, attention layers),
+//   * O projection accumulated over the shards,
+//   * SwiGLU gate/up product with the gating fused into the epilogue,
+//   * SwiGLU down product accumulated over the MLP shards in ring order
+//     (same page, section 2, gated MLP layers: local accumulation, no all-reduce).
+//
+// C[M][N] = A[M][K] * B[N][K]^T, A and B bf16 K-major, fp32 accumulation in tensor
+// memory. One persistent CTA per SM walks output tiles of 128 x 256:
+//   warp 0      TMA producer: 64-wide K slices of A and B into a 4-stage ring of
+//               128B-swizzled shared-memory buffers (mbarrier transaction counts)
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and one
+//               lane issues tcgen05.mma (M=128, N=256, K=16) and tcgen05.commit
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows (one row per thread),
+//               fused residual add or SiLU gating, bf16 rounding, global stores;
+//               the second accumulator lets the epilogue of a tile overlap the
+//               main loop of the next.
+// Ring order: with ring_rows > 0 the K loop of a tile whose rows belong to rank
+// r = m0 / ring_rows starts at K block r * ring_kblocks and wraps around, so rank r
+// takes MLP shard (r + t) mod D at step t, and the partial products of the shards
+// are summed in the on-chip accumulator.
+#include "tsp_device.cuh"
+#include "tsp_internal.h"
+
+namespace tsp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int THREADS = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+
+// Epilogue variants of the kernel.
+enum Kind {
+  K_STORE = 0,          // C = bf16(acc)
+  K_RES_BF16 = 1,       // C = bf16(acc + R), R bf16
+  K_SWIGLU = 2,         // C = bf16(silu(acc_gate) * acc_up)
+  K_RES_BF16_OUT32 = 3, // C = bf16(acc + R), C32 = acc + R (fp32), R bf16
+  K_RES_F32 = 4,        // C = bf16(acc + R), R fp32
+};
+
+struct GemmParams {
+  int M, N, K;
+  int b_row0;
+  __nv_bfloat16* C;
+  long long ldc;
+  const void* R;   // residual: bf16 or fp32 depending on the variant
+  long long ldr;
+  float* C32;      // fp32 copy of the output (K_RES_BF16_OUT32)
+  int ring_rows;
+  int ring_kblocks;
+  DevStatus* status;
+  unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&f)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 w;
+    w.x = pack_bf16x2(f[8 * v + 0], f[8 * v + 1]);
+    w.y = pack_bf16x2(f[8 * v + 2], f[8 * v + 3]);
+    w.z = pack_bf16x2(f[8 * v + 4], f[8 * v + 5]);
+    w.w = pack_bf16x2(f[8 * v + 6], f[8 * v + 7]);
+    d[v] = w;
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                  // [STAGES] TMA landed
+  uint64_t* empty = bars + STAGES;        // [STAGES] MMAs reading the stage are done
+  uint64_t* acc_full = bars + 2 * STAGES; // [2] accumulator complete
+  uint64_t* acc_empty = acc_full + 2;     // [2] epilogue drained the accumulator
+  uint64_t* drain = acc_empty + 2;        // [1] every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int numM = (p.M + BM - 1) / BM;
+  const int numN = (p.N + BN - 1) / BN;
+  const int numTiles = numM * numN;
+  const int nkb = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  WaitBound wb{p.status, p.limit_ns, abort_flag};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_parity[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+      const uint64_t keep = l2_policy_evict_last();
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < numTiles; tile += gridDim.x) {
+        const int mt = tile / numN, nt = tile - mt * numN;
+        const int m0 = mt * BM, n0 = nt * BN;
+        int kb = 0;
+        if (p.ring_rows > 0) kb = (int)(((long long)(m0 / p.ring_rows) * p.ring_kblocks) % nkb);
+        for (int i = 0; i < nkb; ++i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, wb, SITE_GEMM_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
+          tma_load_2d_hint(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, p.b_row0 + n0, keep);
+          last_parity[stage] = (int)phase;
+          if (++kb == nkb) kb = 0;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Do not leave while a TMA copy into this CTA's shared memory is in flight.
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      for (int s = 0; s < STAGES; ++s)
+        if (last_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)last_parity[s], wd, SITE_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = make_idesc_bf16(BM, BN, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < numTiles; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wb, SITE_GEMM_MMA)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int i = 0; i < nkb; ++i) {
+          if (!mbar_wait(&full[stage], phase, wb, SITE_GEMM_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(sA + stage * A_BYTES);
+          const uint32_t b0 = smem_addr(sB + stage * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = make_sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = make_sdesc_sw128(b0 + kk * 32, 16, 1024);
+            mma_ss(d_tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA issued above completes before TMEM is released.
+      mma_commit(drain);
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(drain, 0, wd, SITE_DRAIN);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < numTiles; tile += gridDim.x) {
+      const int mt = tile / numN, nt = tile - mt * numN;
+      if (!mbar_wait(&acc_full[acc], acc_phase, wb, SITE_GEMM_EPILOGUE)) break;
+      tc_fence_after();
+      const long long row = (long long)mt * BM + r_in_tile;
+      const bool row_ok = row < p.M;
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if constexpr (EPI == K_SWIGLU) {
+        // columns [0,128) of the tile are gate rows (W1), [128,256) up rows (W3)
+        const int half_n = p.N >> 1;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          const int ocol = nt * (BN / 2) + c;
+          if (ocol >= half_n) break;
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tbase + c, gv);
+          tmem_ld32(tbase + BN / 2 + c, uv);
+          tmem_ld_wait();
+          if (row_ok) {
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float g = __uint_as_float(gv[j]);
+              const float u = __uint_as_float(uv[j]);
+              f[j] = g / (1.0f + __expf(-g)) * u;
+            }
+            store_row32(p.C + row * p.ldc + ocol, f);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const int col = nt * BN + c;
+          if (col >= p.N) break;
+          uint32_t v[32];
+          tmem_ld32(tbase + c, v);
+          tmem_ld_wait();
+          if (row_ok) {
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+            if constexpr (EPI == K_RES_BF16 || EPI == K_RES_BF16_OUT32) {
+              const uint4* r4 = reinterpret_cast<const uint4*>(
+                  static_cast<const __nv_bfloat16*>(p.R) + row * p.ldr + col);
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint4 rv = __ldg(r4 + w);
+                f[8 * w + 0] += bf16_lo(rv.x);
+                f[8 * w + 1] += bf16_hi(rv.x);
+                f[8 * w + 2] += bf16_lo(rv.y);
+                f[8 * w + 3] += bf16_hi(rv.y);
+                f[8 * w + 4] += bf16_lo(rv.z);
+                f[8 * w + 5] += bf16_hi(rv.z);
+                f[8 * w + 6] += bf16_lo(rv.w);
+                f[8 * w + 7] += bf16_hi(rv.w);
+              }
+            }
+            if constexpr (EPI == K_RES_F32) {
+              const float4* r4 =
+                  reinterpret_cast<const float4*>(static_cast<const float*>(p.R) + row * p.ldr + col);
+#pragma unroll
+              for (int w = 0; w < 8; ++w) {
+                const float4 rv = __ldcs(r4 + w);
+                f[4 * w + 0] += rv.x;
+                f[4 * w + 1] += rv.y;
+                f[4 * w + 2] += rv.z;
+                f[4 * w + 3] += rv.w;
+              }
+            }
+            if constexpr (EPI == K_RES_BF16_OUT32) {
+              float4* c4 = reinterpret_cast<float4*>(p.C32 + row * p.ldc + col);
+#pragma unroll
+              for (int w = 0; w < 8; ++w)
+                c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+            }
+            store_row32(p.C + row * p.ldc + col, f);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+template <int EPI>
+tsp_status launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+                      cudaStream_t stream) {
+  auto kernel = gemm_bf16_tcgen05<EPI>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(e, "gemm: cudaFuncSetAttribute");
+  kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "gemm: launch");
+  return TSP_OK;
+}
+
+}  // namespace
+
+tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
+  if (!c.A || !c.B || !c.C || !c.status) return fail(TSP_ERR_INVALID_ARG, "gemm: null pointer");
+  if (c.M <= 0 || c.N <= 0 || c.K <= 0) return fail(TSP_ERR_INVALID_ARG, "gemm: empty shape");
+  if (c.K % BK) return fail(TSP_ERR_UNSUPPORTED, "gemm: K must be a multiple of 64");
+  if (c.epi == EPI_SWIGLU ? (c.N % 64) : (c.N % 32))
+    return fail(TSP_ERR_UNSUPPORTED, "gemm: N must be a multiple of 32 (64 for SwiGLU)");
+  if (c.b_row0 < 0 || c.b_row0 + c.N > c.b_rows)
+    return fail(TSP_ERR_INVALID_ARG, "gemm: B row range out of bounds");
+  if (!aligned16(c.A) || !aligned16(c.B) || !aligned16(c.C) || (c.R && !aligned16(c.R)) ||
+      (c.C32 && !aligned16(c.C32)) || (c.lda % 8) || (c.ldb % 8) || (c.ldc % 8) ||
+      (c.R && (c.ldr % 8)))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: buffers and row strides must be 16-byte aligned");
+  if (c.epi == EPI_RESIDUAL && !c.R) return fail(TSP_ERR_INVALID_ARG, "gemm: residual missing");
+  if (c.C32 && (c.epi != EPI_RESIDUAL || c.residual_f32))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 output needs a bf16 residual");
+  if (c.M > (1ll << 30) || c.N > (1ll << 30) || c.K > (1ll << 30) || c.b_rows > (1ll << 30))
+    return fail(TSP_ERR_UNSUPPORTED, "gemm: dimension too large");
+  if (c.ring_rows > 0 && (c.ring_kblocks <= 0))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: ring order needs ring_kblocks > 0");
+
+  CUtensorMap ta, tb;
+  tsp_status st = make_tmap_2d_bf16(&ta, c.A, (uint64_t)c.K, (uint64_t)c.M,
+                                    (uint64_t)c.lda * 2, BK, BM);
+  if (st != TSP_OK) return st;
+  st = make_tmap_2d_bf16(&tb, c.B, (uint64_t)c.K, (uint64_t)c.b_rows, (uint64_t)c.ldb * 2, BK, BN);
+  if (st != TSP_OK) return st;
+
+  GemmParams p;
+  p.M = (int)c.M;
+  p.N = (int)c.N;
+  p.K = (int)c.K;
+  p.b_row0 = (int)c.b_row0;
+  p.C = static_cast<__nv_bfloat16*>(c.C);
+  p.ldc = c.ldc;
+  p.R = c.R;
+  p.ldr = c.ldr;
+  p.C32 = static_cast<float*>(c.C32);
+  p.ring_rows = (int)c.ring_rows;
+  p.ring_kblocks = (int)c.ring_kblocks;
+  p.status = c.status;
+  p.limit_ns = wait_limit_ns();
+
+  const long long tiles = ((c.M + BM - 1) / BM) * ((c.N + BN - 1) / BN);
+  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+  switch (c.epi) {
+    case EPI_STORE: return launch_epi<K_STORE>(ta, tb, p, grid, stream);
+    case EPI_SWIGLU: return launch_epi<K_SWIGLU>(ta, tb, p, grid, stream);
+    case EPI_RESIDUAL:
+      if (c.residual_f32) return launch_epi<K_RES_F32>(ta, tb, p, grid, stream);
+      if (c.C32) return launch_epi<K_RES_BF16_OUT32>(ta, tb, p, grid, stream);
+      return launch_epi<K_RES_BF16>(ta, tb, p, grid, stream);
+    default: return fail(TSP_ERR_INVALID_ARG, "gemm: unknown epilogue");
+  }
+}
+
+}  // namespace tsp

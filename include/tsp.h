@@ -1,0 +1,256 @@
+/*
+ * tsp.h - C ABI of the GB300 (sm_103a) forward of one Folding Tensor and
+ * Sequence Parallelism (TSP) transformer layer, all D logical ranks on one GPU.
+ *
+ * Source of the method, cited below as [TSP]: the summary page "Folding Tensor and
+ * Sequence Parallelism for Memory-Efficient Transformer Training & Inference"
+ * (gist.science, paper 2604.26294). Section numbers refer to that page:
+ * s1 Problem statement, s2 Methodology, s3 Contributions, s4 Results.
+ *
+ * What the library computes (a layer without normalisation or positional encoding):
+ *     h   = x + Attn(x)        Attn: causal multi-head softmax attention, scale 1/sqrt(d)
+ *     out = h + MLP(h)         MLP(h) = (silu(h W1^T) * (h W3^T)) W2^T
+ * with the tokens of the sequence and the weights split over D ranks as [TSP] s2
+ * describes: each rank owns 1/D of the tokens (zigzag chunks) and 1/D of the
+ * weights; attention iterates over packed W_Q/W_K/W_V/W_O shards (broadcast
+ * schedule), gathers K/V along the sequence and runs causal attention of each
+ * rank's queries against the full K/V; the gated MLP streams W1/W3/W2 shards in
+ * ring order and accumulates each rank's partial outputs locally, without an
+ * all-reduce. On one GPU a "broadcast" or a "ring hand-off" is a read of a shard
+ * in place, and the all-gather is a gather kernel into natural token order.
+ *
+ * Conventions shared by every entry point
+ *   - Element type: bfloat16, passed as its 16-bit pattern (tsp_bf16). Arithmetic
+ *     on tensor cores accumulates in fp32; intermediates stored in HBM (Q, K, V, P,
+ *     O, h, G) are rounded to bf16 with round-to-nearest-even.
+ *   - Pointers are DEVICE pointers unless the name ends in _host. The caller owns
+ *     every buffer; the library allocates no device memory in any call below.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). All device work is enqueued asynchronously on it; calls return
+ *     once the work is enqueued.
+ *   - Activations in the "sharded" layout are rank-major [D, T, H] with
+ *     T = S/D: rank r's rows are its zigzag tokens in local order (chunk r, then
+ *     chunk 2D-1-r, chunk length C = S/(2D)).
+ *   - Status is returned synchronously. Argument and shape problems return
+ *     TSP_ERR_INVALID_ARG / TSP_ERR_UNSUPPORTED before anything is launched; a
+ *     launch failure returns TSP_ERR_CUDA. Device-side waits are bounded: a wait
+ *     that gives up records TSP_ERR_TIMEOUT in the workspace status word, which
+ *     tsp_device_status() reports. tsp_last_error() returns a message for the
+ *     last failing call of the calling thread. No C++ exception crosses the ABI.
+ */
+#ifndef TSP_H_
+#define TSP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t tsp_bf16; /* bfloat16 bit pattern */
+
+typedef enum tsp_status {
+  TSP_OK = 0,
+  TSP_ERR_INVALID_ARG = 1, /* null pointer, bad index, misaligned buffer        */
+  TSP_ERR_UNSUPPORTED = 2, /* shape outside the supported set (see tsp_plan)    */
+  TSP_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed     */
+  TSP_ERR_TIMEOUT = 4      /* a bounded device wait gave up (tsp_device_status) */
+} tsp_status;
+
+typedef struct tsp_plan_s* tsp_plan_t; /* opaque, library-owned, immutable */
+
+/* Derived sizes of a plan (all element counts unless named _bytes). */
+typedef struct tsp_plan_info {
+  int D;            /* logical ranks = shards                                  */
+  int64_t S;        /* tokens                                                  */
+  int hidden;       /* H                                                       */
+  int heads;        /* attention heads h                                       */
+  int head_dim;     /* d = H / h                                               */
+  int ffn;          /* F                                                       */
+  int64_t T;        /* tokens per rank, S / D                                  */
+  int64_t C;        /* zigzag chunk, S / (2D)                                  */
+  int shard_hidden; /* H / D: width of one attention weight shard (h/D heads)  */
+  int shard_ffn;    /* F / D: width of one MLP weight shard                    */
+  int shard_ffn_padded; /* Fp >= F/D: stored width of one MLP shard (zero rows) */
+  int ffn_padded;   /* NF = D * Fp: width of the gated activation G            */
+  /* packed weight buffer (elements from its start) */
+  size_t wpack_qkv;   /* [D][3H/D][H]: shard k = rows of W_Q, W_K, W_V of heads group k */
+  size_t wpack_o;     /* [H][H]: W_O; shard k = columns [k H/D, (k+1) H/D)             */
+  size_t wpack_w13;   /* [NF/128][256][H]: per 128 padded ffn columns, 128 W1 rows then 128 W3 rows */
+  size_t wpack_w2;    /* [H][NF]: W2, shard k = columns [k Fp, (k+1) Fp), zero padded  */
+  size_t wpack_elems; /* total elements of the packed buffer                          */
+  size_t workspace_bytes;
+} tsp_plan_info;
+
+/*
+ * tsp_plan - validate a layer shape and derive sizes. Makes no CUDA call.
+ *   D      logical ranks (shards) >= 1          [TSP] s2, "Unified sharding"
+ *   S      tokens (batch 1)                     [TSP] s2
+ *   hidden H, heads h: head_dim d = H/h must be 64 or 128
+ *   ffn    F, the SwiGLU inner width
+ * Supported iff S % (2D) == 0 (zigzag chunks), heads % D == 0 (whole heads per
+ * attention shard), ffn % D == 0, H % 64 == 0, 1 <= D <= 64 and
+ * 2D <= S <= 2^26; otherwise TSP_ERR_UNSUPPORTED. *out receives a plan that
+ * the caller releases with tsp_plan_destroy.
+ */
+tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t* out);
+void tsp_plan_destroy(tsp_plan_t plan);
+tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info);
+/* Bytes of the caller-allocated workspace every *_fwd call below needs (256-byte
+ * aligned). Its first 256 bytes hold the device status word. */
+size_t tsp_workspace_bytes(tsp_plan_t plan);
+/* Bytes of the packed weight buffer (tsp_plan_info.wpack_elems bf16 elements). */
+size_t tsp_packed_weight_bytes(tsp_plan_t plan);
+
+/*
+ * tsp_workspace_init - zero the workspace status word (enqueued on stream).
+ * Call once after allocating a workspace.
+ */
+tsp_status tsp_workspace_init(tsp_plan_t plan, void* ws, void* stream);
+
+/*
+ * tsp_pack_weights - build the packed, shard-major weight buffer ([TSP] s2:
+ * packed W_Q/W_K/W_V/W_O shards for attention; W1/W2/W3 shards for the ring).
+ * Inputs use the nn.Linear layout [out, in]: Wq/Wk/Wv/Wo [H][H], W1/W3 [F][H],
+ * W2 [H][F]. wpack must hold tsp_packed_weight_bytes(plan) bytes. Padded ffn
+ * columns are written as zero. Run once per weight set.
+ */
+tsp_status tsp_pack_weights(tsp_plan_t plan, const tsp_bf16* Wq, const tsp_bf16* Wk,
+                            const tsp_bf16* Wv, const tsp_bf16* Wo, const tsp_bf16* W1,
+                            const tsp_bf16* W3, const tsp_bf16* W2, tsp_bf16* wpack,
+                            void* stream);
+
+/*
+ * tsp_shard_index - the zigzag map ([TSP] s2, zigzag partitioning that balances
+ * causal attention work). fwd[t] = r*T + l for global token t owned by rank r at
+ * local row l; inv[r*T + l] = t. Both int32 [S]. Either pointer may be NULL.
+ */
+tsp_status tsp_shard_index(tsp_plan_t plan, int32_t* fwd, int32_t* inv, void* stream);
+
+/* tsp_shard: x [S][H] natural order -> xs [D][T][H] zigzag rank-major.
+ * tsp_unshard: the inverse. Buffers must not overlap. */
+tsp_status tsp_shard(tsp_plan_t plan, const tsp_bf16* x, tsp_bf16* xs, void* stream);
+tsp_status tsp_unshard(tsp_plan_t plan, const tsp_bf16* xs, tsp_bf16* x, void* stream);
+
+/*
+ * tsp_attention_fwd - attention block of every rank, no residual ([TSP] s2,
+ * attention layers: broadcast schedule over packed shards, local Q/K/V
+ * projections, K/V all-gather, FlashAttention over zigzag query chunks).
+ *   xs   [D][T][H] sharded layer input
+ *   attn [D][T][H] sharded output Attn(x)
+ * attn may not alias xs or ws.
+ */
+tsp_status tsp_attention_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                             tsp_bf16* attn, void* ws, void* stream);
+
+/*
+ * tsp_mlp_fwd - gated MLP of every rank, no residual ([TSP] s2, gated MLP layers:
+ * W1/W3/W2 shards circulate in a ring; each rank accumulates its partial outputs
+ * locally, with no all-reduce). hs and mlp are [D][T][H] sharded.
+ */
+tsp_status tsp_mlp_fwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
+                       tsp_bf16* mlp, void* ws, void* stream);
+
+/*
+ * tsp_layer_fwd - the whole layer on sharded activations:
+ *   out = h + MLP(h), h = xs + Attn(xs); xs and out [D][T][H]. out may not alias xs.
+ */
+tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                         tsp_bf16* out, void* ws, void* stream);
+
+/*
+ * tsp_layer_fwd_host - the whole layer from and to HOST memory in natural token
+ * order: copies x_host [S][H] to the device, shards it, runs tsp_layer_fwd,
+ * unshards and copies the result to out_host [S][H]. Host buffers should be
+ * pinned (page-locked) for the copies to be asynchronous; the call returns once
+ * the work is enqueued, so synchronise `stream` before reading out_host.
+ */
+tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
+                              tsp_bf16* out_host, void* ws, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Single steps of the hot path. The *_fwd calls above are compositions of these.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * tsp_qkv_projection - step "local projections" of broadcast iteration k
+ * ([TSP] s2, attention layers): every rank multiplies its own tokens by shard k
+ * of W_Q/W_K/W_V. qkv [D*T][3H/D]: columns [0,H/D) Q, [H/D,2H/D) K,
+ * [2H/D,3H/D) V of heads group k (head-major, d columns per head), rows in the
+ * sharded (zigzag) order.
+ */
+tsp_status tsp_qkv_projection(tsp_plan_t plan, int shard, const tsp_bf16* xs,
+                              const tsp_bf16* wpack, tsp_bf16* qkv, void* ws, void* stream);
+
+/*
+ * tsp_kv_allgather - step "All-Gather of K/V along the sequence" ([TSP] s2):
+ * gathers the K and V columns of every rank's qkv rows into natural token order:
+ * kn[t] = K row of token t, vn[t] = V row of token t; kn, vn [S][H/D].
+ */
+tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, tsp_bf16* vn,
+                            void* stream);
+
+/*
+ * tsp_causal_attention - step "FlashAttention" for heads group k ([TSP] s2): every
+ * query row of qkv (zigzag row, global position from the zigzag map) attends to
+ * kn/vn rows 0..position. Writes o[row][k*H/D + j*d + c] for the h/D heads j of
+ * the group; o is [D*T][H] (sharded rows). Scale 1/sqrt(d).
+ */
+tsp_status tsp_causal_attention(tsp_plan_t plan, int shard, const tsp_bf16* qkv,
+                                const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
+                                void* ws, void* stream);
+
+/*
+ * tsp_o_projection - O projection with local accumulation over the attention
+ * shards: out = o * W_O^T (+ residual if not NULL). The K-loop of the product walks
+ * the shards k = 0..D-1 in broadcast order and accumulates in fp32 on chip.
+ * o, residual, out [D*T][H] bf16. If out32 is not NULL (it needs a residual), the
+ * fp32 value of out is also written there ([D*T][H] float), which is how
+ * tsp_layer_fwd keeps h = x + Attn(x) in fp32 for the MLP's residual.
+ */
+tsp_status tsp_o_projection(tsp_plan_t plan, const tsp_bf16* o, const tsp_bf16* wpack,
+                            const tsp_bf16* residual, tsp_bf16* out, float* out32, void* ws,
+                            void* stream);
+
+/*
+ * tsp_swiglu_gate_up - G = silu(hs W1^T) * (hs W3^T) for every MLP shard:
+ * g [D*T][NF], shard k in columns [k Fp, (k+1) Fp) (padded columns are 0).
+ */
+tsp_status tsp_swiglu_gate_up(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
+                              tsp_bf16* g, void* ws, void* stream);
+
+/*
+ * tsp_swiglu_down - out = G W2^T (+ residual) with the ring order of [TSP] s2: for
+ * rows of rank r the K-loop takes shard (r + t) mod D at step t = 0..D-1 and
+ * accumulates the partial outputs locally in fp32 (no all-reduce). The residual is
+ * residual32 ([D*T][H] float) if not NULL, else residual ([D*T][H] bf16) if not
+ * NULL, else none.
+ */
+tsp_status tsp_swiglu_down(tsp_plan_t plan, const tsp_bf16* g, const tsp_bf16* wpack,
+                           const tsp_bf16* residual, const float* residual32, tsp_bf16* out,
+                           void* ws, void* stream);
+
+/*
+ * tsp_device_status - synchronise `stream`, then read and clear the workspace
+ * status word. Returns TSP_OK, TSP_ERR_TIMEOUT (a bounded device wait gave up; the
+ * outputs of the affected call are undefined) or TSP_ERR_CUDA.
+ */
+tsp_status tsp_device_status(void* ws, void* stream);
+
+/*
+ * tsp_wait_selftest - launch one block that waits on a barrier nothing will
+ * arrive at, with a bound of `limit_ns` nanoseconds; the kernel gives up, records
+ * TSP_ERR_TIMEOUT in the status word and returns. Exercises the failure path of
+ * the bounded waits without faulting or hanging the GPU.
+ */
+tsp_status tsp_wait_selftest(void* ws, uint64_t limit_ns, void* stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* tsp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSP_H_ */

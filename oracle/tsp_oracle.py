@@ -63,7 +63,9 @@ __all__ = [
     "multihead_causal_attention",
     "attention_block",
     "silu",
+    "swiglu_gate",
     "swiglu_mlp",
+    "qkv_projection_shard",
     "layer_forward",
     "tsp_layer_forward",
     "causal_pairs_per_rank",
@@ -216,9 +218,25 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+def swiglu_gate(h, W1, W3) -> np.ndarray:
+    """Gated activation G = silu(h W1^T) * (h W3^T)."""
+    return silu(h @ W1.T) * (h @ W3.T)
+
+
 def swiglu_mlp(h, W1, W3, W2) -> np.ndarray:
     """MLP(h) = (silu(h W1^T) * (h W3^T)) W2^T, no residual."""
-    return (silu(h @ W1.T) * (h @ W3.T)) @ W2.T
+    return swiglu_gate(h, W1, W3) @ W2.T
+
+
+def qkv_projection_shard(x, Wq, Wk, Wv, k: int, D: int) -> np.ndarray:
+    """Local projections of broadcast iteration k ([TSP] s2, attention layers).
+
+    x times the rows of heads group k ([k H/D, (k+1) H/D)) of W_Q, W_K and W_V;
+    returns [n, 3H/D] laid out as Q | K | V.
+    """
+    Hd = Wq.shape[0] // D
+    c = slice(k * Hd, (k + 1) * Hd)
+    return np.concatenate([x @ Wq[c].T, x @ Wk[c].T, x @ Wv[c].T], axis=1)
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,100 @@
+"""Helpers shared by the GPU parity tests: moving seeded bf16 bit patterns to the
+device and back, and the tolerance check of the layer outputs.
+
+Tolerance (floating-point outputs, bf16 in / fp32 accumulate) against the float64
+oracle:
+  * relative Frobenius error ||y - y_ref||_F / ||y_ref||_F <= 1e-2, and
+  * every element within 3e-2 + 2^-7 |y_ref| of the oracle.
+The absolute part is the stated 3e-2. The relative part is two bfloat16 half-ulps
+at the element's magnitude (one for the final bf16 rounding of the output, one for
+the bf16 intermediates it was computed from): an output stored in bf16 cannot be
+closer than half an ulp to the exact value, and from |y| = 8 on that half-ulp
+(0.031) alone exceeds 3e-2 (the first token of a 7B-shaped layer reaches |y| = 34,
+ulp 0.25). For |y_ref| <= 1 the bound is within 3.8e-2.
+"""
+import numpy as np
+import torch
+
+import oracle
+import tsp_inputs
+
+REL_FRO = 1e-2
+MAX_ABS = 3e-2
+REL_ELEM = 2.0 ** -7
+
+
+def dev(bits: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bit patterns -> bf16 CUDA tensor (same bits)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return oracle.widen_bf16(bits(t))
+
+
+def errors(got: np.ndarray, want: np.ndarray):
+    err = got - want
+    rel = float(np.linalg.norm(err) / max(np.linalg.norm(want), 1e-30))
+    return rel, float(np.abs(err).max()) if err.size else 0.0
+
+
+def assert_close(got, want, name="", rel_fro=REL_FRO, max_abs=MAX_ABS, rel_elem=REL_ELEM):
+    assert got.shape == want.shape, (name, got.shape, want.shape)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    rel, mx = errors(got, want)
+    excess = float((np.abs(got - want) - rel_elem * np.abs(want)).max()) if got.size else 0.0
+    assert rel <= rel_fro and excess <= max_abs, (
+        f"{name}: rel_fro={rel:.3e} max_abs={mx:.3e} "
+        f"max(|err| - {rel_elem:.4g}|ref|)={excess:.3e}")
+    return rel, mx
+
+
+def rand_bits(shape, seed, std=1.0):
+    return tsp_inputs.normal_bf16_bits(shape, std, seed, 42)
+
+
+class Layer:
+    """Seeded inputs of one layer shape on the device plus their float64 copies."""
+
+    def __init__(self, D, S, H, heads, F, seed=7, names=None):
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        self.cfg = tsp_inputs.LayerConfig("t", D, S, H, heads, F, seed)
+        self.bits = tsp_inputs.layer_inputs(self.cfg, names=names)
+        self.plan = tsp.tsp_plan(D, S, H, heads, F)
+        self.info = self.plan.info
+        self.ws = torch.empty(tsp.tsp_workspace_bytes(self.plan), dtype=torch.uint8, device="cuda")
+        tsp.tsp_workspace_init(self.plan, self.ws)
+        self.d = {k: dev(v) for k, v in self.bits.items()}
+        self.wpack = None
+        if names is None or "W2" in names:
+            self.wpack = torch.empty(tsp.tsp_packed_weight_bytes(self.plan) // 2,
+                                     dtype=torch.bfloat16, device="cuda")
+            tsp.tsp_pack_weights(self.plan, *(self.d[k] for k in
+                                              ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")),
+                                 self.wpack)
+        self._f64 = {}
+
+    def f(self, k):
+        if k not in self._f64:
+            self._f64[k] = oracle.widen_bf16(self.bits[k])
+        return self._f64[k]
+
+    def weights64(self):
+        return {k: self.f(k) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")}
+
+    def sharded_x(self):
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        xs = torch.empty_like(self.d["x"])
+        tsp.tsp_shard(self.plan, self.d["x"], xs)
+        return xs
+
+    def act(self):
+        return torch.empty((self.info.S, self.info.hidden), dtype=torch.bfloat16, device="cuda")
+
+    def check_status(self):
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        assert tsp.tsp_device_status(self.ws) == tsp.TSP_OK, tsp.tsp_last_error()

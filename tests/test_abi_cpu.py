@@ -1,0 +1,127 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and its
+host logic (plan validation, derived sizes, argument checks) behaves. No compute
+call is made here."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import tsp_inputs
+
+tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
+B = tsp._binding
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.library_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return B.load_library()
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = B.declared_functions()
+    assert len(declared) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", B.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = [f for f in declared if f not in exported]
+    assert not missing, missing
+    for f in declared:
+        assert hasattr(lib, f)
+    # the binding wraps every declared call under the same name
+    for f in declared:
+        if f not in ("tsp_plan_destroy",):
+            assert hasattr(tsp, f), f
+
+
+@pytest.mark.parametrize("cfg", tsp_inputs.CONFIGS, ids=lambda c: c.name)
+def test_plan_sizes(lib, cfg):
+    p = tsp.tsp_plan(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn)
+    i = p.info
+    assert (i.D, i.S, i.hidden, i.heads, i.ffn) == (cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn)
+    assert i.head_dim == cfg.head_dim and i.T == cfg.S // cfg.D and i.C == cfg.S // (2 * cfg.D)
+    assert i.shard_hidden * cfg.D == cfg.hidden and i.shard_ffn * cfg.D == cfg.ffn
+    Fp = i.shard_ffn_padded
+    assert Fp >= i.shard_ffn and Fp % 64 == 0 and (cfg.D * Fp) % 128 == 0
+    assert Fp - i.shard_ffn < 128
+    assert i.ffn_padded == cfg.D * Fp
+    H = cfg.hidden
+    assert i.wpack_qkv == 0 and i.wpack_o == 3 * H * H and i.wpack_w13 == 4 * H * H
+    assert i.wpack_w2 == 4 * H * H + 2 * i.ffn_padded * H
+    assert i.wpack_elems == i.wpack_w2 + H * i.ffn_padded
+    assert tsp.tsp_packed_weight_bytes(p) == 2 * i.wpack_elems
+    ws = tsp.tsp_workspace_bytes(p)
+    assert ws == i.workspace_bytes and ws % 256 == 0
+    # workspace holds at least: status, qkv of one shard, K/V, O, h, G, two staging buffers
+    S = cfg.S
+    need = 256 + 2 * S * (3 * i.shard_hidden + 2 * i.shard_hidden + 2 * H + i.ffn_padded + 2 * H) \
+        + 4 * S * H
+    assert need <= ws <= need + 256 * 10
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 256, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),       # D < 1
+    ((3, 256, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),       # S % 2D
+    ((2, 256, 256, 3, 688), B.TSP_ERR_UNSUPPORTED),       # hidden % heads
+    ((2, 256, 256, 8, 688), B.TSP_ERR_UNSUPPORTED),       # head_dim 32
+    ((4, 256, 192, 3, 688), B.TSP_ERR_UNSUPPORTED),       # heads % D
+    ((2, 256, 256, 4, 687), B.TSP_ERR_UNSUPPORTED),       # ffn % D
+    ((2, 2, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),         # S < 2D
+    ((2, 1 << 27, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),   # S too large
+    ((65, 130, 64 * 65, 65, 65), B.TSP_ERR_UNSUPPORTED),  # D > 64
+])
+def test_plan_rejects_unsupported_shapes(lib, args, code):
+    h = ctypes.c_void_p()
+    assert lib.tsp_plan(*args, ctypes.byref(h)) == code
+    assert not h.value
+    assert B.tsp_last_error().startswith("tsp_plan")
+    with pytest.raises(B.TSPError) as e:
+        tsp.tsp_plan(*args)
+    assert e.value.status == code
+
+
+def test_plan_accepts_edge_shapes(lib):
+    for args in [(1, 2, 64, 1, 1), (1, 200, 128, 2, 96), (64, 128, 4096, 64, 64),
+                 (3, 1152, 384, 6, 600), (8, 131072, 4096, 32, 11008)]:
+        p = tsp.tsp_plan(*args)
+        assert p.info.D == args[0]
+
+
+def test_null_and_misaligned_arguments_are_rejected_before_launch(lib):
+    p = tsp.tsp_plan(2, 256, 256, 4, 688)
+    h = p.handle
+    ws = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    assert lib.tsp_layer_fwd(h, None, ctypes.c_void_p(4096), ctypes.c_void_p(8192), ws, None) \
+        == B.TSP_ERR_INVALID_ARG
+    assert "null" in B.tsp_last_error()
+    assert lib.tsp_layer_fwd(h, ctypes.c_void_p(4100), ctypes.c_void_p(4096),
+                             ctypes.c_void_p(8192), ws, None) == B.TSP_ERR_INVALID_ARG
+    assert "aligned" in B.tsp_last_error()
+    assert lib.tsp_layer_fwd(h, ctypes.c_void_p(4096), ctypes.c_void_p(8192),
+                             ctypes.c_void_p(4096), ws, None) == B.TSP_ERR_INVALID_ARG
+    assert "alias" in B.tsp_last_error()
+    assert lib.tsp_layer_fwd(h, ctypes.c_void_p(4096), ctypes.c_void_p(8192),
+                             ctypes.c_void_p(12288), ctypes.c_void_p((1 << 20) + 16), None) \
+        == B.TSP_ERR_INVALID_ARG
+    assert "256-byte" in B.tsp_last_error()
+    assert lib.tsp_qkv_projection(h, 2, ctypes.c_void_p(4096), ctypes.c_void_p(8192),
+                                  ctypes.c_void_p(12288), ws, None) == B.TSP_ERR_INVALID_ARG
+    assert "shard" in B.tsp_last_error()
+    assert lib.tsp_causal_attention(h, -1, ctypes.c_void_p(4096), ctypes.c_void_p(8192),
+                                    ctypes.c_void_p(12288), ctypes.c_void_p(16384), ws, None) \
+        == B.TSP_ERR_INVALID_ARG
+    assert lib.tsp_layer_fwd(None, ctypes.c_void_p(4096), ctypes.c_void_p(8192),
+                             ctypes.c_void_p(12288), ws, None) == B.TSP_ERR_INVALID_ARG
+    assert lib.tsp_wait_selftest(ws, 0, None) == B.TSP_ERR_INVALID_ARG
+    assert lib.tsp_workspace_bytes(None) == 0
+
+
+def test_binding_checks_tensor_sizes_without_calling_the_library(lib):
+    import torch
+    p = tsp.tsp_plan(2, 256, 256, 4, 688)
+    small = torch.empty(10, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        tsp.tsp_layer_fwd(p, small, small, small, small)

@@ -1,0 +1,123 @@
+"""Whole-block and whole-layer parity of the CUDA path against the float64 oracle.
+
+Small shapes are compared element by element; the 7B-shaped workloads run at full
+size in the launch configuration the benchmark times and are compared on 256
+sampled token rows (always holding the first and the last token), which the
+oracle computes one by one against all earlier tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tsp_inputs
+from gpu_util import Layer, assert_close, bits, f64
+
+tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "tiny": (2, 256, 256, 4, 688),
+    "ragged": (2, 200, 128, 2, 96),
+    "d3": (3, 1152, 384, 6, 600),
+    "hd128": (2, 512, 512, 4, 1024),
+    "small": (4, 4096, 1024, 16, 2816),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tsp.load_library()
+
+
+def _unshard(L, t):
+    out = torch.empty_like(t)
+    tsp.tsp_unshard(L.plan, t, out)
+    return out
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_layer_matches_oracle(name):
+    L = Layer(*SHAPES[name], seed=5)
+    xs = L.sharded_x()
+    attn, out = L.act(), L.act()
+    tsp.tsp_attention_fwd(L.plan, xs, L.wpack, attn, L.ws)
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    L.check_status()
+    ref = oracle.layer_forward(L.f("x"), L.weights64(), L.info.heads)
+    assert_close(f64(_unshard(L, attn)), ref["attn"], f"{name} attn")
+    assert_close(f64(_unshard(L, out)), ref["out"], f"{name} out")
+
+
+@pytest.mark.parametrize("name", ["tiny", "d3", "small"])
+def test_mlp_block_matches_oracle(name):
+    L = Layer(*SHAPES[name], seed=6)
+    hs = L.sharded_x()  # any bf16 activations serve as the MLP input
+    mlp = L.act()
+    tsp.tsp_mlp_fwd(L.plan, hs, L.wpack, mlp, L.ws)
+    L.check_status()
+    want = oracle.swiglu_mlp(L.f("x"), L.f("W1"), L.f("W3"), L.f("W2"))
+    assert_close(f64(_unshard(L, mlp)), want, f"{name} mlp")
+
+
+def test_output_is_the_same_for_every_D():
+    """TSP computes the plain layer: one seeded problem, D = 1, 2, 4, 8."""
+    S, H, heads, F = 1024, 512, 8, 1024
+    outs = {}
+    for D in (1, 2, 4, 8):
+        L = Layer(D, S, H, heads, F, seed=9)
+        xs = L.sharded_x()
+        out = L.act()
+        tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+        L.check_status()
+        outs[D] = f64(_unshard(L, out))
+    ref = oracle.layer_forward(L.f("x"), L.weights64(), heads)["out"]
+    for D, o in outs.items():
+        assert_close(o, ref, f"D={D}")
+    for D in (2, 4, 8):
+        assert_close(outs[D], outs[1], f"D={D} vs D=1")
+
+
+def test_host_entry_point_matches_device_path():
+    L = Layer(*SHAPES["d3"], seed=8)
+    xs = L.sharded_x()
+    out = L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    want = bits(_unshard(L, out))
+    x_host = torch.from_numpy(L.bits["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    tsp.tsp_layer_fwd_host(L.plan, x_host, L.wpack, out_host, L.ws)
+    torch.cuda.current_stream().synchronize()
+    L.check_status()
+    assert np.array_equal(out_host.view(torch.int16).numpy().view(np.uint16), want)
+
+
+def test_repeated_calls_are_deterministic():
+    L = Layer(*SHAPES["small"], seed=3)
+    xs = L.sharded_x()
+    a, b = L.act(), L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, a, L.ws)
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, b, L.ws)
+    L.check_status()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["7b-16k", "7b-64k", "7b-128k"])
+def test_7b_layer_sampled_rows(name):
+    cfg = tsp_inputs.config_by_name(name)
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed)
+    xs = L.sharded_x()
+    attn, out = L.act(), L.act()
+    tsp.tsp_attention_fwd(L.plan, xs, L.wpack, attn, L.ws)
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    L.check_status()
+    rows = tsp_inputs.sample_rows(cfg.S, 256, cfg.seed)
+    got_attn = f64(_unshard(L, attn)[torch.from_numpy(rows).cuda()])
+    got_out = f64(_unshard(L, out)[torch.from_numpy(rows).cuda()])
+    del attn, out, xs
+    ref = oracle.layer_forward(L.f("x"), L.weights64(), cfg.heads, rows=rows)
+    assert_close(got_attn, ref["attn"], f"{name} attn rows")
+    assert_close(got_out, ref["out"], f"{name} out rows")

@@ -1,0 +1,209 @@
+"""Per-step parity of the CUDA path against the oracle, through the C ABI.
+
+Steps (the hot path of one TSP layer): zigzag index and shard/unshard (bit-exact),
+weight packing (bit-exact), Q/K/V projection of a shard, K/V all-gather into
+natural order (bit-exact), causal attention of zigzag query rows, O projection,
+SwiGLU gate/up and SwiGLU down in ring order. Shapes span several tiles, a ragged
+tail (S and N not multiples of the tile), odd D, D = 1, head_dim 64 and 128.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tsp_inputs
+from gpu_util import Layer, assert_close, bits, dev, f64, rand_bits
+
+tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "tiny": (2, 256, 256, 4, 688),
+    "ragged": (2, 200, 128, 2, 96),      # S, 3H/D not tile multiples; chunk 50
+    "d3": (3, 1152, 384, 6, 600),        # odd D, chunk 192 (tiles straddle chunks)
+    "d1": (1, 384, 256, 2, 512),         # one rank: zigzag is the identity
+    "hd128": (2, 512, 512, 4, 1024),     # head_dim 128
+    "small": (4, 4096, 1024, 16, 2816),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tsp.load_library()
+
+
+@pytest.fixture(scope="module", params=list(SHAPES), ids=list(SHAPES))
+def layer(request):
+    return Layer(*SHAPES[request.param], seed=11)
+
+
+# ------------------------------------------------------------------ zigzag
+
+@pytest.mark.parametrize("S,D", [(cfg.S, cfg.D) for cfg in tsp_inputs.CONFIGS]
+                         + [(2, 1), (200, 2), (1152, 3), (128, 64), (96, 48)])
+def test_zigzag_index_bit_exact(S, D):
+    plan = tsp.tsp_plan(D, S, 64 * D, D, D)
+    fwd = torch.full((S,), -1, dtype=torch.int32, device="cuda")
+    inv = torch.full((S,), -1, dtype=torch.int32, device="cuda")
+    tsp.tsp_shard_index(plan, fwd, inv)
+    assert np.array_equal(fwd.cpu().numpy(), oracle.zigzag_forward_index(S, D))
+    assert np.array_equal(inv.cpu().numpy(), oracle.zigzag_inverse_index(S, D))
+
+
+def test_shard_unshard_bit_exact(layer):
+    i = layer.info
+    xs = layer.sharded_x()
+    want = oracle.shard_tokens(layer.bits["x"], i.D).reshape(i.S, i.hidden)
+    assert np.array_equal(bits(xs), want)
+    back = torch.empty_like(xs)
+    tsp.tsp_unshard(layer.plan, xs, back)
+    assert np.array_equal(bits(back), layer.bits["x"])
+
+
+def test_pack_weights_layout(layer):
+    """The packed buffer follows the layout include/tsp.h documents."""
+    i = layer.info
+    D, H, Hd, Fd, Fp, NF = i.D, i.hidden, i.shard_hidden, i.shard_ffn, i.shard_ffn_padded, i.ffn_padded
+    b = layer.bits
+    got = bits(layer.wpack)
+    qkv = np.concatenate([np.concatenate([b[w][k * Hd:(k + 1) * Hd] for w in ("Wq", "Wk", "Wv")])
+                          for k in range(D)])
+    assert np.array_equal(got[i.wpack_qkv:i.wpack_o].reshape(3 * H, H), qkv)
+    assert np.array_equal(got[i.wpack_o:i.wpack_w13].reshape(H, H), b["Wo"])
+    # padded ffn index fp -> real ffn row (or none)
+    fp = np.arange(NF)
+    k, loc = fp // Fp, fp % Fp
+    real = np.where(loc < Fd, k * Fd + loc, -1)
+    W1p = np.where(real[:, None] >= 0, b["W1"][np.maximum(real, 0)], 0).astype(np.uint16)
+    W3p = np.where(real[:, None] >= 0, b["W3"][np.maximum(real, 0)], 0).astype(np.uint16)
+    w13 = got[i.wpack_w13:i.wpack_w2].reshape(NF // 128, 256, H)
+    assert np.array_equal(w13[:, :128].reshape(NF, H), W1p)
+    assert np.array_equal(w13[:, 128:].reshape(NF, H), W3p)
+    W2p = np.where(real[None, :] >= 0, b["W2"][:, np.maximum(real, 0)], 0).astype(np.uint16)
+    assert np.array_equal(got[i.wpack_w2:i.wpack_elems].reshape(H, NF), W2p)
+
+
+# ------------------------------------------------------------- attention steps
+
+def test_qkv_projection(layer):
+    i = layer.info
+    xs = layer.sharded_x()
+    x_rows = layer.f("x")[oracle.zigzag_inverse_index(i.S, i.D)]  # sharded row order
+    qkv = torch.empty((i.S, 3 * i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    for k in sorted({0, i.D - 1}):
+        qkv.fill_(float("nan"))
+        tsp.tsp_qkv_projection(layer.plan, k, xs, layer.wpack, qkv, layer.ws)
+        want = oracle.qkv_projection_shard(x_rows, layer.f("Wq"), layer.f("Wk"), layer.f("Wv"), k, i.D)
+        assert_close(f64(qkv), want, f"qkv shard {k}")
+    layer.check_status()
+
+
+def test_kv_allgather_bit_exact(layer):
+    i = layer.info
+    Hd = i.shard_hidden
+    q_bits = rand_bits((i.S, 3 * Hd), 21)
+    kn = torch.empty((i.S, Hd), dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    tsp.tsp_kv_allgather(layer.plan, dev(q_bits), kn, vn)
+    sh = q_bits.reshape(i.D, i.T, 3 * Hd)
+    assert np.array_equal(bits(kn), oracle.unshard_tokens(sh[:, :, Hd:2 * Hd], i.D))
+    assert np.array_equal(bits(vn), oracle.unshard_tokens(sh[:, :, 2 * Hd:], i.D))
+
+
+def test_causal_attention(layer):
+    i = layer.info
+    Hd, d, hpr = i.shard_hidden, i.head_dim, i.heads // i.D
+    q_bits = rand_bits((i.S, 3 * Hd), 31)
+    k_bits = rand_bits((i.S, Hd), 32)
+    v_bits = rand_bits((i.S, Hd), 33)
+    o = torch.full((i.S, i.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pos = oracle.zigzag_inverse_index(i.S, i.D)
+    q, kk, vv = oracle.widen_bf16(q_bits), oracle.widen_bf16(k_bits), oracle.widen_bf16(v_bits)
+    for shard in sorted({0, i.D - 1}):
+        tsp.tsp_causal_attention(layer.plan, shard, dev(q_bits), dev(k_bits), dev(v_bits), o, layer.ws)
+        got = f64(o)[:, shard * Hd:(shard + 1) * Hd]
+        want = oracle.multihead_causal_attention(q[:, :Hd], kk, vv, hpr, q_pos=pos,
+                                                 k_pos=np.arange(i.S))
+        assert_close(got, want, f"attention shard {shard}")
+    layer.check_status()
+
+
+@pytest.mark.parametrize("mode", ["plain", "residual", "residual+fp32 copy"])
+def test_o_projection(layer, mode):
+    i = layer.info
+    o_bits = rand_bits((i.S, i.hidden), 41, std=0.5)
+    r_bits = rand_bits((i.S, i.hidden), 42)
+    out = layer.act()
+    out32 = torch.full((i.S, i.hidden), float("nan"), dtype=torch.float32, device="cuda")
+    tsp.tsp_o_projection(layer.plan, dev(o_bits), layer.wpack,
+                         None if mode == "plain" else dev(r_bits), out, layer.ws,
+                         out32=out32 if mode == "residual+fp32 copy" else None)
+    want = oracle.widen_bf16(o_bits) @ layer.f("Wo").T
+    if mode != "plain":
+        want = want + oracle.widen_bf16(r_bits)
+    assert_close(f64(out), want, "o projection")
+    if mode == "residual+fp32 copy":
+        got32 = out32.double().cpu().numpy()
+        assert_close(got32, want, "o projection fp32 copy", rel_fro=1e-5, max_abs=1e-4)
+        # the bf16 output is the round-to-nearest-even of the fp32 one
+        assert torch.equal(out32.to(torch.bfloat16).view(torch.int16), out.view(torch.int16))
+    layer.check_status()
+
+
+# ------------------------------------------------------------------- MLP steps
+
+def test_swiglu_gate_up(layer):
+    i = layer.info
+    h_bits = rand_bits((i.S, i.hidden), 51)
+    g = torch.full((i.S, i.ffn_padded), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tsp.tsp_swiglu_gate_up(layer.plan, dev(h_bits), layer.wpack, g, layer.ws)
+    G = oracle.swiglu_gate(oracle.widen_bf16(h_bits), layer.f("W1"), layer.f("W3"))
+    got = f64(g).reshape(i.S, i.D, i.shard_ffn_padded)
+    assert_close(got[:, :, :i.shard_ffn].reshape(i.S, i.ffn), G, "swiglu gate/up")
+    assert (got[:, :, i.shard_ffn:] == 0).all(), "padded columns must be zero"
+    layer.check_status()
+
+
+@pytest.mark.parametrize("residual", [None, "bf16", "fp32"])
+def test_swiglu_down_ring(layer, residual):
+    i = layer.info
+    g_bits = rand_bits((i.S, i.ffn_padded), 61, std=0.5)
+    r_bits = rand_bits((i.S, i.hidden), 62)
+    r32 = torch.from_numpy(rand_bits((i.S, i.hidden), 63).astype(np.float32) / 65536.0 - 0.5).cuda()
+    out = layer.act()
+    tsp.tsp_swiglu_down(layer.plan, dev(g_bits), layer.wpack,
+                        dev(r_bits) if residual == "bf16" else None, out, layer.ws,
+                        residual32=r32 if residual == "fp32" else None)
+    G = oracle.widen_bf16(g_bits).reshape(i.S, i.D, i.shard_ffn_padded)[:, :, :i.shard_ffn]
+    want = G.reshape(i.S, i.ffn) @ layer.f("W2").T
+    if residual == "bf16":
+        want = want + oracle.widen_bf16(r_bits)
+    if residual == "fp32":
+        want = want + r32.double().cpu().numpy()
+    assert_close(f64(out), want, "swiglu down")
+    layer.check_status()
+
+
+# -------------------------------------------------- 7B shapes (sampled rows)
+
+@pytest.mark.slow
+def test_7b_projections_sampled_rows():
+    cfg = tsp_inputs.config_by_name("7b-16k")
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed)
+    i = L.info
+    rows = tsp_inputs.sample_rows(i.S, 256, 3)
+    xs = L.sharded_x()
+    x_rows = L.f("x")[oracle.zigzag_inverse_index(i.S, i.D)]
+    qkv = torch.empty((i.S, 3 * i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    for k in (0, 5, 7):
+        tsp.tsp_qkv_projection(L.plan, k, xs, L.wpack, qkv, L.ws)
+        want = oracle.qkv_projection_shard(x_rows[rows], L.f("Wq"), L.f("Wk"), L.f("Wv"), k, i.D)
+        assert_close(f64(qkv)[rows], want, f"7b qkv shard {k}")
+    g_bits = rand_bits((i.S, i.ffn_padded), 71, std=0.5)
+    out = L.act()
+    tsp.tsp_swiglu_down(L.plan, dev(g_bits), L.wpack, None, out, L.ws)
+    G = oracle.widen_bf16(g_bits[rows]).reshape(len(rows), i.D, i.shard_ffn_padded)[:, :, :i.shard_ffn]
+    assert_close(f64(out)[rows], G.reshape(len(rows), i.ffn) @ L.f("W2").T, "7b swiglu down")
+    L.check_status()
