@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import tsp_inputs
-from gpu_util import Layer, assert_close, bits, f64
+from gpu_util import Layer, assert_close, bits, f64, layer_row_scale
 
 tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
 pytestmark = pytest.mark.gpu
@@ -48,7 +48,9 @@ def test_layer_matches_oracle(name):
     L.check_status()
     ref = oracle.layer_forward(L.f("x"), L.weights64(), L.info.heads)
     assert_close(f64(_unshard(L, attn)), ref["attn"], f"{name} attn")
-    assert_close(f64(_unshard(L, out)), ref["out"], f"{name} out")
+    G = oracle.swiglu_gate(ref["h"], L.f("W1"), L.f("W3"))
+    assert_close(f64(_unshard(L, out)), ref["out"], f"{name} out",
+                 scale=layer_row_scale(ref["out"], G))
 
 
 @pytest.mark.parametrize("name", ["tiny", "d3", "small"])
@@ -59,7 +61,8 @@ def test_mlp_block_matches_oracle(name):
     tsp.tsp_mlp_fwd(L.plan, hs, L.wpack, mlp, L.ws)
     L.check_status()
     want = oracle.swiglu_mlp(L.f("x"), L.f("W1"), L.f("W3"), L.f("W2"))
-    assert_close(f64(_unshard(L, mlp)), want, f"{name} mlp")
+    G = oracle.swiglu_gate(L.f("x"), L.f("W1"), L.f("W3"))
+    assert_close(f64(_unshard(L, mlp)), want, f"{name} mlp", scale=layer_row_scale(want, G))
 
 
 def test_output_is_the_same_for_every_D():
@@ -73,11 +76,13 @@ def test_output_is_the_same_for_every_D():
         tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
         L.check_status()
         outs[D] = f64(_unshard(L, out))
-    ref = oracle.layer_forward(L.f("x"), L.weights64(), heads)["out"]
+    full = oracle.layer_forward(L.f("x"), L.weights64(), heads)
+    ref = full["out"]
+    scale = layer_row_scale(ref, oracle.swiglu_gate(full["h"], L.f("W1"), L.f("W3")))
     for D, o in outs.items():
-        assert_close(o, ref, f"D={D}")
+        assert_close(o, ref, f"D={D}", scale=scale)
     for D in (2, 4, 8):
-        assert_close(outs[D], outs[1], f"D={D} vs D=1")
+        assert_close(outs[D], outs[1], f"D={D} vs D=1", scale=scale)
 
 
 def test_host_entry_point_matches_device_path():
@@ -120,4 +125,5 @@ def test_7b_layer_sampled_rows(name):
     del attn, out, xs
     ref = oracle.layer_forward(L.f("x"), L.weights64(), cfg.heads, rows=rows)
     assert_close(got_attn, ref["attn"], f"{name} attn rows")
-    assert_close(got_out, ref["out"], f"{name} out rows")
+    G = oracle.swiglu_gate(ref["h"], L.f("W1"), L.f("W3"))
+    assert_close(got_out, ref["out"], f"{name} out rows", scale=layer_row_scale(ref["out"], G))
