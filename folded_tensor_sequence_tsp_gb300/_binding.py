@@ -21,7 +21,7 @@ __all__ = [
     "TSP_OK", "TSP_ERR_INVALID_ARG", "TSP_ERR_UNSUPPORTED", "TSP_ERR_CUDA", "TSP_ERR_TIMEOUT",
     "tsp_plan", "tsp_get_plan_info", "tsp_workspace_bytes", "tsp_packed_weight_bytes",
     "tsp_workspace_init", "tsp_pack_weights", "tsp_shard_index", "tsp_shard", "tsp_unshard",
-    "tsp_attention_fwd", "tsp_mlp_fwd", "tsp_layer_fwd", "tsp_layer_fwd_host",
+    "tsp_attention_fwd", "tsp_mlp_fwd", "tsp_mlp_fwd_noalloc", "tsp_layer_fwd", "tsp_layer_fwd_host",
     "tsp_qkv_projection", "tsp_kv_allgather", "tsp_causal_attention", "tsp_o_projection",
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
     "tsp_last_error",
@@ -72,6 +72,7 @@ _SIGS = {
     "tsp_unshard": (_I, [_P, _P, _P, _P]),
     "tsp_attention_fwd": (_I, [_P] * 6),
     "tsp_mlp_fwd": (_I, [_P] * 6),
+    "tsp_mlp_fwd_noalloc": (_I, [_P] * 5),
     "tsp_layer_fwd": (_I, [_P] * 6),
     "tsp_layer_fwd_host": (_I, [_P] * 6),
     "tsp_qkv_projection": (_I, [_P, _I, _P, _P, _P, _P, _P]),
@@ -252,6 +253,15 @@ def tsp_attention_fwd(plan, xs, wpack, attn, ws, stream=None):
 
 def tsp_mlp_fwd(plan, hs, wpack, mlp, ws, stream=None):
     _block("tsp_mlp_fwd", plan, hs, wpack, mlp, ws, stream)
+
+
+def tsp_mlp_fwd_noalloc(plan, hs, wpack, mlp, stream=None):
+    """tsp_mlp_fwd without a workspace, for callers that cannot allocate device memory
+    (scratch in the library's static device buffer; see include/tsp.h)."""
+    n = plan.act_elems
+    _check(load_library().tsp_mlp_fwd_noalloc(
+        plan.handle, _dev(hs, "hs", n), _dev(wpack, "wpack", plan.info.wpack_elems),
+        _dev(mlp, "mlp", n), _stream(stream)), "tsp_mlp_fwd_noalloc")
 
 
 def tsp_layer_fwd(plan, xs, wpack, out, ws, stream=None):

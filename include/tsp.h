@@ -169,6 +169,29 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
 tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
                               tsp_bf16* out_host, void* ws, void* stream);
 
+/*
+ * tsp_mlp_fwd_noalloc - tsp_mlp_fwd for callers that cannot allocate device
+ * memory. The page has no counterpart: this entry point exists for library users.
+ * Some callers cannot call cudaMalloc (or any allocating routine, torch's included)
+ * where they run the layer: code inside a custom allocator or memory-pool callback,
+ * plug-ins of an application that owns every device allocation, runtimes that
+ * forbid allocation after start-up. They still pass hs, wpack and mlp ([D][T][H]
+ * as for tsp_mlp_fwd) but no workspace: the gated activation G and the status word
+ * of the bounded device waits live in one static device array of 32 MiB inside the
+ * library, which every GPU that loads the library holds until the process exits.
+ * Limit: S x ffn_padded x 2 bytes <= 32 MiB - 256 (e.g. S = 4096 with hidden 1024
+ * and ffn 2816); larger shapes return TSP_ERR_UNSUPPORTED with a message.
+ * The call allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture. Every call shares the array: calls that overlap on the GPU (other
+ * streams, other threads) race on it and must be serialised by the caller. A device
+ * wait that gives up leaves mlp undefined; this variant has no status query (use
+ * tsp_mlp_fwd with a workspace and tsp_device_status when that report is needed).
+ */
+tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
+                               tsp_bf16* mlp, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Single steps of the hot path. The *_fwd calls above are compositions of these.
  * ------------------------------------------------------------------------- */
