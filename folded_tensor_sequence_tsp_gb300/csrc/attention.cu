@@ -1,46 +1,71 @@
-// attention.cu - causal attention of zigzag query chunks against the gathered K/V
+// attention.cu - causal attention of zigzag query rows against the gathered K/V
 // ("Folding Tensor and Sequence Parallelism for Memory-Efficient Transformer
 // Training & Inference", section 2, attention layers: FlashAttention after the
-// K/V all-gather, zigzag partitioning for causal balance).
+// K/V all-gather; zigzag partitioning for causal balance).
 //
-// Each CTA takes 128 query rows of one head (8 warps x 16 rows). A row r of the
-// rank-major [D][T] layout holds the token at global position pos(r) (zigzag map);
-// it attends to K/V rows 0..pos(r) of the natural-order gathered buffers. K/V tiles
-// of 64 rows are streamed through a double-buffered, XOR-swizzled shared-memory
-// ring with cp.async; S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in,
-// fp32 accumulate); softmax is online in base 2 with the row max and sum kept in
-// registers and reduced across the 4 lanes of a row with warp shuffles. Only K/V
-// tiles that reach past the smallest query position of a warp need the mask;
-// tiles past its largest position are skipped.
+// One CTA computes 128 query rows of one head on the 5th-generation tensor cores:
+//   warp 0      TMA: the Q tile once, then K/V tiles of 128 keys into a 2-stage
+//               ring of 128B-swizzled shared-memory buffers
+//   warp 1      allocates 512 TMEM columns; one lane issues
+//                 S_j  = Q K_j^T          tcgen05.mma, A and B from shared memory
+//                 O   += P_j V_j          tcgen05.mma, A (= P) from tensor memory,
+//                                          B (= V) MN-major from shared memory
+//               with S_{j+1} issued before O += P_j V_j, so the tensor core works
+//               on the next scores while the softmax of the current tile runs
+//   warps 2..5  softmax, one query row per thread (TMEM lane = row): tcgen05.ld of
+//               the S row, mask by global position, row max, exp2, row sum, bf16
+//               P written back to TMEM with tcgen05.st; then the epilogue.
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
 //
-// When the zigzag chunk is a multiple of 128 tokens every 128-row tile lies inside
-// one chunk; CTAs then take tiles in decreasing natural position so the longest
-// (latest) tiles start first.
+// Online softmax in base 2 (scores pre-scaled by log2(e)/sqrt(d)). Each row keeps a
+// reference maximum m and sum l; m only moves (and O and l are rescaled) when the
+// tile maximum exceeds it by more than 8, so P = exp2(s - m) <= 256 and most tiles
+// never touch O. The result is exact softmax: out = O / l at the end.
+//
+// Query row r of the rank-major layout is the token at global position pos(r) of
+// the zigzag map; key t is visible iff t <= pos(r). CTAs of one head run before
+// the next head (K/V of a head stay in L2 across its CTAs) and, when the zigzag
+// chunk is a multiple of 128 tokens, take query tiles in decreasing position, so
+// the longest tiles start first.
 #include "tsp_device.cuh"
 #include "tsp_internal.h"
 
 namespace tsp {
 namespace {
 
-constexpr int ATT_BM = 128;
-constexpr int ATT_BN = 64;
-constexpr int ATT_WARPS = 8;
-constexpr int ATT_THREADS = ATT_WARPS * 32;
+constexpr int QT = 128;      // query rows per CTA
+constexpr int KT = 128;      // keys per tile
+constexpr int NSTAGE = 2;    // K/V ring depth
+constexpr int THREADS = 192;
+constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P0 = 384, TM_P1 = 448;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+
+template <int HD>
+struct Geometry {
+  static constexpr int BOXES = HD / 64;                 // 64-column boxes per row block
+  static constexpr uint32_t Q_BYTES = QT * HD * 2;
+  static constexpr uint32_t K_BYTES = KT * HD * 2;
+  static constexpr uint32_t STAGE_BYTES = 2 * K_BYTES;  // K and V
+  static constexpr size_t USED = 1024 + Q_BYTES + (size_t)NSTAGE * STAGE_BYTES + 256;
+  // The CTA allocates all 512 TMEM columns, so it must be alone on its SM: ask for
+  // more than half of the SM's 228 KB of shared memory.
+  static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+};
 
 struct AttParams {
-  const __nv_bfloat16* qkv;
-  long long ld_qkv;
-  const __nv_bfloat16* kn;
-  const __nv_bfloat16* vn;
-  long long ld_kv;
   __nv_bfloat16* o;
   long long ld_o;
   long long o_col0;
   long long S, T, C;
   int D;
   int heads;
-  int natural_order;  // 1: CTAs walk 128-token tiles in decreasing position
-  float scale_log2;   // log2(e) / sqrt(d)
+  int q_tiles;
+  int natural_order;
+  float scale_log2;
+  DevStatus* status;
+  unsigned long long limit_ns;
 };
 
 __device__ __forceinline__ long long zig_row(long long t, long long C, long long T, int D) {
@@ -53,268 +78,306 @@ __device__ __forceinline__ long long row_pos(long long r, long long C, long long
   return l < C ? rank * C + l : (2 * D - 1 - rank) * C + (l - C);
 }
 
-// Byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile of HD columns.
-template <int HD>
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-  return (uint32_t)(row * (HD * 2) + ((ch ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// Load `rows` rows of HD bf16 (row stride ld elements) starting at global row
-// `first` (rows at or beyond `limit` are zero-filled) into a swizzled tile.
 template <int HD>
-__device__ __forceinline__ void load_tile(uint32_t s_base, const __nv_bfloat16* g, long long ld,
-                                          long long first, long long limit, int rows) {
-  constexpr int CH = HD / 8;
-  for (int i = threadIdx.x; i < rows * CH; i += ATT_THREADS) {
-    const int r = i / CH, ch = i - r * CH;
-    const long long gr = first + r;
-    const bool ok = gr < limit;
-    const __nv_bfloat16* src = g + (ok ? gr : 0) * ld + ch * 8;
-    cp_async16(s_base + swz<HD>(r, ch), src, ok);
-  }
-}
-
-template <int HD>
-__global__ void __launch_bounds__(ATT_THREADS, 1) attention_mma_kernel(const AttParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sQ = smem_addr(smem);
-  const uint32_t sK0 = sQ + ATT_BM * HD * 2;
-  const uint32_t sV0 = sK0 + 2 * ATT_BN * HD * 2;
-  constexpr uint32_t KV_BYTES = ATT_BN * HD * 2;
+__global__ void __launch_bounds__(THREADS, 1)
+    attention_tcgen05_kernel(const __grid_constant__ CUtensorMap tmQ,
+                             const __grid_constant__ CUtensorMap tmK,
+                             const __grid_constant__ CUtensorMap tmV, const AttParams p) {
+  using G = Geometry<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + G::Q_BYTES;  // stage s: K at s*STAGE_BYTES, V at +K_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NSTAGE * G::STAGE_BYTES);
+  uint64_t* q_full = bars;                // [1]
+  uint64_t* kv_full = bars + 1;           // [NSTAGE]
+  uint64_t* kv_empty = kv_full + NSTAGE;  // [NSTAGE]
+  uint64_t* s_full = kv_empty + NSTAGE;   // [2] S_j ready in TMEM
+  uint64_t* p_full = s_full + 2;          // [2] P_j written to TMEM (4 softmax warps)
+  uint64_t* o_done = p_full + 2;          // [2] O += P_j V_j completed
+  uint64_t* drain = o_done + 2;           // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = blockIdx.x % p.heads;
-  const long long tile = blockIdx.x / p.heads;
-  const long long nq_tiles = (p.S + ATT_BM - 1) / ATT_BM;
-
-  // first sharded row of this CTA's 128 query rows
+  const int head = blockIdx.x / p.q_tiles;
+  const int tile = blockIdx.x - head * p.q_tiles;
   long long row0;
   if (p.natural_order) {
-    const long long nat_tile = nq_tiles - 1 - tile;
-    row0 = zig_row(nat_tile * ATT_BM, p.C, p.T, p.D);
+    row0 = zig_row((long long)(p.q_tiles - 1 - tile) * QT, p.C, p.T, p.D);
   } else {
-    row0 = tile * ATT_BM;
+    row0 = (long long)tile * QT;
   }
+  // keys needed by this CTA: 0 .. largest position among its rows
+  long long max_pos;
+  if (p.natural_order) {
+    max_pos = row_pos(row0 + QT - 1, p.C, p.T, p.D);
+  } else {
+    max_pos = 0;
+    const long long last = min(row0 + QT, p.S);
+    for (long long r = row0; r < last; ++r) max_pos = max(max_pos, row_pos(r, p.C, p.T, p.D));
+  }
+  const int n_tiles = (int)(max_pos / KT) + 1;
+  const int col_q = head * HD;  // Q columns inside qkv; K/V columns inside kn/vn
 
-  // position range of this warp's 16 rows and of the whole CTA
-  __shared__ long long s_wmax[ATT_WARPS];
-  long long w_min = p.S, w_max = -1;
-  const int g = lane >> 2, t4 = lane & 3;
-  const long long my_r0 = row0 + warp * 16 + g, my_r1 = my_r0 + 8;
-  const long long pos0 = my_r0 < p.S ? row_pos(my_r0, p.C, p.T, p.D) : -1;
-  const long long pos1 = my_r1 < p.S ? row_pos(my_r1, p.C, p.T, p.D) : -1;
-  {
-    long long mn = min(pos0 < 0 ? p.S : pos0, pos1 < 0 ? p.S : pos1);
-    long long mx = max(pos0, pos1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
-    w_min = mn;
-    w_max = mx;
-  }
-  if (lane == 0) s_wmax[warp] = w_max;
-  __syncthreads();
-  long long cta_max = 0;
-#pragma unroll
-  for (int w = 0; w < ATT_WARPS; ++w) cta_max = max(cta_max, s_wmax[w]);
-
-  const __nv_bfloat16* Kg = p.kn + head * HD;
-  const __nv_bfloat16* Vg = p.vn + head * HD;
-  const int nkv = (int)(cta_max / ATT_BN) + 1;
-
-  // Q tile and the first K/V tile
-  load_tile<HD>(sQ, p.qkv + head * HD, p.ld_qkv, row0, p.S, ATT_BM);
-  cp_async_commit();
-  load_tile<HD>(sK0, Kg, p.ld_kv, 0, p.S, ATT_BN);
-  load_tile<HD>(sV0, Vg, p.ld_kv, 0, p.S, ATT_BN);
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();
-
-  // Q fragments of this warp's 16 rows (A operand), kept in registers
-  uint32_t qf[HD / 16][4];
-#pragma unroll
-  for (int ks = 0; ks < HD / 16; ++ks) {
-    const int r = warp * 16 + (lane & 15);
-    const int ch = ks * 2 + (lane >> 4);
-    ldsm_x4(sQ + swz<HD>(r, ch), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-  }
-
-  float oacc[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  for (int j = 0; j < nkv; ++j) {
-    if (j + 1 < nkv) {
-      const uint32_t nb = (uint32_t)((j + 1) & 1) * KV_BYTES;
-      load_tile<HD>(sK0 + nb, Kg, p.ld_kv, (long long)(j + 1) * ATT_BN, p.S, ATT_BN);
-      load_tile<HD>(sV0 + nb, Vg, p.ld_kv, (long long)(j + 1) * ATT_BN, p.S, ATT_BN);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&o_done[b], 1);
     }
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  WaitBound wb{p.status, p.limit_ns, abort_flag};
 
-    const long long kv0 = (long long)j * ATT_BN;
-    if (kv0 <= w_max) {
-      const uint32_t sK = sK0 + (uint32_t)(j & 1) * KV_BYTES;
-      const uint32_t sV = sV0 + (uint32_t)(j & 1) * KV_BYTES;
-      float s[ATT_BN / 8][4];
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
 #pragma unroll
-      for (int n = 0; n < ATT_BN / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      for (int b = 0; b < G::BOXES; ++b)
+        tma_load_2d(sQ + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b, (int)row0);
+      int last_parity[NSTAGE];
 #pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks) {
+      for (int s = 0; s < NSTAGE; ++s) last_parity[s] = -1;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % NSTAGE;
+        const uint32_t ph = (uint32_t)((j / NSTAGE) & 1);
+        if (!mbar_wait(&kv_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
+        uint8_t* kbuf = sKV + st * G::STAGE_BYTES;
+        uint8_t* vbuf = kbuf + G::K_BYTES;
+        mbar_arrive_expect_tx(&kv_full[st], G::STAGE_BYTES);
 #pragma unroll
-        for (int nb = 0; nb < ATT_BN / 16; ++nb) {
-          const int r = nb * 16 + (lane & 7) + ((lane >> 4) << 3);
-          const int ch = ks * 2 + ((lane >> 3) & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(sK + swz<HD>(r, ch), b0, b1, b2, b3);
-          mma16816(s[2 * nb], qf[ks], b0, b1);
-          mma16816(s[2 * nb + 1], qf[ks], b2, b3);
+        for (int b = 0; b < G::BOXES; ++b) {
+          tma_load_2d(kbuf + b * BOX_BYTES, &tmK, &kv_full[st], col_q + 64 * b, j * KT);
+          tma_load_2d(vbuf + b * BOX_BYTES, &tmV, &kv_full[st], col_q + 64 * b, j * KT);
+        }
+        last_parity[st] = (int)ph;
+      }
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(q_full, 0, wd, SITE_DRAIN);
+      for (int s = 0; s < NSTAGE; ++s)
+        if (last_parity[s] >= 0) mbar_wait(&kv_full[s], (uint32_t)last_parity[s], wd, SITE_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc_s = make_idesc_bf16(QT, KT, false);
+      const uint32_t idesc_o = make_idesc_bf16(QT, HD, true);
+      const uint32_t q_addr = smem_addr(sQ);
+      auto issue_s = [&](int j) {
+        const uint32_t k_addr = smem_addr(sKV + (j % NSTAGE) * G::STAGE_BYTES);
+        const uint32_t d_tmem = tmem + ((j & 1) ? TM_S1 : TM_S0);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
+          mma_ss(d_tmem, make_sdesc_sw128(q_addr + off, 16, 1024),
+                 make_sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[j & 1]);
+      };
+      bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA);
+      if (ok) ok = mbar_wait(&kv_full[0], 0, wb, SITE_ATT_MMA);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) {
+          const int st = (j + 1) % NSTAGE;
+          if (!mbar_wait(&kv_full[st], (uint32_t)(((j + 1) / NSTAGE) & 1), wb, SITE_ATT_MMA)) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!mbar_wait(&p_full[j & 1], (uint32_t)((j >> 1) & 1), wb, SITE_ATT_MMA)) break;
+        tc_fence_after();
+        const uint32_t v_addr = smem_addr(sKV + (j % NSTAGE) * G::STAGE_BYTES + G::K_BYTES);
+        const uint32_t p_tmem = tmem + ((j & 1) ? TM_P1 : TM_P0);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          // B = V: 16 keys (rows) x HD columns, MN-major: 64-column blocks BOX_BYTES
+          // apart, 8-row groups 1024 B apart; A = P: 16 keys = 8 packed columns
+          mma_ts(tmem + TM_O, p_tmem + (uint32_t)(kk * 8),
+                 make_sdesc_sw128(v_addr + (uint32_t)(kk * 2048), BOX_BYTES, 1024), idesc_o,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&o_done[j & 1]);
+        mma_commit(&kv_empty[j % NSTAGE]);
+      }
+      mma_commit(drain);
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(drain, 0, wd, SITE_DRAIN);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int q = warp & 3;
+    const int r_local = q * 32 + lane;
+    const long long grow = row0 + r_local;
+    const bool row_ok = grow < p.S;
+    const long long pos = row_ok ? row_pos(grow, p.C, p.T, p.D) : -1;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    float m_ref = -INFINITY;  // reference maximum (scaled, log2 units)
+    float l = 0.f;
+    bool ok = true;
+    // every lane waits; the warp goes on only if all lanes saw the phase complete
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool mine = mbar_wait(bar, parity, wb, SITE_ATT_SOFTMAX);
+      return __all_sync(0xffffffffu, mine) != 0;
+    };
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!warp_wait(&s_full[j & 1], (uint32_t)((j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t s_tmem = lane_base + ((j & 1) ? TM_S1 : TM_S0);
+      float s[KT];
+#pragma unroll
+      for (int c = 0; c < KT; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(s_tmem + c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(r[e]) * p.scale_log2;
+      }
+      const long long kv0 = (long long)j * KT;
+      if (kv0 + KT - 1 > pos) {
+#pragma unroll
+        for (int e = 0; e < KT; ++e)
+          if (kv0 + e > pos) s[e] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int e = 1; e < KT; ++e) mx = fmaxf(mx, s[e]);
+      // move the reference only when the tile maximum outgrows it by the threshold
+      float factor = 1.f;
+      const bool rescale = mx > m_ref + RESCALE_THRESHOLD;
+      if (rescale) {
+        factor = ex2(m_ref - mx);  // 0 when m_ref is still -inf
+        m_ref = mx;
+      }
+      const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+      l *= factor;
+      if (j > 0 && __any_sync(0xffffffffu, rescale && factor != 1.f)) {
+        // O holds P_0..P_{j-1} V; wait for the last of those products, then rescale
+        if (!warp_wait(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(lane_base + TM_O + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+          tmem_st16(lane_base + TM_O + c, r);
         }
       }
-      // scale into base 2 and mask keys past each row's position
-      const bool need_mask = kv0 + ATT_BN - 1 > w_min;
+      // P_j goes to the buffer P_{j-2} used: its product must have completed
+      if (j >= 2) {
+        if (!warp_wait(&o_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+      }
+      const uint32_t p_tmem = lane_base + ((j & 1) ? TM_P1 : TM_P0);
+      float sum = 0.f;
 #pragma unroll
-      for (int n = 0; n < ATT_BN / 8; ++n) {
+      for (int c = 0; c < KT; c += 32) {
+        uint32_t r[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v = s[n][e] * p.scale_log2;
-          if (need_mask) {
-            const long long kpos = kv0 + n * 8 + 2 * t4 + (e & 1);
-            const long long qpos = (e < 2) ? pos0 : pos1;
-            if (kpos > qpos) v = -INFINITY;
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(s[c + 2 * e] - ref);
+          const float p1 = ex2(s[c + 2 * e + 1] - ref);
+          sum += p0 + p1;
+          r[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(p_tmem + (uint32_t)(c / 2), r);
+      }
+      l += sum;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[j & 1]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && warp_wait(&o_done[(n_tiles - 1) & 1], (uint32_t)(((n_tiles - 1) >> 1) & 1))) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = p.o + grow * p.ld_o + p.o_col0 + col_q;
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + TM_O + c, r);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+            d4[v] = w;
           }
-          s[n][e] = v;
-        }
-      }
-      float mx0 = m0, mx1 = m1;
-#pragma unroll
-      for (int n = 0; n < ATT_BN / 8; ++n) {
-        mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
-        mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
-      }
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      // rows with nothing visible yet keep a finite reference so exp2 gives 0
-      const float ref0 = mx0 == -INFINITY ? 0.f : mx0;
-      const float ref1 = mx1 == -INFINITY ? 0.f : mx1;
-      const float c0 = ex2(m0 - ref0), c1 = ex2(m1 - ref1);
-      m0 = mx0;
-      m1 = mx1;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pf[ATT_BN / 16][4];
-#pragma unroll
-      for (int n = 0; n < ATT_BN / 8; ++n) {
-        const float p0 = ex2(s[n][0] - ref0), p1 = ex2(s[n][1] - ref0);
-        const float p2 = ex2(s[n][2] - ref1), p3 = ex2(s[n][3] - ref1);
-        rs0 += p0 + p1;
-        rs1 += p2 + p3;
-        pf[n >> 1][(n & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-        pf[n >> 1][(n & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-      }
-      l0 = l0 * c0 + rs0;
-      l1 = l1 * c1 + rs1;
-#pragma unroll
-      for (int i = 0; i < HD / 8; ++i) {
-        oacc[i][0] *= c0;
-        oacc[i][1] *= c0;
-        oacc[i][2] *= c1;
-        oacc[i][3] *= c1;
-      }
-      // O += P V; P fragments reuse the S accumulator layout as the A operand
-#pragma unroll
-      for (int ks = 0; ks < ATT_BN / 16; ++ks) {
-        const uint32_t a[4] = {pf[ks][0], pf[ks][1], pf[ks][2], pf[ks][3]};
-#pragma unroll
-        for (int db = 0; db < HD / 16; ++db) {
-          const int r = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int ch = db * 2 + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sV + swz<HD>(r, ch), b0, b1, b2, b3);
-          mma16816(oacc[2 * db], a, b0, b1);
-          mma16816(oacc[2 * db + 1], a, b2, b3);
         }
       }
     }
-    __syncthreads();
   }
 
-  // normalise and store O rows (bf16)
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  __nv_bfloat16* o0 = p.o + my_r0 * p.ld_o + p.o_col0 + head * HD;
-  __nv_bfloat16* o1 = p.o + my_r1 * p.ld_o + p.o_col0 + head * HD;
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) {
-    const int col = i * 8 + 2 * t4;
-    if (my_r0 < p.S)
-      *reinterpret_cast<uint32_t*>(o0 + col) = pack_bf16x2(oacc[i][0] * inv0, oacc[i][1] * inv0);
-    if (my_r1 < p.S)
-      *reinterpret_cast<uint32_t*>(o1 + col) = pack_bf16x2(oacc[i][2] * inv1, oacc[i][3] * inv1);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 template <int HD>
-tsp_status launch_hd(const AttParams& p, cudaStream_t stream) {
-  const size_t smem = (size_t)ATT_BM * HD * 2 + 4ull * ATT_BN * HD * 2;
-  auto kernel = attention_mma_kernel<HD>;
+tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, (uint64_t)c.ld_qkv, (uint64_t)c.S,
+                                    (uint64_t)c.ld_qkv * 2, 64, QT);
+  if (st != TSP_OK) return st;
+  st = make_tmap_2d_bf16(&tk, c.kn, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, KT);
+  if (st != TSP_OK) return st;
+  st = make_tmap_2d_bf16(&tv, c.vn, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, KT);
+  if (st != TSP_OK) return st;
+  auto kernel = attention_tcgen05_kernel<HD>;
+  const size_t smem = Geometry<HD>::SMEM;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attention: cudaFuncSetAttribute");
-  const long long blocks = ((p.S + ATT_BM - 1) / ATT_BM) * p.heads;
-  kernel<<<(unsigned)blocks, ATT_THREADS, smem, stream>>>(p);
+  const long long blocks = (long long)p.q_tiles * p.heads;
+  kernel<<<(unsigned)blocks, THREADS, smem, stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   return e == cudaSuccess ? TSP_OK : cuda_fail(e, "attention: launch");
 }
@@ -323,12 +386,15 @@ tsp_status launch_hd(const AttParams& p, cudaStream_t stream) {
 
 tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   if (c.d != 64 && c.d != 128) return fail(TSP_ERR_UNSUPPORTED, "attention: head_dim 64 or 128");
+  if (!c.qkv || !c.kn || !c.vn || !c.o || !c.status)
+    return fail(TSP_ERR_INVALID_ARG, "attention: null pointer");
+  if ((c.ld_qkv % 8) || (c.ld_kv % 8) || (c.ld_o % 8) || (c.o_col0 % 8))
+    return fail(TSP_ERR_INVALID_ARG, "attention: strides must be multiples of 8 elements");
+  if ((long long)c.heads * c.d > c.ld_kv || (long long)c.heads * c.d > c.ld_qkv ||
+      c.o_col0 + (long long)c.heads * c.d > c.ld_o)
+    return fail(TSP_ERR_INVALID_ARG, "attention: head columns exceed the row width");
+  if (c.S > (1ll << 30)) return fail(TSP_ERR_UNSUPPORTED, "attention: S too large");
   AttParams p;
-  p.qkv = static_cast<const __nv_bfloat16*>(c.qkv);
-  p.ld_qkv = c.ld_qkv;
-  p.kn = static_cast<const __nv_bfloat16*>(c.kn);
-  p.vn = static_cast<const __nv_bfloat16*>(c.vn);
-  p.ld_kv = c.ld_kv;
   p.o = static_cast<__nv_bfloat16*>(c.o);
   p.ld_o = c.ld_o;
   p.o_col0 = c.o_col0;
@@ -337,9 +403,12 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.C = c.C;
   p.D = c.D;
   p.heads = c.heads;
-  p.natural_order = (c.C % ATT_BM == 0) ? 1 : 0;
+  p.q_tiles = (int)((c.S + QT - 1) / QT);
+  p.natural_order = (c.C % QT == 0) ? 1 : 0;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);
-  return c.d == 64 ? launch_hd<64>(p, stream) : launch_hd<128>(p, stream);
+  p.status = c.status;
+  p.limit_ns = wait_limit_ns();
+  return c.d == 64 ? launch_hd<64>(c, p, stream) : launch_hd<128>(c, p, stream);
 }
 
 }  // namespace tsp
