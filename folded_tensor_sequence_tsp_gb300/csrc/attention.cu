@@ -4,8 +4,10 @@
 // K/V all-gather; zigzag partitioning for causal balance).
 //
 // One CTA computes 128 query rows of one head on the 5th-generation tensor cores:
-//   warp 0      TMA: the Q tile once, then K/V tiles of 128 keys into a 2-stage
-//               ring of 128B-swizzled shared-memory buffers
+//   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into two
+//               3-stage rings of 128B-swizzled shared-memory buffers, in the order
+//               the MMAs consume them (K_0, then K_{j+1} before V_j); a K slot frees
+//               as soon as its S MMA completes, a V slot when its PV MMA completes
 //   warp 1      allocates 512 TMEM columns; one lane issues
 //                 S_j  = Q K_j^T          tcgen05.mma, A and B from shared memory
 //                 O   += P_j V_j          tcgen05.mma, A (= P) from tensor memory,
@@ -14,7 +16,10 @@
 //               on the next scores while the softmax of the current tile runs
 //   warps 2..5  softmax, one query row per thread (TMEM lane = row): tcgen05.ld of
 //               the S row, mask by global position, row max, exp2, row sum, bf16
-//               P written back to TMEM with tcgen05.st; then the epilogue.
+//               P written back to TMEM with tcgen05.st; then the epilogue. The four
+//               TMEM loads of a row are in flight together, and the row max and sum
+//               use 8 independent partial accumulators (one warp per SM sub-partition
+//               has no other warp to hide a 128-long dependency chain behind).
 // TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
 //
 // Online softmax in base 2 (scores pre-scaled by log2(e)/sqrt(d)). Each row keeps a
@@ -35,7 +40,8 @@ namespace {
 
 constexpr int QT = 128;      // query rows per CTA
 constexpr int KT = 128;      // keys per tile
-constexpr int NSTAGE = 2;    // K/V ring depth
+constexpr int KSTAGES = 3;   // K ring depth (a K slot frees when its S MMA completes)
+constexpr int VSTAGES = 3;   // V ring depth (a V slot frees when its PV MMA completes)
 constexpr int THREADS = 192;
 constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P0 = 384, TM_P1 = 448;
@@ -47,8 +53,7 @@ struct Geometry {
   static constexpr int BOXES = HD / 64;                 // 64-column boxes per row block
   static constexpr uint32_t Q_BYTES = QT * HD * 2;
   static constexpr uint32_t K_BYTES = KT * HD * 2;
-  static constexpr uint32_t STAGE_BYTES = 2 * K_BYTES;  // K and V
-  static constexpr size_t USED = 1024 + Q_BYTES + (size_t)NSTAGE * STAGE_BYTES + 256;
+  static constexpr size_t USED = 1024 + Q_BYTES + (size_t)(KSTAGES + VSTAGES) * K_BYTES + 256;
   // The CTA allocates all 512 TMEM columns, so it must be alone on its SM: ask for
   // more than half of the SM's 228 KB of shared memory.
   static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
@@ -94,12 +99,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = smem + G::Q_BYTES;  // stage s: K at s*STAGE_BYTES, V at +K_BYTES
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NSTAGE * G::STAGE_BYTES);
-  uint64_t* q_full = bars;                // [1]
-  uint64_t* kv_full = bars + 1;           // [NSTAGE]
-  uint64_t* kv_empty = kv_full + NSTAGE;  // [NSTAGE]
-  uint64_t* s_full = kv_empty + NSTAGE;   // [2] S_j ready in TMEM
+  uint8_t* sK = smem + G::Q_BYTES;             // KSTAGES x K_BYTES
+  uint8_t* sV = sK + KSTAGES * G::K_BYTES;     // VSTAGES x K_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VSTAGES * G::K_BYTES);
+  uint64_t* q_full = bars;                     // [1]
+  uint64_t* k_full = bars + 1;                 // [KSTAGES]
+  uint64_t* k_empty = k_full + KSTAGES;        // [KSTAGES]
+  uint64_t* v_full = k_empty + KSTAGES;        // [VSTAGES]
+  uint64_t* v_empty = v_full + VSTAGES;        // [VSTAGES]
+  uint64_t* s_full = v_empty + VSTAGES;        // [2] S_j ready in TMEM
   uint64_t* p_full = s_full + 2;          // [2] P_j written to TMEM (4 softmax warps)
   uint64_t* o_done = p_full + 2;          // [2] O += P_j V_j completed
   uint64_t* drain = o_done + 2;           // [1]
@@ -129,9 +137,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < KSTAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < VSTAGES; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -162,27 +174,47 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int b = 0; b < G::BOXES; ++b)
         tma_load_2d(sQ + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b, (int)row0);
-      int last_parity[NSTAGE];
+      // loads in the order the MMA warp consumes them: K_0, then K_{j+1}, V_j
+      int k_last[KSTAGES], v_last[VSTAGES];
 #pragma unroll
-      for (int s = 0; s < NSTAGE; ++s) last_parity[s] = -1;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % NSTAGE;
-        const uint32_t ph = (uint32_t)((j / NSTAGE) & 1);
-        if (!mbar_wait(&kv_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
-        uint8_t* kbuf = sKV + st * G::STAGE_BYTES;
-        uint8_t* vbuf = kbuf + G::K_BYTES;
-        mbar_arrive_expect_tx(&kv_full[st], G::STAGE_BYTES);
+      for (int t = 0; t < KSTAGES; ++t) k_last[t] = -1;
 #pragma unroll
-        for (int b = 0; b < G::BOXES; ++b) {
-          tma_load_2d(kbuf + b * BOX_BYTES, &tmK, &kv_full[st], col_q + 64 * b, j * KT);
-          tma_load_2d(vbuf + b * BOX_BYTES, &tmV, &kv_full[st], col_q + 64 * b, j * KT);
-        }
-        last_parity[st] = (int)ph;
+      for (int t = 0; t < VSTAGES; ++t) v_last[t] = -1;
+      auto load_k = [&](int j) {
+        const int st = j % KSTAGES;
+        const uint32_t ph = (uint32_t)((j / KSTAGES) & 1);
+        if (!mbar_wait(&k_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) return false;
+        mbar_arrive_expect_tx(&k_full[st], G::K_BYTES);
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b)
+          tma_load_2d(sK + st * G::K_BYTES + b * BOX_BYTES, &tmK, &k_full[st], col_q + 64 * b,
+                      j * KT);
+        k_last[st] = (int)ph;
+        return true;
+      };
+      auto load_v = [&](int j) {
+        const int st = j % VSTAGES;
+        const uint32_t ph = (uint32_t)((j / VSTAGES) & 1);
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) return false;
+        mbar_arrive_expect_tx(&v_full[st], G::K_BYTES);
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b)
+          tma_load_2d(sV + st * G::K_BYTES + b * BOX_BYTES, &tmV, &v_full[st], col_q + 64 * b,
+                      j * KT);
+        v_last[st] = (int)ph;
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
       }
       WaitBound wd{p.status, p.limit_ns, nullptr};
       mbar_wait(q_full, 0, wd, SITE_DRAIN);
-      for (int s = 0; s < NSTAGE; ++s)
-        if (last_parity[s] >= 0) mbar_wait(&kv_full[s], (uint32_t)last_parity[s], wd, SITE_DRAIN);
+      for (int t = 0; t < KSTAGES; ++t)
+        if (k_last[t] >= 0) mbar_wait(&k_full[t], (uint32_t)k_last[t], wd, SITE_DRAIN);
+      for (int t = 0; t < VSTAGES; ++t)
+        if (v_last[t] >= 0) mbar_wait(&v_full[t], (uint32_t)v_last[t], wd, SITE_DRAIN);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -191,7 +223,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc_o = make_idesc_bf16(QT, HD, true);
       const uint32_t q_addr = smem_addr(sQ);
       auto issue_s = [&](int j) {
-        const uint32_t k_addr = smem_addr(sKV + (j % NSTAGE) * G::STAGE_BYTES);
+        const uint32_t k_addr = smem_addr(sK + (j % KSTAGES) * G::K_BYTES);
         const uint32_t d_tmem = tmem + ((j & 1) ? TM_S1 : TM_S0);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -200,23 +232,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                  make_sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[j & 1]);
+        mma_commit(&k_empty[j % KSTAGES]);
       };
       bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA);
-      if (ok) ok = mbar_wait(&kv_full[0], 0, wb, SITE_ATT_MMA);
+      if (ok) ok = mbar_wait(&k_full[0], 0, wb, SITE_ATT_MMA);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 1 < n_tiles) {
-          const int st = (j + 1) % NSTAGE;
-          if (!mbar_wait(&kv_full[st], (uint32_t)(((j + 1) / NSTAGE) & 1), wb, SITE_ATT_MMA)) break;
+          const int st = (j + 1) % KSTAGES;
+          if (!mbar_wait(&k_full[st], (uint32_t)(((j + 1) / KSTAGES) & 1), wb, SITE_ATT_MMA)) break;
           tc_fence_after();
           issue_s(j + 1);
         }
         if (!mbar_wait(&p_full[j & 1], (uint32_t)((j >> 1) & 1), wb, SITE_ATT_MMA)) break;
+        if (!mbar_wait(&v_full[j % VSTAGES], (uint32_t)((j / VSTAGES) & 1), wb, SITE_ATT_MMA)) break;
         tc_fence_after();
-        const uint32_t v_addr = smem_addr(sKV + (j % NSTAGE) * G::STAGE_BYTES + G::K_BYTES);
+        const uint32_t v_addr = smem_addr(sV + (j % VSTAGES) * G::K_BYTES);
         const uint32_t p_tmem = tmem + ((j & 1) ? TM_P1 : TM_P0);
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk) {
@@ -227,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&o_done[j & 1]);
-        mma_commit(&kv_empty[j % NSTAGE]);
+        mma_commit(&v_empty[j % VSTAGES]);
       }
       mma_commit(drain);
       WaitBound wd{p.status, p.limit_ns, nullptr};
@@ -256,24 +290,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t s_tmem = lane_base + ((j & 1) ? TM_S1 : TM_S0);
-      float s[KT];
-#pragma unroll
-      for (int c = 0; c < KT; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(s_tmem + c, r);
+      // raw scores of this row: four TMEM loads in flight, one wait
+      float sc[KT];
+      {
+        uint32_t ra[32], rb[32], rc[32], rd[32];
+        tmem_ld32(s_tmem + 0, ra);
+        tmem_ld32(s_tmem + 32, rb);
+        tmem_ld32(s_tmem + 64, rc);
+        tmem_ld32(s_tmem + 96, rd);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(r[e]) * p.scale_log2;
+        for (int e = 0; e < 32; ++e) {
+          sc[e] = __uint_as_float(ra[e]);
+          sc[32 + e] = __uint_as_float(rb[e]);
+          sc[64 + e] = __uint_as_float(rc[e]);
+          sc[96 + e] = __uint_as_float(rd[e]);
+        }
       }
       const long long kv0 = (long long)j * KT;
       if (kv0 + KT - 1 > pos) {
 #pragma unroll
         for (int e = 0; e < KT; ++e)
-          if (kv0 + e > pos) s[e] = -INFINITY;
+          if (kv0 + e > pos) sc[e] = -INFINITY;
       }
-      float mx = s[0];
+      // row maximum with 8 independent partial maxima (short dependency chains)
+      float m8[8];
 #pragma unroll
-      for (int e = 1; e < KT; ++e) mx = fmaxf(mx, s[e]);
+      for (int e = 0; e < 8; ++e) m8[e] = sc[e];
+#pragma unroll
+      for (int e = 8; e < KT; ++e) m8[e & 7] = fmaxf(m8[e & 7], sc[e]);
+      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mx = mraw * p.scale_log2;  // scale > 0 keeps the order
       // move the reference only when the tile maximum outgrows it by the threshold
       float factor = 1.f;
       const bool rescale = mx > m_ref + RESCALE_THRESHOLD;
@@ -281,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         factor = ex2(m_ref - mx);  // 0 when m_ref is still -inf
         m_ref = mx;
       }
-      const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+      const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
       l *= factor;
       if (j > 0 && __any_sync(0xffffffffu, rescale && factor != 1.f)) {
         // O holds P_0..P_{j-1} V; wait for the last of those products, then rescale
@@ -308,19 +356,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       const uint32_t p_tmem = lane_base + ((j & 1) ? TM_P1 : TM_P0);
-      float sum = 0.f;
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < KT; c += 32) {
         uint32_t r[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(s[c + 2 * e] - ref);
-          const float p1 = ex2(s[c + 2 * e + 1] - ref);
-          sum += p0 + p1;
+          const float p0 = ex2(fmaf(sc[c + 2 * e], p.scale_log2, neg_ref));
+          const float p1 = ex2(fmaf(sc[c + 2 * e + 1], p.scale_log2, neg_ref));
+          sum8[e & 7] += p0 + p1;
           r[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(p_tmem + (uint32_t)(c / 2), r);
       }
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                        ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l += sum;
       tmem_st_wait();
       tc_fence_before();
