@@ -3,57 +3,65 @@
 // Training & Inference", section 2, attention layers: FlashAttention after the
 // K/V all-gather; zigzag partitioning for causal balance).
 //
-// One CTA computes 128 query rows of one head on the 5th-generation tensor cores:
-//   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into two
-//               3-stage rings of 128B-swizzled shared-memory buffers, in the order
-//               the MMAs consume them (K_0, then K_{j+1} before V_j); a K slot frees
-//               as soon as its S MMA completes, a V slot when its PV MMA completes
-//   warp 1      allocates 512 TMEM columns; one lane issues
-//                 S_j  = Q K_j^T          tcgen05.mma, A and B from shared memory
-//                 O   += P_j V_j          tcgen05.mma, A (= P) from tensor memory,
-//                                          B (= V) MN-major from shared memory
-//               with S_{j+1} issued before O += P_j V_j, so the tensor core works
-//               on the next scores while the softmax of the current tile runs
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): tcgen05.ld of
-//               the S row, mask by global position, row max, exp2, row sum, bf16
-//               P written back to TMEM with tcgen05.st; then the epilogue. The four
-//               TMEM loads of a row are in flight together, and the row max and sum
-//               use 8 independent partial accumulators (one warp per SM sub-partition
-//               has no other warp to hide a 128-long dependency chain behind).
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512).
+// One CTA computes two 128-row query tiles (A and B) of one head on the
+// 5th-generation tensor cores. Both tiles share every K/V tile the CTA loads.
+//   warp 0      TMA: Q_A and Q_B once, then K and V tiles of 128 keys into a
+//               3-stage K ring and a 2-stage V ring of 128B-swizzled shared
+//               memory, in the order the MMAs consume them (K_j, V_j, K_{j+1}, ...)
+//   warp 1      allocates all 512 TMEM columns; one lane issues, per key tile j,
+//                 O_A += P_A V_j,  S_A = Q_A K_{j+1}^T,  O_B += P_B V_j,  S_B = Q_B K_{j+1}^T
+//               (S from shared-memory operands; P read from TMEM as the A operand,
+//               V as an MN-major shared-memory operand). While one tile's softmax
+//               runs, the tensor core works on the other tile's products.
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one query row per
+//               thread (TMEM lane = row), two softmax warps per SM sub-partition so
+//               each hides the other's latencies. tcgen05.ld of the S row (four
+//               loads in flight), mask by global position, row max and sum with 8
+//               partial accumulators, P = exp2(s - m) in bf16 written over the
+//               first 64 columns of the same S with tcgen05.st; then the epilogue.
+// TMEM columns: S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512); P_X
+// occupies the first 64 columns of S_X (two bf16 per column).
 //
-// Online softmax in base 2 (scores pre-scaled by log2(e)/sqrt(d)). Each row keeps a
-// reference maximum m and sum l; m only moves (and O and l are rescaled) when the
-// tile maximum exceeds it by more than 8, so P = exp2(s - m) <= 256 and most tiles
-// never touch O. The result is exact softmax: out = O / l at the end.
+// Ordering: MMAs issued by one thread execute in order, and tcgen05.commit arrives
+// once every earlier MMA of the thread has completed. So S_X(j+1) may overwrite
+// the columns P_X(j) is read from right after O_X += P_X(j) V_j is issued, and the
+// completion of S_X(j) also tells the softmax that O_X += P_X(j-1) V_{j-1} is done.
+//
+// Online softmax in base 2 (scores scaled by log2(e)/sqrt(d) inside the exp
+// argument). Each row keeps a reference maximum m and sum l; m only moves (and O
+// and l are rescaled) when the tile maximum exceeds it by more than 8, so
+// P <= 256 and most tiles never touch O. The result is exact softmax: O / l.
 //
 // Query row r of the rank-major layout is the token at global position pos(r) of
 // the zigzag map; key t is visible iff t <= pos(r). CTAs of one head run before
 // the next head (K/V of a head stay in L2 across its CTAs) and, when the zigzag
-// chunk is a multiple of 128 tokens, take query tiles in decreasing position, so
-// the longest tiles start first.
+// chunk is a multiple of 256 tokens, take query blocks in decreasing position, so
+// the longest blocks start first.
 #include "tsp_device.cuh"
 #include "tsp_internal.h"
 
 namespace tsp {
 namespace {
 
-constexpr int QT = 128;      // query rows per CTA
-constexpr int KT = 128;      // keys per tile
-constexpr int KSTAGES = 3;   // K ring depth (a K slot frees when its S MMA completes)
-constexpr int VSTAGES = 3;   // V ring depth (a V slot frees when its PV MMA completes)
-constexpr int THREADS = 192;
+constexpr int QT = 128;       // query rows per tile (two tiles per CTA)
+constexpr int QB = 2 * QT;    // query rows per CTA
+constexpr int KT = 128;       // keys per tile
+constexpr int KSTAGES = 3;
+constexpr int VSTAGES = 2;
+constexpr int THREADS = 320;  // TMA warp, MMA warp, 2 x 4 softmax warps
 constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
-constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P0 = 384, TM_P1 = 448;
+constexpr uint32_t TM_S0 = 0, TM_O0 = 128, TM_S1 = 256, TM_O1 = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
+__device__ __forceinline__ uint32_t tm_s(int t) { return t ? TM_S1 : TM_S0; }
+__device__ __forceinline__ uint32_t tm_o(int t) { return t ? TM_O1 : TM_O0; }
+
 template <int HD>
 struct Geometry {
-  static constexpr int BOXES = HD / 64;                 // 64-column boxes per row block
-  static constexpr uint32_t Q_BYTES = QT * HD * 2;
-  static constexpr uint32_t K_BYTES = KT * HD * 2;
-  static constexpr size_t USED = 1024 + Q_BYTES + (size_t)(KSTAGES + VSTAGES) * K_BYTES + 256;
+  static constexpr int BOXES = HD / 64;  // 64-column boxes per 128-row block
+  static constexpr uint32_t TILE_BYTES = 128 * HD * 2;
+  static constexpr size_t USED = 1024 + (size_t)(2 + KSTAGES + VSTAGES) * TILE_BYTES + 256;
   // The CTA allocates all 512 TMEM columns, so it must be alone on its SM: ask for
   // more than half of the SM's 228 KB of shared memory.
   static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
@@ -66,7 +74,7 @@ struct AttParams {
   long long S, T, C;
   int D;
   int heads;
-  int q_tiles;
+  int q_blocks;
   int natural_order;
   float scale_log2;
   DevStatus* status;
@@ -89,6 +97,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Number of 128-key tiles the query rows [r0, r0 + QT) need (0 if none is a row).
+__device__ __forceinline__ int tiles_needed(long long r0, const AttParams& p) {
+  if (r0 >= p.S) return 0;
+  long long mx = 0;
+  if (p.natural_order) {
+    mx = row_pos(r0 + QT - 1, p.C, p.T, p.D);
+  } else {
+    const long long last = min(r0 + QT, p.S);
+    for (long long r = r0; r < last; ++r) mx = max(mx, row_pos(r, p.C, p.T, p.D));
+  }
+  return (int)(mx / KT) + 1;
+}
+
+// Each SM sub-partition holds 16K registers and 10 warps put three warps on two of
+// them, so a thread gets at most 168 registers.
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
     attention_tcgen05_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -98,41 +121,31 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + G::Q_BYTES;             // KSTAGES x K_BYTES
-  uint8_t* sV = sK + KSTAGES * G::K_BYTES;     // VSTAGES x K_BYTES
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VSTAGES * G::K_BYTES);
-  uint64_t* q_full = bars;                     // [1]
-  uint64_t* k_full = bars + 1;                 // [KSTAGES]
-  uint64_t* k_empty = k_full + KSTAGES;        // [KSTAGES]
-  uint64_t* v_full = k_empty + KSTAGES;        // [VSTAGES]
-  uint64_t* v_empty = v_full + VSTAGES;        // [VSTAGES]
-  uint64_t* s_full = v_empty + VSTAGES;        // [2] S_j ready in TMEM
-  uint64_t* p_full = s_full + 2;          // [2] P_j written to TMEM (4 softmax warps)
-  uint64_t* o_done = p_full + 2;          // [2] O += P_j V_j completed
-  uint64_t* drain = o_done + 2;           // [1]
+  uint8_t* sQ = smem;                          // tile A, then tile B
+  uint8_t* sK = sQ + 2 * G::TILE_BYTES;        // KSTAGES tiles
+  uint8_t* sV = sK + KSTAGES * G::TILE_BYTES;  // VSTAGES tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VSTAGES * G::TILE_BYTES);
+  uint64_t* q_full = bars;               // [1]
+  uint64_t* k_full = q_full + 1;         // [KSTAGES]
+  uint64_t* k_empty = k_full + KSTAGES;  // [KSTAGES]
+  uint64_t* v_full = k_empty + KSTAGES;  // [VSTAGES]
+  uint64_t* v_empty = v_full + VSTAGES;  // [VSTAGES]
+  uint64_t* s_full = v_empty + VSTAGES;  // [2] per tile: S(j) in TMEM
+  uint64_t* p_full = s_full + 2;         // [2] per tile: P(j) in TMEM (4 warps)
+  uint64_t* o_done = p_full + 2;         // [2] per tile: O += P(j) V_j complete
+  uint64_t* drain = o_done + 2;          // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = blockIdx.x / p.q_tiles;
-  const int tile = blockIdx.x - head * p.q_tiles;
-  long long row0;
-  if (p.natural_order) {
-    row0 = zig_row((long long)(p.q_tiles - 1 - tile) * QT, p.C, p.T, p.D);
-  } else {
-    row0 = (long long)tile * QT;
-  }
-  // keys needed by this CTA: 0 .. largest position among its rows
-  long long max_pos;
-  if (p.natural_order) {
-    max_pos = row_pos(row0 + QT - 1, p.C, p.T, p.D);
-  } else {
-    max_pos = 0;
-    const long long last = min(row0 + QT, p.S);
-    for (long long r = row0; r < last; ++r) max_pos = max(max_pos, row_pos(r, p.C, p.T, p.D));
-  }
-  const int n_tiles = (int)(max_pos / KT) + 1;
+  const int head = blockIdx.x / p.q_blocks;
+  const int blk = blockIdx.x - head * p.q_blocks;
+  const long long row0 = p.natural_order
+                             ? zig_row((long long)(p.q_blocks - 1 - blk) * QB, p.C, p.T, p.D)
+                             : (long long)blk * QB;
+  const int n_a = tiles_needed(row0, p);
+  const int n_b = tiles_needed(row0 + QT, p);
+  const int n_tiles = max(n_a, n_b);
   const int col_q = head * HD;  // Q columns inside qkv; K/V columns inside kn/vn
 
   if (threadIdx.x == 0) {
@@ -145,10 +158,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 4);
-      mbar_init(&o_done[b], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -168,100 +181,102 @@ __global__ void __launch_bounds__(THREADS, 1)
   WaitBound wb{p.status, p.limit_ns, abort_flag};
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && n_tiles > 0) {
       // ------------------------------------------------------------ TMA producer
-      mbar_arrive_expect_tx(q_full, G::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, 2 * G::TILE_BYTES);
 #pragma unroll
-      for (int b = 0; b < G::BOXES; ++b)
-        tma_load_2d(sQ + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b, (int)row0);
-      // loads in the order the MMA warp consumes them: K_0, then K_{j+1}, V_j
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b)
+          tma_load_2d(sQ + t * G::TILE_BYTES + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b,
+                      (int)(row0 + t * QT));
       int k_last[KSTAGES], v_last[VSTAGES];
 #pragma unroll
-      for (int t = 0; t < KSTAGES; ++t) k_last[t] = -1;
+      for (int s = 0; s < KSTAGES; ++s) k_last[s] = -1;
 #pragma unroll
-      for (int t = 0; t < VSTAGES; ++t) v_last[t] = -1;
-      auto load_k = [&](int j) {
-        const int st = j % KSTAGES;
-        const uint32_t ph = (uint32_t)((j / KSTAGES) & 1);
-        if (!mbar_wait(&k_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) return false;
-        mbar_arrive_expect_tx(&k_full[st], G::K_BYTES);
-#pragma unroll
-        for (int b = 0; b < G::BOXES; ++b)
-          tma_load_2d(sK + st * G::K_BYTES + b * BOX_BYTES, &tmK, &k_full[st], col_q + 64 * b,
-                      j * KT);
-        k_last[st] = (int)ph;
-        return true;
-      };
-      auto load_v = [&](int j) {
-        const int st = j % VSTAGES;
-        const uint32_t ph = (uint32_t)((j / VSTAGES) & 1);
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) return false;
-        mbar_arrive_expect_tx(&v_full[st], G::K_BYTES);
+      for (int s = 0; s < VSTAGES; ++s) v_last[s] = -1;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int ks = j % KSTAGES;
+        const uint32_t kph = (uint32_t)((j / KSTAGES) & 1);
+        if (!mbar_wait(&k_empty[ks], kph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
+        mbar_arrive_expect_tx(&k_full[ks], G::TILE_BYTES);
 #pragma unroll
         for (int b = 0; b < G::BOXES; ++b)
-          tma_load_2d(sV + st * G::K_BYTES + b * BOX_BYTES, &tmV, &v_full[st], col_q + 64 * b,
-                      j * KT);
-        v_last[st] = (int)ph;
-        return true;
-      };
-      bool ok = load_k(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
+          tma_load_2d(sK + ks * G::TILE_BYTES + b * BOX_BYTES, &tmK, &k_full[ks],
+                      col_q + 64 * b, j * KT);
+        k_last[ks] = (int)kph;
+        const int vs = j % VSTAGES;
+        const uint32_t vph = (uint32_t)((j / VSTAGES) & 1);
+        if (!mbar_wait(&v_empty[vs], vph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
+        mbar_arrive_expect_tx(&v_full[vs], G::TILE_BYTES);
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b)
+          tma_load_2d(sV + vs * G::TILE_BYTES + b * BOX_BYTES, &tmV, &v_full[vs],
+                      col_q + 64 * b, j * KT);
+        v_last[vs] = (int)vph;
       }
       WaitBound wd{p.status, p.limit_ns, nullptr};
       mbar_wait(q_full, 0, wd, SITE_DRAIN);
-      for (int t = 0; t < KSTAGES; ++t)
-        if (k_last[t] >= 0) mbar_wait(&k_full[t], (uint32_t)k_last[t], wd, SITE_DRAIN);
-      for (int t = 0; t < VSTAGES; ++t)
-        if (v_last[t] >= 0) mbar_wait(&v_full[t], (uint32_t)v_last[t], wd, SITE_DRAIN);
+      for (int s = 0; s < KSTAGES; ++s)
+        if (k_last[s] >= 0) mbar_wait(&k_full[s], (uint32_t)k_last[s], wd, SITE_DRAIN);
+      for (int s = 0; s < VSTAGES; ++s)
+        if (v_last[s] >= 0) mbar_wait(&v_full[s], (uint32_t)v_last[s], wd, SITE_DRAIN);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && n_tiles > 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_s = make_idesc_bf16(QT, KT, false);
       const uint32_t idesc_o = make_idesc_bf16(QT, HD, true);
-      const uint32_t q_addr = smem_addr(sQ);
-      auto issue_s = [&](int j) {
-        const uint32_t k_addr = smem_addr(sK + (j % KSTAGES) * G::K_BYTES);
-        const uint32_t d_tmem = tmem + ((j & 1) ? TM_S1 : TM_S0);
+      // S_t = Q_t K_j^T
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q_addr = smem_addr(sQ + t * G::TILE_BYTES);
+        const uint32_t k_addr = smem_addr(sK + (j % KSTAGES) * G::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (uint32_t)((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
-          mma_ss(d_tmem, make_sdesc_sw128(q_addr + off, 16, 1024),
+          mma_ss(tmem + tm_s(t), make_sdesc_sw128(q_addr + off, 16, 1024),
                  make_sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[j & 1]);
-        mma_commit(&k_empty[j % KSTAGES]);
+        mma_commit(&s_full[t]);
       };
-      bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA);
-      if (ok) ok = mbar_wait(&k_full[0], 0, wb, SITE_ATT_MMA);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) {
-          const int st = (j + 1) % KSTAGES;
-          if (!mbar_wait(&k_full[st], (uint32_t)(((j + 1) / KSTAGES) & 1), wb, SITE_ATT_MMA)) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        if (!mbar_wait(&p_full[j & 1], (uint32_t)((j >> 1) & 1), wb, SITE_ATT_MMA)) break;
-        if (!mbar_wait(&v_full[j % VSTAGES], (uint32_t)((j / VSTAGES) & 1), wb, SITE_ATT_MMA)) break;
-        tc_fence_after();
-        const uint32_t v_addr = smem_addr(sV + (j % VSTAGES) * G::K_BYTES);
-        const uint32_t p_tmem = tmem + ((j & 1) ? TM_P1 : TM_P0);
+      // O_t += P_t V_j; B = V: 16 keys x HD columns per step, MN-major (64-column
+      // blocks BOX_BYTES apart, 8-row groups 1024 B apart); A = P: 8 packed columns
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_addr = smem_addr(sV + (j % VSTAGES) * G::TILE_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          // B = V: 16 keys (rows) x HD columns, MN-major: 64-column blocks BOX_BYTES
-          // apart, 8-row groups 1024 B apart; A = P: 16 keys = 8 packed columns
-          mma_ts(tmem + TM_O, p_tmem + (uint32_t)(kk * 8),
+        for (int kk = 0; kk < KT / 16; ++kk)
+          mma_ts(tmem + tm_o(t), tmem + tm_s(t) + (uint32_t)(kk * 8),
                  make_sdesc_sw128(v_addr + (uint32_t)(kk * 2048), BOX_BYTES, 1024), idesc_o,
                  (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&o_done[t]);
+      };
+      bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA) && mbar_wait(&k_full[0], 0, wb, SITE_ATT_MMA);
+      if (ok) {
+        tc_fence_after();
+        if (n_a > 0) issue_s(0, 0);
+        if (n_b > 0) issue_s(1, 0);
+        mma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (!mbar_wait(&v_full[j % VSTAGES], (uint32_t)((j / VSTAGES) & 1), wb, SITE_ATT_MMA)) break;
+        const bool next_k = j + 1 < n_tiles;
+        if (next_k && !mbar_wait(&k_full[(j + 1) % KSTAGES], (uint32_t)(((j + 1) / KSTAGES) & 1),
+                                 wb, SITE_ATT_MMA))
+          break;
+        for (int t = 0; t < 2; ++t) {
+          const int nt = t ? n_b : n_a;
+          if (j >= nt) continue;
+          if (!mbar_wait(&p_full[t], (uint32_t)(j & 1), wb, SITE_ATT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < nt) issue_s(t, j + 1);
         }
-        mma_commit(&o_done[j & 1]);
+        if (!ok) break;
         mma_commit(&v_empty[j % VSTAGES]);
+        if (next_k) mma_commit(&k_empty[(j + 1) % KSTAGES]);
       }
       mma_commit(drain);
       WaitBound wd{p.status, p.limit_ns, nullptr};
@@ -269,12 +284,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax
-    const int q = warp & 3;
+    const int t = (warp - 2) >> 2;  // query tile of this warpgroup: 0 = A, 1 = B
+    const int q = warp & 3;         // TMEM lane quarter of this warp
     const int r_local = q * 32 + lane;
-    const long long grow = row0 + r_local;
+    const long long grow = row0 + t * QT + r_local;
     const bool row_ok = grow < p.S;
     const long long pos = row_ok ? row_pos(grow, p.C, p.T, p.D) : -1;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t s_tmem = lane_base + tm_s(t);
+    const uint32_t o_tmem = lane_base + tm_o(t);
+    const int my_tiles = t ? n_b : n_a;
     float m_ref = -INFINITY;  // reference maximum (scaled, log2 units)
     float l = 0.f;
     bool ok = true;
@@ -283,13 +302,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool mine = mbar_wait(bar, parity, wb, SITE_ATT_SOFTMAX);
       return __all_sync(0xffffffffu, mine) != 0;
     };
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(&s_full[j & 1], (uint32_t)((j >> 1) & 1))) {
+    for (int j = 0; j < my_tiles; ++j) {
+      // S(j) complete also means O += P(j-1) V_{j-1} is complete (in-order MMAs)
+      if (!warp_wait(&s_full[t], (uint32_t)(j & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_tmem = lane_base + ((j & 1) ? TM_S1 : TM_S0);
       // raw scores of this row: four TMEM loads in flight, one wait
       float sc[KT];
       {
@@ -332,30 +351,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
       l *= factor;
       if (j > 0 && __any_sync(0xffffffffu, rescale && factor != 1.f)) {
-        // O holds P_0..P_{j-1} V; wait for the last of those products, then rescale
-        if (!warp_wait(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < HD; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(lane_base + TM_O + c, r);
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(o_tmem + c, r);
           tmem_ld_wait();
+          uint32_t lo[16], hi[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
-          tmem_st16(lane_base + TM_O + c, r);
+          for (int e = 0; e < 16; ++e) {
+            lo[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+            hi[e] = __float_as_uint(__uint_as_float(r[16 + e]) * factor);
+          }
+          tmem_st16(o_tmem + c, lo);
+          tmem_st16(o_tmem + c + 16, hi);
         }
       }
-      // P_j goes to the buffer P_{j-2} used: its product must have completed
-      if (j >= 2) {
-        if (!warp_wait(&o_done[j & 1], (uint32_t)(((j - 2) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-      }
-      const uint32_t p_tmem = lane_base + ((j & 1) ? TM_P1 : TM_P0);
+      // P = exp2(s*scale - m) in bf16 over the first 64 columns of S
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
@@ -369,25 +380,23 @@ __global__ void __launch_bounds__(THREADS, 1)
           sum8[e & 7] += p0 + p1;
           r[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(p_tmem + (uint32_t)(c / 2), r);
+        tmem_st16(s_tmem + (uint32_t)(c / 2), r);
       }
-      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                        ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      l += sum;
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && warp_wait(&o_done[(n_tiles - 1) & 1], (uint32_t)(((n_tiles - 1) >> 1) & 1))) {
+    if (ok && my_tiles > 0 && warp_wait(&o_done[t], (uint32_t)((my_tiles - 1) & 1))) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* dst = p.o + grow * p.ld_o + p.o_col0 + col_q;
 #pragma unroll
       for (int c = 0; c < HD; c += 32) {
         uint32_t r[32];
-        tmem_ld32(lane_base + TM_O + c, r);
+        tmem_ld32(o_tmem + c, r);
         tmem_ld_wait();
         if (row_ok) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c);
@@ -428,7 +437,7 @@ tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t st
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attention: cudaFuncSetAttribute");
-  const long long blocks = (long long)p.q_tiles * p.heads;
+  const long long blocks = (long long)p.q_blocks * p.heads;
   kernel<<<(unsigned)blocks, THREADS, smem, stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   return e == cudaSuccess ? TSP_OK : cuda_fail(e, "attention: launch");
@@ -455,8 +464,8 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.C = c.C;
   p.D = c.D;
   p.heads = c.heads;
-  p.q_tiles = (int)((c.S + QT - 1) / QT);
-  p.natural_order = (c.C % QT == 0) ? 1 : 0;
+  p.q_blocks = (int)((c.S + QB - 1) / QB);
+  p.natural_order = (c.C % QB == 0) ? 1 : 0;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);
   p.status = c.status;
   p.limit_ns = wait_limit_ns();
