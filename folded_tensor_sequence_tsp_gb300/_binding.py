@@ -207,6 +207,11 @@ def _ws(plan, ws):
     return _dev(ws, "ws", tsp_workspace_bytes(plan), dtype=torch.uint8)
 
 
+def _ws_status(ws):
+    """Workspace of a single-step call: only its 256-byte status word is used."""
+    return _dev(ws, "ws", 256, dtype=torch.uint8)
+
+
 def tsp_workspace_init(plan, ws, stream=None):
     _check(load_library().tsp_workspace_init(plan.handle, _ws(plan, ws), _stream(stream)),
            "tsp_workspace_init")
@@ -280,7 +285,7 @@ def tsp_qkv_projection(plan, shard, xs, wpack, qkv, ws, stream=None):
     _check(load_library().tsp_qkv_projection(
         plan.handle, int(shard), _dev(xs, "xs", plan.act_elems),
         _dev(wpack, "wpack", i.wpack_elems), _dev(qkv, "qkv", i.S * 3 * i.shard_hidden),
-        _ws(plan, ws), _stream(stream)), "tsp_qkv_projection")
+        _ws_status(ws), _stream(stream)), "tsp_qkv_projection")
 
 
 def tsp_kv_allgather(plan, qkv, kn, vn, stream=None):
@@ -296,7 +301,7 @@ def tsp_causal_attention(plan, shard, qkv, kn, vn, o, ws, stream=None):
     n = i.S * i.shard_hidden
     _check(load_library().tsp_causal_attention(
         plan.handle, int(shard), _dev(qkv, "qkv", 3 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
-        _dev(o, "o", plan.act_elems), _ws(plan, ws), _stream(stream)), "tsp_causal_attention")
+        _dev(o, "o", plan.act_elems), _ws_status(ws), _stream(stream)), "tsp_causal_attention")
 
 
 def tsp_o_projection(plan, o, wpack, residual, out, ws, stream=None, out32=None):
@@ -304,7 +309,7 @@ def tsp_o_projection(plan, o, wpack, residual, out, ws, stream=None, out32=None)
     _check(load_library().tsp_o_projection(
         plan.handle, _dev(o, "o", n), _dev(wpack, "wpack", plan.info.wpack_elems),
         _dev(residual, "residual", n, optional=True), _dev(out, "out", n),
-        _dev(out32, "out32", n, torch.float32, optional=True), _ws(plan, ws),
+        _dev(out32, "out32", n, torch.float32, optional=True), _ws_status(ws),
         _stream(stream)), "tsp_o_projection")
 
 
@@ -312,7 +317,7 @@ def tsp_swiglu_gate_up(plan, hs, wpack, g, ws, stream=None):
     i = plan.info
     _check(load_library().tsp_swiglu_gate_up(
         plan.handle, _dev(hs, "hs", plan.act_elems), _dev(wpack, "wpack", i.wpack_elems),
-        _dev(g, "g", i.S * i.ffn_padded), _ws(plan, ws), _stream(stream)), "tsp_swiglu_gate_up")
+        _dev(g, "g", i.S * i.ffn_padded), _ws_status(ws), _stream(stream)), "tsp_swiglu_gate_up")
 
 
 def tsp_swiglu_down(plan, g, wpack, residual, out, ws, stream=None, residual32=None):
@@ -322,7 +327,7 @@ def tsp_swiglu_down(plan, g, wpack, residual, out, ws, stream=None, residual32=N
         plan.handle, _dev(g, "g", i.S * i.ffn_padded), _dev(wpack, "wpack", i.wpack_elems),
         _dev(residual, "residual", n, optional=True),
         _dev(residual32, "residual32", n, torch.float32, optional=True), _dev(out, "out", n),
-        _ws(plan, ws), _stream(stream)), "tsp_swiglu_down")
+        _ws_status(ws), _stream(stream)), "tsp_swiglu_down")
 
 
 def tsp_device_status(ws, stream=None) -> int:

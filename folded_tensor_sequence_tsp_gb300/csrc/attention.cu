@@ -5,9 +5,9 @@
 //
 // One CTA computes two 128-row query tiles (A and B) of one head on the
 // 5th-generation tensor cores. Both tiles share every K/V tile the CTA loads.
-//   warp 0      TMA: Q_A and Q_B once, then K and V tiles of 128 keys into a
-//               3-stage K ring and a 2-stage V ring of 128B-swizzled shared
-//               memory, in the order the MMAs consume them (K_j, V_j, K_{j+1}, ...)
+//   warp 0      TMA: Q_A, Q_B and K_0 (own slot) once, then for each key tile j
+//               the pair (V_j, K_{j+1}) into a 2-stage ring of 128B-swizzled shared
+//               memory (one full and one empty barrier per pair)
 //   warp 1      allocates all 512 TMEM columns; one lane issues, per key tile j,
 //                 O_A += P_A V_j,  S_A = Q_A K_{j+1}^T,  O_B += P_B V_j,  S_B = Q_B K_{j+1}^T
 //               (S from shared-memory operands; P read from TMEM as the A operand,
@@ -16,16 +16,21 @@
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: one query row per
 //               thread (TMEM lane = row), two softmax warps per SM sub-partition so
 //               each hides the other's latencies. tcgen05.ld of the S row (four
-//               loads in flight), mask by global position, row max and sum with 8
-//               partial accumulators, P = exp2(s - m) in bf16 written over the
-//               first 64 columns of the same S with tcgen05.st; then the epilogue.
+//               loads in flight), mask by global position, row max (three-input
+//               max, 4 chains), P = exp2(s - m) with packed f32x2 argument and sum,
+//               rounded to bf16 and written over the first 64 columns of the same S
+//               with tcgen05.st; then the epilogue.
 // TMEM columns: S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512); P_X
 // occupies the first 64 columns of S_X (two bf16 per column).
 //
 // Ordering: MMAs issued by one thread execute in order, and tcgen05.commit arrives
 // once every earlier MMA of the thread has completed. So S_X(j+1) may overwrite
 // the columns P_X(j) is read from right after O_X += P_X(j) V_j is issued, and the
-// completion of S_X(j) also tells the softmax that O_X += P_X(j-1) V_{j-1} is done.
+// completion of S_X(j) also tells the softmax that O_X += P_X(j-1) V_{j-1} is done;
+// only a tile's last product is committed separately (for its epilogue). Every
+// mbarrier operation costs the issuing thread on the order of a hundred cycles, so
+// the MMA warp does three waits and three commits per key tile, and waits for the
+// next K/V stage while tile A's products run.
 //
 // Online softmax in base 2 (scores scaled by log2(e)/sqrt(d) inside the exp
 // argument). Each row keeps a reference maximum m and sum l; m only moves (and O
@@ -46,8 +51,7 @@ namespace {
 constexpr int QT = 128;       // query rows per tile (two tiles per CTA)
 constexpr int QB = 2 * QT;    // query rows per CTA
 constexpr int KT = 128;       // keys per tile
-constexpr int KSTAGES = 3;
-constexpr int VSTAGES = 2;
+constexpr int STAGES = 2;     // ring of (V_j, K_{j+1}) pairs; K_0 comes with Q
 constexpr int THREADS = 320;  // TMA warp, MMA warp, 2 x 4 softmax warps
 constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 constexpr uint32_t TM_S0 = 0, TM_O0 = 128, TM_S1 = 256, TM_O1 = 384;
@@ -61,7 +65,8 @@ template <int HD>
 struct Geometry {
   static constexpr int BOXES = HD / 64;  // 64-column boxes per 128-row block
   static constexpr uint32_t TILE_BYTES = 128 * HD * 2;
-  static constexpr size_t USED = 1024 + (size_t)(2 + KSTAGES + VSTAGES) * TILE_BYTES + 256;
+  // Q_A, Q_B, K_0, then the ring: K slots 0/1 and V slots 0/1
+  static constexpr size_t USED = 1024 + (size_t)(3 + 2 * STAGES) * TILE_BYTES + 256;
   // The CTA allocates all 512 TMEM columns, so it must be alone on its SM: ask for
   // more than half of the SM's 228 KB of shared memory.
   static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
@@ -97,6 +102,34 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// P = exp2(s * scale - m) for one row of 128 scores: bf16 pairs stored to TMEM
+// (64 columns at p_tmem); returns the row sum. The argument and the sum use packed
+// f32x2 FMA/ADD (two elements per instruction): the softmax is bound by instruction
+// issue, not by the exponential unit (moving part of the exponentials to an FMA-pipe
+// polynomial measured slower).
+__device__ __forceinline__ float exp_tile(const float (&sc)[KT], uint32_t p_tmem, float scale,
+                                          float neg_ref) {
+  const uint64_t scale2 = f2_pack(scale, scale), nref2 = f2_pack(neg_ref, neg_ref);
+  uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int c = 0; c < KT; c += 32) {
+    uint32_t r[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(sc[c + 2 * e], sc[c + 2 * e + 1]), scale2, nref2), x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      sum2[e & 3] = f2_add(sum2[e & 3], f2_pack(p0, p1));
+      r[e] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(p_tmem + (uint32_t)(c / 2), r);
+  }
+  const uint64_t s01 = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
+  float a, b;
+  f2_unpack(s01, a, b);
+  return a + b;
+}
+
 // Number of 128-key tiles the query rows [r0, r0 + QT) need (0 if none is a row).
 __device__ __forceinline__ int tiles_needed(long long r0, const AttParams& p) {
   if (r0 >= p.S) return 0;
@@ -122,17 +155,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                          // tile A, then tile B
-  uint8_t* sK = sQ + 2 * G::TILE_BYTES;        // KSTAGES tiles
-  uint8_t* sV = sK + KSTAGES * G::TILE_BYTES;  // VSTAGES tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VSTAGES * G::TILE_BYTES);
-  uint64_t* q_full = bars;               // [1]
-  uint64_t* k_full = q_full + 1;         // [KSTAGES]
-  uint64_t* k_empty = k_full + KSTAGES;  // [KSTAGES]
-  uint64_t* v_full = k_empty + KSTAGES;  // [VSTAGES]
-  uint64_t* v_empty = v_full + VSTAGES;  // [VSTAGES]
-  uint64_t* s_full = v_empty + VSTAGES;  // [2] per tile: S(j) in TMEM
+  uint8_t* sK0 = sQ + 2 * G::TILE_BYTES;      // K_0
+  uint8_t* sK = sK0 + G::TILE_BYTES;          // ring: K_{j+1} in slot j % 2
+  uint8_t* sV = sK + STAGES * G::TILE_BYTES;  // ring: V_j in slot j % 2
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * G::TILE_BYTES);
+  uint64_t* q_full = bars;               // [1] Q_A, Q_B, K_0
+  uint64_t* kv_full = q_full + 1;        // [STAGES] stage j % 2: V_j and K_{j+1}
+  uint64_t* kv_empty = kv_full + STAGES; // [STAGES]
+  uint64_t* s_full = kv_empty + STAGES;  // [2] per tile: S(j) in TMEM
   uint64_t* p_full = s_full + 2;         // [2] per tile: P(j) in TMEM (4 warps)
-  uint64_t* o_done = p_full + 2;         // [2] per tile: O += P(j) V_j complete
+  uint64_t* o_done = p_full + 2;         // [2] per tile: its last O += P V complete
   uint64_t* drain = o_done + 2;          // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -150,13 +182,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < KSTAGES; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-    }
-    for (int s = 0; s < VSTAGES; ++s) {
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -183,100 +211,113 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0 && n_tiles > 0) {
       // ------------------------------------------------------------ TMA producer
-      mbar_arrive_expect_tx(q_full, 2 * G::TILE_BYTES);
+      mbar_arrive_expect_tx(q_full, 3 * G::TILE_BYTES);
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+      for (int b = 0; b < G::BOXES; ++b) {
 #pragma unroll
-        for (int b = 0; b < G::BOXES; ++b)
+        for (int t = 0; t < 2; ++t)
           tma_load_2d(sQ + t * G::TILE_BYTES + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b,
                       (int)(row0 + t * QT));
-      int k_last[KSTAGES], v_last[VSTAGES];
+        tma_load_2d(sK0 + b * BOX_BYTES, &tmK, q_full, col_q + 64 * b, 0);
+      }
+      int last[STAGES];
 #pragma unroll
-      for (int s = 0; s < KSTAGES; ++s) k_last[s] = -1;
-#pragma unroll
-      for (int s = 0; s < VSTAGES; ++s) v_last[s] = -1;
+      for (int s = 0; s < STAGES; ++s) last[s] = -1;
       for (int j = 0; j < n_tiles; ++j) {
-        const int ks = j % KSTAGES;
-        const uint32_t kph = (uint32_t)((j / KSTAGES) & 1);
-        if (!mbar_wait(&k_empty[ks], kph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
-        mbar_arrive_expect_tx(&k_full[ks], G::TILE_BYTES);
+        // stage j % 2 takes V_j and K_{j+1}; its slots held V_{j-2} and K_{j-1}, both
+        // consumed by the MMAs of iteration j-2 (whose commit frees the stage)
+        const int st = j % STAGES;
+        const uint32_t ph = (uint32_t)((j / STAGES) & 1);
+        if (!mbar_wait(&kv_empty[st], ph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
+        const bool has_k = j + 1 < n_tiles;
+        mbar_arrive_expect_tx(&kv_full[st], (has_k ? 2u : 1u) * G::TILE_BYTES);
 #pragma unroll
-        for (int b = 0; b < G::BOXES; ++b)
-          tma_load_2d(sK + ks * G::TILE_BYTES + b * BOX_BYTES, &tmK, &k_full[ks],
+        for (int b = 0; b < G::BOXES; ++b) {
+          tma_load_2d(sV + st * G::TILE_BYTES + b * BOX_BYTES, &tmV, &kv_full[st],
                       col_q + 64 * b, j * KT);
-        k_last[ks] = (int)kph;
-        const int vs = j % VSTAGES;
-        const uint32_t vph = (uint32_t)((j / VSTAGES) & 1);
-        if (!mbar_wait(&v_empty[vs], vph ^ 1u, wb, SITE_ATT_PRODUCER)) break;
-        mbar_arrive_expect_tx(&v_full[vs], G::TILE_BYTES);
-#pragma unroll
-        for (int b = 0; b < G::BOXES; ++b)
-          tma_load_2d(sV + vs * G::TILE_BYTES + b * BOX_BYTES, &tmV, &v_full[vs],
-                      col_q + 64 * b, j * KT);
-        v_last[vs] = (int)vph;
+          if (has_k)
+            tma_load_2d(sK + st * G::TILE_BYTES + b * BOX_BYTES, &tmK, &kv_full[st],
+                        col_q + 64 * b, (j + 1) * KT);
+        }
+        last[st] = (int)ph;
       }
       WaitBound wd{p.status, p.limit_ns, nullptr};
       mbar_wait(q_full, 0, wd, SITE_DRAIN);
-      for (int s = 0; s < KSTAGES; ++s)
-        if (k_last[s] >= 0) mbar_wait(&k_full[s], (uint32_t)k_last[s], wd, SITE_DRAIN);
-      for (int s = 0; s < VSTAGES; ++s)
-        if (v_last[s] >= 0) mbar_wait(&v_full[s], (uint32_t)v_last[s], wd, SITE_DRAIN);
+      for (int s = 0; s < STAGES; ++s)
+        if (last[s] >= 0) mbar_wait(&kv_full[s], (uint32_t)last[s], wd, SITE_DRAIN);
     }
   } else if (warp == 1) {
     if (lane == 0 && n_tiles > 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc_s = make_idesc_bf16(QT, KT, false);
       const uint32_t idesc_o = make_idesc_bf16(QT, HD, true);
+      // base descriptors, built once; each MMA adds a compile-time offset (>> 4) to
+      // the low word. K-major operands: 16-element K steps are 32 B inside a 128 B
+      // swizzle row, 64-element blocks BOX_BYTES apart. V (MN-major): 16-key steps
+      // are 2048 B, 64-column blocks BOX_BYTES apart (LBO), 8-row groups 1 KB (SBO).
+      const uint64_t dq0 = make_sdesc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t dk0 = make_sdesc_sw128(smem_addr(sK0), 16, 1024);
+      const uint64_t dv0 = make_sdesc_sw128(smem_addr(sV), BOX_BYTES, 1024);
+      const uint32_t q_hi = (uint32_t)(dq0 >> 32), k_hi = (uint32_t)(dk0 >> 32);
+      const uint32_t v_hi = (uint32_t)(dv0 >> 32);
+      constexpr uint32_t TILE16 = G::TILE_BYTES >> 4;
       // S_t = Q_t K_j^T
       auto issue_s = [&](int t, int j) {
-        const uint32_t q_addr = smem_addr(sQ + t * G::TILE_BYTES);
-        const uint32_t k_addr = smem_addr(sK + (j % KSTAGES) * G::TILE_BYTES);
+        const uint32_t a_lo = (uint32_t)dq0 + (uint32_t)t * TILE16;
+        // K_0 in its own slot right before the ring; K_j (j >= 1) in ring slot (j-1) % 2
+        const uint32_t b_lo = (uint32_t)dk0 + (j == 0 ? 0u : (uint32_t)(1 + (j - 1) % STAGES) * TILE16);
+        const uint32_t d = tmem + tm_s(t);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * BOX_BYTES + (kk & 3) * 32);
-          mma_ss(tmem + tm_s(t), make_sdesc_sw128(q_addr + off, 16, 1024),
-                 make_sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (uint32_t)(((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4);
+          mma_ss_w(d, a_lo + off, q_hi, b_lo + off, k_hi, idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t]);
       };
-      // O_t += P_t V_j; B = V: 16 keys x HD columns per step, MN-major (64-column
-      // blocks BOX_BYTES apart, 8-row groups 1024 B apart); A = P: 8 packed columns
+      // O_t += P_t V_j; A = P: 16 keys = 8 packed TMEM columns per step
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr = smem_addr(sV + (j % VSTAGES) * G::TILE_BYTES);
+        const uint32_t b_lo = (uint32_t)dv0 + (uint32_t)(j % STAGES) * TILE16;
+        const uint32_t d = tmem + tm_o(t), a = tmem + tm_s(t);
+        const uint32_t first = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
-          mma_ts(tmem + tm_o(t), tmem + tm_s(t) + (uint32_t)(kk * 8),
-                 make_sdesc_sw128(v_addr + (uint32_t)(kk * 2048), BOX_BYTES, 1024), idesc_o,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&o_done[t]);
+          mma_ts_w(d, a + (uint32_t)(kk * 8), b_lo + (uint32_t)(kk * (2048 >> 4)), v_hi, idesc_o,
+                   kk > 0 ? 1u : first);
       };
-      bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA) && mbar_wait(&k_full[0], 0, wb, SITE_ATT_MMA);
+      bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA);
       if (ok) {
         tc_fence_after();
         if (n_a > 0) issue_s(0, 0);
         if (n_b > 0) issue_s(1, 0);
-        mma_commit(&k_empty[0]);
+        ok = mbar_wait(&kv_full[0], 0, wb, SITE_ATT_MMA);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!mbar_wait(&v_full[j % VSTAGES], (uint32_t)((j / VSTAGES) & 1), wb, SITE_ATT_MMA)) break;
-        const bool next_k = j + 1 < n_tiles;
-        if (next_k && !mbar_wait(&k_full[(j + 1) % KSTAGES], (uint32_t)(((j + 1) / KSTAGES) & 1),
-                                 wb, SITE_ATT_MMA))
-          break;
+        // stage j % 2 (V_j, K_{j+1}) has landed
         for (int t = 0; t < 2; ++t) {
           const int nt = t ? n_b : n_a;
-          if (j >= nt) continue;
-          if (!mbar_wait(&p_full[t], (uint32_t)(j & 1), wb, SITE_ATT_MMA)) {
+          if (j < nt) {
+            if (!mbar_wait(&p_full[t], (uint32_t)(j & 1), wb, SITE_ATT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, j);
+            if (j + 1 < nt) {
+              issue_s(t, j + 1);
+            } else {
+              mma_commit(&o_done[t]);  // the tile's last product
+            }
+          }
+          // while tile A's products run, wait for the next stage
+          if (t == 0 && j + 1 < n_tiles &&
+              !mbar_wait(&kv_full[(j + 1) % STAGES], (uint32_t)(((j + 1) / STAGES) & 1), wb,
+                         SITE_ATT_MMA)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < nt) issue_s(t, j + 1);
         }
         if (!ok) break;
-        mma_commit(&v_empty[j % VSTAGES]);
-        if (next_k) mma_commit(&k_empty[(j + 1) % KSTAGES]);
+        mma_commit(&kv_empty[j % STAGES]);  // V_j and K_{j+1} are consumed
       }
       mma_commit(drain);
       WaitBound wd{p.status, p.limit_ns, nullptr};
@@ -332,14 +373,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int e = 0; e < KT; ++e)
           if (kv0 + e > pos) sc[e] = -INFINITY;
       }
-      // row maximum with 8 independent partial maxima (short dependency chains)
-      float m8[8];
+      // row maximum: three-input max, 4 independent chains (short dependency chains)
+      float m4[4] = {sc[0], sc[1], sc[2], sc[3]};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m8[e] = sc[e];
+      for (int e = 4; e < KT; e += 8) {
 #pragma unroll
-      for (int e = 8; e < KT; ++e) m8[e & 7] = fmaxf(m8[e & 7], sc[e]);
-      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int k = 0; k < 4; ++k) m4[k] = max3f(m4[k], sc[e + k], sc[e + 4 + k]);
+      }
+      const float mraw = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       const float mx = mraw * p.scale_log2;  // scale > 0 keeps the order
       // move the reference only when the tile maximum outgrows it by the threshold
       float factor = 1.f;
@@ -366,30 +407,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st16(o_tmem + c + 16, hi);
         }
       }
-      // P = exp2(s*scale - m) in bf16 over the first 64 columns of S
-      float sum8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < KT; c += 32) {
-        uint32_t r[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(sc[c + 2 * e], p.scale_log2, neg_ref));
-          const float p1 = ex2(fmaf(sc[c + 2 * e + 1], p.scale_log2, neg_ref));
-          sum8[e & 7] += p0 + p1;
-          r[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(s_tmem + (uint32_t)(c / 2), r);
-      }
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      // P = exp2(s*scale - m) in bf16 over the first 64 columns of S (masked keys: 0)
+      l += exp_tile(sc, s_tmem, p.scale_log2, neg_ref);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && my_tiles > 0 && warp_wait(&o_done[t], (uint32_t)((my_tiles - 1) & 1))) {
+    if (ok && my_tiles > 0 && warp_wait(&o_done[t], 0u)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* dst = p.o + grow * p.ld_o + p.o_col0 + col_q;

@@ -165,6 +165,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc = make_idesc_bf16(BM, BN, false);
+      // base descriptors of stage 0, built once; stages and K steps add offsets
+      const uint64_t da0 = make_sdesc_sw128(smem_addr(sA), 16, 1024);
+      const uint64_t db0 = make_sdesc_sw128(smem_addr(sB), 16, 1024);
+      const uint32_t da_lo = (uint32_t)da0, da_hi = (uint32_t)(da0 >> 32);
+      const uint32_t db_lo = (uint32_t)db0, db_hi = (uint32_t)(db0 >> 32);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -180,14 +185,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(sA + stage * A_BYTES);
-          const uint32_t b0 = smem_addr(sB + stage * B_BYTES);
+          const uint32_t a_lo = da_lo + (uint32_t)stage * (A_BYTES >> 4);
+          const uint32_t b_lo = db_lo + (uint32_t)stage * (B_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = make_sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = make_sdesc_sw128(b0 + kk * 32, 16, 1024);
-            mma_ss(d_tmem, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)  // 16-element K steps: +32 B
+            mma_ss_w(d_tmem, a_lo + kk * 2, da_hi, b_lo + kk * 2, db_hi, idesc,
+                     (i | kk) != 0 ? 1u : 0u);
           mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;

@@ -194,6 +194,8 @@ tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf
 
 /* ---------------------------------------------------------------------------
  * Single steps of the hot path. The *_fwd calls above are compositions of these.
+ * In these calls `ws` only provides the status word of the bounded device waits:
+ * 256 bytes (256-byte aligned, zeroed once) are enough.
  * ------------------------------------------------------------------------- */
 
 /*
