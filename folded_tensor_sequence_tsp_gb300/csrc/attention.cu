@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r_local = q * 32 + lane;
     const long long grow = row0 + t * QT + r_local;
     const bool row_ok = grow < p.S;
-    const long long pos = row_ok ? row_pos(grow, p.C, p.T, p.D) : -1;
+    // S < 2^30 (checked at launch): positions fit in int
+    const int pos = row_ok ? (int)row_pos(grow, p.C, p.T, p.D) : -1;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t s_tmem = lane_base + tm_s(t);
     const uint32_t o_tmem = lane_base + tm_o(t);
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           sc[96 + e] = __uint_as_float(rd[e]);
         }
       }
-      const long long kv0 = (long long)j * KT;
+      const int kv0 = j * KT;
       if (kv0 + KT - 1 > pos) {
 #pragma unroll
         for (int e = 0; e < KT; ++e)
@@ -392,19 +393,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
       l *= factor;
       if (j > 0 && __any_sync(0xffffffffu, rescale && factor != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(o_tmem + c, r);
+        // 16 columns at a time: the 128 scores stay live in registers meanwhile
+#pragma unroll 1
+        for (int c = 0; c < HD; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(o_tmem + c, r);
           tmem_ld_wait();
-          uint32_t lo[16], hi[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            lo[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
-            hi[e] = __float_as_uint(__uint_as_float(r[16 + e]) * factor);
-          }
-          tmem_st16(o_tmem + c, lo);
-          tmem_st16(o_tmem + c + 16, hi);
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+          tmem_st16(o_tmem + c, r);
         }
       }
       // P = exp2(s*scale - m) in bf16 over the first 64 columns of S (masked keys: 0)
