@@ -258,6 +258,20 @@ tsp_status mlp_block(const Plan& p, const void* hs, const void* wpack, const voi
   return swiglu_down(p, g, wpack, residual, residual_f32, out, ws, s);
 }
 
+// Device-side alias of a page-locked (pinned or registered) host buffer, or NULL if
+// the runtime does not map it (pageable memory).
+const void* mapped_host_alias(const void* host) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, host);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return nullptr;
+  if (reinterpret_cast<uintptr_t>(attr.devicePointer) & 15u) return nullptr;
+  return attr.devicePointer;
+}
+
 tsp_status check_plan(tsp_plan_t plan) {
   return plan ? TSP_OK : fail(TSP_ERR_INVALID_ARG, "null plan");
 }
@@ -471,14 +485,27 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
   const size_t bytes = (size_t)p.S * p.H * 2;
   void* a = at<void>(ws, p.ws.stage_in);
   void* b = at<void>(ws, p.ws.stage_out);
-  cudaError_t e = cudaMemcpyAsync(a, x_host, bytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy in");
-  TSP_TRY(launch_zigzag_rows(p, a, b, p.H, true, s));  // b = shard(x)
+  // Page-locked host memory that the runtime maps into the device address space is
+  // read and written by the zigzag kernels themselves (the copy and the permutation
+  // in one pass over the host link); other host memory goes through staging copies.
+  const void* x_dev = mapped_host_alias(x_host);
+  void* out_dev = const_cast<void*>(mapped_host_alias(out_host));
+  if (x_dev) {
+    TSP_TRY(launch_zigzag_rows(p, x_dev, b, p.H, true, s));  // b = shard(x), read from host
+  } else {
+    cudaError_t e = cudaMemcpyAsync(a, x_host, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy in");
+    TSP_TRY(launch_zigzag_rows(p, a, b, p.H, true, s));  // b = shard(x)
+  }
   TSP_TRY(tsp_layer_fwd(plan, static_cast<const tsp_bf16*>(b), wpack, static_cast<tsp_bf16*>(a),
-                        ws, stream));                   // a = layer(b)
-  TSP_TRY(launch_zigzag_rows(p, a, b, p.H, false, s));  // b = unshard(a)
-  e = cudaMemcpyAsync(out_host, b, bytes, cudaMemcpyDeviceToHost, s);
-  if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy out");
+                        ws, stream));  // a = layer(b)
+  if (out_dev) {
+    TSP_TRY(launch_zigzag_rows(p, a, out_dev, p.H, false, s));  // unshard into host memory
+  } else {
+    TSP_TRY(launch_zigzag_rows(p, a, b, p.H, false, s));  // b = unshard(a)
+    cudaError_t e = cudaMemcpyAsync(out_host, b, bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy out");
+  }
   return TSP_OK;
 }
 

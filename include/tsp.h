@@ -161,10 +161,12 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
 
 /*
  * tsp_layer_fwd_host - the whole layer from and to HOST memory in natural token
- * order: copies x_host [S][H] to the device, shards it, runs tsp_layer_fwd,
- * unshards and copies the result to out_host [S][H]. Host buffers should be
- * pinned (page-locked) for the copies to be asynchronous; the call returns once
- * the work is enqueued, so synchronise `stream` before reading out_host.
+ * order: x_host [S][H] in, out_host [S][H] out. Page-locked host buffers (pinned
+ * or registered, i.e. mapped into the device address space) are read and written
+ * by the zigzag shard/unshard kernels directly over the host link, so the copy and
+ * the permutation are one pass; pageable buffers are staged through
+ * cudaMemcpyAsync and the workspace. The call returns once the work is enqueued:
+ * synchronise `stream` before reading out_host.
  */
 tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
                               tsp_bf16* out_host, void* ws, void* stream);

@@ -88,14 +88,19 @@ def test_output_is_the_same_for_every_D():
         assert_close(outs[D], outs[1], f"D={D} vs D=1", scale=scale, max_abs=atol)
 
 
-def test_host_entry_point_matches_device_path():
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_entry_point_matches_device_path(pinned):
+    """Pinned buffers are read/written by the kernels directly, pageable ones are
+    staged through copies: both give the device path's bits."""
     L = Layer(*SHAPES["d3"], seed=8)
     xs = L.sharded_x()
     out = L.act()
     tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
     want = bits(_unshard(L, out))
-    x_host = torch.from_numpy(L.bits["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
+    x_host = torch.from_numpy(L.bits["x"].view(np.int16).copy()).view(torch.bfloat16)
+    out_host = torch.full_like(x_host, float("nan"))
+    if pinned:
+        x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
     tsp.tsp_layer_fwd_host(L.plan, x_host, L.wpack, out_host, L.ws)
     torch.cuda.current_stream().synchronize()
     L.check_status()
