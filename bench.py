@@ -43,9 +43,13 @@ import tsp_inputs  # noqa: E402
 METRIC = "TSP layer fwd tokens/s and TFLOP/s (frac of bf16 TC peak) on 1 GB300"
 DEFAULT_WORKLOAD = "7b-64k"
 
-# DRAM bytes (read + write) per launch from an ncu capture of the kernel as it is
-# now, keyed by kernel; None until a capture of the current kernel exists.
-NCU_TRAFFIC_BYTES = {}
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it is
+# now (profiles/ holds the summaries: 7B shape, 64K tokens, per launch); a kernel
+# missing here has no capture of its current version.
+NCU_TRAFFIC_BYTES = {
+    "attention": 203_879_680 + 51_173_376,      # profiles/attention_7b-64k.md
+    "gemm_gate_up": 3_582_997_000 + 1_464_174_000,  # profiles/gemm_gate_up_7b-64k.md
+}
 
 
 def algorithmic_flops(S, H, F):
