@@ -22,7 +22,8 @@ __all__ = [
     "tsp_plan", "tsp_get_plan_info", "tsp_workspace_bytes", "tsp_packed_weight_bytes",
     "tsp_workspace_init", "tsp_pack_weights", "tsp_shard_index", "tsp_shard", "tsp_unshard",
     "tsp_attention_fwd", "tsp_mlp_fwd", "tsp_mlp_fwd_noalloc", "tsp_layer_fwd", "tsp_layer_fwd_host",
-    "tsp_qkv_projection", "tsp_kv_allgather", "tsp_causal_attention", "tsp_o_projection",
+    "tsp_qkv_projection", "tsp_qkv_projection_gathered", "tsp_kv_allgather",
+    "tsp_causal_attention", "tsp_causal_attention_q", "tsp_o_projection",
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
     "tsp_last_error",
 ]
@@ -77,6 +78,8 @@ _SIGS = {
     "tsp_layer_fwd_host": (_I, [_P] * 6),
     "tsp_qkv_projection": (_I, [_P, _I, _P, _P, _P, _P, _P]),
     "tsp_kv_allgather": (_I, [_P] * 5),
+    "tsp_qkv_projection_gathered": (_I, [_P, _I] + [_P] * 7),
+    "tsp_causal_attention_q": (_I, [_P, _I] + [_P] * 6),
     "tsp_causal_attention": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
     "tsp_o_projection": (_I, [_P] * 8),
     "tsp_swiglu_gate_up": (_I, [_P] * 6),
@@ -286,6 +289,23 @@ def tsp_qkv_projection(plan, shard, xs, wpack, qkv, ws, stream=None):
         plan.handle, int(shard), _dev(xs, "xs", plan.act_elems),
         _dev(wpack, "wpack", i.wpack_elems), _dev(qkv, "qkv", i.S * 3 * i.shard_hidden),
         _ws_status(ws), _stream(stream)), "tsp_qkv_projection")
+
+
+def tsp_qkv_projection_gathered(plan, shard, xs, wpack, q, kn, vn, ws, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    _check(load_library().tsp_qkv_projection_gathered(
+        plan.handle, int(shard), _dev(xs, "xs", plan.act_elems),
+        _dev(wpack, "wpack", i.wpack_elems), _dev(q, "q", n), _dev(kn, "kn", n),
+        _dev(vn, "vn", n), _ws_status(ws), _stream(stream)), "tsp_qkv_projection_gathered")
+
+
+def tsp_causal_attention_q(plan, shard, q, kn, vn, o, ws, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    _check(load_library().tsp_causal_attention_q(
+        plan.handle, int(shard), _dev(q, "q", n), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _dev(o, "o", plan.act_elems), _ws_status(ws), _stream(stream)), "tsp_causal_attention_q")
 
 
 def tsp_kv_allgather(plan, qkv, kn, vn, stream=None):

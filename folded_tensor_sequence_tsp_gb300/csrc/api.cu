@@ -143,11 +143,42 @@ tsp_status qkv_projection(const Plan& p, int k, const void* xs, const void* wpac
   return launch_gemm(c, s);
 }
 
-tsp_status causal_attention(const Plan& p, int k, const void* qkv, const void* kn, const void* vn,
-                            void* o, void* ws, cudaStream_t s) {
+// Q/K/V projection of shard k with the K/V all-gather fused into the epilogue: Q
+// rows stay in sharded order in q [S][H/D]; K and V rows land at their natural token
+// positions in kn, vn [S][H/D].
+tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
+                                   void* q, void* kn, void* vn, void* ws, cudaStream_t s) {
+  GemmCall c{};
+  c.epi = EPI_QKV_SPLIT;
+  c.A = xs;
+  c.lda = p.H;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;
+  c.ldb = p.H;
+  c.b_rows = 3LL * p.H;
+  c.b_row0 = (int64_t)k * 3 * p.Hd;
+  c.N = 3LL * p.Hd;
+  c.K = p.H;
+  c.C = q;
+  c.ldc = p.Hd;
+  c.split_k = kn;
+  c.split_v = vn;
+  c.split_ld = p.Hd;
+  c.split_hd = p.Hd;
+  c.zz_C = p.C;
+  c.zz_T = p.T;
+  c.zz_D = p.D;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+// q holds the Q columns of the shard's heads, row stride ld_q (3H/D for the Q|K|V
+// buffer of tsp_qkv_projection, H/D for the Q buffer of the gathered projection).
+tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
+                            const void* vn, void* o, void* ws, cudaStream_t s) {
   AttentionCall a{};
   a.qkv = qkv;
-  a.ld_qkv = 3LL * p.Hd;
+  a.ld_qkv = ld_q;
   a.kn = kn;
   a.vn = vn;
   a.ld_kv = p.Hd;
@@ -239,14 +270,14 @@ tsp_status swiglu_down(const Plan& p, const void* g, const void* wpack, const vo
 
 tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,
                            void* out, void* out32, void* ws, cudaStream_t s) {
-  void* qkv = at<void>(ws, p.ws.qkv);
+  void* q = at<void>(ws, p.ws.qkv);
   void* kn = at<void>(ws, p.ws.kn);
   void* vn = at<void>(ws, p.ws.vn);
   void* o = at<void>(ws, p.ws.o);
   for (int k = 0; k < p.D; ++k) {  // broadcast iteration k: every rank reads shard k
-    TSP_TRY(qkv_projection(p, k, xs, wpack, qkv, ws, s));
-    TSP_TRY(launch_kv_gather(p, qkv, kn, vn, s));
-    TSP_TRY(causal_attention(p, k, qkv, kn, vn, o, ws, s));
+    // local projections, with the all-gather of K/V written by the GEMM epilogue
+    TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, q, kn, vn, ws, s));
+    TSP_TRY(causal_attention(p, k, q, p.Hd, kn, vn, o, ws, s));
   }
   return o_projection(p, o, wpack, residual, out, out32, ws, s);
 }
@@ -518,6 +549,30 @@ tsp_status tsp_qkv_projection(tsp_plan_t plan, int shard, const tsp_bf16* xs,
   return qkv_projection(plan->p, shard, xs, wpack, qkv, ws, static_cast<cudaStream_t>(stream));
 }
 
+tsp_status tsp_qkv_projection_gathered(tsp_plan_t plan, int shard, const tsp_bf16* xs,
+                                       const tsp_bf16* wpack, tsp_bf16* q, tsp_bf16* kn,
+                                       tsp_bf16* vn, void* ws, void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, q, kn, vn}, "tsp_qkv_projection_gathered"));
+  TSP_TRY(check_ws(ws, "tsp_qkv_projection_gathered"));
+  if (shard < 0 || shard >= plan->p.D)
+    return fail(TSP_ERR_INVALID_ARG, "tsp_qkv_projection_gathered: shard out of range");
+  return qkv_projection_gathered(plan->p, shard, xs, wpack, q, kn, vn, ws,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_causal_attention_q(tsp_plan_t plan, int shard, const tsp_bf16* q,
+                                  const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o, void* ws,
+                                  void* stream) {
+  TSP_TRY(check_plan(plan));
+  TSP_TRY(check_ptrs({q, kn, vn, o}, "tsp_causal_attention_q"));
+  TSP_TRY(check_ws(ws, "tsp_causal_attention_q"));
+  if (shard < 0 || shard >= plan->p.D)
+    return fail(TSP_ERR_INVALID_ARG, "tsp_causal_attention_q: shard out of range");
+  return causal_attention(plan->p, shard, q, plan->p.Hd, kn, vn, o, ws,
+                          static_cast<cudaStream_t>(stream));
+}
+
 tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, tsp_bf16* vn,
                             void* stream) {
   TSP_TRY(check_plan(plan));
@@ -532,7 +587,8 @@ tsp_status tsp_causal_attention(tsp_plan_t plan, int shard, const tsp_bf16* qkv,
   TSP_TRY(check_ptrs({qkv, kn, vn, o}, "tsp_causal_attention"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention"));
   if (shard < 0 || shard >= plan->p.D) return fail(TSP_ERR_INVALID_ARG, "tsp_causal_attention: shard out of range");
-  return causal_attention(plan->p, shard, qkv, kn, vn, o, ws, static_cast<cudaStream_t>(stream));
+  return causal_attention(plan->p, shard, qkv, 3LL * plan->p.Hd, kn, vn, o, ws,
+                          static_cast<cudaStream_t>(stream));
 }
 
 tsp_status tsp_o_projection(tsp_plan_t plan, const tsp_bf16* o, const tsp_bf16* wpack,

@@ -45,6 +45,7 @@ enum Kind {
   K_SWIGLU = 2,         // C = bf16(silu(acc_gate) * acc_up)
   K_RES_BF16_OUT32 = 3, // C = bf16(acc + R), C32 = acc + R (fp32), R bf16
   K_RES_F32 = 4,        // C = bf16(acc + R), R fp32
+  K_QKV_SPLIT = 5,      // Q|K|V columns: Q to C (sharded rows), K and V to natural rows
 };
 
 struct GemmParams {
@@ -55,6 +56,14 @@ struct GemmParams {
   const void* R;   // residual: bf16 or fp32 depending on the variant
   long long ldr;
   float* C32;      // fp32 copy of the output (K_RES_BF16_OUT32)
+  // K_QKV_SPLIT: column sections of width split_hd (Q, K, V); K and V rows go to the
+  // natural token position of the sharded row (zigzag inverse with chunk zz_C, T zz_T)
+  __nv_bfloat16* split_k;
+  __nv_bfloat16* split_v;
+  long long split_ld;
+  int split_hd;
+  long long zz_C, zz_T;
+  int zz_D;
   int ring_rows;
   int ring_kblocks;
   int group_m;  // tile order: group_m row blocks walk down each column block in turn
@@ -237,6 +246,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const long long row = (long long)mt * BM + r_in_tile;
       const bool row_ok = row < p.M;
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      long long nat = 0;  // natural token position of this row (K_QKV_SPLIT)
+      if constexpr (EPI == K_QKV_SPLIT) {
+        const long long rank = row / p.zz_T, l = row - rank * p.zz_T;
+        nat = l < p.zz_C ? rank * p.zz_C + l : (2 * p.zz_D - 1 - rank) * p.zz_C + (l - p.zz_C);
+      }
       if constexpr (EPI == K_SWIGLU) {
         // columns [0,128) of the tile are gate rows (W1), [128,256) up rows (W3)
         const int half_n = p.N >> 1;
@@ -305,7 +319,17 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int w = 0; w < 8; ++w)
                 c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
             }
-            store_row32(p.C + row * p.ldc + col, f);
+            if constexpr (EPI == K_QKV_SPLIT) {
+              // a 32-column chunk never straddles sections (split_hd % 32 == 0)
+              const int sec = col / p.split_hd;
+              const int lc = col - sec * p.split_hd;
+              if (sec == 0)
+                store_row32(p.C + row * p.ldc + lc, f);
+              else
+                store_row32((sec == 1 ? p.split_k : p.split_v) + nat * p.split_ld + lc, f);
+            } else {
+              store_row32(p.C + row * p.ldc + col, f);
+            }
           }
         }
       }
@@ -357,6 +381,12 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   if (c.epi == EPI_RESIDUAL && !c.R) return fail(TSP_ERR_INVALID_ARG, "gemm: residual missing");
   if (c.C32 && (c.epi != EPI_RESIDUAL || c.residual_f32))
     return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 output needs a bf16 residual");
+  if (c.epi == EPI_QKV_SPLIT &&
+      (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N != 3 * c.split_hd ||
+       c.ldc < c.split_hd || c.split_ld < c.split_hd || (c.split_ld % 8) || !aligned16(c.split_k) ||
+       !aligned16(c.split_v) || c.zz_C <= 0 || c.zz_T != 2 * c.zz_C || c.zz_D <= 0 ||
+       c.M != c.zz_T * c.zz_D))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: bad Q/K/V split arguments");
   if (c.M > (1ll << 30) || c.N > (1ll << 30) || c.K > (1ll << 30) || c.b_rows > (1ll << 30))
     return fail(TSP_ERR_UNSUPPORTED, "gemm: dimension too large");
   if (c.ring_rows > 0 && (c.ring_kblocks <= 0))
@@ -379,6 +409,13 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   p.R = c.R;
   p.ldr = c.ldr;
   p.C32 = static_cast<float*>(c.C32);
+  p.split_k = static_cast<__nv_bfloat16*>(c.split_k);
+  p.split_v = static_cast<__nv_bfloat16*>(c.split_v);
+  p.split_ld = c.split_ld;
+  p.split_hd = (int)c.split_hd;
+  p.zz_C = c.zz_C;
+  p.zz_T = c.zz_T;
+  p.zz_D = c.zz_D;
   p.ring_rows = (int)c.ring_rows;
   p.ring_kblocks = (int)c.ring_kblocks;
   // Tile order. If B fits easily in the 129 MB L2 (<= 48 MB), walk row-major: A is
@@ -400,6 +437,7 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   switch (c.epi) {
     case EPI_STORE: return launch_epi<K_STORE>(ta, tb, p, grid, stream);
     case EPI_SWIGLU: return launch_epi<K_SWIGLU>(ta, tb, p, grid, stream);
+    case EPI_QKV_SPLIT: return launch_epi<K_QKV_SPLIT>(ta, tb, p, grid, stream);
     case EPI_RESIDUAL:
       if (c.residual_f32) return launch_epi<K_RES_F32>(ta, tb, p, grid, stream);
       if (c.C32) return launch_epi<K_RES_BF16_OUT32>(ta, tb, p, grid, stream);

@@ -59,7 +59,7 @@ unsigned long long wait_limit_ns();  // bound of the device-side waits
 // ---------------------------------------------------------------- launchers
 // C[M][N] = A[M][K] * B[N][K]^T with the epilogues below. A rows have stride lda
 // elements; B is rows [b_row0, b_row0 + N) of a [b_rows][K] matrix (stride ldb).
-enum GemmEpilogue { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2 };
+enum GemmEpilogue { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_QKV_SPLIT = 3 };
 
 struct GemmCall {
   int epi;
@@ -71,6 +71,11 @@ struct GemmCall {
   const void* R; int64_t ldr;  // residual (EPI_RESIDUAL): bf16, or fp32 if residual_f32
   int residual_f32;
   void* C32;                   // optional fp32 copy of the output (EPI_RESIDUAL, bf16 residual), row stride ldc
+  // EPI_QKV_SPLIT: the N = 3 split_hd columns are Q | K | V; Q rows go to C (ldc),
+  // K and V rows to split_k / split_v (row stride split_ld) at the natural token
+  // position of the sharded row (zigzag chunk zz_C, tokens per rank zz_T, zz_D ranks)
+  void* split_k; void* split_v; int64_t split_ld; int64_t split_hd;
+  int64_t zz_C, zz_T; int zz_D;
   int64_t ring_rows;           // rows per rank for the ring K order, 0 = natural order
   int64_t ring_kblocks;        // 64-wide K blocks per shard
   DevStatus* status;

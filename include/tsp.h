@@ -219,6 +219,18 @@ tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, 
                             void* stream);
 
 /*
+ * tsp_qkv_projection_gathered - the local projections of broadcast iteration k with
+ * the K/V all-gather fused into the GEMM epilogue (the two steps above in one
+ * pass, bit-identical to them): Q rows stay in the sharded order in q [D*T][H/D]
+ * (head-major, d columns per head); the K and V rows of every rank are written at
+ * their natural token positions in kn, vn [S][H/D]. tsp_attention_fwd and
+ * tsp_layer_fwd use this step.
+ */
+tsp_status tsp_qkv_projection_gathered(tsp_plan_t plan, int shard, const tsp_bf16* xs,
+                                       const tsp_bf16* wpack, tsp_bf16* q, tsp_bf16* kn,
+                                       tsp_bf16* vn, void* ws, void* stream);
+
+/*
  * tsp_causal_attention - step "FlashAttention" for heads group k ([TSP] s2): every
  * query row of qkv (zigzag row, global position from the zigzag map) attends to
  * kn/vn rows 0..position. Writes o[row][k*H/D + j*d + c] for the h/D heads j of
@@ -227,6 +239,12 @@ tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, 
 tsp_status tsp_causal_attention(tsp_plan_t plan, int shard, const tsp_bf16* qkv,
                                 const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
                                 void* ws, void* stream);
+
+/* tsp_causal_attention_q - the same step with Q from the q [D*T][H/D] buffer of
+ * tsp_qkv_projection_gathered instead of the Q columns of a Q|K|V buffer. */
+tsp_status tsp_causal_attention_q(tsp_plan_t plan, int shard, const tsp_bf16* q,
+                                  const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
+                                  void* ws, void* stream);
 
 /*
  * tsp_o_projection - O projection with local accumulation over the attention

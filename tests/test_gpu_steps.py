@@ -112,6 +112,40 @@ def test_kv_allgather_bit_exact(layer):
     assert np.array_equal(bits(vn), oracle.unshard_tokens(sh[:, :, 2 * Hd:], i.D))
 
 
+def test_qkv_projection_gathered_bit_exact(layer):
+    """The fused projection + all-gather equals the two steps run separately."""
+    i = layer.info
+    Hd = i.shard_hidden
+    xs = layer.sharded_x()
+    qkv = torch.empty((i.S, 3 * Hd), dtype=torch.bfloat16, device="cuda")
+    kn, vn = (torch.empty((i.S, Hd), dtype=torch.bfloat16, device="cuda") for _ in range(2))
+    q, kn2, vn2 = (torch.full((i.S, Hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+                   for _ in range(3))
+    for k in sorted({0, i.D - 1}):
+        tsp.tsp_qkv_projection(layer.plan, k, xs, layer.wpack, qkv, layer.ws)
+        tsp.tsp_kv_allgather(layer.plan, qkv, kn, vn)
+        tsp.tsp_qkv_projection_gathered(layer.plan, k, xs, layer.wpack, q, kn2, vn2, layer.ws)
+        assert torch.equal(q.view(torch.int16), qkv[:, :Hd].contiguous().view(torch.int16))
+        assert torch.equal(kn2.view(torch.int16), kn.view(torch.int16))
+        assert torch.equal(vn2.view(torch.int16), vn.view(torch.int16))
+    layer.check_status()
+
+
+def test_causal_attention_q_buffer_matches(layer):
+    """Attention reading Q from the Q-only buffer gives the Q|K|V buffer's result."""
+    i = layer.info
+    Hd = i.shard_hidden
+    q_bits = rand_bits((i.S, 3 * Hd), 35)
+    k_bits, v_bits = rand_bits((i.S, Hd), 36), rand_bits((i.S, Hd), 37)
+    o1 = torch.zeros((i.S, i.hidden), dtype=torch.bfloat16, device="cuda")
+    o2 = torch.zeros_like(o1)
+    tsp.tsp_causal_attention(layer.plan, 0, dev(q_bits), dev(k_bits), dev(v_bits), o1, layer.ws)
+    tsp.tsp_causal_attention_q(layer.plan, 0, dev(np.ascontiguousarray(q_bits[:, :Hd])),
+                               dev(k_bits), dev(v_bits), o2, layer.ws)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    layer.check_status()
+
+
 def test_causal_attention(layer):
     i = layer.info
     Hd, d, hpr = i.shard_hidden, i.head_dim, i.heads // i.D
