@@ -65,6 +65,23 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def reduce_max(value, device="cpu"):
+    """Maximum of a per-rank value over all ranks (the job's time is its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_replica, ms_per_step):
+    """Whole-job throughput: every replica processes its own layer of tokens_per_replica
+    tokens; the step takes as long as the slowest replica (ms_per_step, max over ranks)."""
+    return world * tokens_per_replica / (ms_per_step * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -208,11 +225,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, "cuda")
 
     # ---- headline: K whole-layer steps
     for _ in range(args.warmup):
@@ -349,7 +362,7 @@ def run_ours(args, world, rank, local):
     tflops = algorithmic_flops(S, H, F) / (ms * 1e-3) / 1e12
     result = {
         "metric": METRIC,
-        "value": round(world * S / (ms * 1e-3), 1),
+        "value": round(job_tokens_per_s(world, S, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -370,7 +383,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "kernels": kernels,
         "composed_equals_layer_fwd": bool(same),
-        "e2e": {"value": round(world * S / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, S, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": S * H * 2, "d2h_bytes_per_step": S * H * 2},
         "gpu_launches": launches_per_step * args.steps,

@@ -54,6 +54,27 @@ def test_layer_matches_oracle(name):
     assert_close(f64(_unshard(L, out)), ref["out"], f"{name} out", scale=s, max_abs=atol)
 
 
+@pytest.mark.parametrize("shape", [
+    (1, 2, 64, 1, 8),          # one rank, two tokens: a single partial tile everywhere
+    (16, 64, 1024, 16, 1024),  # zigzag chunks of 2 tokens, 4 tokens per rank
+    (64, 128, 4096, 64, 512),  # D = 64: one head and 8 ffn columns per shard
+    (2, 4, 128, 2, 2),         # ffn of 1 column per shard (padded to 64)
+], ids=["S2", "chunk2", "D64", "ffn2"])
+def test_extreme_shapes_match_oracle(shape):
+    L = Layer(*shape, seed=12)
+    xs = L.sharded_x()
+    attn, out = L.act(), L.act()
+    tsp.tsp_attention_fwd(L.plan, xs, L.wpack, attn, L.ws)
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    L.check_status()
+    ref = oracle.layer_forward(L.f("x"), L.weights64(), L.info.heads)
+    assert_close(f64(_unshard(L, attn)), ref["attn"], "attn")
+    W = L.weights64()
+    s, atol = layer_tolerance(ref["out"], oracle.swiglu_gate(ref["h"], W["W1"], W["W3"]),
+                              ref["h"], W)
+    assert_close(f64(_unshard(L, out)), ref["out"], "out", scale=s, max_abs=atol)
+
+
 @pytest.mark.parametrize("name", ["tiny", "d3", "small"])
 def test_mlp_block_matches_oracle(name):
     L = Layer(*SHAPES[name], seed=6)
