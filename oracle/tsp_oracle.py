@@ -68,6 +68,10 @@ __all__ = [
     "qkv_projection_shard",
     "layer_forward",
     "tsp_layer_forward",
+    "silu_grad",
+    "causal_attention_head_backward",
+    "layer_backward",
+    "tsp_layer_backward",
     "causal_pairs_per_rank",
     "layer_flops",
     "rank_parameter_count",
@@ -300,6 +304,157 @@ def tsp_layer_forward(x, W: dict, heads: int, D: int) -> dict:
     outs = hs + acc2
     return {"attn": unshard_tokens(acc, D), "h": unshard_tokens(hs, D),
             "mlp": unshard_tokens(acc2, D), "out": unshard_tokens(outs, D)}
+
+
+# --------------------------------------------------------------------------
+# Backward pass  ([TSP] title: training; the page describes the forward
+# schedules only, so the backward is the chain rule of the same layer, and its
+# sharded restatement runs the forward schedules in reverse)
+# --------------------------------------------------------------------------
+
+def silu_grad(z):
+    """d silu / dz = s (1 + z (1 - s)), s = sigmoid(z)."""
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def causal_attention_head_backward(q, k, v, q_pos, k_pos, do):
+    """Gradients (dq, dk, dv) of one head of causal_attention_head for output grad do.
+
+    With P the softmax weights and O = P v: dv = P^T do, dP = do v^T,
+    dS = P * (dP - rowsum(dP * P)), dq = dS k / sqrt(d), dk = dS^T q / sqrt(d).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    d = q.shape[1]
+    s = (q @ k.T) / math.sqrt(d)
+    visible = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]
+    s = np.where(visible, s, -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    dv = p.T @ do
+    dp = do @ v.T
+    ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+    dq = ds @ k / math.sqrt(d)
+    dk = ds.T @ q / math.sqrt(d)
+    return dq, dk, dv
+
+
+def layer_backward(x, W: dict, heads: int, dout) -> dict:
+    """Gradients of out = h + MLP(h), h = x + Attn(x), for the output gradient dout.
+
+    Returns {"dx", "dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"} (float64, the
+    shapes of x and of the weights).
+    """
+    S, H = x.shape
+    d = H // heads
+    Wq, Wk, Wv, Wo = W["Wq"], W["Wk"], W["Wv"], W["Wo"]
+    W1, W3, W2 = W["W1"], W["W3"], W["W2"]
+    # forward, keeping what the backward needs
+    Q, K, V = x @ Wq.T, x @ Wk.T, x @ Wv.T
+    O = multihead_causal_attention(Q, K, V, heads)
+    h = x + O @ Wo.T
+    A1, A3 = h @ W1.T, h @ W3.T
+    G = silu(A1) * A3
+    # MLP: out = h + G W2^T
+    g = {}
+    g["dW2"] = dout.T @ G
+    dG = dout @ W2
+    dA1 = dG * A3 * silu_grad(A1)
+    dA3 = dG * silu(A1)
+    g["dW1"] = dA1.T @ h
+    g["dW3"] = dA3.T @ h
+    dh = dout + dA1 @ W1 + dA3 @ W3
+    # attention: h = x + O Wo^T
+    g["dWo"] = dh.T @ O
+    dO = dh @ Wo
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    pos = np.arange(S)
+    for j in range(heads):
+        c = slice(j * d, (j + 1) * d)
+        dQ[:, c], dK[:, c], dV[:, c] = causal_attention_head_backward(
+            Q[:, c], K[:, c], V[:, c], pos, pos, dO[:, c])
+    g["dWq"], g["dWk"], g["dWv"] = dQ.T @ x, dK.T @ x, dV.T @ x
+    g["dx"] = dh + dQ @ Wq + dK @ Wk + dV @ Wv
+    return g
+
+
+def tsp_layer_backward(x, W: dict, heads: int, D: int, dout) -> dict:
+    """layer_backward computed rank by rank, the forward schedules run in reverse.
+
+    MLP, ring: at step t rank r holds shard k = (r + t) mod D with its partial
+    weight gradients; it adds its own tokens' contributions (dW2_k += dout_r^T G_rk,
+    dW1_k += dA1_rk^T h_r, dW3_k += dA3_rk^T h_r) and accumulates dh_r locally.
+    Attention, broadcast iteration k: every rank computes dO_rk = dh_r Wo_k and
+    dWo_k += dh_r^T O_rk; the attention backward of its queries yields dQ_rk and
+    contributions to dK_k, dV_k at every key position, which are summed at the
+    key's owner (the reverse of the K/V all-gather); then dx_r and the W_Q/W_K/W_V
+    shard gradients. Returns the same dict as layer_backward (natural order).
+    """
+    S, H = x.shape
+    F = W["W1"].shape[0]
+    hpr, Hd, Fd, T = heads // D, H // D, F // D, S // D
+    d = H // heads
+    xs = shard_tokens(x, D)
+    dos = shard_tokens(dout, D)
+    pos = rank_positions(S, D)
+    every = np.arange(S)
+    # forward activations of every rank (recomputed)
+    Qs, Ks, Vs, Os = {}, {}, {}, {}
+    hs = xs.copy()
+    for k in range(D):
+        c = slice(k * Hd, (k + 1) * Hd)
+        for r in range(D):
+            Qs[r, k] = xs[r] @ W["Wq"][c].T
+        K_all = unshard_tokens(np.stack([xs[r] @ W["Wk"][c].T for r in range(D)]), D)
+        V_all = unshard_tokens(np.stack([xs[r] @ W["Wv"][c].T for r in range(D)]), D)
+        Ks[k], Vs[k] = K_all, V_all
+        for r in range(D):
+            Os[r, k] = multihead_causal_attention(Qs[r, k], K_all, V_all, hpr, pos[r], every)
+            hs[r] = hs[r] + Os[r, k] @ W["Wo"][:, c].T
+    g = {n: np.zeros_like(W[n[1:]]) for n in ("dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2")}
+    # MLP backward, ring schedule
+    dhs = dos.copy()
+    for t in range(D):
+        for r in range(D):
+            k = (r + t) % D
+            f = slice(k * Fd, (k + 1) * Fd)
+            A1, A3 = hs[r] @ W["W1"][f].T, hs[r] @ W["W3"][f].T
+            G = silu(A1) * A3
+            dG = dos[r] @ W["W2"][:, f]
+            dA1 = dG * A3 * silu_grad(A1)
+            dA3 = dG * silu(A1)
+            g["dW2"][:, f] += dos[r].T @ G
+            g["dW1"][f] += dA1.T @ hs[r]
+            g["dW3"][f] += dA3.T @ hs[r]
+            dhs[r] = dhs[r] + dA1 @ W["W1"][f] + dA3 @ W["W3"][f]
+    # attention backward, broadcast schedule
+    dxs = dhs.copy()
+    for k in range(D):
+        c = slice(k * Hd, (k + 1) * Hd)
+        dK_nat, dV_nat = np.zeros((S, Hd)), np.zeros((S, Hd))
+        dQ = {}
+        for r in range(D):
+            dO = dhs[r] @ W["Wo"][:, c]
+            g["dWo"][:, c] += dhs[r].T @ Os[r, k]
+            dQ[r] = np.zeros((T, Hd))
+            for j in range(hpr):
+                cc = slice(j * d, (j + 1) * d)
+                dq, dk, dv = causal_attention_head_backward(
+                    Qs[r, k][:, cc], Ks[k][:, cc], Vs[k][:, cc], pos[r], every, dO[:, cc])
+                dQ[r][:, cc] = dq
+                dK_nat[:, cc] += dk      # summed at the key's owner
+                dV_nat[:, cc] += dv
+        dKs, dVs = shard_tokens(dK_nat, D), shard_tokens(dV_nat, D)
+        for r in range(D):
+            dxs[r] = dxs[r] + dQ[r] @ W["Wq"][c] + dKs[r] @ W["Wk"][c] + dVs[r] @ W["Wv"][c]
+            g["dWq"][c] += dQ[r].T @ xs[r]
+            g["dWk"][c] += dKs[r].T @ xs[r]
+            g["dWv"][c] += dVs[r].T @ xs[r]
+    g["dx"] = unshard_tokens(dxs, D)
+    return g
 
 
 # --------------------------------------------------------------------------

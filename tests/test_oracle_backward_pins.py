@@ -1,0 +1,149 @@
+"""Pins of the oracle's backward pass (CPU only).
+
+The page ("Folding Tensor and Sequence Parallelism for Memory-Efficient Transformer
+Training & Inference") names training but prints no backward formulas, so the
+backward is the chain rule of the forward layer. It is pinned to torch autograd in
+float64 (a library the oracle does not use), to central finite differences on tiny
+inputs, to closed forms, and its rank-by-rank restatement (the forward schedules
+run in reverse) to the plain one for several D. Planted mistakes must be caught.
+"""
+import math
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def _weights(H, F, seed, scale=0.3):
+    rng = np.random.default_rng(seed)
+    W = {k: rng.standard_normal((H, H)) * scale for k in ("Wq", "Wk", "Wv", "Wo")}
+    W["W1"] = rng.standard_normal((F, H)) * scale
+    W["W3"] = rng.standard_normal((F, H)) * scale
+    W["W2"] = rng.standard_normal((H, F)) * scale
+    return W
+
+
+def _torch_layer(x, W, heads):
+    S, H = x.shape
+    d = H // heads
+    sp = lambda a: a.view(S, heads, d).transpose(0, 1)
+    att = torch.nn.functional.scaled_dot_product_attention(
+        sp(x @ W["Wq"].T), sp(x @ W["Wk"].T), sp(x @ W["Wv"].T), is_causal=True)
+    h = x + att.transpose(0, 1).reshape(S, H) @ W["Wo"].T
+    return h + (torch.nn.functional.silu(h @ W["W1"].T) * (h @ W["W3"].T)) @ W["W2"].T
+
+
+def check_layer_backward_vs_autograd(o):
+    S, H, heads, F = 12, 8, 2, 6
+    x, dout = _rand((S, H), 1), _rand((S, H), 2)
+    W = _weights(H, F, 3)
+    got = o.layer_backward(x, W, heads, dout)
+    tx = torch.from_numpy(x).requires_grad_()
+    tW = {k: torch.from_numpy(v).requires_grad_() for k, v in W.items()}
+    _torch_layer(tx, tW, heads).backward(torch.from_numpy(dout))
+    assert np.abs(got["dx"] - tx.grad.numpy()).max() < 1e-10
+    for k in W:
+        assert np.abs(got["d" + k] - tW[k].grad.numpy()).max() < 1e-10, k
+
+
+def check_attention_backward_finite_differences(o):
+    n, d = 5, 3
+    q, k, v, do = (_rand((n, d), s) for s in (4, 5, 6, 7))
+    pos = np.arange(n)
+    dq, dk, dv = o.causal_attention_head_backward(q, k, v, pos, pos, do)
+    loss = lambda q_, k_, v_: float((o.causal_attention_head(q_, k_, v_, pos, pos) * do).sum())
+    eps = 1e-6
+    for arr, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        for idx in np.ndindex(arr.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += eps
+            up = loss(*args)
+            args[which][idx] -= 2 * eps
+            num = (up - loss(*args)) / (2 * eps)
+            assert abs(num - g[idx]) < 1e-7, (which, idx, num, g[idx])
+
+
+def check_closed_forms(o):
+    assert o.silu_grad(np.array(0.0)) == 0.5
+    z = np.linspace(-6, 6, 25)
+    num = (o.silu(z + 1e-6) - o.silu(z - 1e-6)) / 2e-6
+    assert np.abs(o.silu_grad(z) - num).max() < 1e-8
+    # query 0 attends only to key 0: its gradient reaches v_0 alone (dv_0 += do_0)
+    # and none reaches q_0 or k_0 (a one-key softmax is constant)
+    q, k, v, do = (_rand((1, 4), s) for s in (8, 9, 10, 11))
+    dq, dk, dv = o.causal_attention_head_backward(q, k, v, np.array([0]), np.array([0]), do)
+    assert np.abs(dv - do).max() < 1e-15 and np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    # a zero output gradient gives zero gradients everywhere
+    S, H = 6, 4
+    W = _weights(H, 4, 12)
+    g = o.layer_backward(_rand((S, H), 13), W, 2, np.zeros((S, H)))
+    assert all(np.abs(v).max() == 0 for v in g.values())
+
+
+def check_tsp_backward_equals_plain(o):
+    S, H, heads, F = 16, 16, 4, 8
+    x, dout = _rand((S, H), 14), _rand((S, H), 15)
+    W = _weights(H, F, 16)
+    plain = o.layer_backward(x, W, heads, dout)
+    for D in (1, 2, 4):
+        tsp = o.tsp_layer_backward(x, W, heads, D, dout)
+        for key in plain:
+            err = np.abs(tsp[key] - plain[key]).max() / max(np.abs(plain[key]).max(), 1e-30)
+            assert err < 1e-11, (D, key, err)
+
+
+PINS = [check_layer_backward_vs_autograd, check_attention_backward_finite_differences,
+        check_closed_forms, check_tsp_backward_equals_plain]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_backward_pin(pin):
+    pin(oracle)
+
+
+def _mutant(**overrides):
+    ns = types.SimpleNamespace(**{k: getattr(oracle, k) for k in oracle.__all__})
+    for k, v in overrides.items():
+        setattr(ns, k, v)
+    return ns
+
+
+def _attn_bwd_no_rowsum(q, k, v, q_pos, k_pos, do):
+    d = q.shape[1]
+    s = (q @ k.T) / math.sqrt(d)
+    s = np.where(np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
+    p = np.exp(s - s.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    ds = p * (do @ v.T)  # the rowsum term dropped
+    return ds @ k / math.sqrt(d), ds.T @ q / math.sqrt(d), p.T @ do
+
+
+def _layer_bwd_wrong_dw2(x, W, heads, dout):
+    g = oracle.layer_backward(x, W, heads, dout)
+    g["dW2"] = g["dW2"] * 2.0
+    return g
+
+
+MUTANTS = {
+    "attention dS without the row-sum term": dict(causal_attention_head_backward=_attn_bwd_no_rowsum),
+    "silu gradient without the z term": dict(silu_grad=lambda z: 1.0 / (1.0 + np.exp(-z))),
+    "dW2 scaled": dict(layer_backward=_layer_bwd_wrong_dw2),
+}
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_backward_planted_mistake_is_caught(name):
+    caught = 0
+    for pin in PINS:
+        try:
+            pin(_mutant(**MUTANTS[name]))
+        except AssertionError:
+            caught += 1
+    assert caught >= 1, name
