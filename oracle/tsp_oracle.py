@@ -1,4 +1,4 @@
-"""Oracle for the TSP layer forward. TEST INFRASTRUCTURE ONLY.
+"""Oracle for the TSP layer, forward and backward. TEST INFRASTRUCTURE ONLY.
 
 A plain, slow, float64 NumPy restatement of what one transformer layer computes
 under Folding Tensor and Sequence Parallelism (TSP). Only the test suite, the
@@ -70,6 +70,9 @@ __all__ = [
     "tsp_layer_forward",
     "silu_grad",
     "causal_attention_head_backward",
+    "causal_attention_head_backward_rows",
+    "swiglu_mlp_backward",
+    "attention_block_backward",
     "layer_backward",
     "tsp_layer_backward",
     "causal_pairs_per_rank",
@@ -342,34 +345,80 @@ def causal_attention_head_backward(q, k, v, q_pos, k_pos, do):
     return dq, dk, dv
 
 
-def layer_backward(x, W: dict, heads: int, dout) -> dict:
-    """Gradients of out = h + MLP(h), h = x + Attn(x), for the output gradient dout.
+def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_rows,
+                                        q_block: int = 1024):
+    """dq of the query rows q_rows and (dk, dv) of the key rows k_rows of one head.
 
-    Returns {"dx", "dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"} (float64, the
-    shapes of x and of the weights).
+    The same quantities as causal_attention_head_backward, for sequences whose full
+    score matrix does not fit: dq_i depends on query i's own softmax only; dk_j and
+    dv_j sum over every query that sees key j, so all queries are visited, `q_block`
+    rows at a time, each with its softmax over all of its visible keys.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    q_pos, k_pos = np.asarray(q_pos), np.asarray(k_pos)
+    q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
+    d = q.shape[1]
+    dq = causal_attention_head_backward(q[q_rows], k, v, q_pos[q_rows], k_pos, do[q_rows])[0]
+    dk = np.zeros((k_rows.size, d))
+    dv = np.zeros((k_rows.size, d))
+    for lo in range(0, q.shape[0], q_block):
+        r = slice(lo, min(q.shape[0], lo + q_block))
+        s = (q[r] @ k.T) / math.sqrt(d)
+        visible = k_pos[None, :] <= q_pos[r, None]
+        s = np.where(visible, s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        dp = do[r] @ v.T
+        ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+        dk += ds[:, k_rows].T @ q[r] / math.sqrt(d)
+        dv += p[:, k_rows].T @ do[r]
+    return dq, dk, dv
+
+
+def swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None) -> dict:
+    """Gradients of MLP(h) = G W2^T, G = silu(A1) * A3, A1 = h W1^T, A3 = h W3^T,
+    for the output gradient dmlp (the block alone, no residual):
+
+        dW2 = dmlp^T G       dG = dmlp W2
+        dA1 = dG * A3 * silu'(A1)          dA3 = dG * silu(A1)
+        dW1 = dA1^T h        dW3 = dA3^T h        dh = dA1 W1 + dA3 W3
+
+    Returns {"dh", "dW1", "dW3", "dW2"}. With `rows`, dh holds those token rows only
+    (each needs every ffn column of its own row); with `ffn_cols`, dW1 and dW3 hold
+    those rows and dW2 those columns only (each needs every token).
+    """
+    h = np.asarray(h, dtype=np.float64)
+    dmlp = np.asarray(dmlp, dtype=np.float64)
+    r = slice(None) if rows is None else np.asarray(rows)
+    c = slice(None) if ffn_cols is None else np.asarray(ffn_cols)
+    A1, A3 = h[r] @ W1.T, h[r] @ W3.T
+    dG = dmlp[r] @ W2
+    out = {"dh": (dG * A3 * silu_grad(A1)) @ W1 + (dG * silu(A1)) @ W3}
+    A1, A3 = h @ W1[c].T, h @ W3[c].T
+    dG = dmlp @ W2[:, c]
+    out["dW2"] = dmlp.T @ (silu(A1) * A3)
+    out["dW1"] = (dG * A3 * silu_grad(A1)).T @ h
+    out["dW3"] = (dG * silu(A1)).T @ h
+    return out
+
+
+def attention_block_backward(x, Wq, Wk, Wv, Wo, heads: int, dattn) -> dict:
+    """Gradients of attention_block (no residual) for the output gradient dattn.
+
+    With Q = x Wq^T, K = x Wk^T, V = x Wv^T, O the per-head causal attention and
+    Attn = O Wo^T: dWo = dattn^T O, dO = dattn Wo, the per-head attention backward
+    gives dQ, dK, dV, then dWq = dQ^T x (likewise K, V) and
+    dx = dQ Wq + dK Wk + dV Wv. Returns {"dx", "dWq", "dWk", "dWv", "dWo"}.
     """
     S, H = x.shape
     d = H // heads
-    Wq, Wk, Wv, Wo = W["Wq"], W["Wk"], W["Wv"], W["Wo"]
-    W1, W3, W2 = W["W1"], W["W3"], W["W2"]
-    # forward, keeping what the backward needs
     Q, K, V = x @ Wq.T, x @ Wk.T, x @ Wv.T
     O = multihead_causal_attention(Q, K, V, heads)
-    h = x + O @ Wo.T
-    A1, A3 = h @ W1.T, h @ W3.T
-    G = silu(A1) * A3
-    # MLP: out = h + G W2^T
-    g = {}
-    g["dW2"] = dout.T @ G
-    dG = dout @ W2
-    dA1 = dG * A3 * silu_grad(A1)
-    dA3 = dG * silu(A1)
-    g["dW1"] = dA1.T @ h
-    g["dW3"] = dA3.T @ h
-    dh = dout + dA1 @ W1 + dA3 @ W3
-    # attention: h = x + O Wo^T
-    g["dWo"] = dh.T @ O
-    dO = dh @ Wo
+    g = {"dWo": dattn.T @ O}
+    dO = dattn @ Wo
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
     pos = np.arange(S)
     for j in range(heads):
@@ -377,7 +426,26 @@ def layer_backward(x, W: dict, heads: int, dout) -> dict:
         dQ[:, c], dK[:, c], dV[:, c] = causal_attention_head_backward(
             Q[:, c], K[:, c], V[:, c], pos, pos, dO[:, c])
     g["dWq"], g["dWk"], g["dWv"] = dQ.T @ x, dK.T @ x, dV.T @ x
-    g["dx"] = dh + dQ @ Wq + dK @ Wk + dV @ Wv
+    g["dx"] = dQ @ Wq + dK @ Wk + dV @ Wv
+    return g
+
+
+def layer_backward(x, W: dict, heads: int, dout) -> dict:
+    """Gradients of out = h + MLP(h), h = x + Attn(x), for the output gradient dout.
+
+    The residual paths add the identity: dh = dout + (MLP backward of dout) and
+    dx = dh + (attention backward of dh). Returns {"dx", "dWq", "dWk", "dWv",
+    "dWo", "dW1", "dW3", "dW2"} (float64, the shapes of x and of the weights).
+    """
+    Wq, Wk, Wv, Wo = W["Wq"], W["Wk"], W["Wv"], W["Wo"]
+    h = x + attention_block(x, Wq, Wk, Wv, Wo, heads)
+    m = swiglu_mlp_backward(h, W["W1"], W["W3"], W["W2"], dout)
+    dh = dout + m["dh"]
+    a = attention_block_backward(x, Wq, Wk, Wv, Wo, heads, dh)
+    g = {"dW1": m["dW1"], "dW3": m["dW3"], "dW2": m["dW2"]}
+    for n in ("dWq", "dWk", "dWv", "dWo"):
+        g[n] = a[n]
+    g["dx"] = dh + a["dx"]
     return g
 
 

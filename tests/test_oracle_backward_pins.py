@@ -99,8 +99,69 @@ def check_tsp_backward_equals_plain(o):
             assert err < 1e-11, (D, key, err)
 
 
+def check_block_backwards_vs_autograd(o):
+    S, H, heads, F = 10, 8, 2, 6
+    x, dy = _rand((S, H), 17), _rand((S, H), 18)
+    W = _weights(H, F, 19)
+    tW = {k: torch.from_numpy(v).requires_grad_() for k, v in W.items()}
+    # MLP block alone
+    th = torch.from_numpy(x).requires_grad_()
+    ((torch.nn.functional.silu(th @ tW["W1"].T) * (th @ tW["W3"].T)) @ tW["W2"].T).backward(
+        torch.from_numpy(dy))
+    m = o.swiglu_mlp_backward(x, W["W1"], W["W3"], W["W2"], dy)
+    assert np.abs(m["dh"] - th.grad.numpy()).max() < 1e-10
+    for k in ("W1", "W3", "W2"):
+        assert np.abs(m["d" + k] - tW[k].grad.numpy()).max() < 1e-10, k
+    # attention block alone
+    tx = torch.from_numpy(x).requires_grad_()
+    sp = lambda a: a.view(S, heads, H // heads).transpose(0, 1)
+    att = torch.nn.functional.scaled_dot_product_attention(
+        sp(tx @ tW["Wq"].T), sp(tx @ tW["Wk"].T), sp(tx @ tW["Wv"].T), is_causal=True)
+    (att.transpose(0, 1).reshape(S, H) @ tW["Wo"].T).backward(torch.from_numpy(dy))
+    a = o.attention_block_backward(x, W["Wq"], W["Wk"], W["Wv"], W["Wo"], heads, dy)
+    assert np.abs(a["dx"] - tx.grad.numpy()).max() < 1e-10
+    for k in ("Wq", "Wk", "Wv", "Wo"):
+        assert np.abs(a["d" + k] - tW[k].grad.numpy()).max() < 1e-10, k
+
+
+def check_sampled_backwards(o):
+    """The row / column sampled forms give the full forms' entries."""
+    S, H, F = 12, 8, 10
+    h, dy = _rand((S, H), 20), _rand((S, H), 21)
+    W = _weights(H, F, 22)
+    full = o.swiglu_mlp_backward(h, W["W1"], W["W3"], W["W2"], dy)
+    rows, cols = np.array([0, 5, 11]), np.array([1, 4, 9])
+    part = o.swiglu_mlp_backward(h, W["W1"], W["W3"], W["W2"], dy, rows=rows, ffn_cols=cols)
+    assert np.abs(part["dh"] - full["dh"][rows]).max() < 1e-12
+    assert np.abs(part["dW1"] - full["dW1"][cols]).max() < 1e-12
+    assert np.abs(part["dW3"] - full["dW3"][cols]).max() < 1e-12
+    assert np.abs(part["dW2"] - full["dW2"][:, cols]).max() < 1e-12
+    n, d = 11, 4
+    q, k, v, do = (_rand((n, d), s) for s in (23, 24, 25, 26))
+    pos = np.array([0, 1, 2, 8, 9, 10, 3, 4, 5, 6, 7])  # zigzag-like query order
+    kpos = np.arange(n)
+    dq, dk, dv = o.causal_attention_head_backward(q, k, v, pos, kpos, do)
+    qr, kr = np.array([0, 3, 10]), np.array([0, 2, 7, 10])
+    sq, sk, sv = o.causal_attention_head_backward_rows(q, k, v, pos, kpos, do, qr, kr, q_block=3)
+    assert np.abs(sq - dq[qr]).max() < 1e-12
+    assert np.abs(sk - dk[kr]).max() < 1e-12
+    assert np.abs(sv - dv[kr]).max() < 1e-12
+
+
+def check_attention_gradient_sums(o):
+    """Per head, the key gradients sum to zero (each softmax row's dS sums to zero)
+    and the value gradients sum to the output gradients (each P row sums to one)."""
+    n, d = 9, 5
+    q, k, v, do = (_rand((n, d), s) for s in (27, 28, 29, 30))
+    pos = np.arange(n)
+    dq, dk, dv = o.causal_attention_head_backward(q, k, v, pos, pos, do)
+    assert np.abs(dk.sum(axis=0)).max() < 1e-12
+    assert np.abs(dv.sum(axis=0) - do.sum(axis=0)).max() < 1e-12
+
+
 PINS = [check_layer_backward_vs_autograd, check_attention_backward_finite_differences,
-        check_closed_forms, check_tsp_backward_equals_plain]
+        check_closed_forms, check_tsp_backward_equals_plain, check_block_backwards_vs_autograd,
+        check_sampled_backwards, check_attention_gradient_sums]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -131,7 +192,22 @@ def _layer_bwd_wrong_dw2(x, W, heads, dout):
     return g
 
 
+def _mlp_bwd_no_w3_path(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None):
+    g = oracle.swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows, ffn_cols)
+    r = slice(None) if rows is None else rows
+    g["dh"] = g["dh"] - ((dmlp[r] @ W2) * oracle.silu(h[r] @ W1.T)) @ W3
+    return g
+
+
+def _attn_rows_unnormalised(q, k, v, q_pos, k_pos, do, q_rows, k_rows, q_block=1024):
+    dq, dk, dv = oracle.causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do,
+                                                            q_rows, k_rows, q_block)
+    return dq, dk, dv * 1.5
+
+
 MUTANTS = {
+    "MLP dh without the W3 path": dict(swiglu_mlp_backward=_mlp_bwd_no_w3_path),
+    "sampled attention dv scaled": dict(causal_attention_head_backward_rows=_attn_rows_unnormalised),
     "attention dS without the row-sum term": dict(causal_attention_head_backward=_attn_bwd_no_rowsum),
     "silu gradient without the z term": dict(silu_grad=lambda z: 1.0 / (1.0 + np.exp(-z))),
     "dW2 scaled": dict(layer_backward=_layer_bwd_wrong_dw2),
