@@ -25,7 +25,7 @@ __all__ = [
     "tsp_qkv_projection", "tsp_qkv_projection_gathered", "tsp_kv_allgather",
     "tsp_causal_attention", "tsp_causal_attention_q", "tsp_o_projection",
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
-    "tsp_last_error",
+    "tsp_last_error", "tsp_bwd_workspace_bytes", "tsp_mlp_bwd", "tsp_unpack_weight_grads",
 ]
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
@@ -50,7 +50,7 @@ class PlanInfo(ctypes.Structure):
         ("ffn_padded", ctypes.c_int), ("wpack_qkv", ctypes.c_size_t),
         ("wpack_o", ctypes.c_size_t), ("wpack_w13", ctypes.c_size_t),
         ("wpack_w2", ctypes.c_size_t), ("wpack_elems", ctypes.c_size_t),
-        ("workspace_bytes", ctypes.c_size_t),
+        ("workspace_bytes", ctypes.c_size_t), ("bwd_workspace_bytes", ctypes.c_size_t),
     ]
 
     def as_dict(self):
@@ -87,6 +87,9 @@ _SIGS = {
     "tsp_device_status": (_I, [_P, _P]),
     "tsp_wait_selftest": (_I, [_P, ctypes.c_uint64, _P]),
     "tsp_last_error": (ctypes.c_char_p, []),
+    "tsp_bwd_workspace_bytes": (ctypes.c_size_t, [_P]),
+    "tsp_mlp_bwd": (_I, [_P] * 8),
+    "tsp_unpack_weight_grads": (_I, [_P] * 10),
 }
 
 
@@ -359,3 +362,38 @@ def tsp_device_status(ws, stream=None) -> int:
 def tsp_wait_selftest(ws, limit_ns: int, stream=None):
     _check(load_library().tsp_wait_selftest(_dev(ws, "ws", 256, dtype=torch.uint8),
                                             int(limit_ns), _stream(stream)), "tsp_wait_selftest")
+
+
+# ------------------------------------------------------------------ backward
+
+def tsp_bwd_workspace_bytes(plan: Plan) -> int:
+    return load_library().tsp_bwd_workspace_bytes(plan.handle)
+
+
+def _ws_bwd(plan, ws):
+    return _dev(ws, "ws", tsp_bwd_workspace_bytes(plan), dtype=torch.uint8)
+
+
+def tsp_mlp_bwd(plan, hs, wpack, dmlp, dhs, dwpack, ws, stream=None):
+    """Backward of tsp_mlp_fwd: dhs (bf16, sharded) and the W1/W3/W2 sections of the
+    packed fp32 weight gradient dwpack."""
+    n = plan.act_elems
+    i = plan.info
+    _check(load_library().tsp_mlp_bwd(
+        plan.handle, _dev(hs, "hs", n), _dev(wpack, "wpack", i.wpack_elems),
+        _dev(dmlp, "dmlp", n), _dev(dhs, "dhs", n),
+        _dev(dwpack, "dwpack", i.wpack_elems, torch.float32), _ws_bwd(plan, ws),
+        _stream(stream)), "tsp_mlp_bwd")
+
+
+def tsp_unpack_weight_grads(plan, dwpack, dWq=None, dWk=None, dWv=None, dWo=None, dW1=None,
+                            dW3=None, dW2=None, stream=None):
+    i = plan.info
+    H, F = i.hidden, i.ffn
+    f32 = torch.float32
+    _check(load_library().tsp_unpack_weight_grads(
+        plan.handle, _dev(dwpack, "dwpack", i.wpack_elems, f32),
+        _dev(dWq, "dWq", H * H, f32, optional=True), _dev(dWk, "dWk", H * H, f32, optional=True),
+        _dev(dWv, "dWv", H * H, f32, optional=True), _dev(dWo, "dWo", H * H, f32, optional=True),
+        _dev(dW1, "dW1", F * H, f32, optional=True), _dev(dW3, "dW3", F * H, f32, optional=True),
+        _dev(dW2, "dW2", H * F, f32, optional=True), _stream(stream)), "tsp_unpack_weight_grads")

@@ -23,16 +23,11 @@
 #include "tsp_device.cuh"
 #include "tsp_internal.h"
 
-struct tsp_plan_s {
-  tsp::Plan p;
-};
-
 namespace tsp {
 
 namespace {
 thread_local std::string g_last_error;
 
-size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -51,16 +46,6 @@ EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(ptr);
   });
   return fn;
-}
-
-bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
-
-DevStatus* status_of(void* ws) { return static_cast<DevStatus*>(ws); }
-
-template <class T>
-T* at(void* ws, size_t off) {
-  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
 }  // namespace
@@ -121,8 +106,6 @@ unsigned long long wait_limit_ns() {
 }
 
 // ------------------------------------------------------------------ steps
-
-namespace {
 
 tsp_status qkv_projection(const Plan& p, int k, const void* xs, const void* wpack, void* qkv,
                           void* ws, cudaStream_t s) {
@@ -262,12 +245,6 @@ tsp_status swiglu_down(const Plan& p, const void* g, const void* wpack, const vo
   return launch_gemm(c, s);
 }
 
-#define TSP_TRY(expr)              \
-  do {                             \
-    tsp_status st_ = (expr);       \
-    if (st_ != TSP_OK) return st_; \
-  } while (0)
-
 tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,
                            void* out, void* out32, void* ws, cudaStream_t s) {
   void* q = at<void>(ws, p.ws.qkv);
@@ -303,25 +280,6 @@ const void* mapped_host_alias(const void* host) {
   return attr.devicePointer;
 }
 
-tsp_status check_plan(tsp_plan_t plan) {
-  return plan ? TSP_OK : fail(TSP_ERR_INVALID_ARG, "null plan");
-}
-
-tsp_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
-  for (const void* q : ptrs) {
-    if (!q) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": null pointer");
-    if (!al16(q)) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": pointer not 16-byte aligned");
-  }
-  return TSP_OK;
-}
-
-tsp_status check_ws(void* ws, const char* what) {
-  if (!ws) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": null workspace");
-  if (!al256(ws)) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": workspace not 256-byte aligned");
-  return TSP_OK;
-}
-
-}  // namespace
 }  // namespace tsp
 
 using namespace tsp;
@@ -394,6 +352,17 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
   p.ws.stage_in = take(Sz * H * 2);
   p.ws.stage_out = take(Sz * H * 2);
   p.ws.total = off;
+  p.ws.a13 = take(Sz * 2 * p.NF * 2);
+  p.ws.dh32 = take(Sz * H * 4);
+  p.ws.dh = take(Sz * H * 2);
+  p.ws.dob = take(Sz * H * 2);
+  p.ws.lse = take((size_t)heads * Sz * 4);
+  p.ws.delta = take((size_t)heads * Sz * 4);
+  p.ws.qa = take(Sz * H * 2);
+  p.ws.ka = take(Sz * H * 2);
+  p.ws.va = take(Sz * H * 2);
+  p.ws.dqkv = take(Sz * 3 * H * 2);
+  p.ws.total_bwd = off;
 
   tsp_plan_s* obj = new tsp_plan_s;
   obj->p = p;
@@ -405,7 +374,7 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
 void tsp_plan_destroy(tsp_plan_t plan) { delete plan; }
 
 tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   if (!info) return fail(TSP_ERR_INVALID_ARG, "tsp_get_plan_info: null info");
   const Plan& p = plan->p;
   info->D = p.D;
@@ -426,6 +395,7 @@ tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info) {
   info->wpack_w2 = p.wp_w2;
   info->wpack_elems = p.wp_elems;
   info->workspace_bytes = p.ws.total;
+  info->bwd_workspace_bytes = p.ws.total_bwd;
   return TSP_OK;
 }
 
@@ -434,7 +404,7 @@ size_t tsp_workspace_bytes(tsp_plan_t plan) { return plan ? plan->p.ws.total : 0
 size_t tsp_packed_weight_bytes(tsp_plan_t plan) { return plan ? plan->p.wp_elems * 2 : 0; }
 
 tsp_status tsp_workspace_init(tsp_plan_t plan, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ws(ws, "tsp_workspace_init"));
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TSP_OK : cuda_fail(e, "tsp_workspace_init");
@@ -444,27 +414,27 @@ tsp_status tsp_pack_weights(tsp_plan_t plan, const tsp_bf16* Wq, const tsp_bf16*
                             const tsp_bf16* Wv, const tsp_bf16* Wo, const tsp_bf16* W1,
                             const tsp_bf16* W3, const tsp_bf16* W2, tsp_bf16* wpack,
                             void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({Wq, Wk, Wv, Wo, W1, W3, W2, wpack}, "tsp_pack_weights"));
   return launch_pack_weights(plan->p, Wq, Wk, Wv, Wo, W1, W3, W2, wpack,
                              static_cast<cudaStream_t>(stream));
 }
 
 tsp_status tsp_shard_index(tsp_plan_t plan, int32_t* fwd, int32_t* inv, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   if (!fwd && !inv) return TSP_OK;
   return launch_zigzag_index(plan->p, fwd, inv, static_cast<cudaStream_t>(stream));
 }
 
 tsp_status tsp_shard(tsp_plan_t plan, const tsp_bf16* x, tsp_bf16* xs, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({x, xs}, "tsp_shard"));
   if (x == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_shard: buffers overlap");
   return launch_zigzag_rows(plan->p, x, xs, plan->p.H, true, static_cast<cudaStream_t>(stream));
 }
 
 tsp_status tsp_unshard(tsp_plan_t plan, const tsp_bf16* xs, tsp_bf16* x, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({x, xs}, "tsp_unshard"));
   if (x == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_unshard: buffers overlap");
   return launch_zigzag_rows(plan->p, xs, x, plan->p.H, false, static_cast<cudaStream_t>(stream));
@@ -472,7 +442,7 @@ tsp_status tsp_unshard(tsp_plan_t plan, const tsp_bf16* xs, tsp_bf16* x, void* s
 
 tsp_status tsp_attention_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                              tsp_bf16* attn, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, attn}, "tsp_attention_fwd"));
   TSP_TRY(check_ws(ws, "tsp_attention_fwd"));
   if (attn == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_attention_fwd: attn aliases xs");
@@ -482,7 +452,7 @@ tsp_status tsp_attention_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16
 
 tsp_status tsp_mlp_fwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack, tsp_bf16* mlp,
                        void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({hs, wpack, mlp}, "tsp_mlp_fwd"));
   TSP_TRY(check_ws(ws, "tsp_mlp_fwd"));
   if (mlp == hs) return fail(TSP_ERR_INVALID_ARG, "tsp_mlp_fwd: mlp aliases hs");
@@ -491,7 +461,7 @@ tsp_status tsp_mlp_fwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpac
 
 tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                          tsp_bf16* out, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, out}, "tsp_layer_fwd"));
   TSP_TRY(check_ws(ws, "tsp_layer_fwd"));
   if (out == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd: out aliases xs");
@@ -507,7 +477,7 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
 
 tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
                               tsp_bf16* out_host, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   if (!x_host || !out_host) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd_host: null host buffer");
   TSP_TRY(check_ptrs({wpack}, "tsp_layer_fwd_host"));
   TSP_TRY(check_ws(ws, "tsp_layer_fwd_host"));
@@ -542,7 +512,7 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
 
 tsp_status tsp_qkv_projection(tsp_plan_t plan, int shard, const tsp_bf16* xs,
                               const tsp_bf16* wpack, tsp_bf16* qkv, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, qkv}, "tsp_qkv_projection"));
   TSP_TRY(check_ws(ws, "tsp_qkv_projection"));
   if (shard < 0 || shard >= plan->p.D) return fail(TSP_ERR_INVALID_ARG, "tsp_qkv_projection: shard out of range");
@@ -552,7 +522,7 @@ tsp_status tsp_qkv_projection(tsp_plan_t plan, int shard, const tsp_bf16* xs,
 tsp_status tsp_qkv_projection_gathered(tsp_plan_t plan, int shard, const tsp_bf16* xs,
                                        const tsp_bf16* wpack, tsp_bf16* q, tsp_bf16* kn,
                                        tsp_bf16* vn, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, q, kn, vn}, "tsp_qkv_projection_gathered"));
   TSP_TRY(check_ws(ws, "tsp_qkv_projection_gathered"));
   if (shard < 0 || shard >= plan->p.D)
@@ -564,7 +534,7 @@ tsp_status tsp_qkv_projection_gathered(tsp_plan_t plan, int shard, const tsp_bf1
 tsp_status tsp_causal_attention_q(tsp_plan_t plan, int shard, const tsp_bf16* q,
                                   const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o, void* ws,
                                   void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({q, kn, vn, o}, "tsp_causal_attention_q"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention_q"));
   if (shard < 0 || shard >= plan->p.D)
@@ -575,7 +545,7 @@ tsp_status tsp_causal_attention_q(tsp_plan_t plan, int shard, const tsp_bf16* q,
 
 tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, tsp_bf16* vn,
                             void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({qkv, kn, vn}, "tsp_kv_allgather"));
   return launch_kv_gather(plan->p, qkv, kn, vn, static_cast<cudaStream_t>(stream));
 }
@@ -583,7 +553,7 @@ tsp_status tsp_kv_allgather(tsp_plan_t plan, const tsp_bf16* qkv, tsp_bf16* kn, 
 tsp_status tsp_causal_attention(tsp_plan_t plan, int shard, const tsp_bf16* qkv,
                                 const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o, void* ws,
                                 void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({qkv, kn, vn, o}, "tsp_causal_attention"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention"));
   if (shard < 0 || shard >= plan->p.D) return fail(TSP_ERR_INVALID_ARG, "tsp_causal_attention: shard out of range");
@@ -594,7 +564,7 @@ tsp_status tsp_causal_attention(tsp_plan_t plan, int shard, const tsp_bf16* qkv,
 tsp_status tsp_o_projection(tsp_plan_t plan, const tsp_bf16* o, const tsp_bf16* wpack,
                             const tsp_bf16* residual, tsp_bf16* out, float* out32, void* ws,
                             void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({o, wpack, out}, "tsp_o_projection"));
   TSP_TRY(check_ws(ws, "tsp_o_projection"));
   if (residual && !al16(residual)) return fail(TSP_ERR_INVALID_ARG, "tsp_o_projection: residual not 16-byte aligned");
@@ -606,7 +576,7 @@ tsp_status tsp_o_projection(tsp_plan_t plan, const tsp_bf16* o, const tsp_bf16* 
 
 tsp_status tsp_swiglu_gate_up(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
                               tsp_bf16* g, void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({hs, wpack, g}, "tsp_swiglu_gate_up"));
   TSP_TRY(check_ws(ws, "tsp_swiglu_gate_up"));
   return swiglu_gate_up(plan->p, hs, wpack, g, ws, static_cast<cudaStream_t>(stream));
@@ -615,7 +585,7 @@ tsp_status tsp_swiglu_gate_up(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf1
 tsp_status tsp_swiglu_down(tsp_plan_t plan, const tsp_bf16* g, const tsp_bf16* wpack,
                            const tsp_bf16* residual, const float* residual32, tsp_bf16* out,
                            void* ws, void* stream) {
-  TSP_TRY(check_plan(plan));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({g, wpack, out}, "tsp_swiglu_down"));
   TSP_TRY(check_ws(ws, "tsp_swiglu_down"));
   if (residual && !al16(residual)) return fail(TSP_ERR_INVALID_ARG, "tsp_swiglu_down: residual not 16-byte aligned");

@@ -46,6 +46,9 @@ enum Kind {
   K_RES_BF16_OUT32 = 3, // C = bf16(acc + R), C32 = acc + R (fp32), R bf16
   K_RES_F32 = 4,        // C = bf16(acc + R), R fp32
   K_QKV_SPLIT = 5,      // Q|K|V columns: Q to C (sharded rows), K and V to natural rows
+  K_STORE_F32 = 6,      // C32 = acc (fp32): weight gradients
+  K_SWIGLU_SAVE = 7,    // as K_SWIGLU, and the pre-activations (A1|A3 tiles) to C2
+  K_SWIGLU_BWD = 8,     // acc = dG; with A1/A3 from C2: dA1|dA3 to C in C2's packed order
 };
 
 struct GemmParams {
@@ -64,6 +67,8 @@ struct GemmParams {
   int split_hd;
   long long zz_C, zz_T;
   int zz_D;
+  __nv_bfloat16* C2;  // K_SWIGLU_SAVE: pre-activations out; K_SWIGLU_BWD: pre-activations in
+  long long ldc2;
   int ring_rows;
   int ring_kblocks;
   int group_m;  // tile order: group_m row blocks walk down each column block in turn
@@ -98,7 +103,11 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&f)
   }
 }
 
-template <int EPI>
+// A_MN / B_MN: operand stored MN-major, i.e. as a [K][M] (or [K][N]) matrix with
+// M (N) contiguous; its tiles arrive as 64-element x 64-row TMA boxes (8 KB each,
+// the 64-element blocks 8 KB apart, 8-row groups 1 KB apart) and a 16-wide K step
+// is 2 KB. K-major operands arrive as [rows][64] boxes and step 32 B in K.
+template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int numM = (p.M + BM - 1) / BM;
   const int numN = (p.N + BN - 1) / BN;
   const int numTiles = numM * numN;
-  const int nkb = p.K / BK;
+  const int nkb = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -171,8 +180,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
-          tma_load_2d_hint(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, p.b_row0 + n0, keep);
+          if constexpr (A_MN) {
+#pragma unroll
+            for (int b = 0; b < BM / 64; ++b)
+              tma_load_2d(sA + stage * A_BYTES + b * 8192, &tmA, &full[stage], m0 + 64 * b, kb * BK);
+          } else {
+            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m0);
+          }
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int b = 0; b < BN / 64; ++b)
+              tma_load_2d_hint(sB + stage * B_BYTES + b * 8192, &tmB, &full[stage],
+                               p.b_row0 + n0 + 64 * b, kb * BK, keep);
+          } else {
+            tma_load_2d_hint(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, p.b_row0 + n0, keep);
+          }
           last_parity[stage] = (int)phase;
           if (++kb == nkb) kb = 0;
           if (++stage == STAGES) {
@@ -189,10 +211,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = make_idesc_bf16(BM, BN, false);
+      const uint32_t idesc = make_idesc_bf16(BM, BN, B_MN, A_MN);
+      constexpr uint32_t A_STEP = A_MN ? (2048u >> 4) : (32u >> 4);  // one 16-wide K step
+      constexpr uint32_t B_STEP = B_MN ? (2048u >> 4) : (32u >> 4);
       // base descriptors of stage 0, built once; stages and K steps add offsets
-      const uint64_t da0 = make_sdesc_sw128(smem_addr(sA), 16, 1024);
-      const uint64_t db0 = make_sdesc_sw128(smem_addr(sB), 16, 1024);
+      const uint64_t da0 = make_sdesc_sw128(smem_addr(sA), A_MN ? 8192 : 16, 1024);
+      const uint64_t db0 = make_sdesc_sw128(smem_addr(sB), B_MN ? 8192 : 16, 1024);
       const uint32_t da_lo = (uint32_t)da0, da_hi = (uint32_t)(da0 >> 32);
       const uint32_t db_lo = (uint32_t)db0, db_hi = (uint32_t)(db0 >> 32);
       int stage = 0;
@@ -213,8 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_lo = da_lo + (uint32_t)stage * (A_BYTES >> 4);
           const uint32_t b_lo = db_lo + (uint32_t)stage * (B_BYTES >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // 16-element K steps: +32 B
-            mma_ss_w(d_tmem, a_lo + kk * 2, da_hi, b_lo + kk * 2, db_hi, idesc,
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_ss_w(d_tmem, a_lo + kk * A_STEP, da_hi, b_lo + kk * B_STEP, db_hi, idesc,
                      (i | kk) != 0 ? 1u : 0u);
           mma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -251,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const long long rank = row / p.zz_T, l = row - rank * p.zz_T;
         nat = l < p.zz_C ? rank * p.zz_C + l : (2 * p.zz_D - 1 - rank) * p.zz_C + (l - p.zz_C);
       }
-      if constexpr (EPI == K_SWIGLU) {
+      if constexpr (EPI == K_SWIGLU || EPI == K_SWIGLU_SAVE) {
         // columns [0,128) of the tile are gate rows (W1), [128,256) up rows (W3)
         const int half_n = p.N >> 1;
 #pragma unroll 1
@@ -271,6 +295,16 @@ __global__ void __launch_bounds__(THREADS, 1)
               f[j] = g / (1.0f + __expf(-g)) * u;
             }
             store_row32(p.C + row * p.ldc + ocol, f);
+            if constexpr (EPI == K_SWIGLU_SAVE) {
+              float a1[32], a3[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                a1[j] = __uint_as_float(gv[j]);
+                a3[j] = __uint_as_float(uv[j]);
+              }
+              store_row32(p.C2 + row * p.ldc2 + nt * BN + c, a1);
+              store_row32(p.C2 + row * p.ldc2 + nt * BN + BN / 2 + c, a3);
+            }
           }
         }
       } else {
@@ -319,7 +353,37 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int w = 0; w < 8; ++w)
                 c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
             }
-            if constexpr (EPI == K_QKV_SPLIT) {
+            if constexpr (EPI == K_STORE_F32) {
+              float4* c4 = reinterpret_cast<float4*>(p.C32 + row * p.ldc + col);
+#pragma unroll
+              for (int w = 0; w < 8; ++w)
+                c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+            } else if constexpr (EPI == K_SWIGLU_BWD) {
+              // f = dG for padded ffn columns col..col+31 (one 128-column group g);
+              // silu'(a) = s (1 + a (1 - s)), s = sigmoid(a)
+              const int g = col / (BN / 2), j0 = col - g * (BN / 2);
+              const long long c1 = (long long)g * BN + j0, c3 = c1 + BN / 2;
+              // C may alias C2: each element is read, then written, by this thread alone
+              const uint4* a1p = reinterpret_cast<const uint4*>(p.C2 + row * p.ldc2 + c1);
+              const uint4* a3p = reinterpret_cast<const uint4*>(p.C2 + row * p.ldc2 + c3);
+              float d1[32], d3[32];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint4 x1 = a1p[w], x3 = a3p[w];
+                const uint32_t u1[4] = {x1.x, x1.y, x1.z, x1.w}, u3[4] = {x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float a1 = (e & 1) ? bf16_hi(u1[e >> 1]) : bf16_lo(u1[e >> 1]);
+                  const float a3 = (e & 1) ? bf16_hi(u3[e >> 1]) : bf16_lo(u3[e >> 1]);
+                  const float sg = 1.0f / (1.0f + __expf(-a1));
+                  const float dg = f[8 * w + e];
+                  d1[8 * w + e] = dg * a3 * sg * (1.0f + a1 * (1.0f - sg));
+                  d3[8 * w + e] = dg * a1 * sg;
+                }
+              }
+              store_row32(p.C + row * p.ldc + c1, d1);
+              store_row32(p.C + row * p.ldc + c3, d3);
+            } else if constexpr (EPI == K_QKV_SPLIT) {
               // a 32-column chunk never straddles sections (split_hd % 32 == 0)
               const int sec = col / p.split_hd;
               const int lc = col - sec * p.split_hd;
@@ -351,10 +415,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-template <int EPI>
+template <int EPI, bool A_MN, bool B_MN>
 tsp_status launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
                       cudaStream_t stream) {
-  auto kernel = gemm_bf16_tcgen05<EPI>;
+  auto kernel = gemm_bf16_tcgen05<EPI, A_MN, B_MN>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(e, "gemm: cudaFuncSetAttribute");
@@ -367,19 +431,27 @@ tsp_status launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPa
 }  // namespace
 
 tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
-  if (!c.A || !c.B || !c.C || !c.status) return fail(TSP_ERR_INVALID_ARG, "gemm: null pointer");
+  if (!c.A || !c.B || !(c.C || c.epi == EPI_STORE_F32) || !c.status)
+    return fail(TSP_ERR_INVALID_ARG, "gemm: null pointer");
   if (c.M <= 0 || c.N <= 0 || c.K <= 0) return fail(TSP_ERR_INVALID_ARG, "gemm: empty shape");
-  if (c.K % BK) return fail(TSP_ERR_UNSUPPORTED, "gemm: K must be a multiple of 64");
+  // a ragged last K block reads zeros past the end of K (TMA out-of-bounds fill)
+  if (c.ring_rows > 0 && c.K % BK)
+    return fail(TSP_ERR_UNSUPPORTED, "gemm: ring order needs K to be a multiple of 64");
   if (c.epi == EPI_SWIGLU ? (c.N % 64) : (c.N % 32))
     return fail(TSP_ERR_UNSUPPORTED, "gemm: N must be a multiple of 32 (64 for SwiGLU)");
   if (c.b_row0 < 0 || c.b_row0 + c.N > c.b_rows)
     return fail(TSP_ERR_INVALID_ARG, "gemm: B row range out of bounds");
-  if (!aligned16(c.A) || !aligned16(c.B) || !aligned16(c.C) || (c.R && !aligned16(c.R)) ||
+  if (!aligned16(c.A) || !aligned16(c.B) || (c.C && !aligned16(c.C)) || (c.R && !aligned16(c.R)) ||
       (c.C32 && !aligned16(c.C32)) || (c.lda % 8) || (c.ldb % 8) || (c.ldc % 8) ||
       (c.R && (c.ldr % 8)))
     return fail(TSP_ERR_INVALID_ARG, "gemm: buffers and row strides must be 16-byte aligned");
   if (c.epi == EPI_RESIDUAL && !c.R) return fail(TSP_ERR_INVALID_ARG, "gemm: residual missing");
-  if (c.C32 && (c.epi != EPI_RESIDUAL || c.residual_f32))
+  if (c.epi == EPI_STORE_F32 && (!c.C32 || !aligned16(c.C32) || (c.ldc % 4)))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 output missing or misaligned");
+  if ((c.epi == EPI_SWIGLU_SAVE || c.epi == EPI_SWIGLU_BWD) &&
+      (!c.C2 || !aligned16(c.C2) || (c.ldc2 % 8) || c.N % 128))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: SwiGLU pre-activation buffer missing or misaligned");
+  if (c.C32 && c.epi != EPI_STORE_F32 && (c.epi != EPI_RESIDUAL || c.residual_f32))
     return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 output needs a bf16 residual");
   if (c.epi == EPI_QKV_SPLIT &&
       (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N != 3 * c.split_hd ||
@@ -393,10 +465,17 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
     return fail(TSP_ERR_INVALID_ARG, "gemm: ring order needs ring_kblocks > 0");
 
   CUtensorMap ta, tb;
-  tsp_status st = make_tmap_2d_bf16(&ta, c.A, (uint64_t)c.K, (uint64_t)c.M,
-                                    (uint64_t)c.lda * 2, BK, BM);
+  // K-major operands: [rows][K] with boxes of 64 K-elements; MN-major operands:
+  // [K][rows] with boxes of 64 elements x 64 K-rows
+  tsp_status st = c.a_mn ? make_tmap_2d_bf16(&ta, c.A, (uint64_t)c.M, (uint64_t)c.K,
+                                             (uint64_t)c.lda * 2, 64, 64)
+                         : make_tmap_2d_bf16(&ta, c.A, (uint64_t)c.K, (uint64_t)c.M,
+                                             (uint64_t)c.lda * 2, BK, BM);
   if (st != TSP_OK) return st;
-  st = make_tmap_2d_bf16(&tb, c.B, (uint64_t)c.K, (uint64_t)c.b_rows, (uint64_t)c.ldb * 2, BK, BN);
+  st = c.b_mn ? make_tmap_2d_bf16(&tb, c.B, (uint64_t)c.b_rows, (uint64_t)c.K,
+                                  (uint64_t)c.ldb * 2, 64, 64)
+              : make_tmap_2d_bf16(&tb, c.B, (uint64_t)c.K, (uint64_t)c.b_rows,
+                                  (uint64_t)c.ldb * 2, BK, BN);
   if (st != TSP_OK) return st;
 
   GemmParams p;
@@ -416,6 +495,8 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   p.zz_C = c.zz_C;
   p.zz_T = c.zz_T;
   p.zz_D = c.zz_D;
+  p.C2 = static_cast<__nv_bfloat16*>(c.C2);
+  p.ldc2 = c.ldc2;
   p.ring_rows = (int)c.ring_rows;
   p.ring_kblocks = (int)c.ring_kblocks;
   // Tile order. If B fits easily in the 129 MB L2 (<= 48 MB), walk row-major: A is
@@ -434,16 +515,33 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
 
   const long long tiles = ((c.M + BM - 1) / BM) * ((c.N + BN - 1) / BN);
   const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
-  switch (c.epi) {
-    case EPI_STORE: return launch_epi<K_STORE>(ta, tb, p, grid, stream);
-    case EPI_SWIGLU: return launch_epi<K_SWIGLU>(ta, tb, p, grid, stream);
-    case EPI_QKV_SPLIT: return launch_epi<K_QKV_SPLIT>(ta, tb, p, grid, stream);
-    case EPI_RESIDUAL:
-      if (c.residual_f32) return launch_epi<K_RES_F32>(ta, tb, p, grid, stream);
-      if (c.C32) return launch_epi<K_RES_BF16_OUT32>(ta, tb, p, grid, stream);
-      return launch_epi<K_RES_BF16>(ta, tb, p, grid, stream);
-    default: return fail(TSP_ERR_INVALID_ARG, "gemm: unknown epilogue");
+  const int majors = (c.a_mn ? 2 : 0) + (c.b_mn ? 1 : 0);
+  if (majors == 0) {  // forward products
+    switch (c.epi) {
+      case EPI_STORE: return launch_epi<K_STORE, false, false>(ta, tb, p, grid, stream);
+      case EPI_SWIGLU: return launch_epi<K_SWIGLU, false, false>(ta, tb, p, grid, stream);
+      case EPI_SWIGLU_SAVE: return launch_epi<K_SWIGLU_SAVE, false, false>(ta, tb, p, grid, stream);
+      case EPI_QKV_SPLIT: return launch_epi<K_QKV_SPLIT, false, false>(ta, tb, p, grid, stream);
+      case EPI_RESIDUAL:
+        if (c.residual_f32) return launch_epi<K_RES_F32, false, false>(ta, tb, p, grid, stream);
+        if (c.C32) return launch_epi<K_RES_BF16_OUT32, false, false>(ta, tb, p, grid, stream);
+        return launch_epi<K_RES_BF16, false, false>(ta, tb, p, grid, stream);
+      default: break;
+    }
+  } else if (majors == 1) {  // data gradients: B MN-major
+    switch (c.epi) {
+      case EPI_STORE: return launch_epi<K_STORE, false, true>(ta, tb, p, grid, stream);
+      case EPI_SWIGLU_BWD: return launch_epi<K_SWIGLU_BWD, false, true>(ta, tb, p, grid, stream);
+      case EPI_RESIDUAL:
+        if (c.residual_f32) return launch_epi<K_RES_F32, false, true>(ta, tb, p, grid, stream);
+        if (c.C32) return launch_epi<K_RES_BF16_OUT32, false, true>(ta, tb, p, grid, stream);
+        return launch_epi<K_RES_BF16, false, true>(ta, tb, p, grid, stream);
+      default: break;
+    }
+  } else if (majors == 3) {  // weight gradients: both MN-major, fp32 out
+    if (c.epi == EPI_STORE_F32) return launch_epi<K_STORE_F32, true, true>(ta, tb, p, grid, stream);
   }
+  return fail(TSP_ERR_INVALID_ARG, "gemm: unsupported epilogue / operand layout combination");
 }
 
 }  // namespace tsp

@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <string>
 
 #include "../../include/tsp.h"
@@ -25,6 +26,18 @@ struct WorkspaceLayout {
   size_t g;        // [S][NF]  gated activation (sharded rows)
   size_t stage_in, stage_out;  // [S][H] natural-order staging for tsp_layer_fwd_host
   size_t total;
+  // backward calls only (after `total`):
+  size_t a13;      // [S][2NF] SwiGLU pre-activations A1|A3 (W13's packed column order),
+                   //          overwritten in place by their gradients dA1|dA3
+  size_t dh32;     // [S][H]   fp32 gradient of h (dout + MLP backward)
+  size_t dh;       // [S][H]   the same in bf16 (operand of the attention backward)
+  size_t dob;      // [S][H]   gradient of the attention output before W_O
+  size_t lse;      // [heads][S] fp32 log-sum-exp (natural log) of each query row
+  size_t delta;    // [heads][S] fp32 rowsum(dO * O) of each query row
+  size_t qa;       // [D][S][H/D] Q of every shard (sharded rows)
+  size_t ka, va;   // [D][S][H/D] K, V of every shard (natural rows)
+  size_t dqkv;     // [S][3H]  dQ|dK|dV of shard k at columns [3k H/D, 3(k+1) H/D), sharded rows
+  size_t total_bwd;
 };
 
 struct Plan {
@@ -46,6 +59,35 @@ void set_error(const std::string& msg);
 tsp_status fail(tsp_status code, const std::string& msg);
 tsp_status cuda_fail(cudaError_t err, const char* what);
 
+#define TSP_TRY(expr)              \
+  do {                             \
+    tsp_status st_ = (expr);       \
+    if (st_ != TSP_OK) return st_; \
+  } while (0)
+
+inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline DevStatus* status_of(void* ws) { return static_cast<DevStatus*>(ws); }
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Argument checks of the C entry points (they set the error message).
+inline tsp_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+  for (const void* q : ptrs) {
+    if (!q) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": null pointer");
+    if (!al16(q)) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": pointer not 16-byte aligned");
+  }
+  return TSP_OK;
+}
+inline tsp_status check_ws(void* ws, const char* what) {
+  if (!ws) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": null workspace");
+  if (!al256(ws)) return fail(TSP_ERR_INVALID_ARG, std::string(what) + ": workspace not 256-byte aligned");
+  return TSP_OK;
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 // 2D bf16 map: inner dimension `inner` elements (contiguous), `outer` rows,
 // `row_stride_bytes` between rows, box {box_inner, box_outer}, 128-byte swizzle,
@@ -59,12 +101,24 @@ unsigned long long wait_limit_ns();  // bound of the device-side waits
 // ---------------------------------------------------------------- launchers
 // C[M][N] = A[M][K] * B[N][K]^T with the epilogues below. A rows have stride lda
 // elements; B is rows [b_row0, b_row0 + N) of a [b_rows][K] matrix (stride ldb).
-enum GemmEpilogue { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_QKV_SPLIT = 3 };
+enum GemmEpilogue {
+  EPI_STORE = 0,        // C = bf16(acc)
+  EPI_RESIDUAL = 1,     // C = bf16(acc + R)
+  EPI_SWIGLU = 2,       // C = bf16(silu(gate) * up) of each 256-column tile
+  EPI_QKV_SPLIT = 3,    // Q | K | V columns split (see split_* below)
+  EPI_STORE_F32 = 4,    // C32 = acc in fp32 (weight gradients)
+  EPI_SWIGLU_SAVE = 5,  // EPI_SWIGLU, and the raw pre-activations to C2 (same columns)
+  EPI_SWIGLU_BWD = 6,   // acc = dG [.. x NF]; A1|A3 read from C2; dA1|dA3 to C (C2's order)
+};
 
 struct GemmCall {
   int epi;
-  const void* A; int64_t lda; int64_t M;
-  const void* B; int64_t ldb; int64_t b_rows; int64_t b_row0;
+  // A: [M][K] (K-major) or, with a_mn, [K][M]; row stride lda elements.
+  // B: rows [b_row0, b_row0 + N) of a [b_rows][K] matrix, or with b_mn columns
+  // [b_row0, b_row0 + N) of a [K][b_rows] matrix; row stride ldb elements.
+  const void* A; int64_t lda; int64_t M; int a_mn;
+  const void* B; int64_t ldb; int64_t b_rows; int64_t b_row0; int b_mn;
+  void* C2; int64_t ldc2;      // EPI_SWIGLU_SAVE / EPI_SWIGLU_BWD pre-activations
   int64_t N;  // columns of the product (for EPI_SWIGLU: 2x the output columns)
   int64_t K;
   void* C; int64_t ldc;
@@ -100,6 +154,27 @@ tsp_status launch_kv_gather(const Plan& p, const void* qkv, void* kn, void* vn, 
 tsp_status launch_pack_weights(const Plan& p, const void* Wq, const void* Wk, const void* Wv,
                                const void* Wo, const void* W1, const void* W3, const void* W2,
                                void* wpack, cudaStream_t s);
+tsp_status launch_unpack_grads(const Plan& p, const float* dwpack, float* dWq, float* dWk,
+                               float* dWv, float* dWo, float* dW1, float* dW3, float* dW2,
+                               cudaStream_t s);
 tsp_status launch_wait_selftest(DevStatus* st, unsigned long long limit_ns, cudaStream_t s);
 
+// Steps of the forward (api.cu), shared with the backward orchestration.
+tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
+                                   void* q, void* kn, void* vn, void* ws, cudaStream_t s);
+tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
+                            const void* vn, void* o, void* ws, cudaStream_t s);
+tsp_status o_projection(const Plan& p, const void* o, const void* wpack, const void* residual,
+                        void* out, void* out32, void* ws, cudaStream_t s);
+tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,
+                           void* out, void* out32, void* ws, cudaStream_t s);
+
 }  // namespace tsp
+
+struct tsp_plan_s {
+  tsp::Plan p;
+};
+
+inline tsp_status tsp_check_plan(tsp_plan_t plan) {
+  return plan ? TSP_OK : tsp::fail(TSP_ERR_INVALID_ARG, "null plan");
+}

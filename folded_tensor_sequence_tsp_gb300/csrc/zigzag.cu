@@ -145,6 +145,51 @@ __global__ void pack_weights_kernel(PackArgs a) {
   }
 }
 
+// Weight gradients from the packed layout (fp32) to nn.Linear layout (fp32): each
+// natural element reads its packed position (the inverse of pack_weights_kernel's
+// map; padded ffn columns are dropped). Outputs that are NULL are skipped.
+struct UnpackArgs {
+  const float* in;
+  float *dWq, *dWk, *dWv, *dWo, *dW1, *dW3, *dW2;
+  int H, D, Hd, Fd, Fp, NF, F;
+  long long wp_o, wp_w13, wp_w2;
+};
+
+__global__ void unpack_grads_kernel(UnpackArgs a) {
+  const long long HH = (long long)a.H * a.H, FH = (long long)a.F * a.H;
+  const long long total = 4 * HH + 3 * FH;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    long long e = i;
+    if (e < 3 * HH) {  // dWq, dWk, dWv: row of heads group k -> packed row k*3Hd + part*Hd + j
+      const int part = (int)(e / HH);
+      e -= part * HH;
+      float* out = part == 0 ? a.dWq : (part == 1 ? a.dWk : a.dWv);
+      if (!out) continue;
+      const long long row = e / a.H, col = e - row * a.H;
+      const long long k = row / a.Hd, j = row - k * a.Hd;
+      out[e] = a.in[((k * 3 + part) * a.Hd + j) * a.H + col];
+    } else if ((e -= 3 * HH) < HH) {
+      if (a.dWo) a.dWo[e] = a.in[a.wp_o + e];
+    } else if ((e -= HH) < 2 * FH) {  // dW1, dW3: ffn row f -> padded index fp -> group row
+      const int part = (int)(e / FH);
+      e -= part * FH;
+      float* out = part == 0 ? a.dW1 : a.dW3;
+      if (!out) continue;
+      const long long f = e / a.H, col = e - f * a.H;
+      const long long k = f / a.Fd, fp = k * a.Fp + (f - k * a.Fd);
+      const long long prow = (fp / 128) * 256 + part * 128 + (fp & 127);
+      out[e] = a.in[a.wp_w13 + prow * a.H + col];
+    } else {
+      e -= 2 * FH;  // dW2 [H][F]: column f -> packed column fp
+      if (!a.dW2) continue;
+      const long long row = e / a.F, f = e - row * a.F;
+      const long long k = f / a.Fd, fp = k * a.Fp + (f - k * a.Fd);
+      a.dW2[e] = a.in[a.wp_w2 + row * a.NF + fp];
+    }
+  }
+}
+
 // One thread waits on a barrier that nothing arrives at, with a time bound.
 __global__ void wait_selftest_kernel(DevStatus* st, unsigned long long limit_ns) {
   __shared__ uint64_t bar;
@@ -225,6 +270,33 @@ tsp_status launch_pack_weights(const Plan& p, const void* Wq, const void* Wk, co
   const long long total = a.n_qkv + a.n_o + a.n_w13 + a.n_w2;
   pack_weights_kernel<<<grid_for((total + 255) / 256, 16), 256, 0, s>>>(a);
   return check_launch("pack weights launch");
+}
+
+tsp_status launch_unpack_grads(const Plan& p, const float* dwpack, float* dWq, float* dWk,
+                               float* dWv, float* dWo, float* dW1, float* dW3, float* dW2,
+                               cudaStream_t s) {
+  UnpackArgs a;
+  a.in = dwpack;
+  a.dWq = dWq;
+  a.dWk = dWk;
+  a.dWv = dWv;
+  a.dWo = dWo;
+  a.dW1 = dW1;
+  a.dW3 = dW3;
+  a.dW2 = dW2;
+  a.H = p.H;
+  a.D = p.D;
+  a.Hd = p.Hd;
+  a.Fd = p.Fd;
+  a.Fp = p.Fp;
+  a.NF = p.NF;
+  a.F = p.F;
+  a.wp_o = (long long)p.wp_o;
+  a.wp_w13 = (long long)p.wp_w13;
+  a.wp_w2 = (long long)p.wp_w2;
+  const long long total = 4LL * p.H * p.H + 3LL * p.F * p.H;
+  unpack_grads_kernel<<<grid_for((total + 255) / 256, 16), 256, 0, s>>>(a);
+  return check_launch("unpack weight gradients launch");
 }
 
 tsp_status launch_wait_selftest(DevStatus* st, unsigned long long limit_ns, cudaStream_t s) {

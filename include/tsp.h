@@ -80,7 +80,8 @@ typedef struct tsp_plan_info {
   size_t wpack_w13;   /* [NF/128][256][H]: per 128 padded ffn columns, 128 W1 rows then 128 W3 rows */
   size_t wpack_w2;    /* [H][NF]: W2, shard k = columns [k Fp, (k+1) Fp), zero padded  */
   size_t wpack_elems; /* total elements of the packed buffer                          */
-  size_t workspace_bytes;
+  size_t workspace_bytes;     /* tsp_workspace_bytes(plan)     */
+  size_t bwd_workspace_bytes; /* tsp_bwd_workspace_bytes(plan) */
 } tsp_plan_info;
 
 /*
@@ -275,6 +276,48 @@ tsp_status tsp_swiglu_gate_up(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf1
 tsp_status tsp_swiglu_down(tsp_plan_t plan, const tsp_bf16* g, const tsp_bf16* wpack,
                            const tsp_bf16* residual, const float* residual32, tsp_bf16* out,
                            void* ws, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Backward pass. [TSP] (title, s1) is about training but the page describes the
+ * forward schedules only; the backward is the chain rule of the same layer under
+ * those schedules run in reverse: the MLP's ring (rank r at step t holds shard
+ * (r + t) mod D and accumulates its dh locally) and the attention's broadcast
+ * iterations (per shard: dO, the attention backward, whose K/V gradients are
+ * summed at the key's owner - the reverse of the all-gather - then dx).
+ *   - Weight gradients are fp32 in the PACKED layout of tsp_pack_weights:
+ *     dwpack holds tsp_plan_info.wpack_elems floats, each section at the same
+ *     element offset as in wpack, padded ffn entries written as zero.
+ *     tsp_unpack_weight_grads converts them to the nn.Linear layout.
+ *   - The backward calls recompute the forward activations they need from their
+ *     inputs (no state is kept between calls) and need a workspace of
+ *     tsp_bwd_workspace_bytes(plan) bytes (it extends the forward's workspace).
+ *   - Data gradients (bf16) are [D][T][H] sharded like the activations.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the workspace the *_bwd calls need (256-byte aligned). */
+size_t tsp_bwd_workspace_bytes(tsp_plan_t plan);
+
+/*
+ * tsp_mlp_bwd - backward of tsp_mlp_fwd (no residual) for the output gradient
+ * dmlp [D][T][H]: dhs [D][T][H] = dMLP/dh^T dmlp, and the W1, W3, W2 gradients
+ * written into their sections of dwpack (the attention sections are untouched):
+ *   A1|A3 = hs W13^T and G = silu(A1) A3 are recomputed (one GEMM, both saved),
+ *   dW2 = dmlp^T G, dG = dmlp W2 -> dA1 = dG A3 silu'(A1), dA3 = dG silu(A1) (GEMM
+ *   epilogue), dhs = dA1 W1 + dA3 W3 (K loop in ring order), dW1|dW3 = dA13^T hs.
+ * dhs may not alias hs or dmlp.
+ */
+tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
+                       const tsp_bf16* dmlp, tsp_bf16* dhs, float* dwpack, void* ws,
+                       void* stream);
+
+/*
+ * tsp_unpack_weight_grads - packed fp32 weight gradients -> nn.Linear layout fp32:
+ * dWq/dWk/dWv/dWo [H][H], dW1/dW3 [F][H], dW2 [H][F]. Any output may be NULL
+ * (not written).
+ */
+tsp_status tsp_unpack_weight_grads(tsp_plan_t plan, const float* dwpack, float* dWq, float* dWk,
+                                   float* dWv, float* dWo, float* dW1, float* dW3, float* dW2,
+                                   void* stream);
 
 /*
  * tsp_device_status - synchronise `stream`, then read and clear the workspace

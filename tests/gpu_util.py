@@ -116,6 +116,19 @@ def assert_close(got, want, name="", rel_fro=REL_FRO, max_abs=MAX_ABS, rel_elem=
     return rel, mx
 
 
+def grad_tolerance(want):
+    """(row scale, absolute bound) for a gradient: the layer outputs' bound (3e-2 for
+    activations of rms 1) taken relative to the gradient's own rms, so that weight
+    gradients - sums over all S tokens - are held to the same relative accuracy."""
+    rms = float(np.sqrt((want ** 2).mean())) if want.size else 1.0
+    return row_scale(want), MAX_ABS * max(rms, 1e-30)
+
+
+def assert_close_grad(got, want, name=""):
+    s, atol = grad_tolerance(want)
+    return assert_close(got, want, name, scale=s, max_abs=atol)
+
+
 def rand_bits(shape, seed, std=1.0):
     return tsp_inputs.normal_bf16_bits(shape, std, seed, 42)
 
@@ -157,6 +170,35 @@ class Layer:
 
     def act(self):
         return torch.empty((self.info.S, self.info.hidden), dtype=torch.bfloat16, device="cuda")
+
+    def bwd_workspace(self):
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        ws = torch.empty(tsp.tsp_bwd_workspace_bytes(self.plan), dtype=torch.uint8, device="cuda")
+        tsp.tsp_workspace_init(self.plan, ws)
+        self.ws = ws  # check_status reads this workspace's status word from now on
+        return ws
+
+    def shard(self, t):
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        out = torch.empty_like(t)
+        tsp.tsp_shard(self.plan, t, out)
+        return out
+
+    def unshard(self, t):
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        out = torch.empty_like(t)
+        tsp.tsp_unshard(self.plan, t, out)
+        return out
+
+    def grads(self, dwpack):
+        """Packed fp32 weight gradients -> dict of float64 arrays (nn.Linear layout)."""
+        import folded_tensor_sequence_tsp_gb300 as tsp
+        H, F = self.info.hidden, self.info.ffn
+        out = {k: torch.empty(shape, dtype=torch.float32, device="cuda") for k, shape in (
+            ("dWq", (H, H)), ("dWk", (H, H)), ("dWv", (H, H)), ("dWo", (H, H)),
+            ("dW1", (F, H)), ("dW3", (F, H)), ("dW2", (H, F)))}
+        tsp.tsp_unpack_weight_grads(self.plan, dwpack, **out)
+        return {k: v.cpu().numpy().astype(np.float64) for k, v in out.items()}
 
     def check_status(self):
         import folded_tensor_sequence_tsp_gb300 as tsp
