@@ -321,11 +321,15 @@ def silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def causal_attention_head_backward(q, k, v, q_pos, k_pos, do):
+def causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round=None):
     """Gradients (dq, dk, dv) of one head of causal_attention_head for output grad do.
 
     With P the softmax weights and O = P v: dv = P^T do, dP = do v^T,
-    dS = P * (dP - rowsum(dP * P)), dq = dS k / sqrt(d), dk = dS^T q / sqrt(d).
+    dS = P * (dP - Delta), dq = dS k / sqrt(d), dk = dS^T q / sqrt(d), where
+    Delta_i = rowsum(dP_i * P_i), which equals rowsum(do_i * O_i).
+    With `o_round` (a function of an array), Delta is rowsum(do * o_round(O)): the
+    gradient obtained from a rounded copy of the output, such as the bf16 output a
+    kernel stores and reads back.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -339,14 +343,18 @@ def causal_attention_head_backward(q, k, v, q_pos, k_pos, do):
     p /= p.sum(axis=1, keepdims=True)
     dv = p.T @ do
     dp = do @ v.T
-    ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+    if o_round is None:
+        delta = (dp * p).sum(axis=1, keepdims=True)
+    else:
+        delta = (do * o_round(p @ v)).sum(axis=1, keepdims=True)
+    ds = p * (dp - delta)
     dq = ds @ k / math.sqrt(d)
     dk = ds.T @ q / math.sqrt(d)
     return dq, dk, dv
 
 
 def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_rows,
-                                        q_block: int = 1024):
+                                        q_block: int = 1024, o_round=None):
     """dq of the query rows q_rows and (dk, dv) of the key rows k_rows of one head.
 
     The same quantities as causal_attention_head_backward, for sequences whose full
@@ -361,7 +369,8 @@ def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_row
     q_pos, k_pos = np.asarray(q_pos), np.asarray(k_pos)
     q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
     d = q.shape[1]
-    dq = causal_attention_head_backward(q[q_rows], k, v, q_pos[q_rows], k_pos, do[q_rows])[0]
+    dq = causal_attention_head_backward(q[q_rows], k, v, q_pos[q_rows], k_pos, do[q_rows],
+                                        o_round)[0]
     dk = np.zeros((k_rows.size, d))
     dv = np.zeros((k_rows.size, d))
     for lo in range(0, q.shape[0], q_block):
@@ -372,7 +381,11 @@ def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_row
         p = np.exp(s - s.max(axis=1, keepdims=True))
         p /= p.sum(axis=1, keepdims=True)
         dp = do[r] @ v.T
-        ds = p * (dp - (dp * p).sum(axis=1, keepdims=True))
+        if o_round is None:
+            delta = (dp * p).sum(axis=1, keepdims=True)
+        else:
+            delta = (do[r] * o_round(p @ v)).sum(axis=1, keepdims=True)
+        ds = p * (dp - delta)
         dk += ds[:, k_rows].T @ q[r] / math.sqrt(d)
         dv += p[:, k_rows].T @ do[r]
     return dq, dk, dv

@@ -148,6 +148,26 @@ def check_sampled_backwards(o):
     assert np.abs(sv - dv[kr]).max() < 1e-12
 
 
+def check_rounded_output_delta(o):
+    """Delta from the output itself (identity rounding) is the same gradient; a
+    rounded output changes dq/dk but not dv; the sampled form takes the same option."""
+    n, d = 10, 4
+    q, k, v, do = (_rand((n, d), s) for s in (31, 32, 33, 34))
+    pos = np.arange(n)
+    exact = o.causal_attention_head_backward(q, k, v, pos, pos, do)
+    ident = o.causal_attention_head_backward(q, k, v, pos, pos, do, o_round=lambda x: x)
+    for a, b in zip(exact, ident):
+        assert np.abs(a - b).max() < 1e-12
+    coarse = lambda x: np.round(x * 8) / 8
+    rq, rk, rv = o.causal_attention_head_backward(q, k, v, pos, pos, do, o_round=coarse)
+    assert np.abs(rv - exact[2]).max() < 1e-12
+    assert np.abs(rq - exact[0]).max() > 1e-3 and np.abs(rk - exact[1]).max() > 1e-3
+    qr, kr = np.array([1, 7]), np.array([0, 5])
+    sq, sk, sv = o.causal_attention_head_backward_rows(q, k, v, pos, pos, do, qr, kr, q_block=4,
+                                                       o_round=coarse)
+    assert np.abs(sq - rq[qr]).max() < 1e-12 and np.abs(sk - rk[kr]).max() < 1e-12
+
+
 def check_attention_gradient_sums(o):
     """Per head, the key gradients sum to zero (each softmax row's dS sums to zero)
     and the value gradients sum to the output gradients (each P row sums to one)."""
@@ -161,7 +181,7 @@ def check_attention_gradient_sums(o):
 
 PINS = [check_layer_backward_vs_autograd, check_attention_backward_finite_differences,
         check_closed_forms, check_tsp_backward_equals_plain, check_block_backwards_vs_autograd,
-        check_sampled_backwards, check_attention_gradient_sums]
+        check_sampled_backwards, check_attention_gradient_sums, check_rounded_output_delta]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -176,7 +196,7 @@ def _mutant(**overrides):
     return ns
 
 
-def _attn_bwd_no_rowsum(q, k, v, q_pos, k_pos, do):
+def _attn_bwd_no_rowsum(q, k, v, q_pos, k_pos, do, o_round=None):
     d = q.shape[1]
     s = (q @ k.T) / math.sqrt(d)
     s = np.where(np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
@@ -199,9 +219,10 @@ def _mlp_bwd_no_w3_path(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None):
     return g
 
 
-def _attn_rows_unnormalised(q, k, v, q_pos, k_pos, do, q_rows, k_rows, q_block=1024):
+def _attn_rows_unnormalised(q, k, v, q_pos, k_pos, do, q_rows, k_rows, q_block=1024,
+                            o_round=None):
     dq, dk, dv = oracle.causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do,
-                                                            q_rows, k_rows, q_block)
+                                                            q_rows, k_rows, q_block, o_round)
     return dq, dk, dv * 1.5
 
 
