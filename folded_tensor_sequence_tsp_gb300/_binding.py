@@ -26,6 +26,7 @@ __all__ = [
     "tsp_causal_attention", "tsp_causal_attention_q", "tsp_o_projection",
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
     "tsp_last_error", "tsp_bwd_workspace_bytes", "tsp_mlp_bwd", "tsp_unpack_weight_grads",
+    "tsp_attention_bwd", "tsp_layer_bwd", "tsp_causal_attention_lse", "tsp_causal_attention_bwd",
 ]
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
@@ -51,6 +52,7 @@ class PlanInfo(ctypes.Structure):
         ("wpack_o", ctypes.c_size_t), ("wpack_w13", ctypes.c_size_t),
         ("wpack_w2", ctypes.c_size_t), ("wpack_elems", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t), ("bwd_workspace_bytes", ctypes.c_size_t),
+        ("stat_stride", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -90,6 +92,10 @@ _SIGS = {
     "tsp_bwd_workspace_bytes": (ctypes.c_size_t, [_P]),
     "tsp_mlp_bwd": (_I, [_P] * 8),
     "tsp_unpack_weight_grads": (_I, [_P] * 10),
+    "tsp_attention_bwd": (_I, [_P] * 8),
+    "tsp_layer_bwd": (_I, [_P] * 8),
+    "tsp_causal_attention_lse": (_I, [_P, _I] + [_P] * 7),
+    "tsp_causal_attention_bwd": (_I, [_P, _I] + [_P] * 10),
 }
 
 
@@ -397,3 +403,45 @@ def tsp_unpack_weight_grads(plan, dwpack, dWq=None, dWk=None, dWv=None, dWo=None
         _dev(dWv, "dWv", H * H, f32, optional=True), _dev(dWo, "dWo", H * H, f32, optional=True),
         _dev(dW1, "dW1", F * H, f32, optional=True), _dev(dW3, "dW3", F * H, f32, optional=True),
         _dev(dW2, "dW2", H * F, f32, optional=True), _stream(stream)), "tsp_unpack_weight_grads")
+
+
+def _bwd_block(fn_name, plan, a, wpack, g, dx, dwpack, ws, stream):
+    n = plan.act_elems
+    i = plan.info
+    _check(getattr(load_library(), fn_name)(
+        plan.handle, _dev(a, "input", n), _dev(wpack, "wpack", i.wpack_elems),
+        _dev(g, "output gradient", n), _dev(dx, "input gradient", n),
+        _dev(dwpack, "dwpack", i.wpack_elems, torch.float32), _ws_bwd(plan, ws),
+        _stream(stream)), fn_name)
+
+
+def tsp_attention_bwd(plan, xs, wpack, dattn, dxs, dwpack, ws, stream=None):
+    """Backward of tsp_attention_fwd: dxs and the W_Q/W_K/W_V/W_O sections of dwpack."""
+    _bwd_block("tsp_attention_bwd", plan, xs, wpack, dattn, dxs, dwpack, ws, stream)
+
+
+def tsp_layer_bwd(plan, xs, wpack, dout, dxs, dwpack, ws, stream=None):
+    """Backward of tsp_layer_fwd: dxs and every section of dwpack."""
+    _bwd_block("tsp_layer_bwd", plan, xs, wpack, dout, dxs, dwpack, ws, stream)
+
+
+def tsp_causal_attention_lse(plan, shard, q, kn, vn, o, lse, ws, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    nstat = (i.heads // i.D) * i.stat_stride
+    _check(load_library().tsp_causal_attention_lse(
+        plan.handle, int(shard), _dev(q, "q", n), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _dev(o, "o", plan.act_elems), _dev(lse, "lse", nstat, torch.float32), _ws_status(ws),
+        _stream(stream)), "tsp_causal_attention_lse")
+
+
+def tsp_causal_attention_bwd(plan, shard, q, kn, vn, o, dout, lse, delta, dqkv, ws, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    nstat = (i.heads // i.D) * i.stat_stride
+    _check(load_library().tsp_causal_attention_bwd(
+        plan.handle, int(shard), _dev(q, "q", n), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _dev(o, "o", plan.act_elems), _dev(dout, "dout", plan.act_elems),
+        _dev(lse, "lse", nstat, torch.float32), _dev(delta, "delta", nstat, torch.float32),
+        _dev(dqkv, "dqkv", 3 * plan.act_elems), _ws_status(ws), _stream(stream)),
+        "tsp_causal_attention_bwd")

@@ -158,8 +158,10 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
 // q holds the Q columns of the shard's heads, row stride ld_q (3H/D for the Q|K|V
 // buffer of tsp_qkv_projection, H/D for the Q buffer of the gathered projection).
 tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
-                            const void* vn, void* o, void* ws, cudaStream_t s) {
+                            const void* vn, void* o, void* ws, cudaStream_t s, float* lse) {
   AttentionCall a{};
+  a.lse = lse;
+  a.ld_lse = p.ld_stat;
   a.qkv = qkv;
   a.ld_qkv = ld_q;
   a.kn = kn;
@@ -326,6 +328,7 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
   p.Fp = (p.Fd + 63) / 64 * 64;
   if ((long long)D * p.Fp % 128) p.Fp = (p.Fd + 127) / 128 * 128;
   p.NF = D * p.Fp;
+  p.ld_stat = (S + 127) / 128 * 128;
 
   const size_t H = hidden;
   p.wp_qkv = 0;
@@ -356,8 +359,8 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
   p.ws.dh32 = take(Sz * H * 4);
   p.ws.dh = take(Sz * H * 2);
   p.ws.dob = take(Sz * H * 2);
-  p.ws.lse = take((size_t)heads * Sz * 4);
-  p.ws.delta = take((size_t)heads * Sz * 4);
+  p.ws.lse = take((size_t)heads * p.ld_stat * 4);
+  p.ws.delta = take((size_t)heads * p.ld_stat * 4);
   p.ws.qa = take(Sz * H * 2);
   p.ws.ka = take(Sz * H * 2);
   p.ws.va = take(Sz * H * 2);
@@ -396,6 +399,7 @@ tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info) {
   info->wpack_elems = p.wp_elems;
   info->workspace_bytes = p.ws.total;
   info->bwd_workspace_bytes = p.ws.total_bwd;
+  info->stat_stride = p.ld_stat;
   return TSP_OK;
 }
 

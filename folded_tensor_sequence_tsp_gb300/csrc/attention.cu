@@ -76,6 +76,8 @@ struct AttParams {
   __nv_bfloat16* o;
   long long ld_o;
   long long o_col0;
+  float* lse;          // optional: [head][row] base-2 log-sum-exp of the scaled scores
+  long long ld_lse;
   long long S, T, C;
   int D;
   int heads;
@@ -415,6 +417,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && my_tiles > 0 && warp_wait(&o_done[t], 0u)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      // log2 of the softmax denominator in the scaled base-2 domain: P_ij is then
+      // exp2(s_ij * scale_log2 - lse) for the backward pass
+      if (p.lse != nullptr && row_ok) p.lse[(long long)head * p.ld_lse + grow] = m_ref + __log2f(l);
       __nv_bfloat16* dst = p.o + grow * p.ld_o + p.o_col0 + col_q;
 #pragma unroll
       for (int c = 0; c < HD; c += 32) {
@@ -482,6 +487,8 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.o = static_cast<__nv_bfloat16*>(c.o);
   p.ld_o = c.ld_o;
   p.o_col0 = c.o_col0;
+  p.lse = c.lse;
+  p.ld_lse = c.ld_lse;
   p.S = c.S;
   p.T = c.T;
   p.C = c.C;

@@ -1,0 +1,765 @@
+// attention_bwd.cu - backward of the causal attention of zigzag query rows against
+// the gathered K/V ("Folding Tensor and Sequence Parallelism for Memory-Efficient
+// Transformer Training & Inference", section 2, attention layers; the page gives
+// the forward only, this is its chain rule).
+//
+// With s_ij = q_i . k_j (raw), P_ij = exp2(s_ij * scale_log2 - lse_i) (lse from the
+// forward, base 2), dP_ij = dO_i . v_j and Delta_i = sum_c dO_ic O_ic:
+//     dS_ij = P_ij (dP_ij - Delta_i)
+//     dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
+// (scale = 1/sqrt(d)), over visible pairs (key position <= query position).
+//
+// Two kernels, each a CTA per (128-row tile, head) that keeps its accumulators in
+// tensor memory while the other side streams past (no atomics, deterministic):
+//   key-side  (dK, dV): the CTA owns 128 keys (natural order) and streams every
+//             query tile that sees them (Q, dO, lse, Delta), computing
+//             S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and dK += dS^T Q with
+//             P^T and dS^T read from tensor memory as the A operand. Its dK/dV rows
+//             are the gradient at the key's owner (the reverse of the all-gather)
+//             and are written at the zigzag row of the key.
+//   query-side (dQ): the CTA owns 128 query rows (sharded order) and streams the
+//             key tiles they see, computing S = Q K^T, dP = dO V^T and
+//             dQ += dS K.
+// Each streamed 128-row tile is processed as two 64-column halves with their own
+// score / dP tensor-memory columns; warps 2..5 work on half 0 and warps 6..9 on
+// half 1 (one accumulator row per thread), so the element-wise work of one half
+// overlaps the tensor-core products of the other.
+//   warp 0  TMA producer (2-stage ring of streamed tiles; lse/Delta by bulk copy)
+//   warp 1  TMEM allocation (512 columns) and the single MMA-issuing lane
+// TMEM columns: accumulators [0, 256) (key side: dV [0, d), dK [d, 2d); query side:
+// dQ [0, d)); half h: scores [256 + 128h, +64), dP [320 + 128h, +64). The bf16
+// P^T / dS occupy the first 32 columns of the half's own score / dP columns.
+// MMAs issued by one thread execute in order, so the next tile's scores may be
+// issued right after the products that read the previous P / dS.
+#include "tsp_device.cuh"
+#include "tsp_internal.h"
+
+namespace tsp {
+namespace {
+
+constexpr int BT = 128;       // rows of the tile a CTA owns
+constexpr int IT = 128;       // rows of a streamed tile (two halves)
+constexpr int HALF = 64;
+constexpr int STAGES = 2;
+constexpr int THREADS = 320;
+constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+constexpr uint32_t HALF_ROWS_BYTES = HALF * 128;  // 64 rows of a box
+constexpr uint32_t TMEM_COLS = 512;
+
+__device__ __forceinline__ uint32_t tm_sc(int h) { return 256u + 128u * (uint32_t)h; }
+__device__ __forceinline__ uint32_t tm_dp(int h) { return 320u + 128u * (uint32_t)h; }
+
+struct BwdParams {
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  long long ld_dqkv;
+  const float* lse;
+  const float* delta;
+  long long ld_stat;
+  long long S, T, C;
+  int D;
+  int n_outer;   // owned tiles per head
+  int natural;   // zigzag chunk is a multiple of 128: every 128-row tile is one
+                 // contiguous run of positions
+  float scale_log2;
+  float scale;
+  DevStatus* status;
+  unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ long long zig_row(long long t, long long C, long long T, int D) {
+  const long long c = t / C, o = t - c * C;
+  return c < D ? c * T + o : (2 * D - 1 - c) * T + C + o;
+}
+
+__device__ __forceinline__ long long row_pos(long long r, long long C, long long T, int D) {
+  const long long rank = r / T, l = r - rank * T;
+  return l < C ? rank * C + l : (2 * D - 1 - rank) * C + (l - C);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int HD>
+struct KeyGeom {
+  static constexpr int BOXES = HD / 64;
+  static constexpr uint32_t TILE = 128 * HD * 2;
+  // K, V, then per stage Q, dO, lse[128], Delta[128]
+  static constexpr uint32_t STAGE = 2 * TILE + 1024;
+  static constexpr size_t USED = 1024 + 2 * (size_t)TILE + STAGES * (size_t)STAGE + 256;
+  // all 512 TMEM columns: one CTA per SM
+  static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+};
+
+template <int HD>
+struct QueryGeom {
+  static constexpr int BOXES = HD / 64;
+  static constexpr uint32_t TILE = 128 * HD * 2;
+  // Q, dO, then per stage K, V
+  static constexpr uint32_t STAGE = 2 * TILE;
+  static constexpr size_t USED = 1024 + 2 * (size_t)TILE + STAGES * (size_t)STAGE + 256;
+  static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+};
+
+// K-major operand offset (>> 4) of the kk-th 16-wide K step of a [rows][HD] tile
+// stored as 64-column boxes.
+__device__ __forceinline__ uint32_t kmajor_step(int kk) {
+  return (uint32_t)(((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4);
+}
+
+// ============================================================== key side
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    attention_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                             const __grid_constant__ CUtensorMap tmDO,
+                             const __grid_constant__ CUtensorMap tmK,
+                             const __grid_constant__ CUtensorMap tmV, const BwdParams p,
+                             int q_col0, int do_col0) {
+  using G = KeyGeom<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + G::TILE;
+  uint8_t* sStage = sV + G::TILE;  // stage s: Q, dO, lse, Delta
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + STAGES * G::STAGE);
+  uint64_t* kv_full = bars;               // [1]
+  uint64_t* in_full = kv_full + 1;        // [STAGES]
+  uint64_t* in_empty = in_full + STAGES;  // [STAGES]
+  uint64_t* s_full = in_empty + STAGES;   // [2] per half
+  uint64_t* p_full = s_full + 2;          // [2] per half (4 warps)
+  uint64_t* acc_done = p_full + 2;        // [1]
+  uint64_t* drain = acc_done + 1;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  auto sQ = [&](int st) { return sStage + st * G::STAGE; };
+  auto sDO = [&](int st) { return sStage + st * G::STAGE + G::TILE; };
+  auto sLse = [&](int st) { return reinterpret_cast<float*>(sStage + st * G::STAGE + 2 * G::TILE); };
+  auto sDel = [&](int st) { return sLse(st) + 128; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = blockIdx.x / p.n_outer;
+  const int kt = blockIdx.x - head * p.n_outer;  // ascending: most work first
+  const long long k0 = (long long)kt * BT;
+  const int nq = (int)((p.S + IT - 1) / IT);
+  // streamed query tiles: natural order from the diagonal tile on, else every tile
+  const int n_inner = p.natural ? nq - kt : nq;
+  auto row0_of = [&](int idx) -> long long {
+    return p.natural ? zig_row((long long)(kt + idx) * IT, p.C, p.T, p.D) : (long long)idx * IT;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&in_full[s], 1);
+      mbar_init(&in_empty[s], 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], 4);
+    }
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  WaitBound wb{p.status, p.limit_ns, abort_flag};
+  const float* lse_h = p.lse + (long long)head * p.ld_stat;
+  const float* del_h = p.delta + (long long)head * p.ld_stat;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      mbar_arrive_expect_tx(kv_full, 2 * G::TILE);
+#pragma unroll
+      for (int b = 0; b < G::BOXES; ++b) {
+        tma_load_2d(sK + b * BOX_BYTES, &tmK, kv_full, head * HD + 64 * b, (int)k0);
+        tma_load_2d(sV + b * BOX_BYTES, &tmV, kv_full, head * HD + 64 * b, (int)k0);
+      }
+      int last[STAGES] = {-1, -1};
+      for (int idx = 0; idx < n_inner; ++idx) {
+        const int st = idx % STAGES;
+        const uint32_t ph = (uint32_t)((idx / STAGES) & 1);
+        if (!mbar_wait(&in_empty[st], ph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
+        const long long r0 = row0_of(idx);
+        mbar_arrive_expect_tx(&in_full[st], 2 * G::TILE + 1024);
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b) {
+          tma_load_2d(sQ(st) + b * BOX_BYTES, &tmQ, &in_full[st], q_col0 + head * HD + 64 * b,
+                      (int)r0);
+          tma_load_2d(sDO(st) + b * BOX_BYTES, &tmDO, &in_full[st], do_col0 + head * HD + 64 * b,
+                      (int)r0);
+        }
+        bulk_load(sLse(st), lse_h + r0, 512, &in_full[st]);
+        bulk_load(sDel(st), del_h + r0, 512, &in_full[st]);
+        last[st] = (int)ph;
+      }
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(kv_full, 0, wd, SITE_DRAIN);
+      for (int s = 0; s < STAGES; ++s)
+        if (last[s] >= 0) mbar_wait(&in_full[s], (uint32_t)last[s], wd, SITE_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc_s = make_idesc_bf16(BT, HALF, false);
+      const uint32_t idesc_acc = make_idesc_bf16(BT, HD, true);
+      const uint64_t dk0 = make_sdesc_sw128(smem_addr(sK), 16, 1024);
+      const uint64_t dv0 = make_sdesc_sw128(smem_addr(sV), 16, 1024);
+      const uint64_t dst0 = make_sdesc_sw128(smem_addr(sStage), 16, 1024);            // K-major
+      const uint64_t dst0_mn = make_sdesc_sw128(smem_addr(sStage), BOX_BYTES, 1024);  // MN-major
+      const uint32_t k_lo = (uint32_t)dk0, k_hi = (uint32_t)(dk0 >> 32);
+      const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
+      const uint32_t st_lo = (uint32_t)dst0, st_hi = (uint32_t)(dst0 >> 32);
+      const uint32_t mn_lo = (uint32_t)dst0_mn, mn_hi = (uint32_t)(dst0_mn >> 32);
+      // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (64 query columns of stage st)
+      auto issue_sdp = [&](int h, int st) {
+        const uint32_t q_lo = st_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
+        const uint32_t o_lo = q_lo + G::TILE / 16;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss_w(tmem + tm_sc(h), k_lo + kmajor_step(kk), k_hi, q_lo + kmajor_step(kk), st_hi,
+                   idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss_w(tmem + tm_dp(h), v_lo + kmajor_step(kk), v_hi, o_lo + kmajor_step(kk), st_hi,
+                   idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[h]);
+      };
+      // dV += P^T_h dO_h, dK += dS^T_h Q_h (B MN-major: 16 query rows = 2048 B)
+      auto issue_acc = [&](int h, int st, bool first) {
+        const uint32_t q_lo = mn_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
+        const uint32_t o_lo = q_lo + G::TILE / 16;
+#pragma unroll
+        for (int kk = 0; kk < HALF / 16; ++kk)
+          mma_ts_w(tmem + 0, tmem + tm_sc(h) + (uint32_t)(kk * 8), o_lo + (uint32_t)(kk * 128),
+                   mn_hi, idesc_acc, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int kk = 0; kk < HALF / 16; ++kk)
+          mma_ts_w(tmem + HD, tmem + tm_dp(h) + (uint32_t)(kk * 8), q_lo + (uint32_t)(kk * 128),
+                   mn_hi, idesc_acc, (first && kk == 0) ? 0u : 1u);
+      };
+      bool ok = mbar_wait(kv_full, 0, wb, SITE_BWD_MMA) && mbar_wait(&in_full[0], 0, wb, SITE_BWD_MMA);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0);
+        issue_sdp(1, 0);
+      }
+      for (int idx = 0; ok && idx < n_inner; ++idx) {
+        const int st = idx % STAGES;
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(&p_full[h], (uint32_t)(idx & 1), wb, SITE_BWD_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_acc(h, st, idx == 0 && h == 0);
+          if (h == 1) mma_commit(&in_empty[st]);
+          if (idx + 1 < n_inner) {
+            if (h == 0 && !mbar_wait(&in_full[(idx + 1) % STAGES],
+                                     (uint32_t)(((idx + 1) / STAGES) & 1), wb, SITE_BWD_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sdp(h, (idx + 1) % STAGES);
+          }
+        }
+      }
+      if (ok) mma_commit(acc_done);
+      mma_commit(drain);
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(drain, 0, wd, SITE_DRAIN);
+    }
+  } else {
+    // -------------------------------------------------------------- element-wise
+    const int h = (warp - 2) >> 2;  // half of every streamed tile this warpgroup takes
+    const int qq = warp & 3;        // TMEM lane quarter
+    const int r_local = qq * 32 + lane;
+    const long long kp = k0 + r_local;  // key position of this thread's row
+    const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
+    const uint32_t s_t = lane_base + tm_sc(h), d_t = lane_base + tm_dp(h);
+    bool ok = true;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool mine = mbar_wait(bar, parity, wb, SITE_BWD_ELEMENTWISE);
+      return __all_sync(0xffffffffu, mine) != 0;
+    };
+    for (int idx = 0; idx < n_inner; ++idx) {
+      const int st = idx % STAGES;
+      if (!warp_wait(&s_full[h], (uint32_t)(idx & 1)) ||
+          !warp_wait(&in_full[st], (uint32_t)((idx / STAGES) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const long long r0 = row0_of(idx);
+      const float* sl = sLse(st) + h * HALF;
+      const float* sd = sDel(st) + h * HALF;
+      // query position of column c of this half: natural tiles are contiguous
+      const long long qbase = p.natural ? (long long)(kt + idx) * IT + h * HALF : 0;
+      const bool full_vis = p.natural && qbase >= k0 + BT - 1;
+#pragma unroll
+      for (int c = 0; c < HALF; c += 32) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(s_t + (uint32_t)c, rs);
+        tmem_ld32(d_t + (uint32_t)c, rd);
+        tmem_ld_wait();
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c + e + u;
+            bool vis = true;
+            if (!full_vis) {
+              if (p.natural) {
+                vis = kp <= qbase + col;
+              } else {
+                const long long r = r0 + h * HALF + col;
+                vis = r < p.S && kp <= row_pos(r, p.C, p.T, p.D);
+              }
+            }
+            const float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -sl[col]));
+            pv[u] = vis ? pr : 0.f;
+            dv2[u] = vis ? pr * (__uint_as_float(rd[e + u]) - sd[col]) : 0.f;
+          }
+          pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+          dd[e >> 1] = pack_bf16x2(dv2[0], dv2[1]);
+        }
+        tmem_st16(s_t + (uint32_t)(c / 2), pp);
+        tmem_st16(d_t + (uint32_t)(c / 2), dd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[h]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && warp_wait(acc_done, 0u)) {
+      tc_fence_after();
+      const bool row_ok = kp < p.S;
+      const long long orow = row_ok ? zig_row(kp, p.C, p.T, p.D) : 0;
+      __nv_bfloat16* dvp = p.dv + orow * p.ld_dqkv + head * HD;
+      __nv_bfloat16* dkp = p.dk + orow * p.ld_dqkv + head * HD;
+#pragma unroll
+      for (int c = h * (HD / 2); c < (h + 1) * (HD / 2); c += 32) {
+        uint32_t a[32], b[32];
+        tmem_ld32(lane_base + (uint32_t)c, a);
+        tmem_ld32(lane_base + (uint32_t)(HD + c), b);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint4* v4 = reinterpret_cast<uint4*>(dvp + c);
+          uint4* k4 = reinterpret_cast<uint4*>(dkp + c);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 x, y;
+            x.x = pack_bf16x2(__uint_as_float(a[8 * w + 0]), __uint_as_float(a[8 * w + 1]));
+            x.y = pack_bf16x2(__uint_as_float(a[8 * w + 2]), __uint_as_float(a[8 * w + 3]));
+            x.z = pack_bf16x2(__uint_as_float(a[8 * w + 4]), __uint_as_float(a[8 * w + 5]));
+            x.w = pack_bf16x2(__uint_as_float(a[8 * w + 6]), __uint_as_float(a[8 * w + 7]));
+            y.x = pack_bf16x2(__uint_as_float(b[8 * w + 0]) * p.scale, __uint_as_float(b[8 * w + 1]) * p.scale);
+            y.y = pack_bf16x2(__uint_as_float(b[8 * w + 2]) * p.scale, __uint_as_float(b[8 * w + 3]) * p.scale);
+            y.z = pack_bf16x2(__uint_as_float(b[8 * w + 4]) * p.scale, __uint_as_float(b[8 * w + 5]) * p.scale);
+            y.w = pack_bf16x2(__uint_as_float(b[8 * w + 6]) * p.scale, __uint_as_float(b[8 * w + 7]) * p.scale);
+            v4[w] = x;
+            k4[w] = y;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ============================================================== query side
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    attention_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmDO,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const BwdParams p,
+                            int q_col0, int do_col0) {
+  using G = QueryGeom<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = sQ + G::TILE;
+  uint8_t* sStage = sDO + G::TILE;  // stage s: K, V
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + STAGES * G::STAGE);
+  uint64_t* q_full = bars;                // [1]
+  uint64_t* kv_full = q_full + 1;         // [STAGES]
+  uint64_t* kv_empty = kv_full + STAGES;  // [STAGES]
+  uint64_t* s_full = kv_empty + STAGES;   // [2]
+  uint64_t* p_full = s_full + 2;          // [2]
+  uint64_t* acc_done = p_full + 2;        // [1]
+  uint64_t* drain = acc_done + 1;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = blockIdx.x / p.n_outer;
+  const int blk = blockIdx.x - head * p.n_outer;
+  // natural: query tiles in decreasing position (longest first)
+  const long long r0 = p.natural ? zig_row((long long)(p.n_outer - 1 - blk) * BT, p.C, p.T, p.D)
+                                 : (long long)blk * BT;
+  long long max_pos = 0;
+  if (p.natural) {
+    max_pos = row_pos(r0 + BT - 1, p.C, p.T, p.D);
+  } else {
+    const long long last = min(r0 + BT, p.S);
+    for (long long r = r0; r < last; ++r) max_pos = max(max_pos, row_pos(r, p.C, p.T, p.D));
+  }
+  const int n_tiles = (int)(max_pos / IT) + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], 4);
+    }
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  WaitBound wb{p.status, p.limit_ns, abort_flag};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      mbar_arrive_expect_tx(q_full, 2 * G::TILE);
+#pragma unroll
+      for (int b = 0; b < G::BOXES; ++b) {
+        tma_load_2d(sQ + b * BOX_BYTES, &tmQ, q_full, q_col0 + head * HD + 64 * b, (int)r0);
+        tma_load_2d(sDO + b * BOX_BYTES, &tmDO, q_full, do_col0 + head * HD + 64 * b, (int)r0);
+      }
+      int last[STAGES] = {-1, -1};
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % STAGES;
+        const uint32_t ph = (uint32_t)((j / STAGES) & 1);
+        if (!mbar_wait(&kv_empty[st], ph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * G::TILE);
+        uint8_t* sk = sStage + st * G::STAGE;
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b) {
+          tma_load_2d(sk + b * BOX_BYTES, &tmK, &kv_full[st], head * HD + 64 * b, j * IT);
+          tma_load_2d(sk + G::TILE + b * BOX_BYTES, &tmV, &kv_full[st], head * HD + 64 * b, j * IT);
+        }
+        last[st] = (int)ph;
+      }
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(q_full, 0, wd, SITE_DRAIN);
+      for (int s = 0; s < STAGES; ++s)
+        if (last[s] >= 0) mbar_wait(&kv_full[s], (uint32_t)last[s], wd, SITE_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc_s = make_idesc_bf16(BT, HALF, false);
+      const uint32_t idesc_acc = make_idesc_bf16(BT, HD, true);
+      const uint64_t dq0 = make_sdesc_sw128(smem_addr(sQ), 16, 1024);
+      const uint64_t ddo0 = make_sdesc_sw128(smem_addr(sDO), 16, 1024);
+      const uint64_t dst0 = make_sdesc_sw128(smem_addr(sStage), 16, 1024);
+      const uint64_t dst0_mn = make_sdesc_sw128(smem_addr(sStage), BOX_BYTES, 1024);
+      const uint32_t q_lo = (uint32_t)dq0, q_hi = (uint32_t)(dq0 >> 32);
+      const uint32_t o_lo = (uint32_t)ddo0, o_hi = (uint32_t)(ddo0 >> 32);
+      const uint32_t st_lo = (uint32_t)dst0, st_hi = (uint32_t)(dst0 >> 32);
+      const uint32_t mn_lo = (uint32_t)dst0_mn, mn_hi = (uint32_t)(dst0_mn >> 32);
+      // S_h = Q K_h^T, dP_h = dO V_h^T (64 keys of stage st)
+      auto issue_sdp = [&](int h, int st) {
+        const uint32_t k_lo = st_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
+        const uint32_t v_lo = k_lo + G::TILE / 16;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss_w(tmem + tm_sc(h), q_lo + kmajor_step(kk), q_hi, k_lo + kmajor_step(kk), st_hi,
+                   idesc_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss_w(tmem + tm_dp(h), o_lo + kmajor_step(kk), o_hi, v_lo + kmajor_step(kk), st_hi,
+                   idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[h]);
+      };
+      // dQ += dS_h K_h (B MN-major: 16 key rows = 2048 B)
+      auto issue_acc = [&](int h, int st, bool first) {
+        const uint32_t k_lo = mn_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
+#pragma unroll
+        for (int kk = 0; kk < HALF / 16; ++kk)
+          mma_ts_w(tmem + 0, tmem + tm_dp(h) + (uint32_t)(kk * 8), k_lo + (uint32_t)(kk * 128),
+                   mn_hi, idesc_acc, (first && kk == 0) ? 0u : 1u);
+      };
+      bool ok = mbar_wait(q_full, 0, wb, SITE_BWD_MMA) && mbar_wait(&kv_full[0], 0, wb, SITE_BWD_MMA);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0);
+        issue_sdp(1, 0);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % STAGES;
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(&p_full[h], (uint32_t)(j & 1), wb, SITE_BWD_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_acc(h, st, j == 0 && h == 0);
+          if (h == 1) mma_commit(&kv_empty[st]);
+          if (j + 1 < n_tiles) {
+            if (h == 0 && !mbar_wait(&kv_full[(j + 1) % STAGES], (uint32_t)(((j + 1) / STAGES) & 1),
+                                     wb, SITE_BWD_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sdp(h, (j + 1) % STAGES);
+          }
+        }
+      }
+      if (ok) mma_commit(acc_done);
+      mma_commit(drain);
+      WaitBound wd{p.status, p.limit_ns, nullptr};
+      mbar_wait(drain, 0, wd, SITE_DRAIN);
+    }
+  } else {
+    // -------------------------------------------------------------- element-wise
+    const int h = (warp - 2) >> 2;  // key half of every tile this warpgroup takes
+    const int qq = warp & 3;
+    const int r_local = qq * 32 + lane;
+    const long long grow = r0 + r_local;
+    const bool row_ok = grow < p.S;
+    const long long qpos = row_ok ? row_pos(grow, p.C, p.T, p.D) : -1;
+    const float lse = row_ok ? p.lse[(long long)head * p.ld_stat + grow] : 0.f;
+    const float del = row_ok ? p.delta[(long long)head * p.ld_stat + grow] : 0.f;
+    const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
+    const uint32_t s_t = lane_base + tm_sc(h), d_t = lane_base + tm_dp(h);
+    bool ok = true;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool mine = mbar_wait(bar, parity, wb, SITE_BWD_ELEMENTWISE);
+      return __all_sync(0xffffffffu, mine) != 0;
+    };
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!warp_wait(&s_full[h], (uint32_t)(j & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const long long kbase = (long long)j * IT + h * HALF;
+      const bool full_vis = kbase + HALF - 1 <= qpos;
+#pragma unroll
+      for (int c = 0; c < HALF; c += 32) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(s_t + (uint32_t)c, rs);
+        tmem_ld32(d_t + (uint32_t)c, rd);
+        tmem_ld_wait();
+        uint32_t dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const bool vis = full_vis || kbase + c + e + u <= qpos;
+            const float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -lse));
+            ds[u] = vis ? pr * (__uint_as_float(rd[e + u]) - del) : 0.f;
+          }
+          dd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st16(d_t + (uint32_t)(c / 2), dd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[h]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && warp_wait(acc_done, 0u)) {
+      tc_fence_after();
+      __nv_bfloat16* dqp = p.dq + grow * p.ld_dqkv + head * HD;
+#pragma unroll
+      for (int c = h * (HD / 2); c < (h + 1) * (HD / 2); c += 32) {
+        uint32_t a[32];
+        tmem_ld32(lane_base + (uint32_t)c, a);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint4* q4 = reinterpret_cast<uint4*>(dqp + c);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 x;
+            x.x = pack_bf16x2(__uint_as_float(a[8 * w + 0]) * p.scale, __uint_as_float(a[8 * w + 1]) * p.scale);
+            x.y = pack_bf16x2(__uint_as_float(a[8 * w + 2]) * p.scale, __uint_as_float(a[8 * w + 3]) * p.scale);
+            x.z = pack_bf16x2(__uint_as_float(a[8 * w + 4]) * p.scale, __uint_as_float(a[8 * w + 5]) * p.scale);
+            x.w = pack_bf16x2(__uint_as_float(a[8 * w + 6]) * p.scale, __uint_as_float(a[8 * w + 7]) * p.scale);
+            q4[w] = x;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ============================================================== Delta
+// One thread per (row, 8-column chunk); the chunks of a head are consecutive lanes,
+// reduced with shuffles.
+__global__ void attention_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                       long long ld_vec, int heads, int d, long long S,
+                                       float* __restrict__ delta, long long ld_stat) {
+  const int cph = d / 8;  // chunks per head: 8 or 16, divides 32
+  const long long per_row = (long long)heads * cph;
+  const long long total = S * per_row;
+  for (long long base = (long long)blockIdx.x * blockDim.x; base < total;
+       base += (long long)gridDim.x * blockDim.x) {
+    const long long i = base + threadIdx.x;
+    float acc = 0.f;
+    if (i < total) {
+      const long long row = i / per_row, c = i - row * per_row;
+      const uint4 a = o[row * ld_vec + c], b = dout[row * ld_vec + c];
+      const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        acc += bf16_lo(ua[w]) * bf16_lo(ub[w]) + bf16_hi(ua[w]) * bf16_hi(ub[w]);
+    }
+    // total is a multiple of cph and blocks are multiples of 32 threads, so the
+    // lanes of one head's chunks are all in range or all out of range
+    for (int off = 1; off < cph; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (i < total && (i % cph) == 0) {
+      const long long row = i / per_row, head = (i - row * per_row) / cph;
+      delta[head * ld_stat + row] = acc;
+    }
+  }
+}
+
+template <int HD>
+tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStream_t stream) {
+  CUtensorMap tq, tdo, tk, tv;
+  TSP_TRY(make_tmap_2d_bf16(&tq, c.q, (uint64_t)c.ld_q, (uint64_t)c.S, (uint64_t)c.ld_q * 2, 64, 128));
+  TSP_TRY(make_tmap_2d_bf16(&tdo, c.dout, (uint64_t)c.ld_do, (uint64_t)c.S, (uint64_t)c.ld_do * 2, 64, 128));
+  TSP_TRY(make_tmap_2d_bf16(&tk, c.k, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, 128));
+  TSP_TRY(make_tmap_2d_bf16(&tv, c.v, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, 128));
+  const int tiles = (int)((c.S + 127) / 128);
+  {
+    auto kernel = attention_bwd_dkv_kernel<HD>;
+    const size_t smem = KeyGeom<HD>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "attention bwd: cudaFuncSetAttribute");
+    BwdParams pk = p;
+    pk.n_outer = tiles;
+    kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tq, tdo, tk, tv, pk, 0,
+                                                                   (int)c.do_col0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "attention bwd (key side): launch");
+  }
+  {
+    auto kernel = attention_bwd_dq_kernel<HD>;
+    const size_t smem = QueryGeom<HD>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "attention bwd: cudaFuncSetAttribute");
+    BwdParams pq = p;
+    pq.n_outer = tiles;
+    kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tq, tdo, tk, tv, pq, 0,
+                                                                   (int)c.do_col0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "attention bwd (query side): launch");
+  }
+  return TSP_OK;
+}
+
+}  // namespace
+
+tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) {
+  if (c.d != 64 && c.d != 128) return fail(TSP_ERR_UNSUPPORTED, "attention bwd: head_dim 64 or 128");
+  if (!c.q || !c.k || !c.v || !c.dout || !c.lse || !c.delta || !c.dq || !c.dk || !c.dv || !c.status)
+    return fail(TSP_ERR_INVALID_ARG, "attention bwd: null pointer");
+  if ((c.ld_q % 8) || (c.ld_kv % 8) || (c.ld_do % 8) || (c.do_col0 % 8) || (c.ld_dqkv % 8) ||
+      (c.ld_stat % 128) || c.ld_stat < c.S)
+    return fail(TSP_ERR_INVALID_ARG, "attention bwd: bad strides");
+  if ((reinterpret_cast<uintptr_t>(c.lse) | reinterpret_cast<uintptr_t>(c.delta) |
+       reinterpret_cast<uintptr_t>(c.dq) | reinterpret_cast<uintptr_t>(c.dk) |
+       reinterpret_cast<uintptr_t>(c.dv)) & 15u)
+    return fail(TSP_ERR_INVALID_ARG, "attention bwd: buffers must be 16-byte aligned");
+  if ((long long)c.heads * c.d > c.ld_q || (long long)c.heads * c.d > c.ld_kv ||
+      c.do_col0 + (long long)c.heads * c.d > c.ld_do || (long long)c.heads * c.d > c.ld_dqkv)
+    return fail(TSP_ERR_INVALID_ARG, "attention bwd: head columns exceed the row width");
+  if (c.S > (1ll << 30)) return fail(TSP_ERR_UNSUPPORTED, "attention bwd: S too large");
+  BwdParams p{};
+  p.dq = static_cast<__nv_bfloat16*>(c.dq);
+  p.dk = static_cast<__nv_bfloat16*>(c.dk);
+  p.dv = static_cast<__nv_bfloat16*>(c.dv);
+  p.ld_dqkv = c.ld_dqkv;
+  p.lse = c.lse;
+  p.delta = c.delta;
+  p.ld_stat = c.ld_stat;
+  p.S = c.S;
+  p.T = c.T;
+  p.C = c.C;
+  p.D = c.D;
+  p.natural = (c.C % 128 == 0) ? 1 : 0;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);
+  p.scale = 1.0f / sqrtf((float)c.d);
+  p.status = c.status;
+  p.limit_ns = wait_limit_ns();
+  return c.d == 64 ? launch_bwd_hd<64>(c, p, stream) : launch_bwd_hd<128>(c, p, stream);
+}
+
+tsp_status launch_attention_delta(const void* o, const void* dout, int64_t ld, int heads, int d,
+                                  int64_t S, float* delta, int64_t ld_stat, cudaStream_t stream) {
+  if ((ld % 8) || (d != 64 && d != 128) || (long long)heads * d > ld)
+    return fail(TSP_ERR_INVALID_ARG, "attention delta: bad shape");
+  const long long total = S * heads * (d / 8);
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  attention_delta_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const uint4*>(o), static_cast<const uint4*>(dout), ld / 8, heads, d, S, delta,
+      ld_stat);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TSP_OK : cuda_fail(e, "attention delta: launch");
+}
+
+}  // namespace tsp

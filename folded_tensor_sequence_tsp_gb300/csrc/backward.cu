@@ -128,6 +128,126 @@ tsp_status mlp_backward(const Plan& p, const void* hs, const void* wpack, const 
   return weight_grad(p, a13, 2LL * p.NF, hs, p.H, dwpack + p.wp_w13, p.H, ws, s);  // dW13
 }
 
+// ------------------------------------------------------------------ attention
+
+// dO = dattn W_O (every shard's columns), bf16.
+tsp_status o_projection_dgrad(const Plan& p, const void* dattn, const void* wpack, void* dob,
+                              void* ws, cudaStream_t s) {
+  GemmCall c{};
+  c.epi = EPI_STORE;
+  c.A = dattn;
+  c.lda = p.H;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_o;  // [H][H] = [K][N]
+  c.ldb = p.H;
+  c.b_rows = p.H;
+  c.b_mn = 1;
+  c.N = p.H;
+  c.K = p.H;
+  c.C = dob;
+  c.ldc = p.H;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+// dxs = dQKV W_QKV (+ fp32 residual): K loop over the shards in broadcast order.
+tsp_status qkv_dgrad(const Plan& p, const void* dqkv, const void* wpack, const float* residual32,
+                     void* dxs, void* ws, cudaStream_t s) {
+  GemmCall c{};
+  c.epi = residual32 ? EPI_RESIDUAL : EPI_STORE;
+  c.A = dqkv;
+  c.lda = 3LL * p.H;
+  c.M = p.S;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;  // [3H][H] = [K][N]
+  c.ldb = p.H;
+  c.b_rows = p.H;
+  c.b_mn = 1;
+  c.N = p.H;
+  c.K = 3LL * p.H;
+  c.C = dxs;
+  c.ldc = p.H;
+  c.R = residual32;
+  c.ldr = p.H;
+  c.residual_f32 = residual32 ? 1 : 0;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+// Attention backward of shard k's heads: dQ, dK, dV into the shard's columns of dqkv;
+// lse and delta hold the rows of the shard's heads.
+tsp_status attention_shard_backward(const Plan& p, int k, const void* q, const void* kn,
+                                    const void* vn, const void* dob, const float* lse,
+                                    const float* delta, void* dqkv, void* ws, cudaStream_t s) {
+  AttentionBwdCall a{};
+  a.q = q;
+  a.ld_q = p.Hd;
+  a.k = kn;
+  a.v = vn;
+  a.ld_kv = p.Hd;
+  a.dout = dob;
+  a.ld_do = p.H;
+  a.do_col0 = (int64_t)k * p.Hd;
+  a.lse = lse;
+  a.delta = delta;
+  a.ld_stat = p.ld_stat;
+  uint16_t* base = static_cast<uint16_t*>(dqkv) + (int64_t)k * 3 * p.Hd;
+  a.dq = base;
+  a.dk = base + p.Hd;
+  a.dv = base + 2 * p.Hd;
+  a.ld_dqkv = 3LL * p.H;
+  a.S = p.S;
+  a.T = p.T;
+  a.C = p.C;
+  a.D = p.D;
+  a.heads = p.hpr;
+  a.d = p.d;
+  a.status = status_of(ws);
+  return launch_attention_bwd(a, s);
+}
+
+// The attention forward again, keeping every shard's Q, K, V and each row's lse;
+// o = the attention output before W_O (sharded rows).
+tsp_status attention_recompute(const Plan& p, const void* xs, const void* wpack, void* ws,
+                               cudaStream_t s) {
+  uint16_t* qa = at<uint16_t>(ws, p.ws.qa);
+  uint16_t* ka = at<uint16_t>(ws, p.ws.ka);
+  uint16_t* va = at<uint16_t>(ws, p.ws.va);
+  const int64_t shard = p.S * p.Hd;
+  for (int k = 0; k < p.D; ++k) {
+    TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, qa + k * shard, ka + k * shard,
+                                    va + k * shard, ws, s));
+    TSP_TRY(causal_attention(p, k, qa + k * shard, p.Hd, ka + k * shard, va + k * shard,
+                             at<void>(ws, p.ws.o), ws, s,
+                             at<float>(ws, p.ws.lse) + (int64_t)k * p.hpr * p.ld_stat));
+  }
+  return TSP_OK;
+}
+
+// Backward of the attention block for dattn (bf16), after attention_recompute:
+// dxs = (dAttn/dx)^T dattn (+ residual32), and the W_Q/W_K/W_V/W_O gradients.
+tsp_status attention_backward(const Plan& p, const void* xs, const void* wpack, const void* dattn,
+                              const float* residual32, void* dxs, float* dwpack, void* ws,
+                              cudaStream_t s) {
+  const uint16_t* qa = at<uint16_t>(ws, p.ws.qa);
+  const uint16_t* ka = at<uint16_t>(ws, p.ws.ka);
+  const uint16_t* va = at<uint16_t>(ws, p.ws.va);
+  void* o = at<void>(ws, p.ws.o);
+  void* dob = at<void>(ws, p.ws.dob);
+  void* dqkv = at<void>(ws, p.ws.dqkv);
+  float* lse = at<float>(ws, p.ws.lse);
+  float* delta = at<float>(ws, p.ws.delta);
+  TSP_TRY(o_projection_dgrad(p, dattn, wpack, dob, ws, s));
+  TSP_TRY(weight_grad(p, dattn, p.H, o, p.H, dwpack + p.wp_o, p.H, ws, s));  // dWo = dattn^T o
+  TSP_TRY(launch_attention_delta(o, dob, p.H, p.heads, p.d, p.S, delta, p.ld_stat, s));
+  const int64_t shard = p.S * p.Hd;
+  for (int k = 0; k < p.D; ++k)  // broadcast iteration k, in reverse
+    TSP_TRY(attention_shard_backward(p, k, qa + k * shard, ka + k * shard, va + k * shard, dob,
+                                     lse + (int64_t)k * p.hpr * p.ld_stat,
+                                     delta + (int64_t)k * p.hpr * p.ld_stat, dqkv, ws, s));
+  TSP_TRY(qkv_dgrad(p, dqkv, wpack, residual32, dxs, ws, s));
+  return weight_grad(p, dqkv, 3LL * p.H, xs, p.H, dwpack + p.wp_qkv, p.H, ws, s);  // dW_QKV
+}
+
 }  // namespace
 }  // namespace tsp
 
@@ -146,6 +266,71 @@ tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpac
   if (dhs == hs || dhs == dmlp) return fail(TSP_ERR_INVALID_ARG, "tsp_mlp_bwd: dhs aliases an input");
   return mlp_backward(plan->p, hs, wpack, dmlp, nullptr, dhs, nullptr, dwpack, ws,
                       static_cast<cudaStream_t>(stream));
+}
+
+tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                             const tsp_bf16* dattn, tsp_bf16* dxs, float* dwpack, void* ws,
+                             void* stream) {
+  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, dattn, dxs, dwpack}, "tsp_attention_bwd"));
+  TSP_TRY(check_ws(ws, "tsp_attention_bwd"));
+  if (dxs == xs || dxs == dattn) return fail(TSP_ERR_INVALID_ARG, "tsp_attention_bwd: dxs aliases an input");
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TSP_TRY(attention_recompute(p, xs, wpack, ws, s));
+  return attention_backward(p, xs, wpack, dattn, nullptr, dxs, dwpack, ws, s);
+}
+
+tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                         const tsp_bf16* dout, tsp_bf16* dxs, float* dwpack, void* ws,
+                         void* stream) {
+  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, dout, dxs, dwpack}, "tsp_layer_bwd"));
+  TSP_TRY(check_ws(ws, "tsp_layer_bwd"));
+  if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd: dxs aliases an input");
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* h = at<void>(ws, p.ws.h);
+  float* h32 = at<float>(ws, p.ws.h32);
+  void* dh = at<void>(ws, p.ws.dh);
+  float* dh32 = at<float>(ws, p.ws.dh32);
+  // forward recompute: every shard's Q/K/V, lse and o; h = x + o W_O^T
+  TSP_TRY(attention_recompute(p, xs, wpack, ws, s));
+  TSP_TRY(o_projection(p, at<void>(ws, p.ws.o), wpack, xs, h, h32, ws, s));
+  // dh = dout + MLP backward of dout at h (fp32, and bf16 for the products below)
+  TSP_TRY(mlp_backward(p, h, wpack, dout, dout, dh, dh32, dwpack, ws, s));
+  // dx = dh + attention backward of dh
+  return attention_backward(p, xs, wpack, dh, dh32, dxs, dwpack, ws, s);
+}
+
+tsp_status tsp_causal_attention_lse(tsp_plan_t plan, int shard, const tsp_bf16* q,
+                                    const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
+                                    float* lse, void* ws, void* stream) {
+  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_ptrs({q, kn, vn, o, lse}, "tsp_causal_attention_lse"));
+  TSP_TRY(check_ws(ws, "tsp_causal_attention_lse"));
+  if (shard < 0 || shard >= plan->p.D)
+    return fail(TSP_ERR_INVALID_ARG, "tsp_causal_attention_lse: shard out of range");
+  const Plan& p = plan->p;
+  return causal_attention(p, shard, q, p.Hd, kn, vn, o, ws, static_cast<cudaStream_t>(stream), lse);
+}
+
+tsp_status tsp_causal_attention_bwd(tsp_plan_t plan, int shard, const tsp_bf16* q,
+                                    const tsp_bf16* kn, const tsp_bf16* vn, const tsp_bf16* o,
+                                    const tsp_bf16* dout, const float* lse, float* delta,
+                                    tsp_bf16* dqkv, void* ws, void* stream) {
+  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_ptrs({q, kn, vn, o, dout, lse, delta, dqkv}, "tsp_causal_attention_bwd"));
+  TSP_TRY(check_ws(ws, "tsp_causal_attention_bwd"));
+  if (shard < 0 || shard >= plan->p.D)
+    return fail(TSP_ERR_INVALID_ARG, "tsp_causal_attention_bwd: shard out of range");
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t col = (int64_t)shard * p.Hd;
+  TSP_TRY(launch_attention_delta(static_cast<const uint16_t*>(o) + col,
+                                 static_cast<const uint16_t*>(dout) + col, p.H, p.hpr, p.d, p.S,
+                                 delta, p.ld_stat, s));
+  return attention_shard_backward(p, shard, q, kn, vn, dout, lse, delta, dqkv, ws, s);
 }
 
 tsp_status tsp_unpack_weight_grads(tsp_plan_t plan, const float* dwpack, float* dWq, float* dWk,

@@ -30,6 +30,9 @@ enum Site : unsigned int {
   SITE_ATT_SOFTMAX = 6,
   SITE_DRAIN = 7,
   SITE_SELFTEST = 8,
+  SITE_BWD_PRODUCER = 9,
+  SITE_BWD_MMA = 10,
+  SITE_BWD_ELEMENTWISE = 11,
 };
 
 constexpr unsigned int kStatusTimeout = 4;  // == TSP_ERR_TIMEOUT
@@ -128,6 +131,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0),
+// completing on `bar` like the tensor loads.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 

@@ -50,6 +50,7 @@ struct Plan {
   int Fd;   // F / D
   int Fp;   // padded shard width of the MLP
   int NF;   // D * Fp
+  int64_t ld_stat;  // row stride of the per-head row statistics (S rounded up to 128)
   size_t wp_qkv, wp_o, wp_w13, wp_w2, wp_elems;
   WorkspaceLayout ws;
 };
@@ -140,12 +141,35 @@ struct AttentionCall {
   const void* qkv; int64_t ld_qkv;   // Q at columns [j*d, (j+1)*d) for head j of the group
   const void* kn; const void* vn; int64_t ld_kv;
   void* o; int64_t ld_o; int64_t o_col0;
+  float* lse; int64_t ld_lse;  // optional [heads][ld_lse] log-sum-exp (base 2) per row
   int64_t S; int64_t T; int64_t C; int D;
   int heads;  // heads in this call
   int d;
   DevStatus* status;
 };
 tsp_status launch_attention(const AttentionCall& call, cudaStream_t stream);
+
+// Attention backward of the heads of one shard (all ranks' queries).
+//   q [S][ld_q] (sharded rows), k, v [S][ld_kv] (natural rows), head j at columns j*d;
+//   dout [S][ld_do] (sharded rows), head j at columns do_col0 + j*d;
+//   lse, delta [heads][ld_stat] fp32 per sharded row (lse from the forward, base 2;
+//   delta = rowsum(dO * O));
+//   dq, dk, dv [S][ld_dqkv] bf16 written at sharded rows, head j at columns j*d of
+//   each pointer (dK/dV rows at the sharded row of their key position).
+struct AttentionBwdCall {
+  const void* q; int64_t ld_q;
+  const void* k; const void* v; int64_t ld_kv;
+  const void* dout; int64_t ld_do; int64_t do_col0;
+  const float* lse; const float* delta; int64_t ld_stat;
+  void* dq; void* dk; void* dv; int64_t ld_dqkv;
+  int64_t S, T, C; int D;
+  int heads, d;
+  DevStatus* status;
+};
+tsp_status launch_attention_bwd(const AttentionBwdCall& call, cudaStream_t stream);
+// delta[j][r] = sum_c dout[r][j*d + c] * o[r][j*d + c] for heads j < heads, rows r < S
+tsp_status launch_attention_delta(const void* o, const void* dout, int64_t ld, int heads, int d,
+                                  int64_t S, float* delta, int64_t ld_stat, cudaStream_t stream);
 
 tsp_status launch_zigzag_index(const Plan& p, int32_t* fwd, int32_t* inv, cudaStream_t s);
 tsp_status launch_zigzag_rows(const Plan& p, const void* src, void* dst, int64_t width,
@@ -162,8 +186,10 @@ tsp_status launch_wait_selftest(DevStatus* st, unsigned long long limit_ns, cuda
 // Steps of the forward (api.cu), shared with the backward orchestration.
 tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
                                    void* q, void* kn, void* vn, void* ws, cudaStream_t s);
+// lse (optional): [heads/D][ld_stat], the rows of shard k's heads.
 tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
-                            const void* vn, void* o, void* ws, cudaStream_t s);
+                            const void* vn, void* o, void* ws, cudaStream_t s,
+                            float* lse = nullptr);
 tsp_status o_projection(const Plan& p, const void* o, const void* wpack, const void* residual,
                         void* out, void* out32, void* ws, cudaStream_t s);
 tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,

@@ -82,6 +82,7 @@ typedef struct tsp_plan_info {
   size_t wpack_elems; /* total elements of the packed buffer                          */
   size_t workspace_bytes;     /* tsp_workspace_bytes(plan)     */
   size_t bwd_workspace_bytes; /* tsp_bwd_workspace_bytes(plan) */
+  int64_t stat_stride;        /* row stride of per-head row statistics (lse, delta): S rounded up to 128 */
 } tsp_plan_info;
 
 /*
@@ -309,6 +310,58 @@ size_t tsp_bwd_workspace_bytes(tsp_plan_t plan);
 tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
                        const tsp_bf16* dmlp, tsp_bf16* dhs, float* dwpack, void* ws,
                        void* stream);
+
+/*
+ * tsp_attention_bwd - backward of tsp_attention_fwd (no residual) for the output
+ * gradient dattn [D][T][H]: dxs [D][T][H] and the W_Q, W_K, W_V, W_O gradients in
+ * their sections of dwpack (the MLP sections are untouched). Per broadcast
+ * iteration k the forward is recomputed (Q/K/V of shard k with the K/V gather, the
+ * attention with each row's log-sum-exp); then dO = dattn W_O, dW_O = dattn^T O,
+ * Delta = rowsum(dO * O), the attention backward of shard k's heads (dK/dV summed
+ * over every rank's queries, written at the key owner's rows), and finally
+ * dxs = dQKV W_QKV (K loop over the shards in broadcast order) and
+ * dW_QKV = dQKV^T xs. dxs may not alias xs or dattn.
+ */
+tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                             const tsp_bf16* dattn, tsp_bf16* dxs, float* dwpack, void* ws,
+                             void* stream);
+
+/*
+ * tsp_layer_bwd - backward of tsp_layer_fwd for the output gradient dout [D][T][H]:
+ *   dh  = dout + MLP backward of dout at h (h = xs + Attn(xs), recomputed),
+ *   dxs = dh + attention backward of dh,
+ * and every weight gradient in dwpack. dh is kept in fp32 for the residual and
+ * rounded to bf16 once, as the operand of the attention backward's products.
+ * dxs may not alias xs or dout.
+ */
+tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                         const tsp_bf16* dout, tsp_bf16* dxs, float* dwpack, void* ws,
+                         void* stream);
+
+/*
+ * tsp_causal_attention_lse - tsp_causal_attention_q that also writes, for each of
+ * shard k's heads j and query row r, lse[j * stat_stride + r] = log2 of the softmax
+ * denominator of the row in the base-2 domain of the scaled scores, i.e. the
+ * softmax weight of key t is exp2(q.k_t * log2(e)/sqrt(d) - lse). lse is
+ * [H/(D d)][stat_stride] float (tsp_plan_info.stat_stride).
+ */
+tsp_status tsp_causal_attention_lse(tsp_plan_t plan, int shard, const tsp_bf16* q,
+                                    const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
+                                    float* lse, void* ws, void* stream);
+
+/*
+ * tsp_causal_attention_bwd - backward of the attention step of shard k. Inputs: q
+ * [D*T][H/D] (sharded rows), kn, vn [S][H/D] (natural rows), o and dout [D*T][H]
+ * (shard k's columns [k H/D, (k+1) H/D) are read), lse from
+ * tsp_causal_attention_lse. Writes delta [H/(D d)][stat_stride] = rowsum(dout * o)
+ * per head and row, and dQ | dK | dV of the shard's heads into columns
+ * [3k H/D, 3(k+1) H/D) of dqkv [D*T][3H] (sharded rows; the dK/dV row of key t is
+ * the zigzag row of t and sums the contributions of every rank's queries).
+ */
+tsp_status tsp_causal_attention_bwd(tsp_plan_t plan, int shard, const tsp_bf16* q,
+                                    const tsp_bf16* kn, const tsp_bf16* vn, const tsp_bf16* o,
+                                    const tsp_bf16* dout, const float* lse, float* delta,
+                                    tsp_bf16* dqkv, void* ws, void* stream);
 
 /*
  * tsp_unpack_weight_grads - packed fp32 weight gradients -> nn.Linear layout fp32:

@@ -98,14 +98,15 @@ def layer_tolerance(out_ref, G_ref, h_ref, W):
 
 
 def assert_close(got, want, name="", rel_fro=REL_FRO, max_abs=MAX_ABS, rel_elem=REL_ELEM,
-                 scale=None):
+                 scale=None, extra=None):
     assert got.shape == want.shape, (name, got.shape, want.shape)
     assert np.isfinite(got).all(), f"{name}: non-finite values"
     rel, mx = errors(got, want)
     excess, where = 0.0, ""
     if got.size:
         s = row_scale(want) if scale is None else scale
-        ex = (np.abs(got - want) - rel_elem * np.abs(want)) / s
+        allow = rel_elem * np.abs(want) + (0.0 if extra is None else extra)
+        ex = (np.abs(got - want) - allow) / s
         k = np.unravel_index(int(np.argmax(ex)), ex.shape)
         excess = float(ex[k])
         sk = float(np.broadcast_to(s, ex.shape)[k]) if np.ndim(s) else float(s)
@@ -124,9 +125,23 @@ def grad_tolerance(want):
     return row_scale(want), MAX_ABS * max(rms, 1e-30)
 
 
-def assert_close_grad(got, want, name=""):
+def bf16_round(x):
+    """Round float64 values to bfloat16 (through float32, nearest-even)."""
+    return oracle.widen_bf16(tsp_inputs.bf16_bits_from_f32(np.asarray(x, dtype=np.float32)))
+
+
+def assert_close_grad(got, want, name="", noise=None):
+    """assert_close with grad_tolerance. `noise` (the oracle's gradient computed from a
+    bf16-rounded attention output, minus the exact one) adds 4x its row rms to each
+    row's allowance: Delta = rowsum(dO * O) is formed from the stored bf16 output, and
+    rows that attend to few keys (the first positions) amplify that rounding into
+    dq/dk errors of several percent of the gradient's rms, which no bf16-output
+    implementation avoids."""
     s, atol = grad_tolerance(want)
-    return assert_close(got, want, name, scale=s, max_abs=atol)
+    extra = None
+    if noise is not None:
+        extra = 4.0 * np.sqrt((noise ** 2).mean(axis=1, keepdims=True))
+    return assert_close(got, want, name, scale=s, max_abs=atol, extra=extra)
 
 
 def rand_bits(shape, seed, std=1.0):

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import Layer, assert_close_grad, dev, f64, rand_bits
+from gpu_util import Layer, assert_close_grad, bf16_round, dev, f64, rand_bits
 
 tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
 pytestmark = pytest.mark.gpu
@@ -89,3 +89,135 @@ def test_unpack_weight_grads_inverts_the_packing():
     back = L.grads(packed32)
     for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2"):
         assert np.array_equal(back["d" + k], L.f(k)), k
+
+
+# ---------------------------------------------------------------- attention
+
+ATT_SHAPES = {
+    "tiny": (2, 256, 256, 4, 688),        # zigzag chunk 64: tiles mix chunks
+    "ragged": (2, 200, 128, 2, 96),       # partial last tile
+    "d3": (3, 1152, 384, 6, 600),
+    "hd128": (2, 512, 512, 4, 1024),      # chunk 128: contiguous tiles, head_dim 128
+    "small": (4, 4096, 1024, 16, 2816),
+}
+
+
+def _attention_step(L, k, seed):
+    """Synthetic Q (sharded rows), K, V (natural rows), dO (sharded rows) for shard k;
+    GPU forward-with-lse then backward. Returns the inputs' bits and dqkv."""
+    i = L.info
+    S, Hd, H = i.S, i.shard_hidden, i.hidden
+    qb, kb, vb = (rand_bits((S, Hd), seed + j) for j in range(3))
+    dob = rand_bits((S, H), seed + 3)
+    q, kn, vn, do = dev(qb), dev(kb), dev(vb), dev(dob)
+    hpr = i.heads // i.D
+    o = torch.zeros((S, H), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(hpr * i.stat_stride, dtype=torch.float32, device="cuda")
+    delta = torch.empty_like(lse)
+    dqkv = torch.zeros((S, 3 * H), dtype=torch.bfloat16, device="cuda")
+    tsp.tsp_causal_attention_lse(L.plan, k, q, kn, vn, o, lse, L.ws)
+    tsp.tsp_causal_attention_bwd(L.plan, k, q, kn, vn, o, do, lse, delta, dqkv, L.ws)
+    L.check_status()
+    return (qb, kb, vb, dob), dqkv
+
+
+@pytest.mark.parametrize("name", list(ATT_SHAPES))
+def test_attention_step_backward_matches_oracle(name):
+    L = Layer(*ATT_SHAPES[name], seed=31, names=["x"])
+    i = L.info
+    S, D, Hd, d = i.S, i.D, i.shard_hidden, i.head_dim
+    k = D - 1
+    (qb, kb, vb, dob), dqkv = _attention_step(L, k, 32)
+    q, kk, v, do = (oracle.widen_bf16(b) for b in (qb, kb, vb, dob))
+    q_pos = oracle.rank_positions(S, D).reshape(-1)
+    k_pos = np.arange(S)
+    zig = oracle.zigzag_forward_index(S, D)  # sharded row of each token
+    got = f64(dqkv)
+    base = 3 * Hd * k
+    for j in range(i.heads // D):
+        c = slice(j * d, (j + 1) * d)
+        args = (q[:, c], kk[:, c], v[:, c], q_pos, k_pos,
+                do[:, k * Hd + j * d: k * Hd + (j + 1) * d])
+        dq, dk, dv = oracle.causal_attention_head_backward(*args)
+        rq, rk, _ = oracle.causal_attention_head_backward(*args, o_round=bf16_round)
+        assert_close_grad(got[:, base + j * d: base + (j + 1) * d], dq, f"{name} dq head {j}",
+                          noise=rq - dq)
+        assert_close_grad(got[zig, base + Hd + j * d: base + Hd + (j + 1) * d], dk,
+                          f"{name} dk head {j}", noise=rk - dk)
+        assert_close_grad(got[zig, base + 2 * Hd + j * d: base + 2 * Hd + (j + 1) * d], dv,
+                          f"{name} dv head {j}")
+    # other shards' columns are untouched
+    other = np.ones(3 * i.hidden, bool)
+    other[base: base + 3 * Hd] = False
+    assert not got[:, other].any()
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "d3", "hd128", "small"])
+def test_attention_block_backward_matches_oracle(name):
+    L = Layer(*ATT_SHAPES[name], seed=33)
+    ws = L.bwd_workspace()
+    g_bits, g_dev = _dout(L, 34)
+    dxs = L.act()
+    dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+    tsp.tsp_attention_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dxs, dwpack, ws)
+    L.check_status()
+    got = L.grads(dwpack)
+    W = L.weights64()
+    ref = oracle.attention_block_backward(L.f("x"), W["Wq"], W["Wk"], W["Wv"], W["Wo"],
+                                          L.info.heads, oracle.widen_bf16(g_bits))
+    assert_close_grad(f64(L.unshard(dxs)), ref["dx"], f"{name} dx")
+    for k in ("dWq", "dWk", "dWv", "dWo"):
+        assert_close_grad(got[k], ref[k], f"{name} {k}")
+    assert not dwpack[L.info.wpack_w13:].any()  # MLP sections untouched
+
+
+# ---------------------------------------------------------------- whole layer
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "d3", "hd128", "small"])
+def test_layer_backward_matches_oracle(name):
+    L = Layer(*ATT_SHAPES[name], seed=35)
+    ws = L.bwd_workspace()
+    g_bits, g_dev = _dout(L, 36)
+    dxs = L.act()
+    dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+    tsp.tsp_layer_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dxs, dwpack, ws)
+    L.check_status()
+    got = L.grads(dwpack)
+    ref = oracle.layer_backward(L.f("x"), L.weights64(), L.info.heads, oracle.widen_bf16(g_bits))
+    assert_close_grad(f64(L.unshard(dxs)), ref["dx"], f"{name} dx")
+    for k in ("dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"):
+        assert_close_grad(got[k], ref[k], f"{name} {k}")
+
+
+def test_layer_backward_is_the_same_for_every_D():
+    """The sharded backward computes the plain layer's gradients for D = 1, 2, 4, 8."""
+    S, H, heads, F = 1024, 512, 8, 1024
+    outs = {}
+    for D in (1, 2, 4, 8):
+        L = Layer(D, S, H, heads, F, seed=37)
+        ws = L.bwd_workspace()
+        g_bits, g_dev = _dout(L, 38)
+        dxs = L.act()
+        dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+        tsp.tsp_layer_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dxs, dwpack, ws)
+        L.check_status()
+        outs[D] = dict(L.grads(dwpack), dx=f64(L.unshard(dxs)))
+    ref = oracle.layer_backward(L.f("x"), L.weights64(), heads, oracle.widen_bf16(g_bits))
+    for D, g in outs.items():
+        for k, want in ref.items():
+            assert_close_grad(g[k], want, f"D={D} {k}")
+
+
+def test_layer_backward_is_deterministic():
+    L = Layer(*ATT_SHAPES["small"], seed=39)
+    ws = L.bwd_workspace()
+    _, g_dev = _dout(L, 40)
+    xs, dout = L.sharded_x(), L.shard(g_dev)
+    res = []
+    for _ in range(2):
+        dxs = L.act()
+        dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+        tsp.tsp_layer_bwd(L.plan, xs, L.wpack, dout, dxs, dwpack, ws)
+        res.append((dxs.view(torch.int16).clone(), dwpack.clone()))
+    L.check_status()
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
