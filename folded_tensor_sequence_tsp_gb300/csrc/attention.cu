@@ -376,14 +376,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int e = 0; e < KT; ++e)
           if (kv0 + e > pos) sc[e] = -INFINITY;
       }
-      // row maximum: three-input max, 4 independent chains (short dependency chains)
+      // row maximum: three-input max, 4 independent chains (short dependency chains):
+      // sc[0..3] start the chains, 15 steps take 8 scores each (sc[4..123]), and the
+      // last four scores close them
       float m4[4] = {sc[0], sc[1], sc[2], sc[3]};
 #pragma unroll
-      for (int e = 4; e < KT; e += 8) {
+      for (int e = 4; e + 8 <= KT; e += 8) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) m4[k] = max3f(m4[k], sc[e + k], sc[e + 4 + k]);
       }
-      const float mraw = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+      static_assert(KT % 8 == 0, "the tail below covers the last 4 scores");
+      const float mraw = max3f(max3f(m4[0], m4[1], sc[KT - 4]), max3f(m4[2], m4[3], sc[KT - 3]),
+                               fmaxf(sc[KT - 2], sc[KT - 1]));
       const float mx = mraw * p.scale_log2;  // scale > 0 keeps the order
       // move the reference only when the tile maximum outgrows it by the threshold
       float factor = 1.f;

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle
+import tsp_inputs
 from gpu_util import Layer, assert_close_grad, bf16_round, dev, f64, rand_bits
 
 tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
@@ -221,3 +222,73 @@ def test_layer_backward_is_deterministic():
         res.append((dxs.view(torch.int16).clone(), dwpack.clone()))
     L.check_status()
     assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+# ---------------------------------------------------------------- 7B shapes, sampled
+
+@pytest.mark.slow
+def test_7b_mlp_backward_sampled():
+    """MLP backward at the 7B shape and 64K tokens (the benchmark's launch): 256
+    sampled rows of dh and 16 sampled ffn indices of dW1, dW3 (rows) and dW2
+    (columns), each computed by the oracle over every token."""
+    cfg = tsp_inputs.config_by_name("7b-64k")
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed)
+    ws = L.bwd_workspace()
+    g_bits, g_dev = _dout(L, 41)
+    dhs = L.act()
+    dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+    tsp.tsp_mlp_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dhs, dwpack, ws)
+    L.check_status()
+    rows = tsp_inputs.sample_rows(cfg.S, 256, cfg.seed)
+    got_dh = f64(L.unshard(dhs)[torch.from_numpy(rows).cuda()])
+    got = L.grads(dwpack)
+    del dhs, dwpack, ws
+    cols = np.sort(np.random.default_rng(cfg.seed).choice(cfg.ffn, 16, replace=False))
+    W = L.weights64()
+    ref = oracle.swiglu_mlp_backward(L.f("x"), W["W1"], W["W3"], W["W2"],
+                                     oracle.widen_bf16(g_bits), rows=rows, ffn_cols=cols)
+    assert_close_grad(got_dh, ref["dh"], "7b dh rows")
+    assert_close_grad(got["dW1"][cols], ref["dW1"], "7b dW1 rows")
+    assert_close_grad(got["dW3"][cols], ref["dW3"], "7b dW3 rows")
+    assert_close_grad(got["dW2"][:, cols], ref["dW2"], "7b dW2 columns")
+
+
+@pytest.mark.slow
+def test_7b_attention_step_backward_sampled():
+    """Attention backward of one shard (4 heads of 128) at 64K tokens: dq of 256
+    sampled query rows for every head, dk/dv of 256 sampled key rows for head 0 (the
+    oracle visits every query for those)."""
+    cfg = tsp_inputs.config_by_name("7b-64k")
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed, names=["x"])
+    i = L.info
+    S, D, Hd, d = i.S, i.D, i.shard_hidden, i.head_dim
+    k = D - 1
+    (qb, kb, vb, dob), dqkv = _attention_step(L, k, 42)
+    q_rows = tsp_inputs.sample_rows(S, 256, cfg.seed)  # sharded rows
+    k_rows = tsp_inputs.sample_rows(S, 256, cfg.seed + 1)  # key positions
+    zig = oracle.zigzag_forward_index(S, D)
+    base = 3 * Hd * k
+    got_q = f64(dqkv[torch.from_numpy(q_rows).cuda(), base: base + Hd])
+    kz = torch.from_numpy(zig[k_rows]).cuda()
+    got_k = f64(dqkv[kz, base + Hd: base + Hd + d])
+    got_v = f64(dqkv[kz, base + 2 * Hd: base + 2 * Hd + d])
+    del dqkv
+    q, kk, v, do = (oracle.widen_bf16(b) for b in (qb, kb, vb, dob))
+    q_pos = oracle.rank_positions(S, D).reshape(-1)
+    k_pos = np.arange(S)
+    for j in range(i.heads // D):
+        c = slice(j * d, (j + 1) * d)
+        dO = do[:, k * Hd + j * d: k * Hd + (j + 1) * d]
+        # dq of a query needs that query's own softmax row only
+        args = (q[q_rows, c], kk[:, c], v[:, c], q_pos[q_rows], k_pos, dO[q_rows])
+        dq = oracle.causal_attention_head_backward(*args)[0]
+        rq = oracle.causal_attention_head_backward(*args, o_round=bf16_round)[0]
+        assert_close_grad(got_q[:, c], dq, f"7b dq head {j}", noise=rq - dq)
+    # dk, dv of head 0: every query that sees the sampled keys
+    c = slice(0, d)
+    dO = do[:, k * Hd: k * Hd + d]
+    args = (q[:, c], kk[:, c], v[:, c], q_pos, k_pos, dO, q_rows[:1], k_rows)
+    _, dk, dv = oracle.causal_attention_head_backward_rows(*args, q_block=2048)
+    _, rk, _ = oracle.causal_attention_head_backward_rows(*args, q_block=2048, o_round=bf16_round)
+    assert_close_grad(got_k, dk, "7b dk head 0", noise=rk - dk)
+    assert_close_grad(got_v, dv, "7b dv head 0")

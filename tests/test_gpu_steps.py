@@ -164,6 +164,30 @@ def test_causal_attention(layer):
     layer.check_status()
 
 
+def test_causal_attention_sharp_scores_and_first_token(layer):
+    """Scores of std ~9 (q, k ~ N(0, 3^2)): each row's softmax is dominated by one key,
+    so an error in the row maximum shows up as an overflowing or mis-scaled P. The
+    token at position 0 attends to itself alone: its output is its value row, bit
+    for bit, in every head."""
+    i = layer.info
+    Hd, hpr, d = i.shard_hidden, i.heads // i.D, i.head_dim
+    q_bits = rand_bits((i.S, Hd), 51, std=3.0)
+    k_bits = rand_bits((i.S, Hd), 52, std=3.0)
+    v_bits = rand_bits((i.S, Hd), 53)
+    o = torch.full((i.S, i.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    shard = i.D - 1
+    tsp.tsp_causal_attention_q(layer.plan, shard, dev(q_bits), dev(k_bits), dev(v_bits), o,
+                               layer.ws)
+    layer.check_status()
+    got = f64(o)[:, shard * Hd:(shard + 1) * Hd]
+    q, kk, vv = (oracle.widen_bf16(b) for b in (q_bits, k_bits, v_bits))
+    pos = oracle.zigzag_inverse_index(i.S, i.D)
+    want = oracle.multihead_causal_attention(q, kk, vv, hpr, q_pos=pos, k_pos=np.arange(i.S))
+    assert_close(got, want, "sharp attention")
+    first = int(np.nonzero(pos == 0)[0][0])  # sharded row of token 0
+    assert np.array_equal(bits(o[first:first + 1, shard * Hd:(shard + 1) * Hd])[0], v_bits[0])
+
+
 @pytest.mark.parametrize("mode", ["plain", "residual", "residual+fp32 copy"])
 def test_o_projection(layer, mode):
     i = layer.info
