@@ -18,6 +18,9 @@ Reported:
               (host->device copy of x and device->host copy of out every step)
   cpu_baseline the float64 oracle on the host cores, timed on a causal prefix of
               the same workload and scaled by FLOPs to the full workload
+  backward    tsp_layer_bwd on the same workload (a synthetic output gradient):
+              ms per step, tokens/s and algorithmic TFLOP/s
+              (16SH^2 + 12SHF + 5HS(S+1)), plus the attention backward of one shard
   --impl reference  times that oracle alone (the slow reference arm).
 Multi-GPU (torchrun): independent replicas, one per GPU; no collective on the
 data path.
@@ -54,6 +57,20 @@ NCU_TRAFFIC_BYTES = {
 
 def algorithmic_flops(S, H, F):
     return 8 * S * H * H + 6 * S * H * F + 2 * H * S * (S + 1)
+
+
+def algorithmic_bwd_flops(S, H, F):
+    """Backward of one layer: every projection twice (data and weight gradient) and
+    the attention's five products per visible pair (scores, dP, dV, dK, dQ)."""
+    return 16 * S * H * H + 12 * S * H * F + 5 * H * S * (S + 1)
+
+
+def executed_bwd_flops(S, H, F):
+    """What tsp_layer_bwd runs: the forward recompute it needs (Q/K/V, attention,
+    O and gate/up products), the gradient products, and the attention backward as
+    a key-side kernel (4 products per pair) plus a query-side kernel (3)."""
+    recompute = 6 * S * H * H + 2 * H * S * (S + 1) + 2 * S * H * H + 4 * S * H * F
+    return recompute + 16 * S * H * H + 12 * S * H * F + 7 * H * S * (S + 1)
 
 
 def measured_peaks():
@@ -339,7 +356,70 @@ def run_ours(args, world, rank, local):
     kernels["kv_gather_standalone"] = {
         "bound": "hbm", "avg_ms": round(gather_ms, 4), "launches_per_step": 0, "share": 0.0,
         "achieved": round(gather_gbs, 1), "frac": round(gather_gbs / peaks["hbm_gbs"], 4)}
-    del qkv, q, kn, vn, o, h, h32, g, out2
+    del qkv, o, h, h32, g, out2
+
+    # ---- backward: K whole-layer backward steps, then the attention backward step
+    backward = None
+    if not args.no_backward:
+        layer.enable_backward()
+        ws = layer.ws
+        dout = torch.empty_like(xs)
+        tsp.tsp_shard(plan, to_dev(tsp_inputs.normal_bf16_bits((S, H), 1.0, cfg.seed, 77)), dout)
+        dxs = torch.empty_like(xs)
+        dwpack = torch.empty(i.wpack_elems, dtype=torch.float32, device="cuda")
+        for _ in range(args.warmup):
+            layer.backward(xs, dout, dxs, dwpack)
+        barrier()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(args.steps):
+            layer.backward(xs, dout, dxs, dwpack)
+        b1.record(stream)
+        barrier()
+        layer.check()
+        bwd_ms = max_over_ranks(b0.elapsed_time(b1) / args.steps)
+        # attention backward of one shard (Delta, key side, query side) on the
+        # forward's Q/K/V of shard D-1, with a synthetic output gradient
+        o = torch.empty_like(xs)
+        hpr = cfg.heads // D
+        lse = torch.empty(hpr * i.stat_stride, dtype=torch.float32, device="cuda")
+        delta = torch.empty_like(lse)
+        dqkv = torch.empty((S, 3 * H), dtype=torch.bfloat16, device="cuda")
+        tsp.tsp_qkv_projection_gathered(plan, D - 1, xs, wp, q, kn, vn, ws)
+        tsp.tsp_causal_attention_lse(plan, D - 1, q, kn, vn, o, lse, ws)
+        for _ in range(max(1, args.warmup)):
+            tsp.tsp_causal_attention_bwd(plan, D - 1, q, kn, vn, o, dout, lse, delta, dqkv, ws)
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_att = max(3, args.steps // 2)
+        a0.record(stream)
+        for _ in range(n_att):
+            tsp.tsp_causal_attention_bwd(plan, D - 1, q, kn, vn, o, dout, lse, delta, dqkv, ws)
+        a1.record(stream)
+        barrier()
+        layer.check()
+        att_ms = a0.elapsed_time(a1) / n_att
+        att_flops = 5.0 * i.shard_hidden * S * (S + 1)  # five products per visible pair
+        att_tf = att_flops / (att_ms * 1e-3) / 1e12
+        bwd_tf = algorithmic_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12
+        backward = {
+            "step": "tsp_layer_bwd (recomputes the forward activations it uses)",
+            "ms_per_step": round(bwd_ms, 3),
+            "tokens_per_s": round(job_tokens_per_s(world, S, bwd_ms), 1),
+            "tflops_algorithmic": round(world * bwd_tf, 1),
+            "frac_of_peak_sustained": round(bwd_tf / peaks["bf16_tflops_sustained"], 4),
+            "flops_algorithmic_per_step": algorithmic_bwd_flops(S, H, F),
+            "flops_executed_per_step": executed_bwd_flops(S, H, F),
+            "tflops_executed": round(world * executed_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12, 1),
+            "attention_bwd_step": {
+                "calls_per_step": D, "avg_ms": round(att_ms, 4),
+                "tflops_algorithmic": round(att_tf, 1),
+                "frac": round(att_tf / peaks["bf16_tflops_sustained"], 4),
+                "tflops_executed": round(att_tf * 7.0 / 5.0, 1)},
+            "launches_per_step": 4 * D + 11,
+        }
+        del dout, dxs, dwpack, o, lse, delta, dqkv
+    del q, kn, vn
 
     # ---- end to end through the host entry point (pinned buffers)
     x_host = torch.from_numpy(bits["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -389,6 +469,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if backward is not None:
+        result["backward"] = backward
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, v, desc = oracle_sample(cfg, bits, args.cpu_sample_tokens)
         result["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),
@@ -439,6 +521,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[c.name for c in tsp_inputs.CONFIGS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward measurement (tsp_layer_bwd)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=1024)
     args = ap.parse_args()

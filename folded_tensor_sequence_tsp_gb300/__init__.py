@@ -1,4 +1,5 @@
-"""GB300-native (sm_103a) forward of one Folding Tensor and Sequence Parallelism layer.
+"""GB300-native (sm_103a) forward and backward of one Folding Tensor and Sequence
+Parallelism layer.
 
 The computation lives in libtsp.so (C ABI, include/tsp.h); this package holds the
 nvcc build step, a ctypes binding with the C names (argument marshalling only) and
@@ -12,7 +13,8 @@ from ._binding import *  # noqa: F401,F403
 from ._binding import __all__ as _binding_all
 from ._binding import (tsp_layer_fwd, tsp_layer_fwd_host, tsp_pack_weights, tsp_plan,
                        tsp_device_status, tsp_packed_weight_bytes, tsp_workspace_bytes,
-                       tsp_workspace_init, tsp_attention_fwd, tsp_mlp_fwd, TSPError, TSP_OK)
+                       tsp_workspace_init, tsp_attention_fwd, tsp_mlp_fwd, TSPError, TSP_OK,
+                       tsp_bwd_workspace_bytes, tsp_layer_bwd, tsp_unpack_weight_grads)
 
 __all__ = list(_binding_all) + ["TSPLayer"]
 
@@ -58,6 +60,35 @@ class TSPLayer:
     def mlp(self, hs, out=None, stream=None):
         out = self._out(out)
         tsp_mlp_fwd(self.plan, hs, self.wpack, out, self.ws, stream)
+        return out
+
+    def enable_backward(self):
+        """Grow the workspace to the backward's size (it serves the forward too)."""
+        need = tsp_bwd_workspace_bytes(self.plan)
+        if self.ws.numel() < need:
+            self.ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+            tsp_workspace_init(self.plan, self.ws)
+
+    def backward(self, xs, dout, dxs=None, dwpack=None, stream=None):
+        """Gradients of forward(xs) for the output gradient dout (sharded layout):
+        returns (dxs, dwpack), dwpack the packed fp32 weight gradients (see
+        weight_grads)."""
+        self.enable_backward()
+        dxs = self._out(dxs)
+        if dwpack is None:
+            dwpack = torch.empty(self.plan.info.wpack_elems, dtype=torch.float32,
+                                 device=self.device)
+        tsp_layer_bwd(self.plan, xs, self.wpack, dout, dxs, dwpack, self.ws, stream)
+        return dxs, dwpack
+
+    def weight_grads(self, dwpack, stream=None):
+        """Packed fp32 weight gradients -> dict of nn.Linear-layout fp32 tensors."""
+        i = self.plan.info
+        H, F = i.hidden, i.ffn
+        out = {k: torch.empty(shape, dtype=torch.float32, device=self.device) for k, shape in (
+            ("dWq", (H, H)), ("dWk", (H, H)), ("dWv", (H, H)), ("dWo", (H, H)),
+            ("dW1", (F, H)), ("dW3", (F, H)), ("dW2", (H, F)))}
+        tsp_unpack_weight_grads(self.plan, dwpack, stream=stream, **out)
         return out
 
     def forward_host(self, x_host, out_host, stream=None):

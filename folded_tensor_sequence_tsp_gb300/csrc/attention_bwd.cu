@@ -31,6 +31,8 @@
 // P^T / dS occupy the first 32 columns of the half's own score / dP columns.
 // MMAs issued by one thread execute in order, so the next tile's scores may be
 // issued right after the products that read the previous P / dS.
+#include <type_traits>
+
 #include "tsp_device.cuh"
 #include "tsp_internal.h"
 
@@ -309,44 +311,70 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
+      // the half's 64 scores and 64 dP values of this key row: one TMEM round trip
+      uint32_t s0[32], s1[32], g0[32], g1[32];
+      tmem_ld32(s_t, s0);
+      tmem_ld32(s_t + 32, s1);
+      tmem_ld32(d_t, g0);
+      tmem_ld32(d_t + 32, g1);
+      const float4* sl4 = reinterpret_cast<const float4*>(sLse(st) + h * HALF);
+      const float4* sd4 = reinterpret_cast<const float4*>(sDel(st) + h * HALF);
       const long long r0 = row0_of(idx);
-      const float* sl = sLse(st) + h * HALF;
-      const float* sd = sDel(st) + h * HALF;
-      // query position of column c of this half: natural tiles are contiguous
+      // natural tiles are contiguous positions; a tile needs masks only where it
+      // meets the diagonal (or always, in the general zigzag layout)
       const long long qbase = p.natural ? (long long)(kt + idx) * IT + h * HALF : 0;
-      const bool full_vis = p.natural && qbase >= k0 + BT - 1;
+      const bool masked = !p.natural || qbase < k0 + BT - 1;
+      tmem_ld_wait();
+      uint32_t pp[32], dd[32];
+      // P^T = exp2(s * scale_log2 - lse[q]), dS^T = P^T (dP^T - Delta[q]) for 32 columns
+      auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&gv)[32], int c0, auto mask_tag) {
+        constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-      for (int c = 0; c < HALF; c += 32) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32(s_t + (uint32_t)c, rs);
-        tmem_ld32(d_t + (uint32_t)c, rd);
-        tmem_ld_wait();
-        uint32_t pp[16], dd[16];
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = sl4[(c0 + e) >> 2], d4 = sd4[(c0 + e) >> 2];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv2[2];
+          for (int u = 0; u < 4; u += 2) {
+            float p0 = ex2(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lv[u]));
+            float p1 = ex2(fmaf(__uint_as_float(sv[e + u + 1]), p.scale_log2, -lv[u + 1]));
+            uint64_t ds = f2_mul(f2_pack(p0, p1),
+                                 f2_sub(f2_pack(__uint_as_float(gv[e + u]), __uint_as_float(gv[e + u + 1])),
+                                        f2_pack(dl[u], dl[u + 1])));
+            if constexpr (MASK) {
+              bool vis[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c + e + u;
-            bool vis = true;
-            if (!full_vis) {
-              if (p.natural) {
-                vis = kp <= qbase + col;
-              } else {
-                const long long r = r0 + h * HALF + col;
-                vis = r < p.S && kp <= row_pos(r, p.C, p.T, p.D);
+              for (int w = 0; w < 2; ++w) {
+                const int col = h * HALF + c0 + e + u + w;
+                if (p.natural) {
+                  vis[w] = kp <= (long long)(kt + idx) * IT + col;
+                } else {
+                  const long long r = r0 + col;
+                  vis[w] = r < p.S && kp <= row_pos(r, p.C, p.T, p.D);
+                }
               }
+              float d0, d1;
+              f2_unpack(ds, d0, d1);
+              p0 = vis[0] ? p0 : 0.f;
+              p1 = vis[1] ? p1 : 0.f;
+              ds = f2_pack(vis[0] ? d0 : 0.f, vis[1] ? d1 : 0.f);
             }
-            const float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -sl[col]));
-            pv[u] = vis ? pr : 0.f;
-            dv2[u] = vis ? pr * (__uint_as_float(rd[e + u]) - sd[col]) : 0.f;
+            float d0, d1;
+            f2_unpack(ds, d0, d1);
+            pp[(c0 + e + u) >> 1] = pack_bf16x2(p0, p1);
+            dd[(c0 + e + u) >> 1] = pack_bf16x2(d0, d1);
           }
-          pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          dd[e >> 1] = pack_bf16x2(dv2[0], dv2[1]);
         }
-        tmem_st16(s_t + (uint32_t)(c / 2), pp);
-        tmem_st16(d_t + (uint32_t)(c / 2), dd);
+      };
+      if (masked) {
+        chunk(s0, g0, 0, std::true_type{});
+        chunk(s1, g1, 32, std::true_type{});
+      } else {
+        chunk(s0, g0, 0, std::false_type{});
+        chunk(s1, g1, 32, std::false_type{});
       }
+      tmem_st32(s_t, pp);
+      tmem_st32(d_t, dd);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -583,28 +611,42 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
+      uint32_t s0[32], s1[32], g0[32], g1[32];
+      tmem_ld32(s_t, s0);
+      tmem_ld32(s_t + 32, s1);
+      tmem_ld32(d_t, g0);
+      tmem_ld32(d_t + 32, g1);
       const long long kbase = (long long)j * IT + h * HALF;
-      const bool full_vis = kbase + HALF - 1 <= qpos;
-#pragma unroll
-      for (int c = 0; c < HALF; c += 32) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32(s_t + (uint32_t)c, rs);
-        tmem_ld32(d_t + (uint32_t)c, rd);
-        tmem_ld_wait();
-        uint32_t dd[16];
+      const bool masked = kbase + HALF - 1 > qpos;  // some key of the half is in the future
+      tmem_ld_wait();
+      uint32_t dd[32];
+      const uint64_t del2 = f2_pack(del, del);
+      // dS = exp2(s * scale_log2 - lse) (dP - Delta) for 32 key columns
+      auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&gv)[32], int c0, auto mask_tag) {
+        constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float ds[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const bool vis = full_vis || kbase + c + e + u <= qpos;
-            const float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -lse));
-            ds[u] = vis ? pr * (__uint_as_float(rd[e + u]) - del) : 0.f;
+          const float p0 = ex2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -lse));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -lse));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1),
+                           f2_sub(f2_pack(__uint_as_float(gv[e]), __uint_as_float(gv[e + 1])), del2)),
+                    d0, d1);
+          if constexpr (MASK) {
+            d0 = kbase + c0 + e <= qpos ? d0 : 0.f;
+            d1 = kbase + c0 + e + 1 <= qpos ? d1 : 0.f;
           }
-          dd[e >> 1] = pack_bf16x2(ds[0], ds[1]);
+          dd[(c0 + e) >> 1] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(d_t + (uint32_t)(c / 2), dd);
+      };
+      if (masked) {
+        chunk(s0, g0, 0, std::true_type{});
+        chunk(s1, g1, 32, std::true_type{});
+      } else {
+        chunk(s0, g0, 0, std::false_type{});
+        chunk(s1, g1, 32, std::false_type{});
       }
+      tmem_st32(d_t, dd);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -6,7 +6,8 @@
 Steps: qkv (Q/K/V projection of shard 0), gather (K/V all-gather), attention
 (causal attention of shard 0), o_proj (O projection with the fp32 residual copy),
 gate_up (SwiGLU gate/up), down (SwiGLU down with the fp32 residual), shard
-(zigzag rows). Inputs are seeded synthetic bf16 values with the workload's shapes;
+(zigzag rows), attention_bwd (Delta, key-side and query-side attention backward of
+shard 0, after one forward with the log-sum-exp). Inputs are seeded synthetic bf16 values with the workload's shapes;
 only the buffers the step touches are allocated, so a 64K-token step fits in a few
 GB of device memory. Prints the average CUDA-event time per launch (a number taken
 under a profiler is not a measurement).
@@ -38,7 +39,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--step", required=True,
-                    choices=["qkv", "gather", "attention", "o_proj", "gate_up", "down", "shard"])
+                    choices=["qkv", "gather", "attention", "o_proj", "gate_up", "down", "shard",
+                             "attention_bwd"])
     ap.add_argument("--workload", default="7b-64k", choices=[c.name for c in tsp_inputs.CONFIGS])
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
@@ -81,6 +83,16 @@ def main(argv=None):
         h32 = torch.randn((S, H), dtype=torch.float32, device="cuda")
         out = torch.empty((S, H), dtype=torch.bfloat16, device="cuda")
         run = lambda: B.tsp_swiglu_down(plan, g, wpack, None, out, ws, residual32=h32)
+    elif args.step == "attention_bwd":
+        q, kn, vn = _bf16((S, Hd), 12), _bf16((S, Hd), 13), _bf16((S, Hd), 14)
+        dout = _bf16((S, H), 15)
+        o = torch.empty((S, H), dtype=torch.bfloat16, device="cuda")
+        hpr = i.heads // i.D
+        lse = torch.empty(hpr * i.stat_stride, dtype=torch.float32, device="cuda")
+        delta = torch.empty_like(lse)
+        dqkv = torch.empty((S, 3 * H), dtype=torch.bfloat16, device="cuda")
+        B.tsp_causal_attention_lse(plan, 0, q, kn, vn, o, lse, ws)
+        run = lambda: B.tsp_causal_attention_bwd(plan, 0, q, kn, vn, o, dout, lse, delta, dqkv, ws)
     else:
         x = _bf16((S, H), 11)
         xs = torch.empty_like(x)
