@@ -19,18 +19,34 @@
 //             and are written at the zigzag row of the key.
 //   query-side (dQ): the CTA owns 128 query rows (sharded order) and streams the
 //             key tiles they see, computing S = Q K^T, dP = dO V^T and
-//             dQ += dS K.
-// Each streamed 128-row tile is processed as two 64-column halves with their own
-// score / dP tensor-memory columns; warps 2..5 work on half 0 and warps 6..9 on
-// half 1 (one accumulator row per thread), so the element-wise work of one half
-// overlaps the tensor-core products of the other.
-//   warp 0  TMA producer (2-stage ring of streamed tiles; lse/Delta by bulk copy)
+//             dQ += dS K. Its Q and dO rows sit in tensor memory as the A operand
+//             of the first two products.
+// The query side runs every product on a full 128-wide tile (N = 128 or N = d): a
+// tcgen05.mma with M = 128 and K = 16 occupies the tensor pipe for about as long
+// with N = 64 as with N = 128 on this part, so a narrower product runs at half
+// rate. Its element-wise work is split into two phases that depend on different
+// products, and the MMA lane orders its work (S(j+1), dQ(j), dP(j+1), ...) so that
+// one phase runs under the products of the other:
+//   phase a  (after the scores, which it then releases): P = exp2(s scale_log2 - lse);
+//   phase b  (after dP):  dS = P (dP - Delta), stored as bf16 over dP.
+// Warps 2..5 and 6..9 (two warpgroups, one accumulator row per thread) take key
+// columns [0, 64) and [64, 128) of every tile.
+// The key side streams each 128-row query tile as two 64-column halves (score and
+// dP^T products with N = 64): warps 2..5 take half 0 and warps 6..9 half 1, so one
+// half's element-wise work overlaps the other half's products. It keeps these
+// narrower products because its element-wise chain (two exponential-bound phases
+// and two tensor-memory round trips per tile) and its two-deep Q/dO ring, which is
+// what fits in shared memory beside the owned K and V, leave the tensor pipe idle
+// for longer than the halved products cost.
+//   warp 0  TMA producer (key side: 2 stages of Q, dO, lse, Delta; query side:
+//           3 stages of K, V)
 //   warp 1  TMEM allocation (512 columns) and the single MMA-issuing lane
-// TMEM columns: accumulators [0, 256) (key side: dV [0, d), dK [d, 2d); query side:
-// dQ [0, d)); half h: scores [256 + 128h, +64), dP [320 + 128h, +64). The bf16
-// P^T / dS occupy the first 32 columns of the half's own score / dP columns.
-// MMAs issued by one thread execute in order, so the next tile's scores may be
-// issued right after the products that read the previous P / dS.
+// TMEM columns: key side: dV [0, d), dK [d, 2d), half h: scores [256 + 128h, +64),
+// dP^T [320 + 128h, +64), with bf16 P^T / dS^T over the first 32 columns of each.
+// Query side: dQ [0, d), bf16 Q [d, 3d/2), bf16 dO [3d/2, 2d), scores [256, 384),
+// dP [384, 512) with bf16 dS over [384 + 64g, +32) for warpgroup g.
+// MMAs issued by one thread execute in order, so a product may write columns that
+// an earlier-issued product reads.
 #include <type_traits>
 
 #include "tsp_device.cuh"
@@ -40,14 +56,18 @@ namespace tsp {
 namespace {
 
 constexpr int BT = 128;       // rows of the tile a CTA owns
-constexpr int IT = 128;       // rows of a streamed tile (two halves)
-constexpr int HALF = 64;
-constexpr int STAGES = 2;
+constexpr int IT = 128;       // rows of a streamed tile
+constexpr int GCOLS = 64;     // streamed-tile columns per element-wise warpgroup
 constexpr int THREADS = 320;
 constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
-constexpr uint32_t HALF_ROWS_BYTES = HALF * 128;  // 64 rows of a box
 constexpr uint32_t TMEM_COLS = 512;
-
+constexpr uint32_t TM_SC = 256;  // query side: scores S, 128 columns
+constexpr uint32_t TM_DP = 384;  // query side: dP, 128 columns
+// key side: each streamed tile in two 64-column halves h, scores at
+// [256 + 128h, +64) and dP^T at [320 + 128h, +64)
+constexpr int HALF = 64;
+constexpr int STAGES = 2;
+constexpr uint32_t HALF_ROWS_BYTES = HALF * 128;  // 64 rows of a box
 __device__ __forceinline__ uint32_t tm_sc(int h) { return 256u + 128u * (uint32_t)h; }
 __device__ __forceinline__ uint32_t tm_dp(int h) { return 320u + 128u * (uint32_t)h; }
 
@@ -59,6 +79,9 @@ struct BwdParams {
   const float* lse;
   const float* delta;
   long long ld_stat;
+  const __nv_bfloat16* q;     // query-side kernel: owned Q and dO rows, read once
+  const __nv_bfloat16* dout;
+  long long ld_q, ld_do;
   long long S, T, C;
   int D;
   int n_outer;   // owned tiles per head
@@ -101,16 +124,27 @@ template <int HD>
 struct QueryGeom {
   static constexpr int BOXES = HD / 64;
   static constexpr uint32_t TILE = 128 * HD * 2;
-  // Q, dO, then per stage K, V
+  static constexpr int KV_STAGES = 3;
+  // per stage K, V (Q and dO live in tensor memory)
   static constexpr uint32_t STAGE = 2 * TILE;
-  static constexpr size_t USED = 1024 + 2 * (size_t)TILE + STAGES * (size_t)STAGE + 256;
+  static constexpr size_t USED = 1024 + KV_STAGES * (size_t)STAGE + 256;
   static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+  // TMEM columns of the owned rows as bf16 A operands (two values per column)
+  static constexpr uint32_t TM_Q = HD;
+  static constexpr uint32_t TM_DO = HD + HD / 2;
 };
 
 // K-major operand offset (>> 4) of the kk-th 16-wide K step of a [rows][HD] tile
 // stored as 64-column boxes.
 __device__ __forceinline__ uint32_t kmajor_step(int kk) {
   return (uint32_t)(((kk >> 2) * BOX_BYTES + (kk & 3) * 32) >> 4);
+}
+
+// TMEM column of the bf16 A operand for the kk-th 16-wide step of a streamed
+// tile's 128 columns: warpgroup g's 64 values sit in the first 32 columns of its
+// own 64-column block.
+__device__ __forceinline__ uint32_t packed_step(uint32_t base, int kk) {
+  return base + (uint32_t)((kk >> 2) * GCOLS + (kk & 3) * 8);
 }
 
 // ============================================================== key side
@@ -424,27 +458,29 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ============================================================== query side
+// The owned Q and dO rows are copied once into tensor memory and serve as the A
+// operand of S = Q K^T and dP = dO V^T; only the streamed K/V tiles are read from
+// shared memory by the tensor core.
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
-    attention_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
-                            const __grid_constant__ CUtensorMap tmDO,
-                            const __grid_constant__ CUtensorMap tmK,
+    attention_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const BwdParams p,
                             int q_col0, int do_col0) {
   using G = QueryGeom<HD>;
+  constexpr int NS = G::KV_STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sDO = sQ + G::TILE;
-  uint8_t* sStage = sDO + G::TILE;  // stage s: K, V
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + STAGES * G::STAGE);
-  uint64_t* q_full = bars;                // [1]
-  uint64_t* kv_full = q_full + 1;         // [STAGES]
-  uint64_t* kv_empty = kv_full + STAGES;  // [STAGES]
-  uint64_t* s_full = kv_empty + STAGES;   // [2]
-  uint64_t* p_full = s_full + 2;          // [2]
-  uint64_t* acc_done = p_full + 2;        // [1]
+  uint8_t* sStage = smem;  // stage s: K, V
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * G::STAGE);
+  uint64_t* a_full = bars;                // [1] Q and dO rows stored in TMEM (8 warps)
+  uint64_t* kv_full = a_full + 1;         // [NS]
+  uint64_t* kv_empty = kv_full + NS;      // [NS]
+  uint64_t* s_full = kv_empty + NS;       // [1] S(j) in TMEM
+  uint64_t* dp_full = s_full + 1;         // [1] dP(j) in TMEM
+  uint64_t* s_free = dp_full + 1;         // [1] S(j) read by the element-wise warps (8)
+  uint64_t* ds_full = s_free + 1;         // [1] dS(j) stored (8 warps)
+  uint64_t* acc_done = ds_full + 1;       // [1]
   uint64_t* drain = acc_done + 1;         // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -465,21 +501,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = (int)(max_pos / IT) + 1;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    mbar_init(a_full, 8);
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], 4);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(s_free, 8);
+    mbar_init(ds_full, 8);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmDO);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -496,16 +530,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      mbar_arrive_expect_tx(q_full, 2 * G::TILE);
+      int last[NS];
 #pragma unroll
-      for (int b = 0; b < G::BOXES; ++b) {
-        tma_load_2d(sQ + b * BOX_BYTES, &tmQ, q_full, q_col0 + head * HD + 64 * b, (int)r0);
-        tma_load_2d(sDO + b * BOX_BYTES, &tmDO, q_full, do_col0 + head * HD + 64 * b, (int)r0);
-      }
-      int last[STAGES] = {-1, -1};
+      for (int s = 0; s < NS; ++s) last[s] = -1;
       for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % STAGES;
-        const uint32_t ph = (uint32_t)((j / STAGES) & 1);
+        const int st = j % NS;
+        const uint32_t ph = (uint32_t)((j / NS) & 1);
         if (!mbar_wait(&kv_empty[st], ph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
         mbar_arrive_expect_tx(&kv_full[st], 2 * G::TILE);
         uint8_t* sk = sStage + st * G::STAGE;
@@ -517,71 +547,71 @@ __global__ void __launch_bounds__(THREADS, 1)
         last[st] = (int)ph;
       }
       WaitBound wd{p.status, p.limit_ns, nullptr};
-      mbar_wait(q_full, 0, wd, SITE_DRAIN);
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < NS; ++s)
         if (last[s] >= 0) mbar_wait(&kv_full[s], (uint32_t)last[s], wd, SITE_DRAIN);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc_s = make_idesc_bf16(BT, HALF, false);
+      const uint32_t idesc_s = make_idesc_bf16(BT, IT, false);
       const uint32_t idesc_acc = make_idesc_bf16(BT, HD, true);
-      const uint64_t dq0 = make_sdesc_sw128(smem_addr(sQ), 16, 1024);
-      const uint64_t ddo0 = make_sdesc_sw128(smem_addr(sDO), 16, 1024);
       const uint64_t dst0 = make_sdesc_sw128(smem_addr(sStage), 16, 1024);
       const uint64_t dst0_mn = make_sdesc_sw128(smem_addr(sStage), BOX_BYTES, 1024);
-      const uint32_t q_lo = (uint32_t)dq0, q_hi = (uint32_t)(dq0 >> 32);
-      const uint32_t o_lo = (uint32_t)ddo0, o_hi = (uint32_t)(ddo0 >> 32);
       const uint32_t st_lo = (uint32_t)dst0, st_hi = (uint32_t)(dst0 >> 32);
       const uint32_t mn_lo = (uint32_t)dst0_mn, mn_hi = (uint32_t)(dst0_mn >> 32);
-      // S_h = Q K_h^T, dP_h = dO V_h^T (64 keys of stage st)
-      auto issue_sdp = [&](int h, int st) {
-        const uint32_t k_lo = st_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
-        const uint32_t v_lo = k_lo + G::TILE / 16;
+      // S = Q K^T (128 queries x 128 keys of stage st; A = Q in TMEM)
+      auto issue_s = [&](int st) {
+        const uint32_t k_lo = st_lo + (uint32_t)st * G::STAGE / 16;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss_w(tmem + tm_sc(h), q_lo + kmajor_step(kk), q_hi, k_lo + kmajor_step(kk), st_hi,
-                   idesc_s, kk > 0 ? 1u : 0u);
+          mma_ts_w(tmem + TM_SC, tmem + G::TM_Q + (uint32_t)(kk * 8), k_lo + kmajor_step(kk),
+                   st_hi, idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+      };
+      // dP = dO V^T (A = dO in TMEM)
+      auto issue_dp = [&](int st) {
+        const uint32_t v_lo = st_lo + ((uint32_t)st * G::STAGE + G::TILE) / 16;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss_w(tmem + tm_dp(h), o_lo + kmajor_step(kk), o_hi, v_lo + kmajor_step(kk), st_hi,
-                   idesc_s, kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[h]);
+          mma_ts_w(tmem + TM_DP, tmem + G::TM_DO + (uint32_t)(kk * 8), v_lo + kmajor_step(kk),
+                   st_hi, idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(dp_full);
       };
-      // dQ += dS_h K_h (B MN-major: 16 key rows = 2048 B)
-      auto issue_acc = [&](int h, int st, bool first) {
-        const uint32_t k_lo = mn_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
+      // dQ += dS K (B MN-major: 16 key rows = 2048 B per K step)
+      auto issue_dq = [&](int st, bool first) {
+        const uint32_t k_lo = mn_lo + (uint32_t)st * G::STAGE / 16;
 #pragma unroll
-        for (int kk = 0; kk < HALF / 16; ++kk)
-          mma_ts_w(tmem + 0, tmem + tm_dp(h) + (uint32_t)(kk * 8), k_lo + (uint32_t)(kk * 128),
-                   mn_hi, idesc_acc, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < IT / 16; ++kk)
+          mma_ts_w(tmem + 0, packed_step(tmem + TM_DP, kk), k_lo + (uint32_t)(kk * 128), mn_hi,
+                   idesc_acc, (first && kk == 0) ? 0u : 1u);
       };
-      bool ok = mbar_wait(q_full, 0, wb, SITE_BWD_MMA) && mbar_wait(&kv_full[0], 0, wb, SITE_BWD_MMA);
+      bool ok = mbar_wait(a_full, 0, wb, SITE_BWD_MMA) && mbar_wait(&kv_full[0], 0, wb, SITE_BWD_MMA);
       if (ok) {
         tc_fence_after();
-        issue_sdp(0, 0);
-        issue_sdp(1, 0);
+        issue_s(0);
+        issue_dp(0);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % STAGES;
-        for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(&p_full[h], (uint32_t)(j & 1), wb, SITE_BWD_MMA)) {
+        const int st = j % NS;
+        const uint32_t ph = (uint32_t)(j & 1);
+        if (j + 1 < n_tiles) {
+          // next scores as soon as the element-wise warps hold this tile's
+          if (!mbar_wait(&kv_full[(j + 1) % NS], (uint32_t)(((j + 1) / NS) & 1), wb, SITE_BWD_MMA) ||
+              !mbar_wait(s_free, ph, wb, SITE_BWD_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_acc(h, st, j == 0 && h == 0);
-          if (h == 1) mma_commit(&kv_empty[st]);
-          if (j + 1 < n_tiles) {
-            if (h == 0 && !mbar_wait(&kv_full[(j + 1) % STAGES], (uint32_t)(((j + 1) / STAGES) & 1),
-                                     wb, SITE_BWD_MMA)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_sdp(h, (j + 1) % STAGES);
-          }
+          issue_s((j + 1) % NS);
         }
+        if (!mbar_wait(ds_full, ph, wb, SITE_BWD_MMA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dq(st, j == 0);
+        mma_commit(&kv_empty[st]);
+        if (j + 1 < n_tiles) issue_dp((j + 1) % NS);
       }
       if (ok) mma_commit(acc_done);
       mma_commit(drain);
@@ -590,7 +620,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- element-wise
-    const int h = (warp - 2) >> 2;  // key half of every tile this warpgroup takes
+    const int g = (warp - 2) >> 2;  // key half of every streamed tile this warpgroup takes
     const int qq = warp & 3;
     const int r_local = qq * 32 + lane;
     const long long grow = r0 + r_local;
@@ -599,65 +629,102 @@ __global__ void __launch_bounds__(THREADS, 1)
     const float lse = row_ok ? p.lse[(long long)head * p.ld_stat + grow] : 0.f;
     const float del = row_ok ? p.delta[(long long)head * p.ld_stat + grow] : 0.f;
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
-    const uint32_t s_t = lane_base + tm_sc(h), d_t = lane_base + tm_dp(h);
+    const uint32_t s_t = lane_base + TM_SC + (uint32_t)(g * GCOLS);
+    const uint32_t d_t = lane_base + TM_DP + (uint32_t)(g * GCOLS);
+    {
+      // this thread's row of Q (warpgroup 0) or dO (warpgroup 1) into TMEM, two
+      // bf16 values per column, as the A operand of the score / dP products
+      const __nv_bfloat16* src = g == 0 ? p.q + grow * p.ld_q + q_col0 + head * HD
+                                        : p.dout + grow * p.ld_do + do_col0 + head * HD;
+      const uint32_t dst = lane_base + (g == 0 ? G::TM_Q : G::TM_DO);
+#pragma unroll
+      for (int c = 0; c < HD / 2; c += 32) {
+        uint32_t r[32];
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + 2 * c);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const uint4 v = row_ok ? __ldg(s4 + w) : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * w + 0] = v.x;
+          r[4 * w + 1] = v.y;
+          r[4 * w + 2] = v.z;
+          r[4 * w + 3] = v.w;
+        }
+        tmem_st32(dst + (uint32_t)c, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full);
+    }
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
       const bool mine = mbar_wait(bar, parity, wb, SITE_BWD_ELEMENTWISE);
       return __all_sync(0xffffffffu, mine) != 0;
     };
     for (int j = 0; j < n_tiles; ++j) {
-      if (!warp_wait(&s_full[h], (uint32_t)(j & 1))) {
+      const uint32_t ph = (uint32_t)(j & 1);
+      if (!warp_wait(s_full, ph)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t s0[32], s1[32], g0[32], g1[32];
-      tmem_ld32(s_t, s0);
-      tmem_ld32(s_t + 32, s1);
-      tmem_ld32(d_t, g0);
-      tmem_ld32(d_t + 32, g1);
-      const long long kbase = (long long)j * IT + h * HALF;
-      const bool masked = kbase + HALF - 1 > qpos;  // some key of the half is in the future
-      tmem_ld_wait();
-      uint32_t dd[32];
+      // ---- phase a: P of this query row for the group's 64 key columns
+      float pf[64];
+      {
+        uint32_t s0[32], s1[32];
+        tmem_ld32(s_t, s0);
+        tmem_ld32(s_t + 32, s1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          pf[c] = ex2(fmaf(__uint_as_float(s0[c]), p.scale_log2, -lse));
+          pf[32 + c] = ex2(fmaf(__uint_as_float(s1[c]), p.scale_log2, -lse));
+        }
+      }
+      const long long kbase = (long long)j * IT + g * GCOLS;
+      const bool masked = kbase + GCOLS - 1 > qpos;  // some key of the group is in the future
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pf[c] = kbase + c <= qpos ? pf[c] : 0.f;
+      }
+      // ---- phase b: dS = P (dP - Delta)
+      if (!warp_wait(dp_full, ph)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       const uint64_t del2 = f2_pack(del, del);
-      // dS = exp2(s * scale_log2 - lse) (dP - Delta) for 32 key columns
-      auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&gv)[32], int c0, auto mask_tag) {
-        constexpr bool MASK = decltype(mask_tag)::value;
+      uint32_t dd[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t gv[32];
+        tmem_ld32(d_t + (uint32_t)(32 * half), gv);
+        tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[e]), p.scale_log2, -lse));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -lse));
+          const int c = 32 * half + e;
           float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p0, p1),
+          f2_unpack(f2_mul(f2_pack(pf[c], pf[c + 1]),
                            f2_sub(f2_pack(__uint_as_float(gv[e]), __uint_as_float(gv[e + 1])), del2)),
                     d0, d1);
-          if constexpr (MASK) {
-            d0 = kbase + c0 + e <= qpos ? d0 : 0.f;
-            d1 = kbase + c0 + e + 1 <= qpos ? d1 : 0.f;
-          }
-          dd[(c0 + e) >> 1] = pack_bf16x2(d0, d1);
+          dd[c >> 1] = pack_bf16x2(d0, d1);
         }
-      };
-      if (masked) {
-        chunk(s0, g0, 0, std::true_type{});
-        chunk(s1, g1, 32, std::true_type{});
-      } else {
-        chunk(s0, g0, 0, std::false_type{});
-        chunk(s1, g1, 32, std::false_type{});
       }
       tmem_st32(d_t, dd);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[h]);
+      if (lane == 0) mbar_arrive(ds_full);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && warp_wait(acc_done, 0u)) {
       tc_fence_after();
       __nv_bfloat16* dqp = p.dq + grow * p.ld_dqkv + head * HD;
 #pragma unroll
-      for (int c = h * (HD / 2); c < (h + 1) * (HD / 2); c += 32) {
+      for (int c = g * (HD / 2); c < (g + 1) * (HD / 2); c += 32) {
         uint32_t a[32];
         tmem_ld32(lane_base + (uint32_t)c, a);
         tmem_ld_wait();
@@ -743,8 +810,7 @@ tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStre
     if (e != cudaSuccess) return cuda_fail(e, "attention bwd: cudaFuncSetAttribute");
     BwdParams pq = p;
     pq.n_outer = tiles;
-    kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tq, tdo, tk, tv, pq, 0,
-                                                                   (int)c.do_col0);
+    kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tk, tv, pq, 0, (int)c.do_col0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention bwd (query side): launch");
   }
@@ -760,7 +826,8 @@ tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) 
   if ((c.ld_q % 8) || (c.ld_kv % 8) || (c.ld_do % 8) || (c.do_col0 % 8) || (c.ld_dqkv % 8) ||
       (c.ld_stat % 128) || c.ld_stat < c.S)
     return fail(TSP_ERR_INVALID_ARG, "attention bwd: bad strides");
-  if ((reinterpret_cast<uintptr_t>(c.lse) | reinterpret_cast<uintptr_t>(c.delta) |
+  if ((reinterpret_cast<uintptr_t>(c.q) | reinterpret_cast<uintptr_t>(c.dout) |
+       reinterpret_cast<uintptr_t>(c.lse) | reinterpret_cast<uintptr_t>(c.delta) |
        reinterpret_cast<uintptr_t>(c.dq) | reinterpret_cast<uintptr_t>(c.dk) |
        reinterpret_cast<uintptr_t>(c.dv)) & 15u)
     return fail(TSP_ERR_INVALID_ARG, "attention bwd: buffers must be 16-byte aligned");
@@ -776,6 +843,10 @@ tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) 
   p.lse = c.lse;
   p.delta = c.delta;
   p.ld_stat = c.ld_stat;
+  p.q = static_cast<const __nv_bfloat16*>(c.q);
+  p.dout = static_cast<const __nv_bfloat16*>(c.dout);
+  p.ld_q = c.ld_q;
+  p.ld_do = c.ld_do;
   p.S = c.S;
   p.T = c.T;
   p.C = c.C;
