@@ -21,6 +21,8 @@ Reported:
   backward    tsp_layer_bwd on the same workload (a synthetic output gradient):
               ms per step, tokens/s and algorithmic TFLOP/s
               (16SH^2 + 12SHF + 5HS(S+1)), plus the attention backward of one shard
+  cost_model  the library's per-device memory / traffic model of the same layer
+              under DP, TP, SP, TP+SP and TSP on D devices (context)
   --impl reference  times that oracle alone (the slow reference arm).
 Multi-GPU (torchrun): independent replicas, one per GPU; no collective on the
 data path.
@@ -210,6 +212,22 @@ def cpu_cores():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def cost_model_summary(tsp, cfg):
+    """Per-device memory and per-layer received traffic (GB of bf16) of the same layer
+    under DP, TP, SP, TP+SP (2 x D/2 grid) and TSP on D devices, from the library's
+    closed-form model; the pages' comparison, as context for the single-GPU run."""
+    out = {}
+    for name, scheme, D, tp in (("dp", "dp", 1, 0), ("tp", "tp", cfg.D, 0), ("sp", "sp", cfg.D, 0),
+                                (f"tp_sp_2x{cfg.D // 2}", "tp_sp", cfg.D, 2), ("tsp", "tsp", cfg.D, 0)):
+        m = tsp.tsp_cost_model(scheme, D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, tp=tp)
+        mem = m["weight_elems"] + m["weight_inflight_elems"] + m["act_elems"] + m["act_inflight_elems"]
+        out[name] = {"devices": m["devices"], "mem_gb": round(2 * mem / 1e9, 3),
+                     "weights_gb": round(2 * m["weight_elems"] / 1e9, 3),
+                     "acts_gb": round(2 * m["act_elems"] / 1e9, 3),
+                     "recv_gb": round(2 * (m["comm_weight_elems"] + m["comm_act_elems"]) / 1e9, 3)}
+    return out
 
 
 # ------------------------------------------------------------------- ours
@@ -471,6 +489,7 @@ def run_ours(args, world, rank, local):
     }
     if backward is not None:
         result["backward"] = backward
+    result["cost_model"] = cost_model_summary(tsp, cfg)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, v, desc = oracle_sample(cfg, bits, args.cpu_sample_tokens)
         result["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),

@@ -27,6 +27,7 @@ __all__ = [
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
     "tsp_last_error", "tsp_bwd_workspace_bytes", "tsp_mlp_bwd", "tsp_unpack_weight_grads",
     "tsp_attention_bwd", "tsp_layer_bwd", "tsp_causal_attention_lse", "tsp_causal_attention_bwd",
+    "SCHEMES", "tsp_cost_model",
 ]
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
@@ -58,6 +59,17 @@ class PlanInfo(ctypes.Structure):
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
+
+class Cost(ctypes.Structure):
+    _fields_ = [
+        ("devices", ctypes.c_int), ("weight_elems", ctypes.c_double),
+        ("weight_inflight_elems", ctypes.c_double), ("act_elems", ctypes.c_double),
+        ("act_inflight_elems", ctypes.c_double), ("comm_weight_elems", ctypes.c_double),
+        ("comm_act_elems", ctypes.c_double), ("flops", ctypes.c_double),
+    ]
+
+
+SCHEMES = {"dp": 0, "tp": 1, "sp": 2, "tp_sp": 3, "tsp": 4}
 
 _lib = None
 _P = ctypes.c_void_p
@@ -96,6 +108,7 @@ _SIGS = {
     "tsp_layer_bwd": (_I, [_P] * 8),
     "tsp_causal_attention_lse": (_I, [_P, _I] + [_P] * 7),
     "tsp_causal_attention_bwd": (_I, [_P, _I] + [_P] * 10),
+    "tsp_cost_model": (_I, [_I, _I, _I, ctypes.c_int64, _I, _I, _I, ctypes.POINTER(Cost)]),
 }
 
 
@@ -445,3 +458,12 @@ def tsp_causal_attention_bwd(plan, shard, q, kn, vn, o, dout, lse, delta, dqkv, 
         _dev(lse, "lse", nstat, torch.float32), _dev(delta, "delta", nstat, torch.float32),
         _dev(dqkv, "dqkv", 3 * plan.act_elems), _ws_status(ws), _stream(stream)),
         "tsp_causal_attention_bwd")
+
+
+def tsp_cost_model(scheme: str, D: int, S: int, hidden: int, heads: int, ffn: int, tp: int = 0) -> dict:
+    """Per-device memory (elements), communication (elements received) and FLOPs of
+    one layer forward under `scheme` (dp, tp, sp, tp_sp with a tp x D/tp grid, tsp)."""
+    c = Cost()
+    _check(load_library().tsp_cost_model(SCHEMES[scheme], D, tp, S, hidden, heads, ffn,
+                                         ctypes.byref(c)), "tsp_cost_model")
+    return {k: getattr(c, k) for k, _ in Cost._fields_}

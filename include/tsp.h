@@ -372,6 +372,51 @@ tsp_status tsp_unpack_weight_grads(tsp_plan_t plan, const float* dwpack, float* 
                                    float* dWv, float* dWo, float* dW1, float* dW3, float* dW2,
                                    void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Cost model ([TSP] s3, theoretical analysis: memory, communication and FLOPs of
+ * TSP against DP, TP, SP and TP+SP). The page states the comparison in words
+ * only; these closed forms are written from each scheme's sharding rules for the
+ * layer this library computes (batch 1, S tokens), per device and per layer:
+ *   TSP_SCHEME_DP     the whole layer on one device (replicas take other sequences)
+ *   TSP_SCHEME_TP     weights split over D devices by heads / ffn columns, the
+ *                     layer input and residual (x, h) replicated, two ring
+ *                     all-reduces of S x H (attention and MLP outputs)
+ *   TSP_SCHEME_SP     tokens split over D devices, weights replicated, K/V
+ *                     all-gathered over the sequence
+ *   TSP_SCHEME_TP_SP  a tp x (D/tp) grid: weights split over tp, tokens over D/tp;
+ *                     all-reduces in each tp group, K/V all-gathers across groups
+ *   TSP_SCHEME_TSP    weights and tokens split over the same D devices; attention
+ *                     shards broadcast, MLP shards passed around a ring, K/V
+ *                     all-gathered per head group, no all-reduce
+ * Activation elements per token: x and h (2H) plus q, k, v, o, a1, a3, g (4H + 3F).
+ * Communication: elements one device receives in one forward, with ring
+ * collectives (all-reduce of n over g devices: 2 (g-1)/g n; all-gather: (g-1)/g n).
+ * FLOPs: 8SH^2 + 6SHF + 2HS(S+1) per layer (causal attention), divided evenly.
+ * Makes no CUDA call. Shapes must divide evenly (heads, ffn by the weight split, S
+ * by the token split), else TSP_ERR_UNSUPPORTED; tp is read for TP_SP only.
+ * ------------------------------------------------------------------------- */
+typedef enum tsp_scheme {
+  TSP_SCHEME_DP = 0,
+  TSP_SCHEME_TP = 1,
+  TSP_SCHEME_SP = 2,
+  TSP_SCHEME_TP_SP = 3,
+  TSP_SCHEME_TSP = 4
+} tsp_scheme;
+
+typedef struct tsp_cost {
+  int devices;                  /* devices one copy of the layer spans                    */
+  double weight_elems;          /* resident weight elements per device                    */
+  double weight_inflight_elems; /* received weight elements held at once (TSP: one shard) */
+  double act_elems;             /* activation elements per device                         */
+  double act_inflight_elems;    /* gathered K/V held during attention                     */
+  double comm_weight_elems;     /* weight elements received per device per forward        */
+  double comm_act_elems;        /* activation elements received per device per forward    */
+  double flops;                 /* forward FLOPs per device                               */
+} tsp_cost;
+
+tsp_status tsp_cost_model(int scheme, int D, int tp, int64_t S, int hidden, int heads, int ffn,
+                          tsp_cost* out);
+
 /*
  * tsp_device_status - synchronise `stream`, then read and clear the workspace
  * status word. Returns TSP_OK, TSP_ERR_TIMEOUT (a bounded device wait gave up; the
