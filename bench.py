@@ -20,7 +20,8 @@ Reported:
               the same workload and scaled by FLOPs to the full workload
   backward    tsp_layer_bwd on the same workload (a synthetic output gradient):
               ms per step, tokens/s and algorithmic TFLOP/s
-              (16SH^2 + 12SHF + 5HS(S+1)), plus the attention backward of one shard
+              (16SH^2 + 12SHF + 5HS(S+1)), the attention backward of one shard, and
+              the training pair (tsp_layer_fwd_train + tsp_layer_bwd_saved)
   cost_model  the library's per-device memory / traffic model of the same layer
               under DP, TP, SP, TP+SP and TSP on D devices (context)
   --impl reference  times that oracle alone (the slow reference arm).
@@ -417,6 +418,26 @@ def run_ours(args, world, rank, local):
         barrier()
         layer.check()
         att_ms = a0.elapsed_time(a1) / n_att
+        # training pair: the forward keeps o and the row statistics, the backward uses
+        # them instead of running the attention forward again
+        saved = torch.empty(tsp.tsp_saved_bytes(plan), dtype=torch.uint8, device="cuda")
+        for _ in range(args.warmup):
+            layer.forward_train(xs, out, saved)
+            layer.backward_saved(xs, saved, dout, dxs, dwpack)
+        barrier()
+        t = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t[0].record(stream)
+        for _ in range(args.steps):
+            layer.forward_train(xs, out, saved)
+        t[1].record(stream)
+        for _ in range(args.steps):
+            layer.backward_saved(xs, saved, dout, dxs, dwpack)
+        t[2].record(stream)
+        barrier()
+        layer.check()
+        ftr_ms = max_over_ranks(t[0].elapsed_time(t[1]) / args.steps)
+        bsv_ms = max_over_ranks(t[1].elapsed_time(t[2]) / args.steps)
+        del saved
         att_flops = 5.0 * i.shard_hidden * S * (S + 1)  # five products per visible pair
         att_tf = att_flops / (att_ms * 1e-3) / 1e12
         bwd_tf = algorithmic_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12
@@ -435,6 +456,14 @@ def run_ours(args, world, rank, local):
                 "frac": round(att_tf / peaks["bf16_tflops_sustained"], 4),
                 "tflops_executed": round(att_tf * 7.0 / 5.0, 1)},
             "launches_per_step": 4 * D + 11,
+            "training_pair": {
+                "step": "tsp_layer_fwd_train + tsp_layer_bwd_saved (o and lse kept, "
+                        f"{tsp.tsp_saved_bytes(plan) / 2**20:.0f} MiB)",
+                "fwd_train_ms": round(ftr_ms, 3), "bwd_saved_ms": round(bsv_ms, 3),
+                "step_ms": round(ftr_ms + bsv_ms, 3),
+                "tokens_per_s": round(job_tokens_per_s(world, S, ftr_ms + bsv_ms), 1),
+                "tflops_algorithmic": round(world * (algorithmic_flops(S, H, F) + algorithmic_bwd_flops(S, H, F))
+                                            / ((ftr_ms + bsv_ms) * 1e-3) / 1e12, 1)},
         }
         del dout, dxs, dwpack, o, lse, delta, dqkv
     del q, kn, vn

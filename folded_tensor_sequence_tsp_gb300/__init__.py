@@ -14,7 +14,8 @@ from ._binding import __all__ as _binding_all
 from ._binding import (tsp_layer_fwd, tsp_layer_fwd_host, tsp_pack_weights, tsp_plan,
                        tsp_device_status, tsp_packed_weight_bytes, tsp_workspace_bytes,
                        tsp_workspace_init, tsp_attention_fwd, tsp_mlp_fwd, TSPError, TSP_OK,
-                       tsp_bwd_workspace_bytes, tsp_layer_bwd, tsp_unpack_weight_grads)
+                       tsp_bwd_workspace_bytes, tsp_layer_bwd, tsp_unpack_weight_grads,
+                       tsp_saved_bytes, tsp_layer_fwd_train, tsp_layer_bwd_saved)
 
 __all__ = list(_binding_all) + ["TSPLayer"]
 
@@ -79,6 +80,26 @@ class TSPLayer:
             dwpack = torch.empty(self.plan.info.wpack_elems, dtype=torch.float32,
                                  device=self.device)
         tsp_layer_bwd(self.plan, xs, self.wpack, dout, dxs, dwpack, self.ws, stream)
+        return dxs, dwpack
+
+    def forward_train(self, xs, out=None, saved=None, stream=None):
+        """forward() that also keeps what backward_saved() needs; returns (out, saved)."""
+        self.enable_backward()
+        out = self._out(out)
+        if saved is None:
+            saved = torch.empty(tsp_saved_bytes(self.plan), dtype=torch.uint8, device=self.device)
+        tsp_layer_fwd_train(self.plan, xs, self.wpack, out, saved, self.ws, stream)
+        return out, saved
+
+    def backward_saved(self, xs, saved, dout, dxs=None, dwpack=None, stream=None):
+        """backward() from the `saved` of forward_train(xs): same results, without
+        running the attention forward again."""
+        self.enable_backward()
+        dxs = self._out(dxs)
+        if dwpack is None:
+            dwpack = torch.empty(self.plan.info.wpack_elems, dtype=torch.float32,
+                                 device=self.device)
+        tsp_layer_bwd_saved(self.plan, xs, self.wpack, saved, dout, dxs, dwpack, self.ws, stream)
         return dxs, dwpack
 
     def weight_grads(self, dwpack, stream=None):

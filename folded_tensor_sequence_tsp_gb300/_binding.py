@@ -27,7 +27,7 @@ __all__ = [
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
     "tsp_last_error", "tsp_bwd_workspace_bytes", "tsp_mlp_bwd", "tsp_unpack_weight_grads",
     "tsp_attention_bwd", "tsp_layer_bwd", "tsp_causal_attention_lse", "tsp_causal_attention_bwd",
-    "SCHEMES", "tsp_cost_model",
+    "SCHEMES", "tsp_cost_model", "tsp_saved_bytes", "tsp_layer_fwd_train", "tsp_layer_bwd_saved",
 ]
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
@@ -109,6 +109,9 @@ _SIGS = {
     "tsp_causal_attention_lse": (_I, [_P, _I] + [_P] * 7),
     "tsp_causal_attention_bwd": (_I, [_P, _I] + [_P] * 10),
     "tsp_cost_model": (_I, [_I, _I, _I, ctypes.c_int64, _I, _I, _I, ctypes.POINTER(Cost)]),
+    "tsp_saved_bytes": (ctypes.c_size_t, [_P]),
+    "tsp_layer_fwd_train": (_I, [_P] * 7),
+    "tsp_layer_bwd_saved": (_I, [_P] * 9),
 }
 
 
@@ -436,6 +439,32 @@ def tsp_attention_bwd(plan, xs, wpack, dattn, dxs, dwpack, ws, stream=None):
 def tsp_layer_bwd(plan, xs, wpack, dout, dxs, dwpack, ws, stream=None):
     """Backward of tsp_layer_fwd: dxs and every section of dwpack."""
     _bwd_block("tsp_layer_bwd", plan, xs, wpack, dout, dxs, dwpack, ws, stream)
+
+
+def tsp_saved_bytes(plan: Plan) -> int:
+    return load_library().tsp_saved_bytes(plan.handle)
+
+
+def tsp_layer_fwd_train(plan, xs, wpack, out, saved, ws, stream=None):
+    """tsp_layer_fwd that also keeps the attention output and row statistics in
+    `saved` (a uint8 buffer of tsp_saved_bytes) for tsp_layer_bwd_saved."""
+    n = plan.act_elems
+    _check(load_library().tsp_layer_fwd_train(
+        plan.handle, _dev(xs, "xs", n), _dev(wpack, "wpack", plan.info.wpack_elems),
+        _dev(out, "out", n), _dev(saved, "saved", tsp_saved_bytes(plan), dtype=torch.uint8),
+        _ws(plan, ws), _stream(stream)), "tsp_layer_fwd_train")
+
+
+def tsp_layer_bwd_saved(plan, xs, wpack, saved, dout, dxs, dwpack, ws, stream=None):
+    """tsp_layer_bwd using the `saved` of tsp_layer_fwd_train (no attention forward)."""
+    n = plan.act_elems
+    i = plan.info
+    _check(load_library().tsp_layer_bwd_saved(
+        plan.handle, _dev(xs, "xs", n), _dev(wpack, "wpack", i.wpack_elems),
+        _dev(saved, "saved", tsp_saved_bytes(plan), dtype=torch.uint8),
+        _dev(dout, "dout", n), _dev(dxs, "dxs", n),
+        _dev(dwpack, "dwpack", i.wpack_elems, torch.float32), _ws_bwd(plan, ws),
+        _stream(stream)), "tsp_layer_bwd_saved")
 
 
 def tsp_causal_attention_lse(plan, shard, q, kn, vn, o, lse, ws, stream=None):

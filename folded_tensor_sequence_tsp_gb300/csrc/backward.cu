@@ -205,10 +205,11 @@ tsp_status attention_shard_backward(const Plan& p, int k, const void* q, const v
   return launch_attention_bwd(a, s);
 }
 
-// The attention forward again, keeping every shard's Q, K, V and each row's lse;
-// o = the attention output before W_O (sharded rows).
+// The attention forward again, keeping every shard's Q, K, V and, when o is not
+// NULL, the attention output before W_O (sharded rows) and each row's lse. With
+// o == NULL only the projections run (a training forward kept o and lse).
 tsp_status attention_recompute(const Plan& p, const void* xs, const void* wpack, void* ws,
-                               cudaStream_t s) {
+                               cudaStream_t s, void* o, float* lse) {
   uint16_t* qa = at<uint16_t>(ws, p.ws.qa);
   uint16_t* ka = at<uint16_t>(ws, p.ws.ka);
   uint16_t* va = at<uint16_t>(ws, p.ws.va);
@@ -216,25 +217,33 @@ tsp_status attention_recompute(const Plan& p, const void* xs, const void* wpack,
   for (int k = 0; k < p.D; ++k) {
     TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, qa + k * shard, ka + k * shard,
                                     va + k * shard, ws, s));
-    TSP_TRY(causal_attention(p, k, qa + k * shard, p.Hd, ka + k * shard, va + k * shard,
-                             at<void>(ws, p.ws.o), ws, s,
-                             at<float>(ws, p.ws.lse) + (int64_t)k * p.hpr * p.ld_stat));
+    if (o)
+      TSP_TRY(causal_attention(p, k, qa + k * shard, p.Hd, ka + k * shard, va + k * shard, o, ws,
+                               s, lse + (int64_t)k * p.hpr * p.ld_stat));
   }
   return TSP_OK;
 }
 
-// Backward of the attention block for dattn (bf16), after attention_recompute:
-// dxs = (dAttn/dx)^T dattn (+ residual32), and the W_Q/W_K/W_V/W_O gradients.
+// Layout of the activations a training forward keeps (byte offsets, 256-aligned):
+// o [S][H] bf16, then lse [heads][ld_stat] fp32.
+size_t saved_lse_offset(const Plan& p) { return ((size_t)p.S * p.H * 2 + 255) & ~(size_t)255; }
+size_t saved_bytes(const Plan& p) {
+  return saved_lse_offset(p) + (((size_t)p.heads * p.ld_stat * 4 + 255) & ~(size_t)255);
+}
+
+// Backward of the attention block for dattn (bf16), after every shard's Q/K/V are in
+// the workspace: dxs = (dAttn/dx)^T dattn (+ residual32), and the W_Q/W_K/W_V/W_O
+// gradients. o is the attention output before W_O and lse the rows' log-sum-exp
+// ([heads][ld_stat]), either recomputed into the workspace or kept by a training
+// forward.
 tsp_status attention_backward(const Plan& p, const void* xs, const void* wpack, const void* dattn,
                               const float* residual32, void* dxs, float* dwpack, void* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, const void* o, const float* lse) {
   const uint16_t* qa = at<uint16_t>(ws, p.ws.qa);
   const uint16_t* ka = at<uint16_t>(ws, p.ws.ka);
   const uint16_t* va = at<uint16_t>(ws, p.ws.va);
-  void* o = at<void>(ws, p.ws.o);
   void* dob = at<void>(ws, p.ws.dob);
   void* dqkv = at<void>(ws, p.ws.dqkv);
-  float* lse = at<float>(ws, p.ws.lse);
   float* delta = at<float>(ws, p.ws.delta);
   TSP_TRY(o_projection_dgrad(p, dattn, wpack, dob, ws, s));
   TSP_TRY(weight_grad(p, dattn, p.H, o, p.H, dwpack + p.wp_o, p.H, ws, s));  // dWo = dattn^T o
@@ -246,6 +255,22 @@ tsp_status attention_backward(const Plan& p, const void* xs, const void* wpack, 
                                      delta + (int64_t)k * p.hpr * p.ld_stat, dqkv, ws, s));
   TSP_TRY(qkv_dgrad(p, dqkv, wpack, residual32, dxs, ws, s));
   return weight_grad(p, dqkv, 3LL * p.H, xs, p.H, dwpack + p.wp_qkv, p.H, ws, s);  // dW_QKV
+}
+
+// The layer backward once Q/K/V of every shard are in the workspace and o / lse are
+// available: h = x + o W_O^T, dh = dout + MLP backward, dxs = dh + attention backward.
+tsp_status layer_backward_from(const Plan& p, const void* xs, const void* wpack, const void* dout,
+                               void* dxs, float* dwpack, void* ws, cudaStream_t s, const void* o,
+                               const float* lse) {
+  void* h = at<void>(ws, p.ws.h);
+  float* h32 = at<float>(ws, p.ws.h32);
+  void* dh = at<void>(ws, p.ws.dh);
+  float* dh32 = at<float>(ws, p.ws.dh32);
+  TSP_TRY(o_projection(p, o, wpack, xs, h, h32, ws, s));
+  // dh = dout + MLP backward of dout at h (fp32, and bf16 for the products below)
+  TSP_TRY(mlp_backward(p, h, wpack, dout, dout, dh, dh32, dwpack, ws, s));
+  // dx = dh + attention backward of dh
+  return attention_backward(p, xs, wpack, dh, dh32, dxs, dwpack, ws, s, o, lse);
 }
 
 }  // namespace
@@ -277,8 +302,10 @@ tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16
   if (dxs == xs || dxs == dattn) return fail(TSP_ERR_INVALID_ARG, "tsp_attention_bwd: dxs aliases an input");
   const Plan& p = plan->p;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  TSP_TRY(attention_recompute(p, xs, wpack, ws, s));
-  return attention_backward(p, xs, wpack, dattn, nullptr, dxs, dwpack, ws, s);
+  void* o = at<void>(ws, p.ws.o);
+  float* lse = at<float>(ws, p.ws.lse);
+  TSP_TRY(attention_recompute(p, xs, wpack, ws, s, o, lse));
+  return attention_backward(p, xs, wpack, dattn, nullptr, dxs, dwpack, ws, s, o, lse);
 }
 
 tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
@@ -290,17 +317,53 @@ tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
   if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd: dxs aliases an input");
   const Plan& p = plan->p;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* o = at<void>(ws, p.ws.o);
+  float* lse = at<float>(ws, p.ws.lse);
+  // forward recompute: every shard's Q/K/V, lse and o
+  TSP_TRY(attention_recompute(p, xs, wpack, ws, s, o, lse));
+  return layer_backward_from(p, xs, wpack, dout, dxs, dwpack, ws, s, o, lse);
+}
+
+size_t tsp_saved_bytes(tsp_plan_t plan) { return plan ? saved_bytes(plan->p) : 0; }
+
+tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                               tsp_bf16* out, void* saved, void* ws, void* stream) {
+  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, out, saved}, "tsp_layer_fwd_train"));
+  TSP_TRY(check_ws(ws, "tsp_layer_fwd_train"));
+  if (out == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd_train: out aliases xs");
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* o = saved;
+  float* lse = at<float>(saved, saved_lse_offset(p));
+  void* q = at<void>(ws, p.ws.qkv);
+  void* kn = at<void>(ws, p.ws.kn);
+  void* vn = at<void>(ws, p.ws.vn);
+  // the layer forward's steps, with o and each row's lse landing in `saved`
+  for (int k = 0; k < p.D; ++k) {
+    TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, q, kn, vn, ws, s));
+    TSP_TRY(causal_attention(p, k, q, p.Hd, kn, vn, o, ws, s, lse + (int64_t)k * p.hpr * p.ld_stat));
+  }
   void* h = at<void>(ws, p.ws.h);
-  float* h32 = at<float>(ws, p.ws.h32);
-  void* dh = at<void>(ws, p.ws.dh);
-  float* dh32 = at<float>(ws, p.ws.dh32);
-  // forward recompute: every shard's Q/K/V, lse and o; h = x + o W_O^T
-  TSP_TRY(attention_recompute(p, xs, wpack, ws, s));
-  TSP_TRY(o_projection(p, at<void>(ws, p.ws.o), wpack, xs, h, h32, ws, s));
-  // dh = dout + MLP backward of dout at h (fp32, and bf16 for the products below)
-  TSP_TRY(mlp_backward(p, h, wpack, dout, dout, dh, dh32, dwpack, ws, s));
-  // dx = dh + attention backward of dh
-  return attention_backward(p, xs, wpack, dh, dh32, dxs, dwpack, ws, s);
+  void* h32 = at<void>(ws, p.ws.h32);
+  TSP_TRY(o_projection(p, o, wpack, xs, h, h32, ws, s));
+  return mlp_block(p, h, wpack, h32, 1, out, ws, s);
+}
+
+tsp_status tsp_layer_bwd_saved(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                               const void* saved, const tsp_bf16* dout, tsp_bf16* dxs,
+                               float* dwpack, void* ws, void* stream) {
+  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_ptrs({xs, wpack, saved, dout, dxs, dwpack}, "tsp_layer_bwd_saved"));
+  TSP_TRY(check_ws(ws, "tsp_layer_bwd_saved"));
+  if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd_saved: dxs aliases an input");
+  const Plan& p = plan->p;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* o = saved;
+  const float* lse = at<float>(const_cast<void*>(saved), saved_lse_offset(p));
+  // only the projections are recomputed: Q/K/V of every shard, then h
+  TSP_TRY(attention_recompute(p, xs, wpack, ws, s, nullptr, nullptr));
+  return layer_backward_from(p, xs, wpack, dout, dxs, dwpack, ws, s, o, lse);
 }
 
 tsp_status tsp_causal_attention_lse(tsp_plan_t plan, int shard, const tsp_bf16* q,

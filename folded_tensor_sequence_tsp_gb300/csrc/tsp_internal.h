@@ -194,6 +194,9 @@ tsp_status o_projection(const Plan& p, const void* o, const void* wpack, const v
                         void* out, void* out32, void* ws, cudaStream_t s);
 tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,
                            void* out, void* out32, void* ws, cudaStream_t s);
+// G = SwiGLU(hs) then out = G W2^T (+ residual, fp32 when residual_f32) in ring order.
+tsp_status mlp_block(const Plan& p, const void* hs, const void* wpack, const void* residual,
+                     int residual_f32, void* out, void* ws, cudaStream_t s);
 
 }  // namespace tsp
 

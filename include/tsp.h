@@ -339,6 +339,27 @@ tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
                          void* stream);
 
 /*
+ * Training pair: a forward that keeps the attention's output and row statistics,
+ * and a backward that uses them instead of running the attention forward again
+ * (the backward still recomputes the cheap projections: Q/K/V of every shard and h).
+ *
+ * tsp_saved_bytes - bytes of the caller buffer `saved` of the pair: o, the attention
+ *   output before W_O, [D][T][H] bf16 (sharded rows, shard k's heads in columns
+ *   [k H/D, (k+1) H/D)), then, at the next 256-byte boundary, lse [heads][stat_stride]
+ *   fp32, the base-2 log-sum-exp of every head and row (tsp_causal_attention_lse).
+ * tsp_layer_fwd_train - tsp_layer_fwd (bit-identical out) that also fills `saved`.
+ * tsp_layer_bwd_saved - tsp_layer_bwd (bit-identical dxs and dwpack) for the same xs,
+ *   wpack and the `saved` of tsp_layer_fwd_train; needs a tsp_bwd_workspace_bytes
+ *   workspace. dxs may not alias xs or dout.
+ */
+size_t tsp_saved_bytes(tsp_plan_t plan);
+tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                               tsp_bf16* out, void* saved, void* ws, void* stream);
+tsp_status tsp_layer_bwd_saved(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
+                               const void* saved, const tsp_bf16* dout, tsp_bf16* dxs,
+                               float* dwpack, void* ws, void* stream);
+
+/*
  * tsp_causal_attention_lse - tsp_causal_attention_q that also writes, for each of
  * shard k's heads j and query row r, lse[j * stat_stride + r] = log2 of the softmax
  * denominator of the row in the base-2 domain of the scaled scores, i.e. the

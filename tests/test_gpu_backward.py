@@ -224,6 +224,50 @@ def test_layer_backward_is_deterministic():
     assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged", "d3", "hd128", "small"])
+def test_training_pair_equals_layer_fwd_and_bwd(name):
+    """tsp_layer_fwd_train gives tsp_layer_fwd's output bit for bit and keeps o and
+    the row statistics; tsp_layer_bwd_saved then gives tsp_layer_bwd's gradients bit
+    for bit without running the attention forward again. The kept lse equals the
+    forward attention step's lse, and o the attention block's output before W_O."""
+    L = Layer(*ATT_SHAPES[name], seed=41)
+    ws = L.bwd_workspace()
+    _, g_dev = _dout(L, 42)
+    xs, dout = L.sharded_x(), L.shard(g_dev)
+    out_ref, out_tr = L.act(), L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out_ref, ws)
+    saved = torch.full((tsp.tsp_saved_bytes(L.plan),), 0xFF, dtype=torch.uint8, device="cuda")
+    tsp.tsp_layer_fwd_train(L.plan, xs, L.wpack, out_tr, saved, ws)
+    L.check_status()
+    assert torch.equal(out_ref.view(torch.int16), out_tr.view(torch.int16))
+    # the kept o: the attention output before W_O, rank-major rows
+    i = L.info
+    o_kept = saved[: i.S * i.hidden * 2].view(torch.bfloat16).view(i.S, i.hidden)
+    lse_off = (i.S * i.hidden * 2 + 255) // 256 * 256
+    lse_kept = saved[lse_off: lse_off + i.heads * i.stat_stride * 4].view(torch.float32)
+    hpr = i.heads // i.D
+    q = torch.empty((i.S, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    kn, vn = torch.empty_like(q), torch.empty_like(q)
+    o = L.act()
+    lse = torch.empty(hpr * i.stat_stride, dtype=torch.float32, device="cuda")
+    for k in range(i.D):
+        tsp.tsp_qkv_projection_gathered(L.plan, k, xs, L.wpack, q, kn, vn, ws)
+        tsp.tsp_causal_attention_lse(L.plan, k, q, kn, vn, o, lse, ws)
+        seg = lse_kept[k * hpr * i.stat_stride:(k + 1) * hpr * i.stat_stride].view(hpr, i.stat_stride)
+        assert torch.equal(seg[:, :i.S], lse.view(hpr, i.stat_stride)[:, :i.S]), k
+    L.check_status()
+    assert torch.equal(o_kept.view(torch.int16), o.view(torch.int16))
+    # backward from the kept activations
+    dxs_ref, dxs_sv = L.act(), L.act()
+    dw_ref = torch.zeros(i.wpack_elems, dtype=torch.float32, device="cuda")
+    dw_sv = torch.full_like(dw_ref, float("nan"))
+    tsp.tsp_layer_bwd(L.plan, xs, L.wpack, dout, dxs_ref, dw_ref, ws)
+    tsp.tsp_layer_bwd_saved(L.plan, xs, L.wpack, saved, dout, dxs_sv, dw_sv, ws)
+    L.check_status()
+    assert torch.equal(dxs_ref.view(torch.int16), dxs_sv.view(torch.int16))
+    assert torch.equal(dw_ref, dw_sv)
+
+
 # ---------------------------------------------------------------- 7B shapes, sampled
 
 @pytest.mark.slow
