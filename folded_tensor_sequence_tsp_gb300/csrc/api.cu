@@ -18,7 +18,9 @@
 #include <cstdlib>
 #include <mutex>
 #include <new>
+#include <set>
 #include <string>
+#include <tuple>
 
 #include "tsp_device.cuh"
 #include "tsp_internal.h"
@@ -55,6 +57,24 @@ void set_error(const std::string& msg) { g_last_error = msg; }
 tsp_status fail(tsp_status code, const std::string& msg) {
   g_last_error = msg;
   return code;
+}
+
+tsp_status ensure_smem_limit(const void* kernel, int bytes, const char* what) {
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  const auto key = std::make_tuple(kernel, dev, bytes);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(key)) return TSP_OK;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  std::lock_guard<std::mutex> lock(mu);
+  done.insert(key);
+  return TSP_OK;
 }
 
 tsp_status cuda_fail(cudaError_t err, const char* what) {

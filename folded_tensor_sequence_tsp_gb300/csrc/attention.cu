@@ -466,12 +466,11 @@ tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t st
   if (st != TSP_OK) return st;
   auto kernel = attention_tcgen05_kernel<HD>;
   const size_t smem = Geometry<HD>::SMEM;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return cuda_fail(e, "attention: cudaFuncSetAttribute");
+  TSP_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)smem,
+                            "attention: cudaFuncSetAttribute"));
   const long long blocks = (long long)p.q_blocks * p.heads;
   kernel<<<(unsigned)blocks, THREADS, smem, stream>>>(tq, tk, tv, p);
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TSP_OK : cuda_fail(e, "attention: launch");
 }
 

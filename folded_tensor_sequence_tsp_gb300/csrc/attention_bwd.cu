@@ -794,8 +794,9 @@ tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStre
   {
     auto kernel = attention_bwd_dkv_kernel<HD>;
     const size_t smem = KeyGeom<HD>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "attention bwd: cudaFuncSetAttribute");
+    TSP_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)smem,
+                              "attention bwd: cudaFuncSetAttribute"));
+    cudaError_t e;
     BwdParams pk = p;
     pk.n_outer = tiles;
     kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tq, tdo, tk, tv, pk, 0,
@@ -806,8 +807,9 @@ tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStre
   {
     auto kernel = attention_bwd_dq_kernel<HD>;
     const size_t smem = QueryGeom<HD>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "attention bwd: cudaFuncSetAttribute");
+    TSP_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)smem,
+                              "attention bwd: cudaFuncSetAttribute"));
+    cudaError_t e;
     BwdParams pq = p;
     pq.n_outer = tiles;
     kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tk, tv, pq, 0, (int)c.do_col0);

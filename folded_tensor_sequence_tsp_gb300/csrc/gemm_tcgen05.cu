@@ -419,11 +419,10 @@ template <int EPI, bool A_MN, bool B_MN>
 tsp_status launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
                       cudaStream_t stream) {
   auto kernel = gemm_bf16_tcgen05<EPI, A_MN, B_MN>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-  if (e != cudaSuccess) return cuda_fail(e, "gemm: cudaFuncSetAttribute");
+  TSP_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)SMEM_BYTES,
+                            "gemm: cudaFuncSetAttribute"));
   kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm: launch");
   return TSP_OK;
 }

@@ -55,6 +55,11 @@ struct Plan {
   WorkspaceLayout ws;
 };
 
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per (kernel, device):
+// the setting lasts for the context, so later launches make no driver call here
+// (which also keeps a stream capture free of it).
+tsp_status ensure_smem_limit(const void* kernel, int bytes, const char* what);
+
 // Thread-local error message for tsp_last_error.
 void set_error(const std::string& msg);
 tsp_status fail(tsp_status code, const std::string& msg);

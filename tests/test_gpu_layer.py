@@ -158,3 +158,30 @@ def test_7b_layer_sampled_rows(name):
     s, atol = layer_tolerance(ref["out"], oracle.swiglu_gate(ref["h"], W["W1"], W["W3"]),
                               ref["h"], W)
     assert_close(got_out, ref["out"], f"{name} out rows", scale=s, max_abs=atol)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_layer_forward_replays_from_a_cuda_graph(name):
+    """tsp_layer_fwd enqueues only kernels on the caller's stream (no allocation, no
+    synchronisation), so it can be captured into a CUDA graph; replays give the eager
+    result bit for bit."""
+    cfg = tsp_inputs.config_by_name(name)
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed)
+    xs = L.sharded_x()
+    eager, replay = L.act(), L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, eager, L.ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tsp.tsp_layer_fwd(L.plan, xs, L.wpack, replay, L.ws)  # warm-up outside capture
+        with torch.cuda.graph(g, stream=s):
+            tsp.tsp_layer_fwd(L.plan, xs, L.wpack, replay, L.ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        replay.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(eager.view(torch.int16), replay.view(torch.int16))
+    L.check_status()
