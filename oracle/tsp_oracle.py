@@ -27,7 +27,8 @@ What the page fixes, and what this module writes out:
     layer's result.
 
 Readings taken where the page is silent (each is listed in the design notes):
-  * no normalisation, no positional encoding, no dropout, batch 1;
+  * no normalisation, no positional encoding, no dropout; a micro-batch is B
+    independent sequences (each rank owns its zigzag chunks of every sequence);
   * softmax scale 1/sqrt(head_dim); causal mask j <= i over global positions,
     diagonal included;
   * W1 = gate (through SiLU), W3 = up, W2 = down; silu(z) = z / (1 + e^-z);
@@ -68,6 +69,11 @@ __all__ = [
     "qkv_projection_shard",
     "layer_forward",
     "tsp_layer_forward",
+    "zigzag_forward_index_batched",
+    "shard_tokens_batched",
+    "unshard_tokens_batched",
+    "layer_forward_batched",
+    "tsp_layer_forward_batched",
     "silu_grad",
     "causal_attention_head_backward",
     "causal_attention_head_backward_rows",
@@ -307,6 +313,98 @@ def tsp_layer_forward(x, W: dict, heads: int, D: int) -> dict:
     outs = hs + acc2
     return {"attn": unshard_tokens(acc, D), "h": unshard_tokens(hs, D),
             "mlp": unshard_tokens(acc2, D), "out": unshard_tokens(outs, D)}
+
+
+# --------------------------------------------------------------------------
+# Micro-batches  ([TSP] s4, scalability: the smaller per-device footprint lets a
+# device take larger micro-batches). A micro-batch is B independent sequences of
+# S tokens each. Every rank owns its two zigzag chunks of EACH sequence, so rank
+# r's local activations are [B, S/D, H] (sequence-major) and the rank-major
+# layout of the micro-batch is [D, B, S/D, H]. Tokens of different sequences
+# never attend to each other; the MLP is per token.
+# --------------------------------------------------------------------------
+
+def zigzag_forward_index_batched(S: int, D: int, B: int) -> np.ndarray:
+    """fwd[b*S + t] = row of token t of sequence b in the rank-major [D, B, S/D] layout.
+
+    Token t of sequence b sits on rank r at local row l (the single-sequence zigzag
+    map), i.e. at row (r*B + b)*(S/D) + l.
+    """
+    rank, local = zigzag_owner(S, D)
+    T = S // D
+    seq = np.arange(B, dtype=np.int64)[:, None]
+    return ((rank[None, :] * B + seq) * T + local[None, :]).reshape(-1)
+
+
+def shard_tokens_batched(x: np.ndarray, D: int) -> np.ndarray:
+    """[B, S, ...] natural order -> [D, B, S/D, ...]: rank r's rows of every sequence."""
+    B, S = x.shape[:2]
+    rest = x.shape[2:]
+    out = np.empty((B * S,) + rest, dtype=x.dtype)
+    out[zigzag_forward_index_batched(S, D, B)] = x.reshape((B * S,) + rest)
+    return out.reshape((D, B, S // D) + rest)
+
+
+def unshard_tokens_batched(xs: np.ndarray, D: int) -> np.ndarray:
+    """Inverse of shard_tokens_batched: [D, B, S/D, ...] -> [B, S, ...]."""
+    B, T = xs.shape[1], xs.shape[2]
+    rest = xs.shape[3:]
+    flat = xs.reshape((D * B * T,) + rest)
+    return flat[zigzag_forward_index_batched(D * T, D, B)].reshape((B, D * T) + rest)
+
+
+def layer_forward_batched(x, W: dict, heads: int, rows=None) -> dict:
+    """The plain layer on each sequence of a micro-batch x [B, S, H] on its own.
+
+    Returns layer_forward's dict with a leading batch axis ([B, S or len(rows), H]).
+    """
+    res = [layer_forward(x[b], W, heads, rows=rows) for b in range(x.shape[0])]
+    return {key: np.stack([r[key] for r in res]) for key in res[0]}
+
+
+def tsp_layer_forward_batched(x, W: dict, heads: int, D: int) -> dict:
+    """tsp_layer_forward for a micro-batch x [B, S, H], rank by rank.
+
+    Rank r holds xs[r] = [B, S/D, H], its zigzag chunks of every sequence. In
+    broadcast iteration k every rank projects all of its rows with shard k; the
+    K/V rows of every rank are gathered per sequence into natural order, and rank
+    r's queries of sequence b attend (by global position) to sequence b's keys only;
+    each rank accumulates O_rk W_O,k^T locally. The MLP ring passes shard
+    (r + t) mod D to rank r at step t for all of its B*S/D rows at once, with local
+    accumulation and no all-reduce. Returns [B, S, H] arrays in natural order.
+    """
+    B, S, H = x.shape
+    F = W["W1"].shape[0]
+    if heads % D or F % D or S % (2 * D):
+        raise ValueError("TSP needs heads % D == 0, ffn % D == 0 and S % 2D == 0")
+    hpr, Hd, Fd = heads // D, H // D, F // D
+    xs = shard_tokens_batched(x, D)                     # [D, B, T, H]
+    pos = rank_positions(S, D)
+    every = np.arange(S)
+
+    acc = np.zeros(xs.shape)
+    for k in range(D):                      # broadcast iteration: shard k goes to all
+        c = slice(k * Hd, (k + 1) * Hd)
+        Wo_k = W["Wo"][:, c]
+        q = xs @ W["Wq"][c].T                            # local projections, [D, B, T, Hd]
+        k_all = unshard_tokens_batched(xs @ W["Wk"][c].T, D)   # [B, S, Hd] per sequence
+        v_all = unshard_tokens_batched(xs @ W["Wv"][c].T, D)
+        for r in range(D):
+            for b in range(B):
+                o = multihead_causal_attention(q[r, b], k_all[b], v_all[b], hpr, pos[r], every)
+                acc[r, b] += o @ Wo_k.T                  # local accumulation over k
+    hs = xs + acc
+
+    acc2 = np.zeros(xs.shape)
+    for t in range(D):                      # ring step
+        for r in range(D):
+            k = (r + t) % D
+            f = slice(k * Fd, (k + 1) * Fd)
+            g = silu(hs[r] @ W["W1"][f].T) * (hs[r] @ W["W3"][f].T)
+            acc2[r] += g @ W["W2"][:, f].T
+    outs = hs + acc2
+    return {"attn": unshard_tokens_batched(acc, D), "h": unshard_tokens_batched(hs, D),
+            "mlp": unshard_tokens_batched(acc2, D), "out": unshard_tokens_batched(outs, D)}
 
 
 # --------------------------------------------------------------------------

@@ -52,6 +52,12 @@ def _rand_weights(H, F, seed, scale=0.3):
     return W
 
 
+def oracle_plain_layer(x, W, heads):
+    """The single-sequence plain layer, which the pins above tie to torch's routines;
+    the batched pins compare against it, never against a mutant."""
+    return oracle.layer_forward(x, W, heads)
+
+
 # ---------------------------------------------------------------- pin checks
 
 def check_zigzag_golden(o):
@@ -225,10 +231,83 @@ def check_rank_counts(o):
     assert o.layer_flops(4, 2, 3) == 8 * 4 * 4 + 6 * 4 * 2 * 3 + 2 * 2 * 4 * 5
 
 
+def check_zigzag_batched_golden(o):
+    # Rank-major micro-batch layout [D][B][S/D], hand-worked (tests/golden).
+    g = _read_golden("zigzag_batched_S8_D2_B2.txt")
+    fwd = o.zigzag_forward_index_batched(8, 2, 2)
+    inv = np.empty_like(fwd)
+    inv[fwd] = np.arange(16)
+    for r in range(2):
+        for b in range(2):
+            blk = inv[(r * 2 + b) * 4:(r * 2 + b + 1) * 4]
+            assert blk.tolist() == [int(v) for v in g[f"{r}.{b}"]], (r, b)
+
+
+def check_zigzag_batched_layout(o):
+    for S, D, B in ((16, 4, 3), (64, 2, 2), (96, 3, 5), (48, 1, 2)):
+        T = S // D
+        fwd = o.zigzag_forward_index_batched(S, D, B)
+        assert sorted(fwd.tolist()) == list(range(B * S))          # a permutation
+        # every rank holds exactly T tokens of every sequence, at the same positions
+        # as the single-sequence map (1/D of each sequence's tokens per rank)
+        single = o.rank_positions(S, D)
+        for b in range(B):
+            rows = fwd[b * S:(b + 1) * S]
+            rank = rows // (B * T)
+            assert (np.bincount(rank, minlength=D) == T).all()
+            assert ((rows // T) % B == b).all()
+            for r in range(D):
+                mine = np.sort(np.flatnonzero(rank == r))
+                assert mine.tolist() == sorted(single[r].tolist())
+        assert np.array_equal(o.zigzag_forward_index_batched(S, D, 1),
+                              o.zigzag_forward_index(S, D))            # B = 1
+        x = _rand((B, S, 3), 60)
+        xs = o.shard_tokens_batched(x, D)
+        assert xs.shape == (D, B, T, 3)
+        for r in range(D):
+            for b in range(B):
+                assert np.array_equal(xs[r, b], x[b][single[r]])
+        assert np.array_equal(o.unshard_tokens_batched(xs, D), x)
+
+
+def check_tsp_batched_equals_plain(o):
+    # A micro-batch through the TSP schedules gives each sequence's plain layer.
+    S, H, heads, F, B = 32, 16, 4, 24, 3
+    x = _rand((B, S, H), 61)
+    W = _rand_weights(H, F, 62)
+    plain = [oracle_plain_layer(x[b], W, heads) for b in range(B)]
+    batched = o.layer_forward_batched(x, W, heads)
+    for D in (1, 2, 4):
+        tsp = o.tsp_layer_forward_batched(x, W, heads, D)
+        for key in ("attn", "h", "mlp", "out"):
+            for b in range(B):
+                want = plain[b][key]
+                scale = np.abs(want).max()
+                assert np.abs(tsp[key][b] - want).max() / scale < 1e-12, (D, key, b)
+                assert np.abs(batched[key][b] - want).max() / scale < 1e-12, (key, b)
+
+
+def check_batched_sequences_independent(o):
+    # Changing one sequence of the micro-batch leaves the others' outputs unchanged
+    # (no attention across sequences, per-token MLP).
+    S, H, heads, F, B, D = 16, 8, 2, 8, 3, 2
+    x = _rand((B, S, H), 63)
+    W = _rand_weights(H, F, 64)
+    a = o.tsp_layer_forward_batched(x, W, heads, D)
+    y = x.copy()
+    y[1] = _rand((S, H), 65)
+    c = o.tsp_layer_forward_batched(y, W, heads, D)
+    for b in (0, 2):
+        assert np.array_equal(a["out"][b], c["out"][b]), b
+    assert not np.allclose(a["out"][1], c["out"][1])
+
+
 PINS = [check_zigzag_golden, check_zigzag_bruteforce, check_zigzag_balance,
         check_shard_roundtrip, check_attention_hand_example, check_attention_vs_sdpa,
         check_attention_closed_forms, check_attention_positions, check_silu_and_mlp,
-        check_layer_vs_torch, check_sampled_rows, check_tsp_equals_plain, check_rank_counts]
+        check_layer_vs_torch, check_sampled_rows, check_tsp_equals_plain, check_rank_counts,
+        check_zigzag_batched_golden, check_zigzag_batched_layout, check_tsp_batched_equals_plain,
+        check_batched_sequences_independent]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -259,6 +338,14 @@ def _attn_head_mutant(scale=None, strict=False, shift=0):
     return f
 
 
+def _one_long_sequence(x, W, heads, D):
+    """Mistake: the micro-batch treated as one sequence of B*S tokens (later sequences
+    attend to earlier ones)."""
+    B, S, H = x.shape
+    r = oracle.tsp_layer_forward(x.reshape(B * S, H), W, heads, D)
+    return {k: v.reshape(B, S, H) for k, v in r.items()}
+
+
 def _run_pins(o):
     failed = 0
     for pin in PINS:
@@ -280,6 +367,9 @@ MUTANTS = {
     "zigzag without fold": dict(rank_positions=lambda S, D: np.arange(S).reshape(D, S // D)),
     "pairs dropped +1": dict(causal_pairs_per_rank=lambda S, D: np.bincount(
         oracle.zigzag_owner(S, D)[0], weights=np.arange(S), minlength=D).astype(np.int64)),
+    "micro-batch sequence-major": dict(zigzag_forward_index_batched=lambda S, D, B: (
+        np.arange(B)[:, None] * S + oracle.zigzag_forward_index(S, D)[None, :]).reshape(-1)),
+    "micro-batch as one sequence": dict(tsp_layer_forward_batched=_one_long_sequence),
 }
 
 

@@ -7,7 +7,8 @@ numbers, rounds them to bfloat16 bit patterns and names the workloads.
 Workloads follow the evaluation setup of "Folding Tensor and Sequence
 Parallelism for Memory-Efficient Transformer Training & Inference" (section 4,
 Results): a 7B-parameter dense transformer at 16K-128K tokens, plus two small
-shapes that the oracle finishes in seconds. All are batch 1 with
+shapes that the oracle finishes in seconds. All are batch 1 (a micro-batch of
+several sequences is drawn on request) with
 x ~ N(0, 1) and every weight ~ N(0, 0.02), drawn from a Philox counter-based
 generator (NumPy) and rounded to bfloat16 with round-to-nearest-even.
 
@@ -107,15 +108,18 @@ def normal_bf16_bits(shape, std: float, seed: int, stream: int) -> np.ndarray:
 _STREAMS = {"x": 0, "Wq": 1, "Wk": 2, "Wv": 3, "Wo": 4, "W1": 5, "W3": 6, "W2": 7}
 
 
-def layer_inputs(cfg: LayerConfig, seed: int | None = None, names=None) -> dict:
+def layer_inputs(cfg: LayerConfig, seed: int | None = None, names=None, batch: int = 1) -> dict:
     """Return the seeded bf16 bit patterns (uint16 arrays) of one workload.
 
-    Keys: x [S, H]; Wq, Wk, Wv, Wo [H, H]; W1, W3 [F, H]; W2 [H, F].
-    ``names`` restricts the draw to a subset of keys.
+    Keys: x [S, H] (or [batch, S, H] for a micro-batch of `batch` sequences);
+    Wq, Wk, Wv, Wo [H, H]; W1, W3 [F, H]; W2 [H, F]. ``names`` restricts the draw
+    to a subset of keys. The sequences of a micro-batch are consecutive draws of
+    the same stream, so sequence 0 equals the batch-1 x of the same seed.
     """
     seed = cfg.seed if seed is None else seed
     H, F, S = cfg.hidden, cfg.ffn, cfg.S
-    shapes = {"x": (S, H), "Wq": (H, H), "Wk": (H, H), "Wv": (H, H), "Wo": (H, H),
+    xshape = (S, H) if batch == 1 else (batch, S, H)
+    shapes = {"x": xshape, "Wq": (H, H), "Wk": (H, H), "Wv": (H, H), "Wo": (H, H),
               "W1": (F, H), "W3": (F, H), "W2": (H, F)}
     out = {}
     for k in (names or shapes):
