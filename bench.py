@@ -25,6 +25,8 @@ Reported:
   cost_model  the library's per-device memory / traffic model of the same layer
               under DP, TP, SP, TP+SP and TSP on D devices (context)
   --impl reference  times that oracle alone (the slow reference arm).
+  --batch B   a micro-batch of B sequences of the workload's length (forward,
+              e2e and kernels; the backward takes one sequence per plan)
 Multi-GPU (torchrun): independent replicas, one per GPU; no collective on the
 data path.
 """
@@ -190,7 +192,8 @@ def oracle_sample(cfg, bits, n_tokens, repeats=1):
     """
     import oracle  # the oracle is timed here only as the CPU baseline / reference arm
     n = int(min(n_tokens, cfg.S))
-    x = oracle.widen_bf16(bits["x"][:n])
+    xb = bits["x"] if bits["x"].ndim == 2 else bits["x"][0]  # first sequence of a micro-batch
+    x = oracle.widen_bf16(xb[:n])
     W = {k: oracle.widen_bf16(bits[k]) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")}
     times = []
     for _ in range(repeats):
@@ -245,10 +248,12 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     cfg = tsp_inputs.config_by_name(args.workload)
     S, H, F, D = cfg.S, cfg.hidden, cfg.ffn, cfg.D
-    bits = tsp_inputs.layer_inputs(cfg)
+    Bm = args.batch              # sequences of the micro-batch
+    N = Bm * S                   # tokens of one step
+    bits = tsp_inputs.layer_inputs(cfg, batch=Bm)
     to_dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
     dev = {k: to_dev(v) for k, v in bits.items()}
-    layer = tsp.TSPLayer(D, S, H, cfg.heads, F, dev)
+    layer = tsp.TSPLayer(D, S, H, cfg.heads, F, dev, batch=Bm)
     plan, i = layer.plan, layer.plan.info
     xs = torch.empty_like(dev["x"])
     tsp.tsp_shard(plan, dev["x"], xs)
@@ -283,14 +288,14 @@ def run_ours(args, world, rank, local):
     launches_per_step = 2 * D + 3
 
     # ---- per-kernel pass: the same kernels through the single-step entry points
-    qkv = torch.empty((S, 3 * i.shard_hidden), dtype=torch.bfloat16, device="cuda")
-    q = torch.empty((S, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
-    kn = torch.empty((S, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    qkv = torch.empty((N, 3 * i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((N, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    kn = torch.empty((N, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
     vn = torch.empty_like(kn)
     o = torch.empty_like(xs)
     h = torch.empty_like(xs)
     h32 = torch.empty(xs.shape, dtype=torch.float32, device="cuda")
-    g = torch.empty((S, i.ffn_padded), dtype=torch.bfloat16, device="cuda")
+    g = torch.empty((N, i.ffn_padded), dtype=torch.bfloat16, device="cuda")
     out2 = torch.empty_like(xs)
     ws, wp = layer.ws, layer.wpack
     names = ["gemm_qkv", "attention", "gemm_o", "gemm_gate_up", "gemm_down"]
@@ -341,11 +346,11 @@ def run_ours(args, world, rank, local):
     barrier()
     gather_ms = ga.elapsed_time(gb) / 20
     per_launch_work = {
-        "gemm_qkv": ("tensor", 2.0 * S * H * 3 * i.shard_hidden),
-        "attention": ("tensor", 2.0 * i.shard_hidden * S * (S + 1)),
-        "gemm_o": ("tensor", 2.0 * S * H * H),
-        "gemm_gate_up": ("tensor", 4.0 * S * H * F),
-        "gemm_down": ("tensor", 2.0 * S * F * H),
+        "gemm_qkv": ("tensor", 2.0 * N * H * 3 * i.shard_hidden),
+        "attention": ("tensor", 2.0 * i.shard_hidden * S * (S + 1) * Bm),
+        "gemm_o": ("tensor", 2.0 * N * H * H),
+        "gemm_gate_up": ("tensor", 4.0 * N * H * F),
+        "gemm_down": ("tensor", 2.0 * N * F * H),
     }
     peaks, peak_src = measured_peaks()
     kernels = {}
@@ -371,7 +376,7 @@ def run_ours(args, world, rank, local):
                 "unit": "TFLOP/s" if kd["bound"] == "tensor" else "GB/s",
                 "frac": kd["frac"], "traffic": NCU_TRAFFIC_BYTES.get(dom),
                 "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kd['bound'] == 'tensor' else 'hbm_gbs'})"}
-    gather_gbs = 8.0 * S * i.shard_hidden / (gather_ms * 1e-3) / 1e9
+    gather_gbs = 8.0 * N * i.shard_hidden / (gather_ms * 1e-3) / 1e9
     kernels["kv_gather_standalone"] = {
         "bound": "hbm", "avg_ms": round(gather_ms, 4), "launches_per_step": 0, "share": 0.0,
         "achieved": round(gather_gbs, 1), "frac": round(gather_gbs / peaks["hbm_gbs"], 4)}
@@ -379,7 +384,7 @@ def run_ours(args, world, rank, local):
 
     # ---- backward: K whole-layer backward steps, then the attention backward step
     backward = None
-    if not args.no_backward:
+    if not args.no_backward and Bm == 1:  # the backward takes one sequence per plan
         layer.enable_backward()
         ws = layer.ws
         dout = torch.empty_like(xs)
@@ -486,10 +491,10 @@ def run_ours(args, world, rank, local):
     layer.check()
     e2e_ms = max_over_ranks(statistics.mean(e_ms))
 
-    tflops = algorithmic_flops(S, H, F) / (ms * 1e-3) / 1e12
+    tflops = Bm * algorithmic_flops(S, H, F) / (ms * 1e-3) / 1e12
     result = {
         "metric": METRIC,
-        "value": round(job_tokens_per_s(world, S, ms), 1),
+        "value": round(job_tokens_per_s(world, N, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -503,16 +508,17 @@ def run_ours(args, world, rank, local):
         "tflops": round(world * tflops, 1),
         "frac_of_peak": round(tflops / peaks["bf16_tflops"], 4),
         "frac_of_peak_sustained": round(tflops / peaks["bf16_tflops_sustained"], 4),
-        "config": {"workload": cfg.name, "D": D, "S": S, "hidden": H, "heads": cfg.heads,
-                   "head_dim": cfg.head_dim, "ffn": F, "batch": 1,
+        "config": {"workload": cfg.name + (f"-b{Bm}" if Bm > 1 else ""), "D": D, "S": S,
+                   "hidden": H, "heads": cfg.heads, "head_dim": cfg.head_dim, "ffn": F,
+                   "batch": Bm,
                    "parallelism": f"tsp{D} on one GPU" + (f", {world} replicas" if world > 1 else ""),
                    "l2": "no flush: x (512 MiB at 64K) and weights exceed the 129 MB L2"},
         "roofline": roofline,
         "kernels": kernels,
         "composed_equals_layer_fwd": bool(same),
-        "e2e": {"value": round(job_tokens_per_s(world, S, e2e_ms), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, N, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 3),
-                "h2d_bytes_per_step": S * H * 2, "d2h_bytes_per_step": S * H * 2},
+                "h2d_bytes_per_step": N * H * 2, "d2h_bytes_per_step": N * H * 2},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -550,8 +556,9 @@ def run_reference(args, world, rank, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * statistics.mean(times), 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "D": cfg.D, "S": cfg.S, "hidden": cfg.hidden,
-                   "heads": cfg.heads, "head_dim": cfg.head_dim, "ffn": cfg.ffn, "batch": 1},
+        "config": {"workload": cfg.name + (f"-b{args.batch}" if args.batch > 1 else ""),
+                   "D": cfg.D, "S": cfg.S, "hidden": cfg.hidden, "heads": cfg.heads,
+                   "head_dim": cfg.head_dim, "ffn": cfg.ffn, "batch": args.batch},
         "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -571,6 +578,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward measurement (tsp_layer_bwd)")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="sequences of the micro-batch (forward only; e.g. --workload 7b-16k "
+                         "--batch 4 is 4 x 16K tokens)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=1024)
     args = ap.parse_args()

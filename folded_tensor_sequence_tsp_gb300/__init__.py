@@ -12,6 +12,7 @@ import torch
 from ._binding import *  # noqa: F401,F403
 from ._binding import __all__ as _binding_all
 from ._binding import (tsp_layer_fwd, tsp_layer_fwd_host, tsp_pack_weights, tsp_plan,
+                       tsp_plan_batched,
                        tsp_device_status, tsp_packed_weight_bytes, tsp_workspace_bytes,
                        tsp_workspace_init, tsp_attention_fwd, tsp_mlp_fwd, TSPError, TSP_OK,
                        tsp_bwd_workspace_bytes, tsp_layer_bwd, tsp_unpack_weight_grads,
@@ -25,12 +26,14 @@ class TSPLayer:
 
     weights: dict of bfloat16 CUDA tensors Wq, Wk, Wv, Wo [H, H], W1, W3 [F, H],
     W2 [H, F] (nn.Linear layout). Activations passed to forward() are in the
-    sharded [D, S/D, H] layout (see tsp_shard).
+    sharded [D, S/D, H] layout (see tsp_shard), or [D, batch, S/D, H] for a
+    micro-batch of `batch` sequences (forward only).
     """
 
-    def __init__(self, D, S, hidden, heads, ffn, weights, device=None):
+    def __init__(self, D, S, hidden, heads, ffn, weights, device=None, batch=1):
         self.device = torch.device(device or "cuda")
-        self.plan = tsp_plan(D, S, hidden, heads, ffn)
+        self.plan = (tsp_plan(D, S, hidden, heads, ffn) if batch == 1
+                     else tsp_plan_batched(D, S, batch, hidden, heads, ffn))
         self.wpack = torch.empty(tsp_packed_weight_bytes(self.plan) // 2, dtype=torch.bfloat16,
                                  device=self.device)
         self.ws = torch.empty(tsp_workspace_bytes(self.plan), dtype=torch.uint8, device=self.device)
@@ -41,7 +44,7 @@ class TSPLayer:
     @property
     def shape(self):
         i = self.plan.info
-        return (i.D, i.T, i.hidden)
+        return (i.D, i.T, i.hidden) if i.batch == 1 else (i.D, i.batch, i.T, i.hidden)
 
     def _out(self, out):
         if out is None:

@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "TSPError", "PlanInfo", "Plan", "load_library", "library_path", "declared_functions",
     "TSP_OK", "TSP_ERR_INVALID_ARG", "TSP_ERR_UNSUPPORTED", "TSP_ERR_CUDA", "TSP_ERR_TIMEOUT",
-    "tsp_plan", "tsp_get_plan_info", "tsp_workspace_bytes", "tsp_packed_weight_bytes",
+    "tsp_plan", "tsp_plan_batched", "tsp_get_plan_info", "tsp_workspace_bytes", "tsp_packed_weight_bytes",
     "tsp_workspace_init", "tsp_pack_weights", "tsp_shard_index", "tsp_shard", "tsp_unshard",
     "tsp_attention_fwd", "tsp_mlp_fwd", "tsp_mlp_fwd_noalloc", "tsp_layer_fwd", "tsp_layer_fwd_host",
     "tsp_qkv_projection", "tsp_qkv_projection_gathered", "tsp_kv_allgather",
@@ -27,7 +27,7 @@ __all__ = [
     "tsp_swiglu_gate_up", "tsp_swiglu_down", "tsp_device_status", "tsp_wait_selftest",
     "tsp_last_error", "tsp_bwd_workspace_bytes", "tsp_mlp_bwd", "tsp_unpack_weight_grads",
     "tsp_attention_bwd", "tsp_layer_bwd", "tsp_causal_attention_lse", "tsp_causal_attention_bwd",
-    "SCHEMES", "tsp_cost_model", "tsp_saved_bytes", "tsp_layer_fwd_train", "tsp_layer_bwd_saved",
+    "SCHEMES", "tsp_cost_model", "tsp_cost_model_batched", "tsp_cost_max_batch", "tsp_saved_bytes", "tsp_layer_fwd_train", "tsp_layer_bwd_saved",
 ]
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
@@ -53,7 +53,7 @@ class PlanInfo(ctypes.Structure):
         ("wpack_o", ctypes.c_size_t), ("wpack_w13", ctypes.c_size_t),
         ("wpack_w2", ctypes.c_size_t), ("wpack_elems", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t), ("bwd_workspace_bytes", ctypes.c_size_t),
-        ("stat_stride", ctypes.c_int64),
+        ("stat_stride", ctypes.c_int64), ("batch", ctypes.c_int), ("tokens", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -76,6 +76,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGS = {
     "tsp_plan": (_I, [_I, ctypes.c_int64, _I, _I, _I, ctypes.POINTER(_P)]),
+    "tsp_plan_batched": (_I, [_I, ctypes.c_int64, _I, _I, _I, _I, ctypes.POINTER(_P)]),
     "tsp_plan_destroy": (None, [_P]),
     "tsp_get_plan_info": (_I, [_P, ctypes.POINTER(PlanInfo)]),
     "tsp_workspace_bytes": (ctypes.c_size_t, [_P]),
@@ -109,6 +110,10 @@ _SIGS = {
     "tsp_causal_attention_lse": (_I, [_P, _I] + [_P] * 7),
     "tsp_causal_attention_bwd": (_I, [_P, _I] + [_P] * 10),
     "tsp_cost_model": (_I, [_I, _I, _I, ctypes.c_int64, _I, _I, _I, ctypes.POINTER(Cost)]),
+    "tsp_cost_model_batched": (_I, [_I, _I, _I, ctypes.c_int64, _I, _I, _I, _I,
+                                    ctypes.POINTER(Cost)]),
+    "tsp_cost_max_batch": (_I, [_I, _I, _I, ctypes.c_int64, _I, _I, _I, _I, ctypes.c_double,
+                                ctypes.POINTER(ctypes.c_int64)]),
     "tsp_saved_bytes": (ctypes.c_size_t, [_P]),
     "tsp_layer_fwd_train": (_I, [_P] * 7),
     "tsp_layer_bwd_saved": (_I, [_P] * 9),
@@ -209,13 +214,22 @@ class Plan:
     # shapes used by the checks below
     @property
     def act_elems(self):
-        return self.info.S * self.info.hidden
+        return self.info.tokens * self.info.hidden
 
 
 def tsp_plan(D: int, S: int, hidden: int, heads: int, ffn: int) -> Plan:
     lib = load_library()
     h = _P()
     _check(lib.tsp_plan(D, S, hidden, heads, ffn, ctypes.byref(h)), "tsp_plan")
+    return Plan(h, lib)
+
+
+def tsp_plan_batched(D: int, S: int, batch: int, hidden: int, heads: int, ffn: int) -> Plan:
+    """Plan for a micro-batch of `batch` sequences of S tokens (layout [D, B, S/D, H])."""
+    lib = load_library()
+    h = _P()
+    _check(lib.tsp_plan_batched(D, S, batch, hidden, heads, ffn, ctypes.byref(h)),
+           "tsp_plan_batched")
     return Plan(h, lib)
 
 
@@ -255,7 +269,7 @@ def tsp_pack_weights(plan, Wq, Wk, Wv, Wo, W1, W3, W2, wpack, stream=None):
 
 
 def tsp_shard_index(plan, fwd, inv, stream=None):
-    S = plan.info.S
+    S = plan.info.tokens
     _check(load_library().tsp_shard_index(
         plan.handle, _dev(fwd, "fwd", S, torch.int32, optional=True),
         _dev(inv, "inv", S, torch.int32, optional=True), _stream(stream)), "tsp_shard_index")
@@ -312,13 +326,13 @@ def tsp_qkv_projection(plan, shard, xs, wpack, qkv, ws, stream=None):
     i = plan.info
     _check(load_library().tsp_qkv_projection(
         plan.handle, int(shard), _dev(xs, "xs", plan.act_elems),
-        _dev(wpack, "wpack", i.wpack_elems), _dev(qkv, "qkv", i.S * 3 * i.shard_hidden),
+        _dev(wpack, "wpack", i.wpack_elems), _dev(qkv, "qkv", i.tokens * 3 * i.shard_hidden),
         _ws_status(ws), _stream(stream)), "tsp_qkv_projection")
 
 
 def tsp_qkv_projection_gathered(plan, shard, xs, wpack, q, kn, vn, ws, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     _check(load_library().tsp_qkv_projection_gathered(
         plan.handle, int(shard), _dev(xs, "xs", plan.act_elems),
         _dev(wpack, "wpack", i.wpack_elems), _dev(q, "q", n), _dev(kn, "kn", n),
@@ -327,7 +341,7 @@ def tsp_qkv_projection_gathered(plan, shard, xs, wpack, q, kn, vn, ws, stream=No
 
 def tsp_causal_attention_q(plan, shard, q, kn, vn, o, ws, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     _check(load_library().tsp_causal_attention_q(
         plan.handle, int(shard), _dev(q, "q", n), _dev(kn, "kn", n), _dev(vn, "vn", n),
         _dev(o, "o", plan.act_elems), _ws_status(ws), _stream(stream)), "tsp_causal_attention_q")
@@ -335,7 +349,7 @@ def tsp_causal_attention_q(plan, shard, q, kn, vn, o, ws, stream=None):
 
 def tsp_kv_allgather(plan, qkv, kn, vn, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     _check(load_library().tsp_kv_allgather(
         plan.handle, _dev(qkv, "qkv", 3 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
         _stream(stream)), "tsp_kv_allgather")
@@ -343,7 +357,7 @@ def tsp_kv_allgather(plan, qkv, kn, vn, stream=None):
 
 def tsp_causal_attention(plan, shard, qkv, kn, vn, o, ws, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     _check(load_library().tsp_causal_attention(
         plan.handle, int(shard), _dev(qkv, "qkv", 3 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
         _dev(o, "o", plan.act_elems), _ws_status(ws), _stream(stream)), "tsp_causal_attention")
@@ -362,14 +376,14 @@ def tsp_swiglu_gate_up(plan, hs, wpack, g, ws, stream=None):
     i = plan.info
     _check(load_library().tsp_swiglu_gate_up(
         plan.handle, _dev(hs, "hs", plan.act_elems), _dev(wpack, "wpack", i.wpack_elems),
-        _dev(g, "g", i.S * i.ffn_padded), _ws_status(ws), _stream(stream)), "tsp_swiglu_gate_up")
+        _dev(g, "g", i.tokens * i.ffn_padded), _ws_status(ws), _stream(stream)), "tsp_swiglu_gate_up")
 
 
 def tsp_swiglu_down(plan, g, wpack, residual, out, ws, stream=None, residual32=None):
     i = plan.info
     n = plan.act_elems
     _check(load_library().tsp_swiglu_down(
-        plan.handle, _dev(g, "g", i.S * i.ffn_padded), _dev(wpack, "wpack", i.wpack_elems),
+        plan.handle, _dev(g, "g", i.tokens * i.ffn_padded), _dev(wpack, "wpack", i.wpack_elems),
         _dev(residual, "residual", n, optional=True),
         _dev(residual32, "residual32", n, torch.float32, optional=True), _dev(out, "out", n),
         _ws_status(ws), _stream(stream)), "tsp_swiglu_down")
@@ -469,7 +483,7 @@ def tsp_layer_bwd_saved(plan, xs, wpack, saved, dout, dxs, dwpack, ws, stream=No
 
 def tsp_causal_attention_lse(plan, shard, q, kn, vn, o, lse, ws, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     nstat = (i.heads // i.D) * i.stat_stride
     _check(load_library().tsp_causal_attention_lse(
         plan.handle, int(shard), _dev(q, "q", n), _dev(kn, "kn", n), _dev(vn, "vn", n),
@@ -479,7 +493,7 @@ def tsp_causal_attention_lse(plan, shard, q, kn, vn, o, lse, ws, stream=None):
 
 def tsp_causal_attention_bwd(plan, shard, q, kn, vn, o, dout, lse, delta, dqkv, ws, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     nstat = (i.heads // i.D) * i.stat_stride
     _check(load_library().tsp_causal_attention_bwd(
         plan.handle, int(shard), _dev(q, "q", n), _dev(kn, "kn", n), _dev(vn, "vn", n),
@@ -496,3 +510,23 @@ def tsp_cost_model(scheme: str, D: int, S: int, hidden: int, heads: int, ffn: in
     _check(load_library().tsp_cost_model(SCHEMES[scheme], D, tp, S, hidden, heads, ffn,
                                          ctypes.byref(c)), "tsp_cost_model")
     return {k: getattr(c, k) for k, _ in Cost._fields_}
+
+
+def tsp_cost_model_batched(scheme: str, D: int, S: int, batch: int, hidden: int, heads: int,
+                           ffn: int, tp: int = 0) -> dict:
+    """tsp_cost_model for a micro-batch of `batch` sequences of S tokens."""
+    c = Cost()
+    _check(load_library().tsp_cost_model_batched(SCHEMES[scheme], D, tp, S, batch, hidden, heads,
+                                                 ffn, ctypes.byref(c)), "tsp_cost_model_batched")
+    return {k: getattr(c, k) for k, _ in Cost._fields_}
+
+
+def tsp_cost_max_batch(scheme: str, D: int, S: int, hidden: int, heads: int, ffn: int,
+                       layers: int, mem_bytes: float, tp: int = 0) -> int:
+    """Largest micro-batch of S-token sequences whose per-device bf16 footprint for
+    `layers` layers fits in mem_bytes under `scheme` (0 if one sequence does not)."""
+    out = ctypes.c_int64()
+    _check(load_library().tsp_cost_max_batch(SCHEMES[scheme], D, tp, S, hidden, heads, ffn,
+                                             layers, float(mem_bytes), ctypes.byref(out)),
+           "tsp_cost_max_batch")
+    return int(out.value)

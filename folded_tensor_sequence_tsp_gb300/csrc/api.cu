@@ -133,7 +133,7 @@ tsp_status qkv_projection(const Plan& p, int k, const void* xs, const void* wpac
   c.epi = EPI_STORE;
   c.A = xs;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;
   c.ldb = p.H;
   c.b_rows = 3LL * p.H;
@@ -155,7 +155,7 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
   c.epi = EPI_QKV_SPLIT;
   c.A = xs;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;
   c.ldb = p.H;
   c.b_rows = 3LL * p.H;
@@ -171,6 +171,7 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
   c.zz_C = p.C;
   c.zz_T = p.T;
   c.zz_D = p.D;
+  c.zz_B = p.B;
   c.status = status_of(ws);
   return launch_gemm(c, s);
 }
@@ -194,6 +195,7 @@ tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q,
   a.T = p.T;
   a.C = p.C;
   a.D = p.D;
+  a.B = p.B;
   a.heads = p.hpr;
   a.d = p.d;
   a.status = status_of(ws);
@@ -207,7 +209,7 @@ tsp_status o_projection(const Plan& p, const void* o, const void* wpack, const v
   c.epi = residual ? EPI_RESIDUAL : EPI_STORE;
   c.A = o;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_o;
   c.ldb = p.H;
   c.b_rows = p.H;
@@ -229,7 +231,7 @@ tsp_status swiglu_gate_up(const Plan& p, const void* hs, const void* wpack, void
   c.epi = EPI_SWIGLU;
   c.A = hs;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_w13;
   c.ldb = p.H;
   c.b_rows = 2LL * p.NF;
@@ -249,7 +251,7 @@ tsp_status swiglu_down(const Plan& p, const void* g, const void* wpack, const vo
   c.epi = residual ? EPI_RESIDUAL : EPI_STORE;
   c.A = g;
   c.lda = p.NF;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_w2;
   c.ldb = p.NF;
   c.b_rows = p.H;
@@ -261,7 +263,7 @@ tsp_status swiglu_down(const Plan& p, const void* g, const void* wpack, const vo
   c.R = residual;
   c.ldr = p.H;
   c.residual_f32 = residual_f32;
-  c.ring_rows = p.T;
+  c.ring_rows = (int64_t)p.B * p.T;  // rank r's rows of every sequence
   c.ring_kblocks = p.Fp / 64;
   c.status = status_of(ws);
   return launch_gemm(c, s);
@@ -319,12 +321,22 @@ using namespace tsp;
 extern "C" {
 
 tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t* out) {
+  return tsp_plan_batched(D, S, 1, hidden, heads, ffn, out);
+}
+
+tsp_status tsp_plan_batched(int D, int64_t S, int batch, int hidden, int heads, int ffn,
+                            tsp_plan_t* out) {
   TSP_GUARD_BEGIN
   if (!out) return fail(TSP_ERR_INVALID_ARG, "tsp_plan: null output");
   *out = nullptr;
   if (D < 1 || D > 64) return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: D must be in [1, 64]");
   if (S < 2LL * D || S > (1LL << 26) || S % (2LL * D))
     return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: S must be a multiple of 2D in [2D, 2^26]");
+  if (batch < 1 || (int64_t)batch * S > (1LL << 26))
+    return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: batch must be >= 1 with batch * S <= 2^26");
+  if (batch > 1 && (S / D) % 128)
+    return fail(TSP_ERR_UNSUPPORTED,
+                "tsp_plan: a micro-batch of several sequences needs S/D % 128 == 0");
   if (heads < 1 || hidden < 1 || hidden % heads)
     return fail(TSP_ERR_UNSUPPORTED, "tsp_plan: hidden must be a multiple of heads");
   const int d = hidden / heads;
@@ -336,6 +348,8 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
   Plan p{};
   p.D = D;
   p.S = S;
+  p.B = batch;
+  p.N = (int64_t)batch * S;
   p.H = hidden;
   p.heads = heads;
   p.d = d;
@@ -348,7 +362,7 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
   p.Fp = (p.Fd + 63) / 64 * 64;
   if ((long long)D * p.Fp % 128) p.Fp = (p.Fd + 127) / 128 * 128;
   p.NF = D * p.Fp;
-  p.ld_stat = (S + 127) / 128 * 128;
+  p.ld_stat = (p.N + 127) / 128 * 128;
 
   const size_t H = hidden;
   p.wp_qkv = 0;
@@ -357,7 +371,7 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
   p.wp_w2 = p.wp_w13 + 2 * (size_t)p.NF * H;
   p.wp_elems = p.wp_w2 + H * (size_t)p.NF;
 
-  const size_t Sz = (size_t)S;
+  const size_t Sz = (size_t)p.N;  // rows of the activation buffers
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -402,6 +416,8 @@ tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info) {
   const Plan& p = plan->p;
   info->D = p.D;
   info->S = p.S;
+  info->batch = p.B;
+  info->tokens = p.N;
   info->hidden = p.H;
   info->heads = p.heads;
   info->head_dim = p.d;
@@ -507,7 +523,7 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
   TSP_TRY(check_ws(ws, "tsp_layer_fwd_host"));
   const Plan& p = plan->p;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t bytes = (size_t)p.S * p.H * 2;
+  const size_t bytes = (size_t)p.N * p.H * 2;
   void* a = at<void>(ws, p.ws.stage_in);
   void* b = at<void>(ws, p.ws.stage_out);
   // Page-locked host memory that the runtime maps into the device address space is

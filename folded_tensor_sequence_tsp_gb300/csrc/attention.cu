@@ -38,7 +38,9 @@
 // P <= 256 and most tiles never touch O. The result is exact softmax: O / l.
 //
 // Query row r of the rank-major layout is the token at global position pos(r) of
-// the zigzag map; key t is visible iff t <= pos(r). CTAs of one head run before
+// the zigzag map; key t is visible iff t <= pos(r). A micro-batch of B sequences
+// (rank-major [D][B][T] query rows, natural K/V rows b*S + t) adds a grid dimension:
+// blockIdx.y is the sequence, whose queries see only its own keys. CTAs of one head run before
 // the next head (K/V of a head stay in L2 across its CTAs) and, when the zigzag
 // chunk is a multiple of 256 tokens, take query blocks in decreasing position, so
 // the longest blocks start first.
@@ -78,8 +80,9 @@ struct AttParams {
   long long o_col0;
   float* lse;          // optional: [head][row] base-2 log-sum-exp of the scaled scores
   long long ld_lse;
-  long long S, T, C;
+  long long S, T, C;  // one sequence
   int D;
+  int B;               // sequences of the micro-batch (blockIdx.y)
   int heads;
   int q_blocks;
   int natural_order;
@@ -96,6 +99,12 @@ __device__ __forceinline__ long long zig_row(long long t, long long C, long long
 __device__ __forceinline__ long long row_pos(long long r, long long C, long long T, int D) {
   const long long rank = r / T, l = r - rank * T;
   return l < C ? rank * C + l : (2 * D - 1 - rank) * C + (l - C);
+}
+
+// Row of the micro-batch's [D][B][T] layout that holds row v of sequence `seq`'s
+// own [D][T] layout (the identity when B == 1).
+__device__ __forceinline__ long long batch_row(long long v, int seq, const AttParams& p) {
+  return v + ((v / p.T) * (p.B - 1) + seq) * p.T;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -181,6 +190,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_b = tiles_needed(row0 + QT, p);
   const int n_tiles = max(n_a, n_b);
   const int col_q = head * HD;  // Q columns inside qkv; K/V columns inside kn/vn
+  const int seq = blockIdx.y;
+  const int kv_row0 = (int)(seq * p.S);  // first natural K/V row of the sequence
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -219,8 +230,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           tma_load_2d(sQ + t * G::TILE_BYTES + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b,
-                      (int)(row0 + t * QT));
-        tma_load_2d(sK0 + b * BOX_BYTES, &tmK, q_full, col_q + 64 * b, 0);
+                      (int)batch_row(row0 + t * QT, seq, p));
+        tma_load_2d(sK0 + b * BOX_BYTES, &tmK, q_full, col_q + 64 * b, kv_row0);
       }
       int last[STAGES];
 #pragma unroll
@@ -236,10 +247,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int b = 0; b < G::BOXES; ++b) {
           tma_load_2d(sV + st * G::TILE_BYTES + b * BOX_BYTES, &tmV, &kv_full[st],
-                      col_q + 64 * b, j * KT);
+                      col_q + 64 * b, kv_row0 + j * KT);
           if (has_k)
             tma_load_2d(sK + st * G::TILE_BYTES + b * BOX_BYTES, &tmK, &kv_full[st],
-                        col_q + 64 * b, (j + 1) * KT);
+                        col_q + 64 * b, kv_row0 + (j + 1) * KT);
         }
         last[st] = (int)ph;
       }
@@ -330,10 +341,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t = (warp - 2) >> 2;  // query tile of this warpgroup: 0 = A, 1 = B
     const int q = warp & 3;         // TMEM lane quarter of this warp
     const int r_local = q * 32 + lane;
-    const long long grow = row0 + t * QT + r_local;
-    const bool row_ok = grow < p.S;
+    const long long vrow = row0 + t * QT + r_local;  // row in the sequence's own layout
+    const bool row_ok = vrow < p.S;
+    const long long grow = batch_row(vrow, seq, p);  // row in the micro-batch's layout
     // S < 2^30 (checked at launch): positions fit in int
-    const int pos = row_ok ? (int)row_pos(grow, p.C, p.T, p.D) : -1;
+    const int pos = row_ok ? (int)row_pos(vrow, p.C, p.T, p.D) : -1;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t s_tmem = lane_base + tm_s(t);
     const uint32_t o_tmem = lane_base + tm_o(t);
@@ -457,19 +469,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int HD>
 tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
-  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, (uint64_t)c.ld_qkv, (uint64_t)c.S,
+  const uint64_t rows = (uint64_t)c.S * (uint64_t)p.B;
+  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, (uint64_t)c.ld_qkv, rows,
                                     (uint64_t)c.ld_qkv * 2, 64, QT);
   if (st != TSP_OK) return st;
-  st = make_tmap_2d_bf16(&tk, c.kn, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, KT);
+  st = make_tmap_2d_bf16(&tk, c.kn, (uint64_t)c.ld_kv, rows, (uint64_t)c.ld_kv * 2, 64, KT);
   if (st != TSP_OK) return st;
-  st = make_tmap_2d_bf16(&tv, c.vn, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, KT);
+  st = make_tmap_2d_bf16(&tv, c.vn, (uint64_t)c.ld_kv, rows, (uint64_t)c.ld_kv * 2, 64, KT);
   if (st != TSP_OK) return st;
   auto kernel = attention_tcgen05_kernel<HD>;
   const size_t smem = Geometry<HD>::SMEM;
   TSP_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)smem,
                             "attention: cudaFuncSetAttribute"));
   const long long blocks = (long long)p.q_blocks * p.heads;
-  kernel<<<(unsigned)blocks, THREADS, smem, stream>>>(tq, tk, tv, p);
+  kernel<<<dim3((unsigned)blocks, (unsigned)p.B), THREADS, smem, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TSP_OK : cuda_fail(e, "attention: launch");
 }
@@ -485,7 +498,12 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   if ((long long)c.heads * c.d > c.ld_kv || (long long)c.heads * c.d > c.ld_qkv ||
       c.o_col0 + (long long)c.heads * c.d > c.ld_o)
     return fail(TSP_ERR_INVALID_ARG, "attention: head columns exceed the row width");
-  if (c.S > (1ll << 30)) return fail(TSP_ERR_UNSUPPORTED, "attention: S too large");
+  const int B = c.B > 0 ? c.B : 1;
+  if (c.S * B > (1ll << 30) || B > 65535)
+    return fail(TSP_ERR_UNSUPPORTED, "attention: too many rows");
+  // with several sequences a 128-row query tile must not straddle two ranks' blocks
+  if (B > 1 && c.T % QT)
+    return fail(TSP_ERR_UNSUPPORTED, "attention: a micro-batch needs S/D % 128 == 0");
   AttParams p;
   p.o = static_cast<__nv_bfloat16*>(c.o);
   p.ld_o = c.ld_o;
@@ -496,6 +514,7 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.T = c.T;
   p.C = c.C;
   p.D = c.D;
+  p.B = B;
   p.heads = c.heads;
   p.q_blocks = (int)((c.S + QB - 1) / QB);
   p.natural_order = (c.C % QB == 0) ? 1 : 0;

@@ -278,6 +278,17 @@ tsp_status layer_backward_from(const Plan& p, const void* xs, const void* wpack,
 
 using namespace tsp;
 
+namespace {
+// The backward calls take one sequence per plan (tsp_plan, or tsp_plan_batched
+// with batch 1).
+tsp_status check_single_sequence(tsp_plan_t plan, const char* what) {
+  TSP_TRY(tsp_check_plan(plan));
+  if (plan->p.B != 1)
+    return fail(TSP_ERR_UNSUPPORTED, std::string(what) + ": the backward takes one sequence per plan");
+  return TSP_OK;
+}
+}  // namespace
+
 extern "C" {
 
 size_t tsp_bwd_workspace_bytes(tsp_plan_t plan) { return plan ? plan->p.ws.total_bwd : 0; }
@@ -285,7 +296,7 @@ size_t tsp_bwd_workspace_bytes(tsp_plan_t plan) { return plan ? plan->p.ws.total
 tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
                        const tsp_bf16* dmlp, tsp_bf16* dhs, float* dwpack, void* ws,
                        void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_mlp_bwd"));
   TSP_TRY(check_ptrs({hs, wpack, dmlp, dhs, dwpack}, "tsp_mlp_bwd"));
   TSP_TRY(check_ws(ws, "tsp_mlp_bwd"));
   if (dhs == hs || dhs == dmlp) return fail(TSP_ERR_INVALID_ARG, "tsp_mlp_bwd: dhs aliases an input");
@@ -296,7 +307,7 @@ tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpac
 tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                              const tsp_bf16* dattn, tsp_bf16* dxs, float* dwpack, void* ws,
                              void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_attention_bwd"));
   TSP_TRY(check_ptrs({xs, wpack, dattn, dxs, dwpack}, "tsp_attention_bwd"));
   TSP_TRY(check_ws(ws, "tsp_attention_bwd"));
   if (dxs == xs || dxs == dattn) return fail(TSP_ERR_INVALID_ARG, "tsp_attention_bwd: dxs aliases an input");
@@ -311,7 +322,7 @@ tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16
 tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                          const tsp_bf16* dout, tsp_bf16* dxs, float* dwpack, void* ws,
                          void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_layer_bwd"));
   TSP_TRY(check_ptrs({xs, wpack, dout, dxs, dwpack}, "tsp_layer_bwd"));
   TSP_TRY(check_ws(ws, "tsp_layer_bwd"));
   if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd: dxs aliases an input");
@@ -328,7 +339,7 @@ size_t tsp_saved_bytes(tsp_plan_t plan) { return plan ? saved_bytes(plan->p) : 0
 
 tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                                tsp_bf16* out, void* saved, void* ws, void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_layer_fwd_train"));
   TSP_TRY(check_ptrs({xs, wpack, out, saved}, "tsp_layer_fwd_train"));
   TSP_TRY(check_ws(ws, "tsp_layer_fwd_train"));
   if (out == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd_train: out aliases xs");
@@ -353,7 +364,7 @@ tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf
 tsp_status tsp_layer_bwd_saved(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                                const void* saved, const tsp_bf16* dout, tsp_bf16* dxs,
                                float* dwpack, void* ws, void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_layer_bwd_saved"));
   TSP_TRY(check_ptrs({xs, wpack, saved, dout, dxs, dwpack}, "tsp_layer_bwd_saved"));
   TSP_TRY(check_ws(ws, "tsp_layer_bwd_saved"));
   if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd_saved: dxs aliases an input");
@@ -369,7 +380,7 @@ tsp_status tsp_layer_bwd_saved(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf
 tsp_status tsp_causal_attention_lse(tsp_plan_t plan, int shard, const tsp_bf16* q,
                                     const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
                                     float* lse, void* ws, void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_causal_attention_lse"));
   TSP_TRY(check_ptrs({q, kn, vn, o, lse}, "tsp_causal_attention_lse"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention_lse"));
   if (shard < 0 || shard >= plan->p.D)
@@ -382,7 +393,7 @@ tsp_status tsp_causal_attention_bwd(tsp_plan_t plan, int shard, const tsp_bf16* 
                                     const tsp_bf16* kn, const tsp_bf16* vn, const tsp_bf16* o,
                                     const tsp_bf16* dout, const float* lse, float* delta,
                                     tsp_bf16* dqkv, void* ws, void* stream) {
-  TSP_TRY(tsp_check_plan(plan));
+  TSP_TRY(check_single_sequence(plan, "tsp_causal_attention_bwd"));
   TSP_TRY(check_ptrs({q, kn, vn, o, dout, lse, delta, dqkv}, "tsp_causal_attention_bwd"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention_bwd"));
   if (shard < 0 || shard >= plan->p.D)

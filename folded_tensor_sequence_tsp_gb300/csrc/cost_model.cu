@@ -3,14 +3,18 @@
 // Memory-Efficient Transformer Training & Inference", section 3, theoretical
 // analysis). The page states the comparison in words; the closed forms below are
 // written from each scheme's sharding rules for the layer this library computes
-// (causal attention with h heads + SwiGLU of width F, batch 1, S tokens). Host
-// code only: no CUDA call.
+// (causal attention with h heads + SwiGLU of width F, S tokens per sequence, a
+// micro-batch of B sequences). Host code only: no CUDA call.
 //
 // Per token the layer keeps boundary activations x and h (2H elements) and inner
 // activations q, k, v, o (4H) and a1, a3, g (3F). Weights: 4H^2 + 3HF elements.
 // Communication counts what one device receives in one forward of the layer, with
 // ring collectives: all-reduce of n elements over g devices = 2 (g-1)/g n received,
 // all-gather of n = (g-1)/g n, broadcast of a shard = the shard (non-owners).
+// A micro-batch ([TSP] s4: TSP's smaller footprint admits larger micro-batches)
+// multiplies every activation term, the activation traffic and the FLOPs by B; the
+// weights, and the weight traffic of TSP, serve the whole micro-batch once.
+#include <cmath>
 #include <cstdint>
 
 #include "tsp.h"
@@ -24,10 +28,11 @@ double layer_flops(double S, double H, double F) {
 
 }  // namespace
 
-extern "C" tsp_status tsp_cost_model(int scheme, int D, int tp, int64_t S, int hidden, int heads,
-                                     int ffn, tsp_cost* out) {
+extern "C" tsp_status tsp_cost_model_batched(int scheme, int D, int tp, int64_t S, int batch,
+                                             int hidden, int heads, int ffn, tsp_cost* out) {
   using tsp::fail;
   if (!out) return fail(TSP_ERR_INVALID_ARG, "tsp_cost_model: out is NULL");
+  if (batch < 1) return fail(TSP_ERR_INVALID_ARG, "tsp_cost_model: batch must be >= 1");
   if (D < 1 || S < 1 || hidden < 1 || heads < 1 || ffn < 1 || hidden % heads)
     return fail(TSP_ERR_INVALID_ARG, "tsp_cost_model: bad layer shape");
   const double s = (double)S, H = hidden, F = ffn, Dd = D;
@@ -90,6 +95,42 @@ extern "C" tsp_status tsp_cost_model(int scheme, int D, int tp, int64_t S, int h
     default:
       return fail(TSP_ERR_INVALID_ARG, "tsp_cost_model: unknown scheme");
   }
+  const double b = batch;
+  c.act_elems *= b;
+  c.act_inflight_elems *= b;
+  c.comm_act_elems *= b;
+  c.flops *= b;
   *out = c;
+  return TSP_OK;
+}
+
+extern "C" tsp_status tsp_cost_model(int scheme, int D, int tp, int64_t S, int hidden, int heads,
+                                     int ffn, tsp_cost* out) {
+  return tsp_cost_model_batched(scheme, D, tp, S, 1, hidden, heads, ffn, out);
+}
+
+extern "C" tsp_status tsp_cost_max_batch(int scheme, int D, int tp, int64_t S, int hidden,
+                                         int heads, int ffn, int layers, double mem_bytes,
+                                         int64_t* out) {
+  using tsp::fail;
+  if (!out) return fail(TSP_ERR_INVALID_ARG, "tsp_cost_max_batch: out is NULL");
+  if (layers < 1 || !(mem_bytes >= 0.0) || !std::isfinite(mem_bytes))
+    return fail(TSP_ERR_INVALID_ARG, "tsp_cost_max_batch: layers >= 1 and a finite mem_bytes >= 0");
+  tsp_cost one;
+  tsp_status st = tsp_cost_model_batched(scheme, D, tp, S, 1, hidden, heads, ffn, &one);
+  if (st != TSP_OK) return st;
+  // bytes(B) = 2 (L (W + B A) + W_inflight + B A_inflight): every layer keeps its
+  // weights and activations, one layer's received buffers exist at a time
+  const double L = layers;
+  const double fixed = 2.0 * (L * one.weight_elems + one.weight_inflight_elems);
+  const double per_seq = 2.0 * (L * one.act_elems + one.act_inflight_elems);
+  auto fits = [&](double bb) { return fixed + bb * per_seq <= mem_bytes; };
+  double bmax = 0.0;
+  if (fits(1.0)) {
+    bmax = std::floor((mem_bytes - fixed) / per_seq);
+    while (bmax > 1.0 && !fits(bmax)) bmax -= 1.0;  // guard the rounding of the division
+    while (fits(bmax + 1.0)) bmax += 1.0;
+  }
+  *out = (int64_t)bmax;
   return TSP_OK;
 }

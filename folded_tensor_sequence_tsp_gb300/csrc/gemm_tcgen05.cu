@@ -66,7 +66,7 @@ struct GemmParams {
   long long split_ld;
   int split_hd;
   long long zz_C, zz_T;
-  int zz_D;
+  int zz_D, zz_B;
   __nv_bfloat16* C2;  // K_SWIGLU_SAVE: pre-activations out; K_SWIGLU_BWD: pre-activations in
   long long ldc2;
   int ring_rows;
@@ -272,8 +272,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       long long nat = 0;  // natural token position of this row (K_QKV_SPLIT)
       if constexpr (EPI == K_QKV_SPLIT) {
-        const long long rank = row / p.zz_T, l = row - rank * p.zz_T;
-        nat = l < p.zz_C ? rank * p.zz_C + l : (2 * p.zz_D - 1 - rank) * p.zz_C + (l - p.zz_C);
+        // sharded row (rank*B + b)*T + l of a micro-batch -> natural row b*S + pos
+        const long long rb = row / p.zz_T, l = row - rb * p.zz_T;
+        const long long rank = rb / p.zz_B, b = rb - rank * p.zz_B;
+        nat = b * (p.zz_T * p.zz_D) +
+              (l < p.zz_C ? rank * p.zz_C + l : (2 * p.zz_D - 1 - rank) * p.zz_C + (l - p.zz_C));
       }
       if constexpr (EPI == K_SWIGLU || EPI == K_SWIGLU_SAVE) {
         // columns [0,128) of the tile are gate rows (W1), [128,256) up rows (W3)
@@ -456,7 +459,7 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
       (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N != 3 * c.split_hd ||
        c.ldc < c.split_hd || c.split_ld < c.split_hd || (c.split_ld % 8) || !aligned16(c.split_k) ||
        !aligned16(c.split_v) || c.zz_C <= 0 || c.zz_T != 2 * c.zz_C || c.zz_D <= 0 ||
-       c.M != c.zz_T * c.zz_D))
+       c.M != c.zz_T * c.zz_D * (c.zz_B > 0 ? c.zz_B : 1)))
     return fail(TSP_ERR_INVALID_ARG, "gemm: bad Q/K/V split arguments");
   if (c.M > (1ll << 30) || c.N > (1ll << 30) || c.K > (1ll << 30) || c.b_rows > (1ll << 30))
     return fail(TSP_ERR_UNSUPPORTED, "gemm: dimension too large");
@@ -494,6 +497,7 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   p.zz_C = c.zz_C;
   p.zz_T = c.zz_T;
   p.zz_D = c.zz_D;
+  p.zz_B = c.zz_B > 0 ? c.zz_B : 1;
   p.C2 = static_cast<__nv_bfloat16*>(c.C2);
   p.ldc2 = c.ldc2;
   p.ring_rows = (int)c.ring_rows;

@@ -15,7 +15,7 @@
 
 namespace {
 
-// 32 MiB: the status word (first 256 bytes) and G = [S][ffn_padded] bf16.
+// 32 MiB: the status word (first 256 bytes) and G = [tokens][ffn_padded] bf16.
 constexpr size_t kNoallocScratchBytes = 32ull << 20;
 constexpr size_t kNoallocStatusBytes = 256;
 
@@ -62,11 +62,11 @@ extern "C" tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs,
     return tsp::fail(TSP_ERR_INVALID_ARG, "tsp_mlp_fwd_noalloc: pointer not 16-byte aligned");
   if (static_cast<const void*>(mlp) == static_cast<const void*>(hs))
     return tsp::fail(TSP_ERR_INVALID_ARG, "tsp_mlp_fwd_noalloc: mlp aliases hs");
-  const size_t g_bytes = (size_t)info.S * (size_t)info.ffn_padded * 2;
+  const size_t g_bytes = (size_t)info.tokens * (size_t)info.ffn_padded * 2;
   if (g_bytes > kNoallocScratchBytes - kNoallocStatusBytes) {
     char buf[200];
     snprintf(buf, sizeof buf,
-             "tsp_mlp_fwd_noalloc: this shape needs %zu bytes of scratch (S x ffn_padded x 2), "
+             "tsp_mlp_fwd_noalloc: this shape needs %zu bytes of scratch (tokens x ffn_padded x 2), "
              "more than the %zu available in the static buffer; use tsp_mlp_fwd with a workspace",
              g_bytes, kNoallocScratchBytes - kNoallocStatusBytes);
     return tsp::fail(TSP_ERR_UNSUPPORTED, buf);
@@ -88,7 +88,7 @@ extern "C" tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs,
   up.epi = tsp::EPI_SWIGLU;
   up.A = hs;
   up.lda = info.hidden;
-  up.M = info.S;
+  up.M = info.tokens;
   up.B = w + info.wpack_w13;
   up.ldb = info.hidden;
   up.b_rows = 2LL * info.ffn_padded;
@@ -105,7 +105,7 @@ extern "C" tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs,
   down.epi = tsp::EPI_STORE;
   down.A = g;
   down.lda = info.ffn_padded;
-  down.M = info.S;
+  down.M = info.tokens;
   down.B = w + info.wpack_w2;
   down.ldb = info.ffn_padded;
   down.b_rows = info.hidden;
@@ -114,7 +114,7 @@ extern "C" tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs,
   down.K = info.ffn_padded;
   down.C = mlp;
   down.ldc = info.hidden;
-  down.ring_rows = info.T;
+  down.ring_rows = (int64_t)info.batch * info.T;
   down.ring_kblocks = info.shard_ffn_padded / 64;
   down.status = status;
   return tsp::launch_gemm(down, s);

@@ -15,16 +15,17 @@ namespace tsp {
 
 struct DevStatus;
 
-// Layout of the caller's workspace (byte offsets, each 256-byte aligned).
+// Layout of the caller's workspace (byte offsets, each 256-byte aligned). N = B*S
+// rows: every token of the micro-batch.
 struct WorkspaceLayout {
   size_t status;   // DevStatus
-  size_t qkv;      // [S][3H/D] Q|K|V of the current attention shard (sharded rows)
-  size_t kn, vn;   // [S][H/D] K and V of the current shard in natural token order
-  size_t o;        // [S][H]   attention output before the O projection (sharded rows)
-  size_t h;        // [S][H]   h = x + Attn(x) (sharded rows), bf16: input of the MLP
-  size_t h32;      // [S][H]   the same h in fp32: the residual of the MLP block
-  size_t g;        // [S][NF]  gated activation (sharded rows)
-  size_t stage_in, stage_out;  // [S][H] natural-order staging for tsp_layer_fwd_host
+  size_t qkv;      // [N][3H/D] Q|K|V of the current attention shard (sharded rows)
+  size_t kn, vn;   // [N][H/D] K and V of the current shard in natural token order
+  size_t o;        // [N][H]   attention output before the O projection (sharded rows)
+  size_t h;        // [N][H]   h = x + Attn(x) (sharded rows), bf16: input of the MLP
+  size_t h32;      // [N][H]   the same h in fp32: the residual of the MLP block
+  size_t g;        // [N][NF]  gated activation (sharded rows)
+  size_t stage_in, stage_out;  // [N][H] natural-order staging for tsp_layer_fwd_host
   size_t total;
   // backward calls only (after `total`):
   size_t a13;      // [S][2NF] SwiGLU pre-activations A1|A3 (W13's packed column order),
@@ -42,7 +43,9 @@ struct WorkspaceLayout {
 
 struct Plan {
   int D;
-  int64_t S;
+  int64_t S;  // tokens of one sequence
+  int B;      // sequences of the micro-batch (rank-major layout [D][B][T][H])
+  int64_t N;  // B * S: rows of every GEMM and of the activation buffers
   int H, heads, d, F;
   int64_t T, C;
   int Hd;   // H / D
@@ -50,7 +53,7 @@ struct Plan {
   int Fd;   // F / D
   int Fp;   // padded shard width of the MLP
   int NF;   // D * Fp
-  int64_t ld_stat;  // row stride of the per-head row statistics (S rounded up to 128)
+  int64_t ld_stat;  // row stride of the per-head row statistics (N rounded up to 128)
   size_t wp_qkv, wp_o, wp_w13, wp_w2, wp_elems;
   WorkspaceLayout ws;
 };
@@ -133,21 +136,24 @@ struct GemmCall {
   void* C32;                   // optional fp32 copy of the output (EPI_RESIDUAL, bf16 residual), row stride ldc
   // EPI_QKV_SPLIT: the N = 3 split_hd columns are Q | K | V; Q rows go to C (ldc),
   // K and V rows to split_k / split_v (row stride split_ld) at the natural token
-  // position of the sharded row (zigzag chunk zz_C, tokens per rank zz_T, zz_D ranks)
+  // position of the sharded row (zigzag chunk zz_C, tokens per rank zz_T, zz_D ranks,
+  // zz_B sequences: sharded row (r*zz_B + b)*zz_T + l -> natural row b*S + pos(r, l))
   void* split_k; void* split_v; int64_t split_ld; int64_t split_hd;
-  int64_t zz_C, zz_T; int zz_D;
+  int64_t zz_C, zz_T; int zz_D; int zz_B;
   int64_t ring_rows;           // rows per rank for the ring K order, 0 = natural order
   int64_t ring_kblocks;        // 64-wide K blocks per shard
   DevStatus* status;
 };
 tsp_status launch_gemm(const GemmCall& call, cudaStream_t stream);
 
+// Rows of qkv, o and lse are the sharded rows of a micro-batch of B sequences
+// ([D][B][T] rank-major); kn/vn rows are natural rows b*S + t. B = 0 means 1.
 struct AttentionCall {
   const void* qkv; int64_t ld_qkv;   // Q at columns [j*d, (j+1)*d) for head j of the group
   const void* kn; const void* vn; int64_t ld_kv;
   void* o; int64_t ld_o; int64_t o_col0;
   float* lse; int64_t ld_lse;  // optional [heads][ld_lse] log-sum-exp (base 2) per row
-  int64_t S; int64_t T; int64_t C; int D;
+  int64_t S; int64_t T; int64_t C; int D; int B;
   int heads;  // heads in this call
   int d;
   DevStatus* status;

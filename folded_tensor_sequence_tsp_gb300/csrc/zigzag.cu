@@ -6,7 +6,10 @@
 // (local rows 0..C-1) and chunk 2D-1-r (local rows C..2C-1), which gives every rank
 // the same causal attention work. Token t therefore sits at row
 //     zig(t) = r*T + l   (T = S/D)
-// of the rank-major [D][T][...] layout.
+// of the rank-major [D][T][...] layout. A micro-batch of B sequences (section 4,
+// scalability: larger micro-batches) keeps every rank's rows of all sequences
+// together: token t of sequence b (natural row b*S + t) sits at row
+//     (r*B + b)*T + l   of the rank-major [D][B][T][...] layout.
 //
 // K/V all-gather along the sequence (same section): every rank's K and V columns
 // of the current attention shard are gathered into one natural-order buffer.
@@ -22,14 +25,19 @@ namespace {
 
 struct Zig {
   long long C, T;
-  int D;
-  __device__ __forceinline__ long long row_of(long long t) const {
+  int D, B;
+  // sharded row of natural row n = b*S + t (S = D*T)
+  __device__ __forceinline__ long long row_of(long long n) const {
+    const long long b = n / (T * D);
+    const long long t = n - b * (T * D);
     const long long c = t / C;
     const long long o = t - c * C;
-    return c < D ? c * T + o : (2 * D - 1 - c) * T + C + o;
+    const long long r = c < D ? c : 2 * D - 1 - c;
+    return (r * B + b) * T + (c < D ? o : C + o);
   }
 };
 
+// S here (and in the kernels below) is the number of natural rows: B * tokens.
 __global__ void zigzag_index_kernel(int32_t* __restrict__ fwd, int32_t* __restrict__ inv,
                                     long long S, Zig z) {
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < S;
@@ -220,27 +228,27 @@ tsp_status check_launch(const char* what) {
 }  // namespace
 
 tsp_status launch_zigzag_index(const Plan& p, int32_t* fwd, int32_t* inv, cudaStream_t s) {
-  Zig z{p.C, p.T, p.D};
-  zigzag_index_kernel<<<grid_for((p.S + 255) / 256, 8), 256, 0, s>>>(fwd, inv, p.S, z);
+  Zig z{p.C, p.T, p.D, p.B};
+  zigzag_index_kernel<<<grid_for((p.N + 255) / 256, 8), 256, 0, s>>>(fwd, inv, p.N, z);
   return check_launch("zigzag index launch");
 }
 
 tsp_status launch_zigzag_rows(const Plan& p, const void* src, void* dst, int64_t width,
                               bool to_sharded, cudaStream_t s) {
   if ((width * 2) % 16) return fail(TSP_ERR_UNSUPPORTED, "zigzag rows: row bytes % 16 != 0");
-  Zig z{p.C, p.T, p.D};
+  Zig z{p.C, p.T, p.D, p.B};
   const int vpr = (int)(width * 2 / 16);
-  zigzag_rows_kernel<4><<<grid_for(p.S, 8), 256, 0, s>>>(static_cast<const uint4*>(src),
-                                                          static_cast<uint4*>(dst), p.S, vpr,
+  zigzag_rows_kernel<4><<<grid_for(p.N, 8), 256, 0, s>>>(static_cast<const uint4*>(src),
+                                                          static_cast<uint4*>(dst), p.N, vpr,
                                                           to_sharded ? 1 : 0, z);
   return check_launch("zigzag rows launch");
 }
 
 tsp_status launch_kv_gather(const Plan& p, const void* qkv, void* kn, void* vn, cudaStream_t s) {
-  Zig z{p.C, p.T, p.D};
+  Zig z{p.C, p.T, p.D, p.B};
   const int vec_hd = p.Hd * 2 / 16;
-  kv_gather_kernel<<<grid_for((p.S + 7) / 8, 16), 256, 0, s>>>(
-      static_cast<const uint4*>(qkv), static_cast<uint4*>(kn), static_cast<uint4*>(vn), p.S,
+  kv_gather_kernel<<<grid_for((p.N + 7) / 8, 16), 256, 0, s>>>(
+      static_cast<const uint4*>(qkv), static_cast<uint4*>(kn), static_cast<uint4*>(vn), p.N,
       vec_hd, z);
   return check_launch("kv gather launch");
 }

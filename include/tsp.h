@@ -30,7 +30,8 @@
  *     once the work is enqueued.
  *   - Activations in the "sharded" layout are rank-major [D, T, H] with
  *     T = S/D: rank r's rows are its zigzag tokens in local order (chunk r, then
- *     chunk 2D-1-r, chunk length C = S/(2D)).
+ *     chunk 2D-1-r, chunk length C = S/(2D)). A plan for a micro-batch of B
+ *     sequences (tsp_plan_batched) uses [D, B, T, H] instead.
  *   - Status is returned synchronously. Argument and shape problems return
  *     TSP_ERR_INVALID_ARG / TSP_ERR_UNSUPPORTED before anything is launched; a
  *     launch failure returns TSP_ERR_CUDA. Device-side waits are bounded: a wait
@@ -82,7 +83,9 @@ typedef struct tsp_plan_info {
   size_t wpack_elems; /* total elements of the packed buffer                          */
   size_t workspace_bytes;     /* tsp_workspace_bytes(plan)     */
   size_t bwd_workspace_bytes; /* tsp_bwd_workspace_bytes(plan) */
-  int64_t stat_stride;        /* row stride of per-head row statistics (lse, delta): S rounded up to 128 */
+  int64_t stat_stride;        /* row stride of per-head row statistics (lse, delta): tokens rounded up to 128 */
+  int batch;                  /* B: sequences of the micro-batch (1 for tsp_plan)  */
+  int64_t tokens;             /* N = B * S: rows of every activation buffer        */
 } tsp_plan_info;
 
 /*
@@ -97,6 +100,27 @@ typedef struct tsp_plan_info {
  * the caller releases with tsp_plan_destroy.
  */
 tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t* out);
+
+/*
+ * tsp_plan_batched - a plan for a micro-batch of `batch` independent sequences of S
+ * tokens each ([TSP] s4: the smaller per-device footprint of TSP admits larger
+ * micro-batches). Every rank owns its two zigzag chunks of EACH sequence, so the
+ * sharded layout of every activation becomes rank-major [D][B][T][H]: rank r's rows
+ * of sequence b are rows (r*B + b)*T .. (r*B + b)*T + T-1, in the single-sequence
+ * local order. Natural (unsharded) buffers are [B][S][H]. Queries attend only to
+ * the keys of their own sequence; the projections and the MLP run over all
+ * N = B*S rows at once (one weight-shard pass serves the whole micro-batch).
+ * Every forward entry point, the shard/unshard and index calls and the single
+ * steps take such a plan; in the buffer sizes stated below, read N = B*S rows where
+ * a size says S or D*T. The backward calls (tsp_*_bwd, the training pair and
+ * tsp_causal_attention_lse) take batch 1 only and return TSP_ERR_UNSUPPORTED
+ * otherwise. Supported iff tsp_plan's conditions hold, batch >= 1,
+ * batch * S <= 2^26 and, for batch > 1, T = S/D is a multiple of 128 (a 128-row
+ * query tile of the attention kernel never spans two ranks' blocks).
+ * tsp_plan(D, S, ...) is tsp_plan_batched(D, S, 1, ...).
+ */
+tsp_status tsp_plan_batched(int D, int64_t S, int batch, int hidden, int heads, int ffn,
+                            tsp_plan_t* out);
 void tsp_plan_destroy(tsp_plan_t plan);
 tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info);
 /* Bytes of the caller-allocated workspace every *_fwd call below needs (256-byte
@@ -127,10 +151,13 @@ tsp_status tsp_pack_weights(tsp_plan_t plan, const tsp_bf16* Wq, const tsp_bf16*
  * tsp_shard_index - the zigzag map ([TSP] s2, zigzag partitioning that balances
  * causal attention work). fwd[t] = r*T + l for global token t owned by rank r at
  * local row l; inv[r*T + l] = t. Both int32 [S]. Either pointer may be NULL.
+ * With a micro-batch (tsp_plan_batched): fwd[b*S + t] = (r*B + b)*T + l and inv its
+ * inverse, both int32 [B*S].
  */
 tsp_status tsp_shard_index(tsp_plan_t plan, int32_t* fwd, int32_t* inv, void* stream);
 
-/* tsp_shard: x [S][H] natural order -> xs [D][T][H] zigzag rank-major.
+/* tsp_shard: x [S][H] natural order -> xs [D][T][H] zigzag rank-major
+ * (micro-batch: x [B][S][H] -> xs [D][B][T][H]).
  * tsp_unshard: the inverse. Buffers must not overlap. */
 tsp_status tsp_shard(tsp_plan_t plan, const tsp_bf16* x, tsp_bf16* xs, void* stream);
 tsp_status tsp_unshard(tsp_plan_t plan, const tsp_bf16* xs, tsp_bf16* x, void* stream);
@@ -183,7 +210,7 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
  * as for tsp_mlp_fwd) but no workspace: the gated activation G and the status word
  * of the bounded device waits live in one static device array of 32 MiB inside the
  * library, which every GPU that loads the library holds until the process exits.
- * Limit: S x ffn_padded x 2 bytes <= 32 MiB - 256 (e.g. S = 4096 with hidden 1024
+ * Limit: tokens (B x S) x ffn_padded x 2 bytes <= 32 MiB - 256 (e.g. S = 4096 with hidden 1024
  * and ffn 2816); larger shapes return TSP_ERR_UNSUPPORTED with a message.
  * The call allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
  * The first call on a device looks the array's device address up
@@ -437,6 +464,31 @@ typedef struct tsp_cost {
 
 tsp_status tsp_cost_model(int scheme, int D, int tp, int64_t S, int hidden, int heads, int ffn,
                           tsp_cost* out);
+
+/*
+ * tsp_cost_model_batched - the same model for a micro-batch of `batch` sequences of
+ * S tokens ([TSP] s4, scalability: TSP's smaller per-device footprint lets a device
+ * take larger micro-batches). Every sequence is split like the single one, so
+ * act_elems, act_inflight_elems, comm_act_elems and flops are `batch` times those
+ * of tsp_cost_model; the weight terms (and TSP's weight traffic, which one pass of
+ * the shards serves for the whole micro-batch) do not change. batch >= 1, else
+ * TSP_ERR_INVALID_ARG. tsp_cost_model is batch 1.
+ */
+tsp_status tsp_cost_model_batched(int scheme, int D, int tp, int64_t S, int batch, int hidden,
+                                  int heads, int ffn, tsp_cost* out);
+
+/*
+ * tsp_cost_max_batch - the largest micro-batch B whose bf16 footprint on one device
+ * fits in mem_bytes under `scheme` for a model of `layers` such layers:
+ *   bytes(B) = 2 * (layers * (weight_elems + B * act_elems)
+ *                   + weight_inflight_elems + B * act_inflight_elems)
+ * (every layer keeps its weights and activations, as training does; one layer's
+ * received shard and gathered K/V exist at a time), with the batch-1 terms of
+ * tsp_cost_model. *out = 0 if one sequence does not fit. layers >= 1 and a finite
+ * mem_bytes >= 0, else TSP_ERR_INVALID_ARG; shape errors as tsp_cost_model.
+ */
+tsp_status tsp_cost_max_batch(int scheme, int D, int tp, int64_t S, int hidden, int heads,
+                              int ffn, int layers, double mem_bytes, int64_t* out);
 
 /*
  * tsp_device_status - synchronise `stream`, then read and clear the workspace

@@ -18,7 +18,10 @@ Sharding rules (the same readings as the rest of this repository):
   * activations per token: x and h (boundary), q, k, v, o (head columns) and
     a1, a3, g (ffn columns);
   * TP keeps x and h on every device of its group; TP+SP uses a tp x (D/tp) grid,
-    device d = sigma * tp + g with weight shard g and token group sigma.
+    device d = sigma * tp + g with weight shard g and token group sigma;
+  * a micro-batch of B sequences ([TSP] s4, scalability): every sequence is split
+    the same way, so a device holds its tokens of each sequence; the weights (and
+    the weight traffic of TSP) serve the whole micro-batch once.
 """
 from __future__ import annotations
 
@@ -93,9 +96,10 @@ def _visible_pairs(tokens):
     return int(sum(int(t) + 1 for t in tokens))
 
 
-def simulate(scheme, D, S, H, heads, F, tp=0):
-    """Per-device counts of one layer forward; every device of a balanced layout
-    gets the same numbers, which are returned (a ValueError if they differ)."""
+def simulate(scheme, D, S, H, heads, F, tp=0, batch=1):
+    """Per-device counts of one layer forward of a micro-batch of `batch` sequences;
+    every device of a balanced layout gets the same numbers, which are returned (a
+    ValueError if they differ)."""
     d_head = H // heads
     P_all = 4 * H * H + 3 * H * F
     per = []
@@ -118,31 +122,34 @@ def simulate(scheme, D, S, H, heads, F, tp=0):
         g, G = dv["wg"]
         r, R = dv["tg"]
         ig, IG = dv["inner"]
-        toks = _tokens(S, r, R)
+        toks = _tokens(S, r, R)          # this device's positions in each sequence
+        ntok = batch * len(toks)         # ... over every sequence of the micro-batch
         # resident weights: the device's own shard
         weights = _shard_elems(ATT + MLP, H, F, heads, g, G)
         # activations: boundary tensors x, h on all columns of the device's tokens;
         # inner tensors on the device's token rows and its head / ffn columns
         head_cols = int(_weight_shard("Wo", H, F, heads, ig, IG)[0].sum())
         ffn_cols = int(_weight_shard("W2", H, F, heads, ig, IG)[0].sum())
-        acts = len(toks) * (2 * H) + len(toks) * (4 * head_cols + 3 * ffn_cols)
+        acts = ntok * (2 * H) + ntok * (4 * head_cols + 3 * ffn_cols)
         c = dict(devices=n_dev, weight_elems=weights, weight_inflight_elems=0, act_elems=acts,
                  act_inflight_elems=0, comm_weight_elems=0, comm_act_elems=0, flops=0)
+        # every activation collective runs once per sequence of the micro-batch
         if scheme == "tp":
-            ar = _ring_allreduce(S * H, D)[d]
+            ar = sum(int(_ring_allreduce(S * H, D)[d]) for _ in range(batch))
             c["comm_act_elems"] = 2 * ar
         elif scheme == "sp":
             blocks = [len(_tokens(S, q, D)) * 2 * H for q in range(D)]
-            c["comm_act_elems"] = int(_ring_allgather(blocks)[d])
-            c["act_inflight_elems"] = sum(blocks)
+            c["comm_act_elems"] = sum(int(_ring_allgather(blocks)[d]) for _ in range(batch))
+            c["act_inflight_elems"] = batch * sum(blocks)
         elif scheme == "tp_sp":
             sg = D // tp
             grp_tokens = len(toks)
-            c["comm_act_elems"] = 2 * int(_ring_allreduce(grp_tokens * H, tp)[g])
             kv_cols = 2 * (H // tp)
             blocks = [len(_tokens(S, q, sg)) * kv_cols for q in range(sg)]
-            c["comm_act_elems"] += int(_ring_allgather(blocks)[r])
-            c["act_inflight_elems"] = sum(blocks)
+            for _ in range(batch):
+                c["comm_act_elems"] += 2 * int(_ring_allreduce(grp_tokens * H, tp)[g])
+                c["comm_act_elems"] += int(_ring_allgather(blocks)[r])
+            c["act_inflight_elems"] = batch * sum(blocks)
         elif scheme == "tsp":
             # attention: broadcast iteration k sends shard k to every other device;
             # each iteration all-gathers head group k's K/V of every device's tokens
@@ -150,10 +157,10 @@ def simulate(scheme, D, S, H, heads, F, tp=0):
             att_in, kv_in, kv_buf = 0, 0, 0
             for k in range(D):
                 if k != d:
-                    att_in += _shard_elems(ATT, H, F, heads, k, D)
+                    att_in += _shard_elems(ATT, H, F, heads, k, D)   # once per micro-batch
                 blocks = [len(_tokens(S, q, D)) * kv_cols for q in range(D)]
-                kv_in += int(_ring_allgather(blocks)[d])
-                kv_buf = max(kv_buf, sum(blocks))
+                kv_in += sum(int(_ring_allgather(blocks)[d]) for _ in range(batch))
+                kv_buf = max(kv_buf, batch * sum(blocks))
             # MLP ring: at step t = 1..D-1 device d receives shard (d + t) mod D
             ring_in = sum(_shard_elems(MLP, H, F, heads, (d + t) % D, D) for t in range(1, D))
             c["comm_weight_elems"] = att_in + ring_in
@@ -171,7 +178,7 @@ def simulate(scheme, D, S, H, heads, F, tp=0):
         else:
             applied = weights
             pair_width = head_cols
-        c["flops"] = 2 * len(toks) * applied + 4 * pair_width * _visible_pairs(toks)
+        c["flops"] = 2 * ntok * applied + 4 * pair_width * batch * _visible_pairs(toks)
         assert pair_width % d_head == 0
         per.append(c)
     first = per[0]
@@ -179,3 +186,21 @@ def simulate(scheme, D, S, H, heads, F, tp=0):
         if c != first:
             raise ValueError(f"{scheme}: devices differ: {first} vs {c}")
     return first
+
+
+def memory_elems(c, layers=1):
+    """Elements one device holds for `layers` layers of counts c: every layer's
+    resident weights and activations, and one layer's in-flight buffers at a time."""
+    return (layers * (c["weight_elems"] + c["act_elems"])
+            + c["weight_inflight_elems"] + c["act_inflight_elems"])
+
+
+def max_micro_batch(scheme, D, S, H, heads, F, mem_bytes, layers=1, tp=0, limit=4096):
+    """Largest micro-batch whose bf16 footprint (memory_elems x 2 bytes) fits in
+    mem_bytes, found by simulating B = 1, 2, ... (0 if even one sequence does not fit)."""
+    best = 0
+    for b in range(1, limit + 1):
+        if 2 * memory_elems(simulate(scheme, D, S, H, heads, F, tp=tp, batch=b), layers) > mem_bytes:
+            break
+        best = b
+    return best

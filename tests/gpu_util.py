@@ -151,11 +151,12 @@ def rand_bits(shape, seed, std=1.0):
 class Layer:
     """Seeded inputs of one layer shape on the device plus their float64 copies."""
 
-    def __init__(self, D, S, H, heads, F, seed=7, names=None):
+    def __init__(self, D, S, H, heads, F, seed=7, names=None, batch=1):
         import folded_tensor_sequence_tsp_gb300 as tsp
         self.cfg = tsp_inputs.LayerConfig("t", D, S, H, heads, F, seed)
-        self.bits = tsp_inputs.layer_inputs(self.cfg, names=names)
-        self.plan = tsp.tsp_plan(D, S, H, heads, F)
+        self.bits = tsp_inputs.layer_inputs(self.cfg, names=names, batch=batch)
+        self.plan = (tsp.tsp_plan(D, S, H, heads, F) if batch == 1
+                     else tsp.tsp_plan_batched(D, S, batch, H, heads, F))
         self.info = self.plan.info
         self.ws = torch.empty(tsp.tsp_workspace_bytes(self.plan), dtype=torch.uint8, device="cuda")
         tsp.tsp_workspace_init(self.plan, self.ws)
@@ -184,7 +185,8 @@ class Layer:
         return xs
 
     def act(self):
-        return torch.empty((self.info.S, self.info.hidden), dtype=torch.bfloat16, device="cuda")
+        return torch.empty((self.info.tokens, self.info.hidden), dtype=torch.bfloat16,
+                           device="cuda")
 
     def bwd_workspace(self):
         import folded_tensor_sequence_tsp_gb300 as tsp

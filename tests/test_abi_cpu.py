@@ -125,3 +125,37 @@ def test_binding_checks_tensor_sizes_without_calling_the_library(lib):
     small = torch.empty(10, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         tsp.tsp_layer_fwd(p, small, small, small, small)
+
+
+def test_batched_plan_sizes_and_limits(lib):
+    """A micro-batch plan: B*S rows everywhere, same weights, backward refused."""
+    one = tsp.tsp_plan(4, 4096, 1024, 16, 2816)
+    for batch in (1, 2, 3, 8):
+        p = tsp.tsp_plan_batched(4, 4096, batch, 1024, 16, 2816)
+        i = p.info
+        assert i.batch == batch and i.tokens == batch * 4096 and i.S == 4096
+        assert i.T == 1024 and i.C == 512
+        assert i.wpack_elems == one.info.wpack_elems          # weights do not grow
+        assert i.stat_stride == batch * 4096
+        # every activation buffer grows with the micro-batch: the workspace is
+        # (up to alignment) B times the single-sequence one
+        assert abs(i.workspace_bytes - batch * (one.info.workspace_bytes - 256) - 256) <= 256 * 12
+        assert p.act_elems == batch * 4096 * 1024
+    assert tsp.tsp_plan_batched(2, 256, 1, 256, 4, 688).info.tokens == 256
+    h = ctypes.c_void_p()
+    # T = S/D must be a multiple of 128 for B > 1; batch >= 1; B*S <= 2^26
+    assert lib.tsp_plan_batched(2, 200, 2, 256, 4, 688, ctypes.byref(h)) == B.TSP_ERR_UNSUPPORTED
+    assert "128" in B.tsp_last_error()
+    assert lib.tsp_plan_batched(2, 200, 1, 256, 4, 688, ctypes.byref(h)) == B.TSP_OK
+    lib.tsp_plan_destroy(h)
+    assert lib.tsp_plan_batched(2, 256, 0, 256, 4, 688, ctypes.byref(h)) == B.TSP_ERR_UNSUPPORTED
+    assert lib.tsp_plan_batched(8, 1 << 23, 16, 4096, 32, 11008,
+                                ctypes.byref(h)) == B.TSP_ERR_UNSUPPORTED
+    # backward calls take one sequence per plan; refused before any launch
+    p = tsp.tsp_plan_batched(2, 256, 2, 256, 4, 688)
+    ws = ctypes.c_void_p(1 << 20)
+    a = [ctypes.c_void_p(4096 * k) for k in range(1, 6)]
+    assert lib.tsp_layer_bwd(p.handle, *a, ws, None) == B.TSP_ERR_UNSUPPORTED
+    assert "one sequence" in B.tsp_last_error()
+    assert lib.tsp_mlp_bwd(p.handle, *a, ws, None) == B.TSP_ERR_UNSUPPORTED
+    assert lib.tsp_layer_fwd_train(p.handle, *a[:4], ws, None) == B.TSP_ERR_UNSUPPORTED

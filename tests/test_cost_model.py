@@ -210,3 +210,59 @@ def test_hand_worked_example(scheme, want):
     for k in FIELDS:
         assert sim[k] == want[k], ("simulator", k, sim[k], want[k])
         assert got[k] == want[k], ("model", k, got[k], want[k])
+
+
+# ------------------------------------------------------- micro-batches ([TSP] s4)
+
+BATCH_CASES = [c for c in CASES if c[3] is SHAPES[1] or (c[1] == 8)]
+
+
+@pytest.mark.parametrize("batch", [2, 3])
+@pytest.mark.parametrize("scheme,D,tp,shp", BATCH_CASES,
+                         ids=[f"{c[0]}-D{c[1]}-tp{c[2]}-S{c[3]['S']}" for c in BATCH_CASES])
+def test_batched_model_equals_brute_force_count(scheme, D, tp, shp, batch):
+    got = B.tsp_cost_model_batched(scheme, D, shp["S"], batch, shp["H"], shp["heads"], shp["F"], tp=tp)
+    want = cost_sim.simulate(scheme, D, shp["S"], shp["H"], shp["heads"], shp["F"], tp=tp, batch=batch)
+    for k in FIELDS:
+        assert got[k] == pytest.approx(want[k], rel=1e-12, abs=1e-9), (k, got[k], want[k])
+    one = B.tsp_cost_model(scheme, D, shp["S"], shp["H"], shp["heads"], shp["F"], tp=tp)
+    assert got["weight_elems"] == one["weight_elems"]          # weights serve the batch once
+    assert got["comm_weight_elems"] == one["comm_weight_elems"]
+
+
+@pytest.mark.parametrize("scheme,D,tp", [("dp", 1, 0), ("tp", 4, 0), ("sp", 4, 0),
+                                         ("tp_sp", 4, 2), ("tsp", 4, 0)])
+def test_max_micro_batch_equals_brute_force_search(scheme, D, tp):
+    shp = SHAPES[1]
+    for layers in (1, 3):
+        for budget in (1e3, 2e4, 6.5e4, 1.3e5, 4e5):
+            got = B.tsp_cost_max_batch(scheme, D, shp["S"], shp["H"], shp["heads"], shp["F"],
+                                       layers, budget, tp=tp)
+            want = cost_sim.max_micro_batch(scheme, D, shp["S"], shp["H"], shp["heads"], shp["F"],
+                                            budget, layers=layers, tp=tp)
+            assert got == want, (layers, budget, got, want)
+
+
+def test_max_micro_batch_boundaries():
+    shp = SHAPES[0]
+    c = cost_sim.simulate("tsp", 4, shp["S"], shp["H"], shp["heads"], shp["F"], batch=5)
+    exact = 2 * cost_sim.memory_elems(c, layers=2)       # exactly five sequences fit
+    args = ("tsp", 4, shp["S"], shp["H"], shp["heads"], shp["F"], 2)
+    assert B.tsp_cost_max_batch(*args, exact) == 5
+    assert B.tsp_cost_max_batch(*args, exact - 1) == 4
+    assert B.tsp_cost_max_batch(*args, 0.0) == 0
+    with pytest.raises(B.TSPError):
+        B.tsp_cost_max_batch(*args[:-1], 0, 1e9)             # layers < 1
+    with pytest.raises(B.TSPError):
+        B.tsp_cost_model_batched("tsp", 4, shp["S"], 0, shp["H"], shp["heads"], shp["F"])
+
+
+def test_tsp_admits_the_largest_micro_batch():
+    """[TSP] s4: the smaller per-device footprint lets TSP take larger micro-batches.
+    A 32-layer 7B-shaped model on D = 8 devices of 288 GB: TSP's largest micro-batch
+    is at least that of TP, SP and TP+SP at 16K and 64K tokens, and above TP's."""
+    for S in (16384, 65536):
+        m = {s: B.tsp_cost_max_batch(s, 8, S, 4096, 32, 11008, 32, 288e9, tp=tp)
+             for s, tp in (("tp", 0), ("sp", 0), ("tp_sp", 2), ("tsp", 0))}
+        assert m["tsp"] >= max(m.values()) and m["tsp"] > m["tp"], (S, m)
+        assert m["tsp"] >= 1

@@ -1,0 +1,150 @@
+"""Micro-batches of several sequences on the CUDA path against the float64 oracle.
+
+The page credits TSP's smaller per-device footprint with room for larger
+micro-batches ("Folding Tensor and Sequence Parallelism for Memory-Efficient
+Transformer Training & Inference", section 4, scalability). A micro-batch plan
+holds B independent sequences; every rank owns its zigzag chunks of each of them
+(rank-major [D, B, S/D, H]). Checked here: the index map and the shard/unshard
+copies bit for bit, the blocks and the layer against the oracle on every
+sequence, the batched call bit-identical to one call per sequence, and the
+7B-shaped layer at 4 x 16K tokens on sampled rows of every sequence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tsp_inputs
+from gpu_util import Layer, assert_close, bits, dev, f64, layer_row_scale, layer_tolerance
+
+tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "tiny-b3": ((2, 256, 256, 4, 688), 3),
+    "d3-b2": ((3, 1152, 384, 6, 600), 2),
+    "hd128-b2": ((2, 512, 512, 4, 1024), 2),
+    "small-b2": ((4, 4096, 1024, 16, 2816), 2),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tsp.load_library()
+
+
+def _unshard(L, t):
+    """Sharded [D*B*T, H] -> natural [B, S, H]."""
+    out = torch.empty_like(t)
+    tsp.tsp_unshard(L.plan, t, out)
+    return out.view(L.info.batch, L.info.S, L.info.hidden)
+
+
+def test_index_and_shard_bit_exact():
+    for D, S, B in ((2, 256, 3), (3, 1152, 2), (8, 16384, 4), (1, 256, 5)):
+        plan = tsp.tsp_plan_batched(D, S, B, 64 * D, D, D)
+        fwd = torch.empty(B * S, dtype=torch.int32, device="cuda")
+        inv = torch.empty(B * S, dtype=torch.int32, device="cuda")
+        tsp.tsp_shard_index(plan, fwd, inv)
+        want = oracle.zigzag_forward_index_batched(S, D, B)
+        assert np.array_equal(fwd.cpu().numpy(), want), (D, S, B)
+        winv = np.empty_like(want)
+        winv[want] = np.arange(B * S)
+        assert np.array_equal(inv.cpu().numpy(), winv), (D, S, B)
+        H = 64 * D
+        xb = tsp_inputs.normal_bf16_bits((B, S, H), 1.0, 77, 3)
+        x = dev(xb)
+        xs = torch.empty_like(x)
+        tsp.tsp_shard(plan, x, xs)
+        want_s = oracle.shard_tokens_batched(xb, D)
+        assert np.array_equal(bits(xs).reshape(want_s.shape), want_s), (D, S, B)
+        back = torch.empty_like(x)
+        tsp.tsp_unshard(plan, xs, back)
+        assert np.array_equal(bits(back), xb)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_batched_layer_matches_oracle(name):
+    shape, batch = SHAPES[name]
+    L = Layer(*shape, seed=21, batch=batch)
+    xs = L.sharded_x()
+    attn, mlp, out = L.act(), L.act(), L.act()
+    tsp.tsp_attention_fwd(L.plan, xs, L.wpack, attn, L.ws)
+    tsp.tsp_mlp_fwd(L.plan, xs, L.wpack, mlp, L.ws)
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    L.check_status()
+    W = L.weights64()
+    x = L.f("x")
+    ref = oracle.layer_forward_batched(x, W, L.info.heads)
+    got_attn, got_mlp, got_out = (f64(_unshard(L, t)) for t in (attn, mlp, out))
+    for b in range(batch):
+        assert_close(got_attn[b], ref["attn"][b], f"{name} seq {b} attn")
+        want = oracle.swiglu_mlp(x[b], W["W1"], W["W3"], W["W2"])
+        G = oracle.swiglu_gate(x[b], W["W1"], W["W3"])
+        assert_close(got_mlp[b], want, f"{name} seq {b} mlp", scale=layer_row_scale(want, G))
+        s, atol = layer_tolerance(ref["out"][b], oracle.swiglu_gate(ref["h"][b], W["W1"], W["W3"]),
+                                  ref["h"][b], W)
+        assert_close(got_out[b], ref["out"][b], f"{name} seq {b} out", scale=s, max_abs=atol)
+
+
+@pytest.mark.parametrize("name", ["tiny-b3", "small-b2"])
+def test_batched_call_equals_one_call_per_sequence(name):
+    """Each output row depends only on its own sequence and takes the same K order
+    and key tiles either way, so the micro-batch gives the single-sequence bits."""
+    shape, batch = SHAPES[name]
+    L = Layer(*shape, seed=22, batch=batch)
+    out = L.act()
+    tsp.tsp_layer_fwd(L.plan, L.sharded_x(), L.wpack, out, L.ws)
+    L.check_status()
+    got = bits(_unshard(L, out))
+    one = tsp.tsp_plan(*shape)
+    ws = torch.empty(tsp.tsp_workspace_bytes(one), dtype=torch.uint8, device="cuda")
+    tsp.tsp_workspace_init(one, ws)
+    for b in range(batch):
+        x = L.d["x"][b].contiguous()
+        xs, o, nat = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+        tsp.tsp_shard(one, x, xs)
+        tsp.tsp_layer_fwd(one, xs, L.wpack, o, ws)
+        tsp.tsp_unshard(one, o, nat)
+        assert tsp.tsp_device_status(ws) == tsp.TSP_OK
+        assert np.array_equal(bits(nat), got[b]), f"sequence {b}"
+
+
+def test_batched_host_entry_point_matches_device_path():
+    shape, batch = SHAPES["d3-b2"]
+    L = Layer(*shape, seed=23, batch=batch)
+    out = L.act()
+    tsp.tsp_layer_fwd(L.plan, L.sharded_x(), L.wpack, out, L.ws)
+    want = bits(_unshard(L, out))
+    x_host = torch.from_numpy(L.bits["x"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    out_host = torch.full_like(x_host, float("nan")).pin_memory()
+    tsp.tsp_layer_fwd_host(L.plan, x_host, L.wpack, out_host, L.ws)
+    torch.cuda.current_stream().synchronize()
+    L.check_status()
+    assert np.array_equal(out_host.view(torch.int16).numpy().view(np.uint16), want)
+
+
+@pytest.mark.slow
+def test_7b_16k_micro_batch_of_4_sampled_rows():
+    """The 7B-shaped layer on 4 sequences of 16K tokens (65,536 rows, the launch
+    configuration the benchmark's micro-batch workload times), 64 sampled rows of
+    every sequence against the oracle."""
+    cfg = tsp_inputs.config_by_name("7b-16k")
+    batch = 4
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed, batch=batch)
+    xs = L.sharded_x()
+    out = L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    L.check_status()
+    nat = _unshard(L, out)
+    W = L.weights64()
+    x = L.f("x")
+    for b in range(batch):
+        rows = tsp_inputs.sample_rows(cfg.S, 64, cfg.seed + b)
+        got = f64(nat[b][torch.from_numpy(rows).cuda()])
+        ref = oracle.layer_forward(x[b], W, cfg.heads, rows=rows)
+        s, atol = layer_tolerance(ref["out"], oracle.swiglu_gate(ref["h"], W["W1"], W["W3"]),
+                                  ref["h"], W)
+        assert_close(got, ref["out"], f"7b-16k seq {b} out rows", scale=s, max_abs=atol)
