@@ -39,11 +39,16 @@
 //
 // Query row r of the rank-major layout is the token at global position pos(r) of
 // the zigzag map; key t is visible iff t <= pos(r). A micro-batch of B sequences
-// (rank-major [D][B][T] query rows, natural K/V rows b*S + t) adds a grid dimension:
-// blockIdx.y is the sequence, whose queries see only its own keys. CTAs of one head run before
-// the next head (K/V of a head stay in L2 across its CTAs) and, when the zigzag
-// chunk is a multiple of 256 tokens, take query blocks in decreasing position, so
-// the longest blocks start first.
+// has rank-major [D][B][T] query rows and natural K/V rows b*S + t; the queries of
+// sequence b see only its own keys.
+//
+// CTA order. The (sequence, head) pairs of the call are cut into groups whose K/V
+// fit together in a share of L2 (one 64K-token head alone; every head of a 16K
+// sequence together). Groups run one after the other, so their K/V stay in L2
+// across their CTAs. Inside a group the CTAs go query block by query block, every
+// pair of the group at each block, and, when the zigzag chunk is a multiple of 256
+// tokens, in decreasing position: the longest blocks of every pair start first
+// (longest-first over the whole group, not only within one head).
 #include "tsp_device.cuh"
 #include "tsp_internal.h"
 
@@ -82,9 +87,10 @@ struct AttParams {
   long long ld_lse;
   long long S, T, C;  // one sequence
   int D;
-  int B;               // sequences of the micro-batch (blockIdx.y)
+  int B;               // sequences of the micro-batch
   int heads;
-  int q_blocks;
+  int q_blocks;        // 256-row query blocks per (sequence, head)
+  int group;           // (sequence, head) pairs whose CTAs interleave
   int natural_order;
   float scale_log2;
   DevStatus* status;
@@ -181,8 +187,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = blockIdx.x / p.q_blocks;
-  const int blk = blockIdx.x - head * p.q_blocks;
+  // CTA -> group g, query block blk, pair (sequence, head) of the group
+  const int pairs = p.heads * p.B;
+  const int per_group = p.q_blocks * p.group;
+  const int g = (int)(blockIdx.x / (unsigned)per_group);
+  const int in_g = min(p.group, pairs - g * p.group);
+  const int rem = (int)blockIdx.x - g * per_group;
+  const int blk = rem / in_g;
+  const int pair = g * p.group + (rem - blk * in_g);
+  const int head = pair % p.heads;
+  const int seq = pair / p.heads;
   const long long row0 = p.natural_order
                              ? zig_row((long long)(p.q_blocks - 1 - blk) * QB, p.C, p.T, p.D)
                              : (long long)blk * QB;
@@ -190,7 +204,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_b = tiles_needed(row0 + QT, p);
   const int n_tiles = max(n_a, n_b);
   const int col_q = head * HD;  // Q columns inside qkv; K/V columns inside kn/vn
-  const int seq = blockIdx.y;
   const int kv_row0 = (int)(seq * p.S);  // first natural K/V row of the sequence
 
   if (threadIdx.x == 0) {
@@ -481,8 +494,8 @@ tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t st
   const size_t smem = Geometry<HD>::SMEM;
   TSP_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)smem,
                             "attention: cudaFuncSetAttribute"));
-  const long long blocks = (long long)p.q_blocks * p.heads;
-  kernel<<<dim3((unsigned)blocks, (unsigned)p.B), THREADS, smem, stream>>>(tq, tk, tv, p);
+  const long long blocks = (long long)p.q_blocks * p.heads * p.B;
+  kernel<<<(unsigned)blocks, THREADS, smem, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TSP_OK : cuda_fail(e, "attention: launch");
 }
@@ -499,7 +512,7 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
       c.o_col0 + (long long)c.heads * c.d > c.ld_o)
     return fail(TSP_ERR_INVALID_ARG, "attention: head columns exceed the row width");
   const int B = c.B > 0 ? c.B : 1;
-  if (c.S * B > (1ll << 30) || B > 65535)
+  if (c.S * B > (1ll << 30) || (long long)((c.S + QB - 1) / QB) * c.heads * B > (1ll << 31) - 1)
     return fail(TSP_ERR_UNSUPPORTED, "attention: too many rows");
   // with several sequences a 128-row query tile must not straddle two ranks' blocks
   if (B > 1 && c.T % QT)
@@ -517,6 +530,13 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.B = B;
   p.heads = c.heads;
   p.q_blocks = (int)((c.S + QB - 1) / QB);
+  {
+    // pairs per group: their K and V (2 * S * d bf16 each) within 48 MB of the L2
+    const long long kv_bytes = 4LL * c.S * c.d;
+    const long long fit = (48LL << 20) / kv_bytes;
+    const long long pairs = (long long)c.heads * B;
+    p.group = (int)(fit < 1 ? 1 : (fit > pairs ? pairs : fit));
+  }
   p.natural_order = (c.C % QB == 0) ? 1 : 0;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);
   p.status = c.status;
