@@ -25,8 +25,7 @@ Reported:
   cost_model  the library's per-device memory / traffic model of the same layer
               under DP, TP, SP, TP+SP and TSP on D devices (context)
   --impl reference  times that oracle alone (the slow reference arm).
-  --batch B   a micro-batch of B sequences of the workload's length (forward,
-              e2e and kernels; the backward takes one sequence per plan)
+  --batch B   a micro-batch of B sequences of the workload's length
 Multi-GPU (torchrun): independent replicas, one per GPU; no collective on the
 data path.
 """
@@ -384,11 +383,11 @@ def run_ours(args, world, rank, local):
 
     # ---- backward: K whole-layer backward steps, then the attention backward step
     backward = None
-    if not args.no_backward and Bm == 1:  # the backward takes one sequence per plan
+    if not args.no_backward:
         layer.enable_backward()
         ws = layer.ws
         dout = torch.empty_like(xs)
-        tsp.tsp_shard(plan, to_dev(tsp_inputs.normal_bf16_bits((S, H), 1.0, cfg.seed, 77)), dout)
+        tsp.tsp_shard(plan, to_dev(tsp_inputs.normal_bf16_bits((N, H), 1.0, cfg.seed, 77)), dout)
         dxs = torch.empty_like(xs)
         dwpack = torch.empty(i.wpack_elems, dtype=torch.float32, device="cuda")
         for _ in range(args.warmup):
@@ -408,7 +407,7 @@ def run_ours(args, world, rank, local):
         hpr = cfg.heads // D
         lse = torch.empty(hpr * i.stat_stride, dtype=torch.float32, device="cuda")
         delta = torch.empty_like(lse)
-        dqkv = torch.empty((S, 3 * H), dtype=torch.bfloat16, device="cuda")
+        dqkv = torch.empty((N, 3 * H), dtype=torch.bfloat16, device="cuda")
         tsp.tsp_qkv_projection_gathered(plan, D - 1, xs, wp, q, kn, vn, ws)
         tsp.tsp_causal_attention_lse(plan, D - 1, q, kn, vn, o, lse, ws)
         for _ in range(max(1, args.warmup)):
@@ -443,18 +442,18 @@ def run_ours(args, world, rank, local):
         ftr_ms = max_over_ranks(t[0].elapsed_time(t[1]) / args.steps)
         bsv_ms = max_over_ranks(t[1].elapsed_time(t[2]) / args.steps)
         del saved
-        att_flops = 5.0 * i.shard_hidden * S * (S + 1)  # five products per visible pair
+        att_flops = 5.0 * i.shard_hidden * S * (S + 1) * Bm  # five products per visible pair
         att_tf = att_flops / (att_ms * 1e-3) / 1e12
-        bwd_tf = algorithmic_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12
+        bwd_tf = Bm * algorithmic_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12
         backward = {
             "step": "tsp_layer_bwd (recomputes the forward activations it uses)",
             "ms_per_step": round(bwd_ms, 3),
-            "tokens_per_s": round(job_tokens_per_s(world, S, bwd_ms), 1),
+            "tokens_per_s": round(job_tokens_per_s(world, N, bwd_ms), 1),
             "tflops_algorithmic": round(world * bwd_tf, 1),
             "frac_of_peak_sustained": round(bwd_tf / peaks["bf16_tflops_sustained"], 4),
-            "flops_algorithmic_per_step": algorithmic_bwd_flops(S, H, F),
-            "flops_executed_per_step": executed_bwd_flops(S, H, F),
-            "tflops_executed": round(world * executed_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12, 1),
+            "flops_algorithmic_per_step": Bm * algorithmic_bwd_flops(S, H, F),
+            "flops_executed_per_step": Bm * executed_bwd_flops(S, H, F),
+            "tflops_executed": round(world * Bm * executed_bwd_flops(S, H, F) / (bwd_ms * 1e-3) / 1e12, 1),
             "attention_bwd_step": {
                 "calls_per_step": D, "avg_ms": round(att_ms, 4),
                 "tflops_algorithmic": round(att_tf, 1),
@@ -466,8 +465,8 @@ def run_ours(args, world, rank, local):
                         f"{tsp.tsp_saved_bytes(plan) / 2**20:.0f} MiB)",
                 "fwd_train_ms": round(ftr_ms, 3), "bwd_saved_ms": round(bsv_ms, 3),
                 "step_ms": round(ftr_ms + bsv_ms, 3),
-                "tokens_per_s": round(job_tokens_per_s(world, S, ftr_ms + bsv_ms), 1),
-                "tflops_algorithmic": round(world * (algorithmic_flops(S, H, F) + algorithmic_bwd_flops(S, H, F))
+                "tokens_per_s": round(job_tokens_per_s(world, N, ftr_ms + bsv_ms), 1),
+                "tflops_algorithmic": round(world * Bm * (algorithmic_flops(S, H, F) + algorithmic_bwd_flops(S, H, F))
                                             / ((ftr_ms + bsv_ms) * 1e-3) / 1e12, 1)},
         }
         del dout, dxs, dwpack, o, lse, delta, dqkv
@@ -579,8 +578,8 @@ def main():
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward measurement (tsp_layer_bwd)")
     ap.add_argument("--batch", type=int, default=1,
-                    help="sequences of the micro-batch (forward only; e.g. --workload 7b-16k "
-                         "--batch 4 is 4 x 16K tokens)")
+                    help="sequences of the micro-batch (e.g. --workload 7b-16k --batch 4 is "
+                         "4 x 16K tokens)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--ref-sample-tokens", type=int, default=1024)
     args = ap.parse_args()

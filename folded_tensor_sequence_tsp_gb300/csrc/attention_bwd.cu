@@ -47,6 +47,11 @@
 // dP [384, 512) with bf16 dS over [384 + 64g, +32) for warpgroup g.
 // MMAs issued by one thread execute in order, so a product may write columns that
 // an earlier-issued product reads.
+// A micro-batch of B sequences (rank-major [D][B][T] sharded rows, natural K/V rows
+// b*S + t) pairs every CTA with one (sequence, head); the CTA order is the forward
+// kernel's: (sequence, head) pairs in groups whose K/V fit in 48 MB of L2, and
+// inside a group the owned tiles go tile index by tile index across the pairs, the
+// longest first.
 #include <type_traits>
 
 #include "tsp_device.cuh"
@@ -82,9 +87,12 @@ struct BwdParams {
   const __nv_bfloat16* q;     // query-side kernel: owned Q and dO rows, read once
   const __nv_bfloat16* dout;
   long long ld_q, ld_do;
-  long long S, T, C;
+  long long S, T, C;  // one sequence
   int D;
-  int n_outer;   // owned tiles per head
+  int B;         // sequences of the micro-batch
+  int heads;     // heads of the call
+  int group;     // (sequence, head) pairs whose CTAs interleave
+  int n_outer;   // owned tiles per (sequence, head)
   int natural;   // zigzag chunk is a multiple of 128: every 128-row tile is one
                  // contiguous run of positions
   float scale_log2;
@@ -101,6 +109,27 @@ __device__ __forceinline__ long long zig_row(long long t, long long C, long long
 __device__ __forceinline__ long long row_pos(long long r, long long C, long long T, int D) {
   const long long rank = r / T, l = r - rank * T;
   return l < C ? rank * C + l : (2 * D - 1 - rank) * C + (l - C);
+}
+
+// Row of the micro-batch's [D][B][T] layout that holds row v of sequence `seq`'s
+// own [D][T] layout (the identity when B == 1).
+__device__ __forceinline__ long long batch_row(long long v, int seq, const BwdParams& p) {
+  return v + ((v / p.T) * (p.B - 1) + seq) * p.T;
+}
+
+// CTA -> (owned tile index, sequence, head) in the grouped order described above.
+struct CtaPos {
+  int tile, seq, head;
+};
+__device__ __forceinline__ CtaPos cta_pos(const BwdParams& p) {
+  const int pairs = p.heads * p.B;
+  const int per_group = p.n_outer * p.group;
+  const int grp = (int)(blockIdx.x / (unsigned)per_group);
+  const int in_g = min(p.group, pairs - grp * p.group);
+  const int rem = (int)blockIdx.x - grp * per_group;
+  const int tile = rem / in_g;
+  const int pair = grp * p.group + (rem - tile * in_g);
+  return CtaPos{tile, pair / p.heads, pair % p.heads};
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -179,9 +208,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto sDel = [&](int st) { return sLse(st) + 128; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = blockIdx.x / p.n_outer;
-  const int kt = blockIdx.x - head * p.n_outer;  // ascending: most work first
+  const CtaPos cp = cta_pos(p);
+  const int head = cp.head, seq = cp.seq;
+  const int kt = cp.tile;  // ascending: most work first
   const long long k0 = (long long)kt * BT;
+  const int kv_row0 = (int)(seq * p.S);  // first natural K/V row of the sequence
   const int nq = (int)((p.S + IT - 1) / IT);
   // streamed query tiles: natural order from the diagonal tile on, else every tile
   const int n_inner = p.natural ? nq - kt : nq;
@@ -226,15 +257,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive_expect_tx(kv_full, 2 * G::TILE);
 #pragma unroll
       for (int b = 0; b < G::BOXES; ++b) {
-        tma_load_2d(sK + b * BOX_BYTES, &tmK, kv_full, head * HD + 64 * b, (int)k0);
-        tma_load_2d(sV + b * BOX_BYTES, &tmV, kv_full, head * HD + 64 * b, (int)k0);
+        tma_load_2d(sK + b * BOX_BYTES, &tmK, kv_full, head * HD + 64 * b, kv_row0 + (int)k0);
+        tma_load_2d(sV + b * BOX_BYTES, &tmV, kv_full, head * HD + 64 * b, kv_row0 + (int)k0);
       }
       int last[STAGES] = {-1, -1};
       for (int idx = 0; idx < n_inner; ++idx) {
         const int st = idx % STAGES;
         const uint32_t ph = (uint32_t)((idx / STAGES) & 1);
         if (!mbar_wait(&in_empty[st], ph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
-        const long long r0 = row0_of(idx);
+        // the tile's rows in the micro-batch layout (contiguous: a 128-row tile never
+        // spans two ranks' blocks when B > 1)
+        const long long r0 = batch_row(row0_of(idx), seq, p);
         mbar_arrive_expect_tx(&in_full[st], 2 * G::TILE + 1024);
 #pragma unroll
         for (int b = 0; b < G::BOXES; ++b) {
@@ -418,7 +451,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && warp_wait(acc_done, 0u)) {
       tc_fence_after();
       const bool row_ok = kp < p.S;
-      const long long orow = row_ok ? zig_row(kp, p.C, p.T, p.D) : 0;
+      const long long orow = row_ok ? batch_row(zig_row(kp, p.C, p.T, p.D), seq, p) : 0;
       __nv_bfloat16* dvp = p.dv + orow * p.ld_dqkv + head * HD;
       __nv_bfloat16* dkp = p.dk + orow * p.ld_dqkv + head * HD;
 #pragma unroll
@@ -486,8 +519,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = blockIdx.x / p.n_outer;
-  const int blk = blockIdx.x - head * p.n_outer;
+  const CtaPos cp = cta_pos(p);
+  const int head = cp.head, seq = cp.seq;
+  const int blk = cp.tile;
+  const int kv_row0 = (int)(seq * p.S);  // first natural K/V row of the sequence
   // natural: query tiles in decreasing position (longest first)
   const long long r0 = p.natural ? zig_row((long long)(p.n_outer - 1 - blk) * BT, p.C, p.T, p.D)
                                  : (long long)blk * BT;
@@ -541,8 +576,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* sk = sStage + st * G::STAGE;
 #pragma unroll
         for (int b = 0; b < G::BOXES; ++b) {
-          tma_load_2d(sk + b * BOX_BYTES, &tmK, &kv_full[st], head * HD + 64 * b, j * IT);
-          tma_load_2d(sk + G::TILE + b * BOX_BYTES, &tmV, &kv_full[st], head * HD + 64 * b, j * IT);
+          tma_load_2d(sk + b * BOX_BYTES, &tmK, &kv_full[st], head * HD + 64 * b, kv_row0 + j * IT);
+          tma_load_2d(sk + G::TILE + b * BOX_BYTES, &tmV, &kv_full[st], head * HD + 64 * b,
+                      kv_row0 + j * IT);
         }
         last[st] = (int)ph;
       }
@@ -623,9 +659,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int g = (warp - 2) >> 2;  // key half of every streamed tile this warpgroup takes
     const int qq = warp & 3;
     const int r_local = qq * 32 + lane;
-    const long long grow = r0 + r_local;
-    const bool row_ok = grow < p.S;
-    const long long qpos = row_ok ? row_pos(grow, p.C, p.T, p.D) : -1;
+    const long long vrow = r0 + r_local;  // row in the sequence's own layout
+    const bool row_ok = vrow < p.S;
+    const long long qpos = row_ok ? row_pos(vrow, p.C, p.T, p.D) : -1;
+    const long long grow = batch_row(vrow, seq, p);  // row in the micro-batch's layout
     const float lse = row_ok ? p.lse[(long long)head * p.ld_stat + grow] : 0.f;
     const float del = row_ok ? p.delta[(long long)head * p.ld_stat + grow] : 0.f;
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
@@ -786,11 +823,13 @@ __global__ void attention_delta_kernel(const uint4* __restrict__ o, const uint4*
 template <int HD>
 tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStream_t stream) {
   CUtensorMap tq, tdo, tk, tv;
-  TSP_TRY(make_tmap_2d_bf16(&tq, c.q, (uint64_t)c.ld_q, (uint64_t)c.S, (uint64_t)c.ld_q * 2, 64, 128));
-  TSP_TRY(make_tmap_2d_bf16(&tdo, c.dout, (uint64_t)c.ld_do, (uint64_t)c.S, (uint64_t)c.ld_do * 2, 64, 128));
-  TSP_TRY(make_tmap_2d_bf16(&tk, c.k, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, 128));
-  TSP_TRY(make_tmap_2d_bf16(&tv, c.v, (uint64_t)c.ld_kv, (uint64_t)c.S, (uint64_t)c.ld_kv * 2, 64, 128));
+  const uint64_t rows = (uint64_t)c.S * (uint64_t)p.B;
+  TSP_TRY(make_tmap_2d_bf16(&tq, c.q, (uint64_t)c.ld_q, rows, (uint64_t)c.ld_q * 2, 64, 128));
+  TSP_TRY(make_tmap_2d_bf16(&tdo, c.dout, (uint64_t)c.ld_do, rows, (uint64_t)c.ld_do * 2, 64, 128));
+  TSP_TRY(make_tmap_2d_bf16(&tk, c.k, (uint64_t)c.ld_kv, rows, (uint64_t)c.ld_kv * 2, 64, 128));
+  TSP_TRY(make_tmap_2d_bf16(&tv, c.v, (uint64_t)c.ld_kv, rows, (uint64_t)c.ld_kv * 2, 64, 128));
   const int tiles = (int)((c.S + 127) / 128);
+  const unsigned ctas = (unsigned)((long long)tiles * c.heads * p.B);
   {
     auto kernel = attention_bwd_dkv_kernel<HD>;
     const size_t smem = KeyGeom<HD>::SMEM;
@@ -799,8 +838,7 @@ tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStre
     cudaError_t e;
     BwdParams pk = p;
     pk.n_outer = tiles;
-    kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tq, tdo, tk, tv, pk, 0,
-                                                                   (int)c.do_col0);
+    kernel<<<ctas, THREADS, smem, stream>>>(tq, tdo, tk, tv, pk, 0, (int)c.do_col0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention bwd (key side): launch");
   }
@@ -812,7 +850,7 @@ tsp_status launch_bwd_hd(const AttentionBwdCall& c, const BwdParams& p, cudaStre
     cudaError_t e;
     BwdParams pq = p;
     pq.n_outer = tiles;
-    kernel<<<(unsigned)(tiles * c.heads), THREADS, smem, stream>>>(tk, tv, pq, 0, (int)c.do_col0);
+    kernel<<<ctas, THREADS, smem, stream>>>(tk, tv, pq, 0, (int)c.do_col0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention bwd (query side): launch");
   }
@@ -826,7 +864,7 @@ tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) 
   if (!c.q || !c.k || !c.v || !c.dout || !c.lse || !c.delta || !c.dq || !c.dk || !c.dv || !c.status)
     return fail(TSP_ERR_INVALID_ARG, "attention bwd: null pointer");
   if ((c.ld_q % 8) || (c.ld_kv % 8) || (c.ld_do % 8) || (c.do_col0 % 8) || (c.ld_dqkv % 8) ||
-      (c.ld_stat % 128) || c.ld_stat < c.S)
+      (c.ld_stat % 128) || c.ld_stat < c.S * (c.B > 0 ? c.B : 1))
     return fail(TSP_ERR_INVALID_ARG, "attention bwd: bad strides");
   if ((reinterpret_cast<uintptr_t>(c.q) | reinterpret_cast<uintptr_t>(c.dout) |
        reinterpret_cast<uintptr_t>(c.lse) | reinterpret_cast<uintptr_t>(c.delta) |
@@ -836,7 +874,10 @@ tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) 
   if ((long long)c.heads * c.d > c.ld_q || (long long)c.heads * c.d > c.ld_kv ||
       c.do_col0 + (long long)c.heads * c.d > c.ld_do || (long long)c.heads * c.d > c.ld_dqkv)
     return fail(TSP_ERR_INVALID_ARG, "attention bwd: head columns exceed the row width");
-  if (c.S > (1ll << 30)) return fail(TSP_ERR_UNSUPPORTED, "attention bwd: S too large");
+  const int B = c.B > 0 ? c.B : 1;
+  if (c.S * B > (1ll << 30)) return fail(TSP_ERR_UNSUPPORTED, "attention bwd: too many rows");
+  if (B > 1 && c.T % 128)
+    return fail(TSP_ERR_UNSUPPORTED, "attention bwd: a micro-batch needs S/D % 128 == 0");
   BwdParams p{};
   p.dq = static_cast<__nv_bfloat16*>(c.dq);
   p.dk = static_cast<__nv_bfloat16*>(c.dk);
@@ -853,6 +894,14 @@ tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) 
   p.T = c.T;
   p.C = c.C;
   p.D = c.D;
+  p.B = B;
+  p.heads = c.heads;
+  {
+    // pairs per group: their K and V (2 * S * d bf16 each) within 48 MB of the L2
+    const long long fit = (48LL << 20) / (4LL * c.S * c.d);
+    const long long pairs = (long long)c.heads * B;
+    p.group = (int)(fit < 1 ? 1 : (fit > pairs ? pairs : fit));
+  }
   p.natural = (c.C % 128 == 0) ? 1 : 0;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);
   p.scale = 1.0f / sqrtf((float)c.d);

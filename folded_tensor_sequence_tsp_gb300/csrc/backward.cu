@@ -13,6 +13,8 @@
 //     attention backward of every rank's queries, whose K/V gradients land at the
 //     key's owner (the reverse of the all-gather), then dx and the shard's weight
 //     gradients.
+// A micro-batch runs every product over all B*S rows: the weight gradients sum the
+// tokens of every sequence, the attention backward keeps each sequence to itself.
 // Weight gradients are fp32, in the packed layout of the weights (a float array of
 // wpack_elems), so each shard's gradient is contiguous like the shard itself.
 #include "tsp_device.cuh"
@@ -30,7 +32,7 @@ tsp_status swiglu_gate_up_save(const Plan& p, const void* hs, const void* wpack,
   c.epi = EPI_SWIGLU_SAVE;
   c.A = hs;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_w13;
   c.ldb = p.H;
   c.b_rows = 2LL * p.NF;
@@ -52,7 +54,7 @@ tsp_status swiglu_dgate(const Plan& p, const void* dmlp, const void* wpack, void
   c.epi = EPI_SWIGLU_BWD;
   c.A = dmlp;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_w2;  // [H][NF] = [K][N]
   c.ldb = p.NF;
   c.b_rows = p.NF;
@@ -74,7 +76,7 @@ tsp_status swiglu_dinput(const Plan& p, const void* da13, const void* wpack, con
   c.epi = residual ? EPI_RESIDUAL : EPI_STORE;
   c.A = da13;
   c.lda = 2LL * p.NF;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_w13;  // [2NF][H] = [K][N]
   c.ldb = p.H;
   c.b_rows = p.H;
@@ -86,14 +88,15 @@ tsp_status swiglu_dinput(const Plan& p, const void* da13, const void* wpack, con
   c.R = residual;
   c.ldr = p.H;
   c.C32 = out32;
-  c.ring_rows = p.T;
+  c.ring_rows = (int64_t)p.B * p.T;  // rank r's rows of every sequence
   c.ring_kblocks = 2LL * p.Fp / 64;
   c.status = status_of(ws);
   return launch_gemm(c, s);
 }
 
-// Weight gradient dW[M][N] = A^T B over the S tokens: A [S][M], B [S][N] (both
-// token-major, i.e. MN-major operands), fp32 out with row stride ldc.
+// Weight gradient dW[M][N] = A^T B over the N = B*S tokens of the micro-batch:
+// A [N][M], B [N][N] (both token-major, i.e. MN-major operands), fp32 out with row
+// stride ldc.
 tsp_status weight_grad(const Plan& p, const void* A, int64_t M, const void* B, int64_t N,
                        float* dW, int64_t ldc, void* ws, cudaStream_t s) {
   GemmCall c{};
@@ -107,7 +110,7 @@ tsp_status weight_grad(const Plan& p, const void* A, int64_t M, const void* B, i
   c.b_rows = N;
   c.b_mn = 1;
   c.N = N;
-  c.K = p.S;
+  c.K = p.N;
   c.C32 = dW;
   c.ldc = ldc;
   c.status = status_of(ws);
@@ -137,7 +140,7 @@ tsp_status o_projection_dgrad(const Plan& p, const void* dattn, const void* wpac
   c.epi = EPI_STORE;
   c.A = dattn;
   c.lda = p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_o;  // [H][H] = [K][N]
   c.ldb = p.H;
   c.b_rows = p.H;
@@ -157,7 +160,7 @@ tsp_status qkv_dgrad(const Plan& p, const void* dqkv, const void* wpack, const f
   c.epi = residual32 ? EPI_RESIDUAL : EPI_STORE;
   c.A = dqkv;
   c.lda = 3LL * p.H;
-  c.M = p.S;
+  c.M = p.N;
   c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;  // [3H][H] = [K][N]
   c.ldb = p.H;
   c.b_rows = p.H;
@@ -199,6 +202,7 @@ tsp_status attention_shard_backward(const Plan& p, int k, const void* q, const v
   a.T = p.T;
   a.C = p.C;
   a.D = p.D;
+  a.B = p.B;
   a.heads = p.hpr;
   a.d = p.d;
   a.status = status_of(ws);
@@ -213,7 +217,7 @@ tsp_status attention_recompute(const Plan& p, const void* xs, const void* wpack,
   uint16_t* qa = at<uint16_t>(ws, p.ws.qa);
   uint16_t* ka = at<uint16_t>(ws, p.ws.ka);
   uint16_t* va = at<uint16_t>(ws, p.ws.va);
-  const int64_t shard = p.S * p.Hd;
+  const int64_t shard = p.N * p.Hd;
   for (int k = 0; k < p.D; ++k) {
     TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, qa + k * shard, ka + k * shard,
                                     va + k * shard, ws, s));
@@ -225,8 +229,8 @@ tsp_status attention_recompute(const Plan& p, const void* xs, const void* wpack,
 }
 
 // Layout of the activations a training forward keeps (byte offsets, 256-aligned):
-// o [S][H] bf16, then lse [heads][ld_stat] fp32.
-size_t saved_lse_offset(const Plan& p) { return ((size_t)p.S * p.H * 2 + 255) & ~(size_t)255; }
+// o [N][H] bf16, then lse [heads][ld_stat] fp32.
+size_t saved_lse_offset(const Plan& p) { return ((size_t)p.N * p.H * 2 + 255) & ~(size_t)255; }
 size_t saved_bytes(const Plan& p) {
   return saved_lse_offset(p) + (((size_t)p.heads * p.ld_stat * 4 + 255) & ~(size_t)255);
 }
@@ -247,8 +251,8 @@ tsp_status attention_backward(const Plan& p, const void* xs, const void* wpack, 
   float* delta = at<float>(ws, p.ws.delta);
   TSP_TRY(o_projection_dgrad(p, dattn, wpack, dob, ws, s));
   TSP_TRY(weight_grad(p, dattn, p.H, o, p.H, dwpack + p.wp_o, p.H, ws, s));  // dWo = dattn^T o
-  TSP_TRY(launch_attention_delta(o, dob, p.H, p.heads, p.d, p.S, delta, p.ld_stat, s));
-  const int64_t shard = p.S * p.Hd;
+  TSP_TRY(launch_attention_delta(o, dob, p.H, p.heads, p.d, p.N, delta, p.ld_stat, s));
+  const int64_t shard = p.N * p.Hd;
   for (int k = 0; k < p.D; ++k)  // broadcast iteration k, in reverse
     TSP_TRY(attention_shard_backward(p, k, qa + k * shard, ka + k * shard, va + k * shard, dob,
                                      lse + (int64_t)k * p.hpr * p.ld_stat,
@@ -278,17 +282,6 @@ tsp_status layer_backward_from(const Plan& p, const void* xs, const void* wpack,
 
 using namespace tsp;
 
-namespace {
-// The backward calls take one sequence per plan (tsp_plan, or tsp_plan_batched
-// with batch 1).
-tsp_status check_single_sequence(tsp_plan_t plan, const char* what) {
-  TSP_TRY(tsp_check_plan(plan));
-  if (plan->p.B != 1)
-    return fail(TSP_ERR_UNSUPPORTED, std::string(what) + ": the backward takes one sequence per plan");
-  return TSP_OK;
-}
-}  // namespace
-
 extern "C" {
 
 size_t tsp_bwd_workspace_bytes(tsp_plan_t plan) { return plan ? plan->p.ws.total_bwd : 0; }
@@ -296,7 +289,7 @@ size_t tsp_bwd_workspace_bytes(tsp_plan_t plan) { return plan ? plan->p.ws.total
 tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
                        const tsp_bf16* dmlp, tsp_bf16* dhs, float* dwpack, void* ws,
                        void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_mlp_bwd"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({hs, wpack, dmlp, dhs, dwpack}, "tsp_mlp_bwd"));
   TSP_TRY(check_ws(ws, "tsp_mlp_bwd"));
   if (dhs == hs || dhs == dmlp) return fail(TSP_ERR_INVALID_ARG, "tsp_mlp_bwd: dhs aliases an input");
@@ -307,7 +300,7 @@ tsp_status tsp_mlp_bwd(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpac
 tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                              const tsp_bf16* dattn, tsp_bf16* dxs, float* dwpack, void* ws,
                              void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_attention_bwd"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, dattn, dxs, dwpack}, "tsp_attention_bwd"));
   TSP_TRY(check_ws(ws, "tsp_attention_bwd"));
   if (dxs == xs || dxs == dattn) return fail(TSP_ERR_INVALID_ARG, "tsp_attention_bwd: dxs aliases an input");
@@ -322,7 +315,7 @@ tsp_status tsp_attention_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16
 tsp_status tsp_layer_bwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                          const tsp_bf16* dout, tsp_bf16* dxs, float* dwpack, void* ws,
                          void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_layer_bwd"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, dout, dxs, dwpack}, "tsp_layer_bwd"));
   TSP_TRY(check_ws(ws, "tsp_layer_bwd"));
   if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd: dxs aliases an input");
@@ -339,7 +332,7 @@ size_t tsp_saved_bytes(tsp_plan_t plan) { return plan ? saved_bytes(plan->p) : 0
 
 tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                                tsp_bf16* out, void* saved, void* ws, void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_layer_fwd_train"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, out, saved}, "tsp_layer_fwd_train"));
   TSP_TRY(check_ws(ws, "tsp_layer_fwd_train"));
   if (out == xs) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_fwd_train: out aliases xs");
@@ -364,7 +357,7 @@ tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf
 tsp_status tsp_layer_bwd_saved(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wpack,
                                const void* saved, const tsp_bf16* dout, tsp_bf16* dxs,
                                float* dwpack, void* ws, void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_layer_bwd_saved"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({xs, wpack, saved, dout, dxs, dwpack}, "tsp_layer_bwd_saved"));
   TSP_TRY(check_ws(ws, "tsp_layer_bwd_saved"));
   if (dxs == xs || dxs == dout) return fail(TSP_ERR_INVALID_ARG, "tsp_layer_bwd_saved: dxs aliases an input");
@@ -380,7 +373,7 @@ tsp_status tsp_layer_bwd_saved(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf
 tsp_status tsp_causal_attention_lse(tsp_plan_t plan, int shard, const tsp_bf16* q,
                                     const tsp_bf16* kn, const tsp_bf16* vn, tsp_bf16* o,
                                     float* lse, void* ws, void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_causal_attention_lse"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({q, kn, vn, o, lse}, "tsp_causal_attention_lse"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention_lse"));
   if (shard < 0 || shard >= plan->p.D)
@@ -393,7 +386,7 @@ tsp_status tsp_causal_attention_bwd(tsp_plan_t plan, int shard, const tsp_bf16* 
                                     const tsp_bf16* kn, const tsp_bf16* vn, const tsp_bf16* o,
                                     const tsp_bf16* dout, const float* lse, float* delta,
                                     tsp_bf16* dqkv, void* ws, void* stream) {
-  TSP_TRY(check_single_sequence(plan, "tsp_causal_attention_bwd"));
+  TSP_TRY(tsp_check_plan(plan));
   TSP_TRY(check_ptrs({q, kn, vn, o, dout, lse, delta, dqkv}, "tsp_causal_attention_bwd"));
   TSP_TRY(check_ws(ws, "tsp_causal_attention_bwd"));
   if (shard < 0 || shard >= plan->p.D)
@@ -402,7 +395,7 @@ tsp_status tsp_causal_attention_bwd(tsp_plan_t plan, int shard, const tsp_bf16* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t col = (int64_t)shard * p.Hd;
   TSP_TRY(launch_attention_delta(static_cast<const uint16_t*>(o) + col,
-                                 static_cast<const uint16_t*>(dout) + col, p.H, p.hpr, p.d, p.S,
+                                 static_cast<const uint16_t*>(dout) + col, p.H, p.hpr, p.d, p.N,
                                  delta, p.ld_stat, s));
   return attention_shard_backward(p, shard, q, kn, vn, dout, lse, delta, dqkv, ws, s);
 }

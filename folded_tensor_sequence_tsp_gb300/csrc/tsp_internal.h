@@ -174,6 +174,7 @@ struct AttentionBwdCall {
   const float* lse; const float* delta; int64_t ld_stat;
   void* dq; void* dk; void* dv; int64_t ld_dqkv;
   int64_t S, T, C; int D;
+  int B;  // sequences of the micro-batch ([D][B][T] sharded rows, K/V rows b*S + t); 0 = 1
   int heads, d;
   DevStatus* status;
 };

@@ -110,13 +110,13 @@ tsp_status tsp_plan(int D, int64_t S, int hidden, int heads, int ffn, tsp_plan_t
  * local order. Natural (unsharded) buffers are [B][S][H]. Queries attend only to
  * the keys of their own sequence; the projections and the MLP run over all
  * N = B*S rows at once (one weight-shard pass serves the whole micro-batch).
- * Every forward entry point, the shard/unshard and index calls and the single
- * steps take such a plan; in the buffer sizes stated below, read N = B*S rows where
- * a size says S or D*T. The backward calls (tsp_*_bwd, the training pair and
- * tsp_causal_attention_lse) take batch 1 only and return TSP_ERR_UNSUPPORTED
- * otherwise. Supported iff tsp_plan's conditions hold, batch >= 1,
- * batch * S <= 2^26 and, for batch > 1, T = S/D is a multiple of 128 (a 128-row
- * query tile of the attention kernel never spans two ranks' blocks).
+ * Every entry point takes such a plan; in the buffer sizes stated below, read
+ * N = B*S rows where a size says S or D*T (the lse / delta statistics hold
+ * stat_stride >= N entries per head). The backward calls return the gradients of
+ * the sum over the micro-batch: input gradients per sequence, weight gradients
+ * summed over every sequence's tokens. Supported iff tsp_plan's conditions hold,
+ * batch >= 1, batch * S <= 2^26 and, for batch > 1, T = S/D is a multiple of 128
+ * (a 128-row query tile of the attention kernels never spans two ranks' blocks).
  * tsp_plan(D, S, ...) is tsp_plan_batched(D, S, 1, ...).
  */
 tsp_status tsp_plan_batched(int D, int64_t S, int batch, int hidden, int heads, int ffn,

@@ -80,6 +80,7 @@ __all__ = [
     "swiglu_mlp_backward",
     "attention_block_backward",
     "layer_backward",
+    "layer_backward_batched",
     "tsp_layer_backward",
     "causal_pairs_per_rank",
     "layer_flops",
@@ -557,6 +558,19 @@ def layer_backward(x, W: dict, heads: int, dout) -> dict:
     for n in ("dWq", "dWk", "dWv", "dWo"):
         g[n] = a[n]
     g["dx"] = dh + a["dx"]
+    return g
+
+
+def layer_backward_batched(x, W: dict, heads: int, dout) -> dict:
+    """Gradients of the sum over a micro-batch x [B, S, H] for dout [B, S, H].
+
+    The sequences are independent: each sequence's input gradient is its own
+    layer_backward's, and a weight gradient is the sum of the sequences' weight
+    gradients. Returns layer_backward's keys, "dx" with a leading batch axis.
+    """
+    res = [layer_backward(x[b], W, heads, dout[b]) for b in range(x.shape[0])]
+    g = {k: sum(r[k] for r in res) for k in res[0] if k != "dx"}
+    g["dx"] = np.stack([r["dx"] for r in res])
     return g
 
 

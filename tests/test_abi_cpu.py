@@ -151,11 +151,8 @@ def test_batched_plan_sizes_and_limits(lib):
     assert lib.tsp_plan_batched(2, 256, 0, 256, 4, 688, ctypes.byref(h)) == B.TSP_ERR_UNSUPPORTED
     assert lib.tsp_plan_batched(8, 1 << 23, 16, 4096, 32, 11008,
                                 ctypes.byref(h)) == B.TSP_ERR_UNSUPPORTED
-    # backward calls take one sequence per plan; refused before any launch
-    p = tsp.tsp_plan_batched(2, 256, 2, 256, 4, 688)
-    ws = ctypes.c_void_p(1 << 20)
-    a = [ctypes.c_void_p(4096 * k) for k in range(1, 6)]
-    assert lib.tsp_layer_bwd(p.handle, *a, ws, None) == B.TSP_ERR_UNSUPPORTED
-    assert "one sequence" in B.tsp_last_error()
-    assert lib.tsp_mlp_bwd(p.handle, *a, ws, None) == B.TSP_ERR_UNSUPPORTED
-    assert lib.tsp_layer_fwd_train(p.handle, *a[:4], ws, None) == B.TSP_ERR_UNSUPPORTED
+    # the saved activations of the training pair and the backward workspace grow
+    # with the micro-batch too
+    p2 = tsp.tsp_plan_batched(4, 4096, 2, 1024, 16, 2816)
+    assert tsp.tsp_saved_bytes(p2) >= 2 * 4096 * 1024 * 2 + 16 * 2 * 4096 * 4
+    assert tsp.tsp_bwd_workspace_bytes(p2) > 2 * (tsp.tsp_bwd_workspace_bytes(one) - 256 * 40)

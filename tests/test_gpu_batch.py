@@ -6,8 +6,10 @@ Transformer Training & Inference", section 4, scalability). A micro-batch plan
 holds B independent sequences; every rank owns its zigzag chunks of each of them
 (rank-major [D, B, S/D, H]). Checked here: the index map and the shard/unshard
 copies bit for bit, the blocks and the layer against the oracle on every
-sequence, the batched call bit-identical to one call per sequence, and the
-7B-shaped layer at 4 x 16K tokens on sampled rows of every sequence.
+sequence, the batched call bit-identical to one call per sequence, the
+7B-shaped layer at 4 x 16K tokens on sampled rows of every sequence, and the
+backward: per-sequence input gradients and weight gradients summed over the
+micro-batch, against the oracle and against one call per sequence.
 """
 import numpy as np
 import pytest
@@ -15,7 +17,8 @@ import torch
 
 import oracle
 import tsp_inputs
-from gpu_util import Layer, assert_close, bits, dev, f64, layer_row_scale, layer_tolerance
+from gpu_util import (Layer, assert_close, assert_close_grad, bits, dev, f64, layer_row_scale,
+                      layer_tolerance, rand_bits)
 
 tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
 pytestmark = pytest.mark.gpu
@@ -148,3 +151,87 @@ def test_7b_16k_micro_batch_of_4_sampled_rows():
         s, atol = layer_tolerance(ref["out"], oracle.swiglu_gate(ref["h"], W["W1"], W["W3"]),
                                   ref["h"], W)
         assert_close(got, ref["out"], f"7b-16k seq {b} out rows", scale=s, max_abs=atol)
+
+
+# ---------------------------------------------------------------- backward
+
+def _batched_dout(L, seed):
+    b = rand_bits((L.info.tokens, L.info.hidden), seed)
+    return b.reshape(L.info.batch, L.info.S, L.info.hidden), dev(b)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_batched_layer_backward_matches_oracle(name):
+    shape, batch = SHAPES[name]
+    L = Layer(*shape, seed=24, batch=batch)
+    ws = L.bwd_workspace()
+    g_bits, g_dev = _batched_dout(L, 25)
+    dxs = L.act()
+    dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+    tsp.tsp_layer_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dxs, dwpack, ws)
+    L.check_status()
+    got = L.grads(dwpack)
+    ref = oracle.layer_backward_batched(L.f("x"), L.weights64(), L.info.heads,
+                                        oracle.widen_bf16(g_bits))
+    dx = f64(_unshard(L, dxs))
+    for b in range(batch):
+        assert_close_grad(dx[b], ref["dx"][b], f"{name} seq {b} dx")
+    for k in ("dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"):
+        assert_close_grad(got[k], ref[k], f"{name} {k}")
+
+
+@pytest.mark.parametrize("name", ["tiny-b3", "small-b2"])
+def test_batched_backward_equals_one_call_per_sequence(name):
+    """Input gradients are row-wise and per sequence: bit-identical to one backward
+    per sequence. Weight gradients sum every sequence's tokens in one K loop, so
+    they equal the sum of the per-sequence gradients up to fp32 summation order."""
+    shape, batch = SHAPES[name]
+    L = Layer(*shape, seed=26, batch=batch)
+    ws = L.bwd_workspace()
+    _, g_dev = _batched_dout(L, 27)
+    dxs = L.act()
+    dwpack = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+    tsp.tsp_layer_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dxs, dwpack, ws)
+    L.check_status()
+    got_dx = bits(_unshard(L, dxs))
+    one = tsp.tsp_plan(*shape)
+    ws1 = torch.empty(tsp.tsp_bwd_workspace_bytes(one), dtype=torch.uint8, device="cuda")
+    tsp.tsp_workspace_init(one, ws1)
+    S, H = L.info.S, L.info.hidden
+    dsum = torch.zeros_like(dwpack)
+    for b in range(batch):
+        x = L.d["x"][b].contiguous()
+        g = g_dev[b * S:(b + 1) * S].contiguous()
+        xs, gs, dx1, nat = (torch.empty_like(x) for _ in range(4))
+        tsp.tsp_shard(one, x, xs)
+        tsp.tsp_shard(one, g, gs)
+        dw1 = torch.zeros_like(dwpack)
+        tsp.tsp_layer_bwd(one, xs, L.wpack, gs, dx1, dw1, ws1)
+        tsp.tsp_unshard(one, dx1, nat)
+        assert tsp.tsp_device_status(ws1) == tsp.TSP_OK
+        assert np.array_equal(bits(nat), got_dx[b]), f"sequence {b} dx"
+        dsum += dw1
+    want = dsum.double().cpu().numpy()
+    have = dwpack.double().cpu().numpy()
+    assert_close_grad(have, want, f"{name} packed weight gradients")
+
+
+def test_batched_training_pair_equals_layer_fwd_and_bwd():
+    shape, batch = SHAPES["d3-b2"]
+    L = Layer(*shape, seed=28, batch=batch)
+    ws = L.bwd_workspace()
+    _, g_dev = _batched_dout(L, 29)
+    xs, dout = L.sharded_x(), L.shard(g_dev)
+    out_ref, out_tr = L.act(), L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out_ref, ws)
+    saved = torch.full((tsp.tsp_saved_bytes(L.plan),), 0xFF, dtype=torch.uint8, device="cuda")
+    tsp.tsp_layer_fwd_train(L.plan, xs, L.wpack, out_tr, saved, ws)
+    assert torch.equal(out_ref.view(torch.int16), out_tr.view(torch.int16))
+    dxs_ref, dxs_sv = L.act(), L.act()
+    dw_ref = torch.zeros(L.info.wpack_elems, dtype=torch.float32, device="cuda")
+    dw_sv = torch.full_like(dw_ref, float("nan"))
+    tsp.tsp_layer_bwd(L.plan, xs, L.wpack, dout, dxs_ref, dw_ref, ws)
+    tsp.tsp_layer_bwd_saved(L.plan, xs, L.wpack, saved, dout, dxs_sv, dw_sv, ws)
+    L.check_status()
+    assert torch.equal(dxs_ref.view(torch.int16), dxs_sv.view(torch.int16))
+    assert torch.equal(dw_ref, dw_sv)

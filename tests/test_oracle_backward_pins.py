@@ -53,6 +53,33 @@ def check_layer_backward_vs_autograd(o):
         assert np.abs(got["d" + k] - tW[k].grad.numpy()).max() < 1e-10, k
 
 
+def _torch_layer_batched(x, W, heads):
+    """The layer on a micro-batch [B, S, H]: torch's batched causal attention keeps
+    every sequence to itself."""
+    Bn, S, H = x.shape
+    d = H // heads
+    sp = lambda a: a.view(Bn, S, heads, d).transpose(1, 2)
+    att = torch.nn.functional.scaled_dot_product_attention(
+        sp(x @ W["Wq"].T), sp(x @ W["Wk"].T), sp(x @ W["Wv"].T), is_causal=True)
+    h = x + att.transpose(1, 2).reshape(Bn, S, H) @ W["Wo"].T
+    return h + (torch.nn.functional.silu(h @ W["W1"].T) * (h @ W["W3"].T)) @ W["W2"].T
+
+
+def check_batched_backward_vs_autograd(o):
+    # the gradient of the summed micro-batch loss, against torch autograd in float64
+    Bn, S, H, heads, F = 3, 10, 8, 2, 6
+    x, dout = _rand((Bn, S, H), 4), _rand((Bn, S, H), 5)
+    W = _weights(H, F, 6)
+    got = o.layer_backward_batched(x, W, heads, dout)
+    tx = torch.from_numpy(x).requires_grad_()
+    tW = {k: torch.from_numpy(v).requires_grad_() for k, v in W.items()}
+    _torch_layer_batched(tx, tW, heads).backward(torch.from_numpy(dout))
+    assert got["dx"].shape == x.shape
+    assert np.abs(got["dx"] - tx.grad.numpy()).max() < 1e-10
+    for k in W:
+        assert np.abs(got["d" + k] - tW[k].grad.numpy()).max() < 1e-10, k
+
+
 def check_attention_backward_finite_differences(o):
     n, d = 5, 3
     q, k, v, do = (_rand((n, d), s) for s in (4, 5, 6, 7))
@@ -181,7 +208,8 @@ def check_attention_gradient_sums(o):
 
 PINS = [check_layer_backward_vs_autograd, check_attention_backward_finite_differences,
         check_closed_forms, check_tsp_backward_equals_plain, check_block_backwards_vs_autograd,
-        check_sampled_backwards, check_attention_gradient_sums, check_rounded_output_delta]
+        check_sampled_backwards, check_attention_gradient_sums, check_rounded_output_delta,
+        check_batched_backward_vs_autograd]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -226,7 +254,14 @@ def _attn_rows_unnormalised(q, k, v, q_pos, k_pos, do, q_rows, k_rows, q_block=1
     return dq, dk, dv * 1.5
 
 
+def _batched_bwd_mean(x, W, heads, dout):
+    """Mistake: weight gradients averaged over the micro-batch instead of summed."""
+    g = oracle.layer_backward_batched(x, W, heads, dout)
+    return {k: (v if k == "dx" else v / x.shape[0]) for k, v in g.items()}
+
+
 MUTANTS = {
+    "micro-batch weight gradients averaged": dict(layer_backward_batched=_batched_bwd_mean),
     "MLP dh without the W3 path": dict(swiglu_mlp_backward=_mlp_bwd_no_w3_path),
     "sampled attention dv scaled": dict(causal_attention_head_backward_rows=_attn_rows_unnormalised),
     "attention dS without the row-sum term": dict(causal_attention_head_backward=_attn_bwd_no_rowsum),
