@@ -27,7 +27,7 @@ class TSPLayer:
     weights: dict of bfloat16 CUDA tensors Wq, Wk, Wv, Wo [H, H], W1, W3 [F, H],
     W2 [H, F] (nn.Linear layout). Activations passed to forward() are in the
     sharded [D, S/D, H] layout (see tsp_shard), or [D, batch, S/D, H] for a
-    micro-batch of `batch` sequences (forward only).
+    micro-batch of `batch` sequences.
     """
 
     def __init__(self, D, S, hidden, heads, ffn, weights, device=None, batch=1):

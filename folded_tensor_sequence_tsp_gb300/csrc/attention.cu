@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = o_done + 2;          // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // the output row of tile A / B's first row and the head: the softmax warps read
+  // them back for their epilogue instead of holding them across the key loop
+  long long* out_row0 = reinterpret_cast<long long*>(tmem_slot + 2);  // [2]
+  int* out_head = reinterpret_cast<int*>(out_row0 + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA -> group g, query block blk, pair (sequence, head) of the group
@@ -219,6 +223,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    // a 128-row tile's rows are contiguous in the micro-batch layout too
+    out_row0[0] = batch_row(row0, seq, p);
+    out_row0[1] = batch_row(row0 + QT, seq, p);
+    *out_head = head;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
@@ -356,7 +364,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r_local = q * 32 + lane;
     const long long vrow = row0 + t * QT + r_local;  // row in the sequence's own layout
     const bool row_ok = vrow < p.S;
-    const long long grow = batch_row(vrow, seq, p);  // row in the micro-batch's layout
     // S < 2^30 (checked at launch): positions fit in int
     const int pos = row_ok ? (int)row_pos(vrow, p.C, p.T, p.D) : -1;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
@@ -445,11 +452,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && my_tiles > 0 && warp_wait(&o_done[t], 0u)) {
       tc_fence_after();
+      const long long grow = out_row0[t] + r_local;  // row in the micro-batch's layout
+      const int ohead = *out_head;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       // log2 of the softmax denominator in the scaled base-2 domain: P_ij is then
       // exp2(s_ij * scale_log2 - lse) for the backward pass
-      if (p.lse != nullptr && row_ok) p.lse[(long long)head * p.ld_lse + grow] = m_ref + __log2f(l);
-      __nv_bfloat16* dst = p.o + grow * p.ld_o + p.o_col0 + col_q;
+      if (p.lse != nullptr && row_ok) p.lse[(long long)ohead * p.ld_lse + grow] = m_ref + __log2f(l);
+      __nv_bfloat16* dst = p.o + grow * p.ld_o + p.o_col0 + ohead * HD;
 #pragma unroll
       for (int c = 0; c < HD; c += 32) {
         uint32_t r[32];

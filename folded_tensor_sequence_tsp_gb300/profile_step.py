@@ -3,7 +3,8 @@
     python -m folded_tensor_sequence_tsp_gb300.profile_step --step attention \
         --workload 7b-64k --launches 3
 
-Steps: qkv (Q/K/V projection of shard 0), gather (K/V all-gather), attention
+Steps: qkv (Q/K/V projection of shard 0), qkv_gathered (the same with the K/V
+all-gather in its epilogue, as the layer runs it), gather (K/V all-gather), attention
 (causal attention of shard 0), o_proj (O projection with the fp32 residual copy),
 gate_up (SwiGLU gate/up), down (SwiGLU down with the fp32 residual), shard
 (zigzag rows), attention_bwd (Delta, key-side and query-side attention backward of
@@ -39,8 +40,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--step", required=True,
-                    choices=["qkv", "gather", "attention", "o_proj", "gate_up", "down", "shard",
-                             "attention_bwd"])
+                    choices=["qkv", "qkv_gathered", "gather", "attention", "o_proj", "gate_up",
+                             "down", "shard", "attention_bwd"])
     ap.add_argument("--workload", default="7b-64k", choices=[c.name for c in tsp_inputs.CONFIGS])
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
@@ -54,12 +55,16 @@ def main(argv=None):
     ws = None
     if args.step not in ("gather", "shard"):  # single steps use only the status word
         ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    need_w = args.step in ("qkv", "o_proj", "gate_up", "down")
+    need_w = args.step in ("qkv", "qkv_gathered", "o_proj", "gate_up", "down")
     wpack = _bf16((i.wpack_elems,), 1, 0.02) if need_w else None
 
     if args.step == "qkv":
         xs, qkv = _bf16((S, H), 2), torch.empty((S, 3 * Hd), dtype=torch.bfloat16, device="cuda")
         run = lambda: B.tsp_qkv_projection(plan, 0, xs, wpack, qkv, ws)
+    elif args.step == "qkv_gathered":
+        xs = _bf16((S, H), 2)
+        q, kn, vn = (torch.empty((S, Hd), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+        run = lambda: B.tsp_qkv_projection_gathered(plan, 0, xs, wpack, q, kn, vn, ws)
     elif args.step == "gather":
         qkv = _bf16((S, 3 * Hd), 3)
         kn = torch.empty((S, Hd), dtype=torch.bfloat16, device="cuda")
