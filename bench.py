@@ -286,6 +286,25 @@ def run_ours(args, world, rank, local):
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
     launches_per_step = 2 * D + 3
 
+    # ---- end to end through the host entry point (pinned buffers), right after the
+    # headline steps so that both run in the same thermal and power state
+    x_host = torch.from_numpy(bits["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        layer.forward_host(x_host, out_host)
+    barrier()
+    e_ms = []
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.forward_host(x_host, out_host)
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    layer.check()
+    e2e_ms = max_over_ranks(statistics.mean(e_ms))
+
     # ---- per-kernel pass: the same kernels through the single-step entry points
     qkv = torch.empty((N, 3 * i.shard_hidden), dtype=torch.bfloat16, device="cuda")
     q = torch.empty((N, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
@@ -471,24 +490,6 @@ def run_ours(args, world, rank, local):
         }
         del dout, dxs, dwpack, o, lse, delta, dqkv
     del q, kn, vn
-
-    # ---- end to end through the host entry point (pinned buffers)
-    x_host = torch.from_numpy(bits["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-    for _ in range(max(1, args.warmup)):
-        layer.forward_host(x_host, out_host)
-    barrier()
-    e_ms = []
-    for _ in range(args.steps):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        layer.forward_host(x_host, out_host)
-        b.record(stream)
-        b.synchronize()
-        e_ms.append(a.elapsed_time(b))
-    layer.check()
-    e2e_ms = max_over_ranks(statistics.mean(e_ms))
 
     tflops = Bm * algorithmic_flops(S, H, F) / (ms * 1e-3) / 1e12
     result = {

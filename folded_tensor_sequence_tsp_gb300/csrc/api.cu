@@ -290,6 +290,103 @@ tsp_status mlp_block(const Plan& p, const void* hs, const void* wpack, const voi
   return swiglu_down(p, g, wpack, residual, residual_f32, out, ws, s);
 }
 
+// Down projection of rank r's rows only (rows [r B T, (r+1) B T), every sequence of the
+// micro-batch), with the fp32 residual; the ring order starts at shard r as in the
+// whole-layer launch. When T is a multiple of the 128-row tile, every row block and
+// K order is the whole-layer launch's, so the result is the same bit for bit.
+tsp_status swiglu_down_rank(const Plan& p, int r, const void* g, const void* wpack,
+                            const float* residual32, void* out, void* ws, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.T, r0 = (int64_t)r * rows;
+  GemmCall c{};
+  c.epi = EPI_RESIDUAL;
+  c.A = static_cast<const uint16_t*>(g) + r0 * p.NF;
+  c.lda = p.NF;
+  c.M = rows;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_w2;
+  c.ldb = p.NF;
+  c.b_rows = p.H;
+  c.b_row0 = 0;
+  c.N = p.H;
+  c.K = p.NF;
+  c.C = static_cast<uint16_t*>(out) + r0 * p.H;
+  c.ldc = p.H;
+  c.R = residual32 + r0 * p.H;
+  c.ldr = p.H;
+  c.residual_f32 = 1;
+  c.ring_rows = rows;
+  c.ring_rank0 = r;
+  c.ring_kblocks = p.Fp / 64;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+// A non-blocking stream per device for the device-to-host copies of
+// tsp_layer_fwd_host, created on first use and kept for the life of the process.
+tsp_status copy_stream(cudaStream_t* out) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "copy stream: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(TSP_ERR_UNSUPPORTED, "copy stream: device index >= 64");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev]) {
+    e = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "copy stream: cudaStreamCreateWithFlags");
+  }
+  *out = streams[dev];
+  return TSP_OK;
+}
+
+// The MLP of tsp_layer_fwd_host with its way back to pinned host memory overlapped:
+// G for every row, then per rank r the down projection of r's rows on `s` while the
+// copy engine moves the previous ranks' output rows to out_host on a side stream.
+// Rank r's rows of sequence b are two runs of C natural rows (chunks r and 2D-1-r),
+// so each goes back with one cudaMemcpyAsync. `s` waits for the last copy.
+tsp_status mlp_block_to_host(const Plan& p, const void* hs, const void* wpack,
+                             const float* residual32, void* out_dev_rows, tsp_bf16* out_host,
+                             void* ws, cudaStream_t s) {
+  void* g = at<void>(ws, p.ws.g);
+  TSP_TRY(swiglu_gate_up(p, hs, wpack, g, ws, s));
+  cudaStream_t s2 = nullptr;
+  TSP_TRY(copy_stream(&s2));
+  cudaEvent_t ready = nullptr, copied = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&copied, cudaEventDisableTiming);
+  tsp_status st = TSP_OK;
+  if (e != cudaSuccess) st = cuda_fail(e, "tsp_layer_fwd_host: cudaEventCreate");
+  const size_t run_bytes = (size_t)p.C * p.H * 2;
+  const uint16_t* src = static_cast<const uint16_t*>(out_dev_rows);
+  for (int r = 0; st == TSP_OK && r < p.D; ++r) {
+    st = swiglu_down_rank(p, r, g, wpack, residual32, out_dev_rows, ws, s);
+    if (st != TSP_OK) break;
+    // the copies of rank r start once its rows are written (a wait on an event uses
+    // the record made just before it, so one event serves every rank)
+    e = cudaEventRecord(ready, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s2, ready, 0);
+    for (int b = 0; e == cudaSuccess && b < p.B; ++b) {
+      const int64_t row = ((int64_t)r * p.B + b) * p.T;  // first sharded row of (r, b)
+      const int64_t nat0 = (int64_t)b * p.S + (int64_t)r * p.C;
+      const int64_t nat1 = (int64_t)b * p.S + (int64_t)(2 * p.D - 1 - r) * p.C;
+      e = cudaMemcpyAsync(out_host + nat0 * p.H, src + row * p.H, run_bytes,
+                          cudaMemcpyDeviceToHost, s2);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(out_host + nat1 * p.H, src + (row + p.C) * p.H, run_bytes,
+                            cudaMemcpyDeviceToHost, s2);
+    }
+    if (e != cudaSuccess) st = cuda_fail(e, "tsp_layer_fwd_host: copy out");
+  }
+  // the caller's stream goes on only after every copy enqueued above
+  if (copied) {
+    e = cudaEventRecord(copied, s2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied, 0);
+    if (e != cudaSuccess && st == TSP_OK) st = cuda_fail(e, "tsp_layer_fwd_host: join");
+  }
+  if (ready) cudaEventDestroy(ready);
+  if (copied) cudaEventDestroy(copied);
+  return st;
+}
+
 // Device-side alias of a page-locked (pinned or registered) host buffer, or NULL if
 // the runtime does not map it (pageable memory).
 const void* mapped_host_alias(const void* host) {
@@ -537,6 +634,14 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
     cudaError_t e = cudaMemcpyAsync(a, x_host, bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy in");
     TSP_TRY(launch_zigzag_rows(p, a, b, p.H, true, s));  // b = shard(x)
+  }
+  if (out_dev && p.T % 128 == 0) {
+    // h = x + Attn(x); then the MLP, whose output rows go back to the pinned host
+    // buffer rank by rank while the next rank's down projection runs
+    void* h = at<void>(ws, p.ws.h);
+    float* h32 = at<float>(ws, p.ws.h32);
+    TSP_TRY(attention_block(p, b, wpack, b, h, h32, ws, s));
+    return mlp_block_to_host(p, h, wpack, h32, a, out_host, ws, s);
   }
   TSP_TRY(tsp_layer_fwd(plan, static_cast<const tsp_bf16*>(b), wpack, static_cast<tsp_bf16*>(a),
                         ws, stream));  // a = layer(b)

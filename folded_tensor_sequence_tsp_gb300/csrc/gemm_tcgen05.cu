@@ -18,7 +18,8 @@
 //               the second accumulator lets the epilogue of a tile overlap the
 //               main loop of the next.
 // Ring order: with ring_rows > 0 the K loop of a tile whose rows belong to rank
-// r = m0 / ring_rows starts at K block r * ring_kblocks and wraps around, so rank r
+// r = ring_rank0 + m0 / ring_rows starts at K block r * ring_kblocks and wraps
+// around (ring_rank0: the rank of the launch's first row), so rank r
 // takes MLP shard (r + t) mod D at step t, and the partial products of the shards
 // are summed in the on-chip accumulator.
 #include "tsp_device.cuh"
@@ -71,6 +72,7 @@ struct GemmParams {
   long long ldc2;
   int ring_rows;
   int ring_kblocks;
+  int ring_rank0;
   int group_m;  // tile order: group_m row blocks walk down each column block in turn
   DevStatus* status;
   unsigned long long limit_ns;
@@ -173,7 +175,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tile_coords(tile, numM, numN, p.group_m, mt, nt);
         const int m0 = mt * BM, n0 = nt * BN;
         int kb = 0;
-        if (p.ring_rows > 0) kb = (int)(((long long)(m0 / p.ring_rows) * p.ring_kblocks) % nkb);
+        if (p.ring_rows > 0)
+          kb = (int)(((long long)(p.ring_rank0 + m0 / p.ring_rows) * p.ring_kblocks) % nkb);
         for (int i = 0; i < nkb; ++i) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wb, SITE_GEMM_PRODUCER)) {
             ok = false;
@@ -502,6 +505,7 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   p.ldc2 = c.ldc2;
   p.ring_rows = (int)c.ring_rows;
   p.ring_kblocks = (int)c.ring_kblocks;
+  p.ring_rank0 = c.ring_rank0;
   // Tile order. If B fits easily in the 129 MB L2 (<= 48 MB), walk row-major: A is
   // read once and B stays cached. Otherwise group about 32 MB of A row blocks
   // (128 x K bf16 each) so each B column block is fetched once per group: the

@@ -142,6 +142,7 @@ struct GemmCall {
   int64_t zz_C, zz_T; int zz_D; int zz_B;
   int64_t ring_rows;           // rows per rank for the ring K order, 0 = natural order
   int64_t ring_kblocks;        // 64-wide K blocks per shard
+  int ring_rank0;              // rank of the launch's first row (ring order)
   DevStatus* status;
 };
 tsp_status launch_gemm(const GemmCall& call, cudaStream_t stream);

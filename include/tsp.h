@@ -190,12 +190,18 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
 
 /*
  * tsp_layer_fwd_host - the whole layer from and to HOST memory in natural token
- * order: x_host [S][H] in, out_host [S][H] out. Page-locked host buffers (pinned
- * or registered, i.e. mapped into the device address space) are read and written
- * by the zigzag shard/unshard kernels directly over the host link, so the copy and
- * the permutation are one pass; pageable buffers are staged through
- * cudaMemcpyAsync and the workspace. The call returns once the work is enqueued:
- * synchronise `stream` before reading out_host.
+ * order: x_host [S][H] in, out_host [S][H] out. A page-locked input (pinned or
+ * registered, i.e. mapped into the device address space) is read by the zigzag
+ * shard kernel directly over the host link, so the copy and the permutation are
+ * one pass. A page-locked output comes back rank by rank: the down projection runs
+ * per rank on `stream`, and each rank's rows (two runs of C natural rows per
+ * sequence) are copied to out_host by the copy engine on a library-owned
+ * non-blocking stream of the device (created on first use, kept until exit) while
+ * the next ranks compute; `stream` then waits for the last copy. This needs
+ * S/D % 128 == 0; otherwise the unshard kernel writes the mapped output directly.
+ * The result is the same bit for bit either way. Pageable buffers are staged
+ * through cudaMemcpyAsync and the workspace. The call returns once the work is
+ * enqueued: synchronise `stream` before reading out_host.
  */
 tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
                               tsp_bf16* out_host, void* ws, void* stream);
