@@ -54,6 +54,7 @@ class PlanInfo(ctypes.Structure):
         ("wpack_w2", ctypes.c_size_t), ("wpack_elems", ctypes.c_size_t),
         ("workspace_bytes", ctypes.c_size_t), ("bwd_workspace_bytes", ctypes.c_size_t),
         ("stat_stride", ctypes.c_int64), ("batch", ctypes.c_int), ("tokens", ctypes.c_int64),
+        ("attention_group", ctypes.c_int),
     ]
 
     def as_dict(self):

@@ -147,10 +147,12 @@ tsp_status qkv_projection(const Plan& p, int k, const void* xs, const void* wpac
 }
 
 // Q/K/V projection of shard k with the K/V all-gather fused into the epilogue: Q
-// rows stay in sharded order in q [S][H/D]; K and V rows land at their natural token
-// positions in kn, vn [S][H/D].
+// rows stay in sharded order in q [S][ld]; K and V rows land at their natural token
+// positions in kn, vn [S][ld] (ld >= H/D elements; the shard's H/D columns start at
+// each pointer).
 tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
-                                   void* q, void* kn, void* vn, void* ws, cudaStream_t s) {
+                                   void* q, void* kn, void* vn, int64_t ld, void* ws,
+                                   cudaStream_t s) {
   GemmCall c{};
   c.epi = EPI_QKV_SPLIT;
   c.A = xs;
@@ -163,10 +165,10 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
   c.N = 3LL * p.Hd;
   c.K = p.H;
   c.C = q;
-  c.ldc = p.Hd;
+  c.ldc = ld;
   c.split_k = kn;
   c.split_v = vn;
-  c.split_ld = p.Hd;
+  c.split_ld = ld;
   c.split_hd = p.Hd;
   c.zz_C = p.C;
   c.zz_T = p.T;
@@ -176,10 +178,18 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
   return launch_gemm(c, s);
 }
 
-// q holds the Q columns of the shard's heads, row stride ld_q (3H/D for the Q|K|V
-// buffer of tsp_qkv_projection, H/D for the Q buffer of the gathered projection).
-tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
-                            const void* vn, void* o, void* ws, cudaStream_t s, float* lse) {
+tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
+                                   void* q, void* kn, void* vn, void* ws, cudaStream_t s) {
+  return qkv_projection_gathered(p, k, xs, wpack, q, kn, vn, p.Hd, ws, s);
+}
+
+// Attention of the heads of shards k .. k + n - 1 in one launch: q holds their Q
+// columns (row stride ld_q: 3H/D for the Q|K|V buffer of tsp_qkv_projection, n H/D
+// for the Q buffer of the gathered projection), kn / vn their K / V columns (row
+// stride ld_kv); o receives columns [k H/D, (k + n) H/D).
+tsp_status causal_attention_shards(const Plan& p, int k, int n, const void* qkv, int64_t ld_q,
+                                   const void* kn, const void* vn, int64_t ld_kv, void* o,
+                                   void* ws, cudaStream_t s, float* lse) {
   AttentionCall a{};
   a.lse = lse;
   a.ld_lse = p.ld_stat;
@@ -187,7 +197,7 @@ tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q,
   a.ld_qkv = ld_q;
   a.kn = kn;
   a.vn = vn;
-  a.ld_kv = p.Hd;
+  a.ld_kv = ld_kv;
   a.o = o;
   a.ld_o = p.H;
   a.o_col0 = (int64_t)k * p.Hd;
@@ -196,10 +206,37 @@ tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q,
   a.C = p.C;
   a.D = p.D;
   a.B = p.B;
-  a.heads = p.hpr;
+  a.heads = n * p.hpr;
   a.d = p.d;
   a.status = status_of(ws);
   return launch_attention(a, s);
+}
+
+tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
+                            const void* vn, void* o, void* ws, cudaStream_t s, float* lse) {
+  return causal_attention_shards(p, k, 1, qkv, ld_q, kn, vn, p.Hd, o, ws, s, lse);
+}
+
+// The broadcast iterations of the attention block up to O (before W_O): per shard k
+// the local projections with the fused K/V all-gather, then causal attention. The
+// attention of p.G_att consecutive shards runs as one launch (their Q/K/V side by side
+// in the workspace) when one shard alone would not fill the GPU with CTAs; each
+// head's result is the same bit for bit. lse (optional) as for causal_attention.
+tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, void* o, void* ws,
+                            cudaStream_t s, float* lse) {
+  uint16_t* q = at<uint16_t>(ws, p.ws.qkv);
+  uint16_t* kn = at<uint16_t>(ws, p.ws.kn);
+  uint16_t* vn = at<uint16_t>(ws, p.ws.vn);
+  const int G = p.G_att;
+  const int64_t ld = (int64_t)G * p.Hd;
+  for (int k = 0; k < p.D; k += G) {  // broadcast iterations k .. k + G - 1
+    for (int j = 0; j < G; ++j)  // local projections, K/V all-gather in the epilogue
+      TSP_TRY(qkv_projection_gathered(p, k + j, xs, wpack, q + j * p.Hd, kn + j * p.Hd,
+                                      vn + j * p.Hd, ld, ws, s));
+    TSP_TRY(causal_attention_shards(p, k, G, q, ld, kn, vn, ld, o, ws, s,
+                                    lse ? lse + (int64_t)k * p.hpr * p.ld_stat : nullptr));
+  }
+  return TSP_OK;
 }
 
 // out = o W_O^T (+ residual, bf16); with out32 also the fp32 value of out.
@@ -271,15 +308,8 @@ tsp_status swiglu_down(const Plan& p, const void* g, const void* wpack, const vo
 
 tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, const void* residual,
                            void* out, void* out32, void* ws, cudaStream_t s) {
-  void* q = at<void>(ws, p.ws.qkv);
-  void* kn = at<void>(ws, p.ws.kn);
-  void* vn = at<void>(ws, p.ws.vn);
   void* o = at<void>(ws, p.ws.o);
-  for (int k = 0; k < p.D; ++k) {  // broadcast iteration k: every rank reads shard k
-    // local projections, with the all-gather of K/V written by the GEMM epilogue
-    TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, q, kn, vn, ws, s));
-    TSP_TRY(causal_attention(p, k, q, p.Hd, kn, vn, o, ws, s));
-  }
+  TSP_TRY(attention_shards(p, xs, wpack, o, ws, s, nullptr));
   return o_projection(p, o, wpack, residual, out, out32, ws, s);
 }
 
@@ -460,6 +490,19 @@ tsp_status tsp_plan_batched(int D, int64_t S, int batch, int hidden, int heads, 
   if ((long long)D * p.Fp % 128) p.Fp = (p.Fd + 127) / 128 * 128;
   p.NF = D * p.Fp;
   p.ld_stat = (p.N + 127) / 128 * 128;
+  {
+    // shards per attention launch: the fewest that give 512 CTAs (two 128-row query
+    // tiles each; about 3.4 per SM on 152 SMs), so that short sequences do not leave
+    // most SMs idle in the launch's tail; 1 for long sequences
+    const int64_t ctas = (S + 255) / 256 * (int64_t)(heads / D) * batch;
+    int G = D;
+    for (int g = 1; g <= D; ++g)
+      if (D % g == 0 && ctas * g >= 512) {
+        G = g;
+        break;
+      }
+    p.G_att = G;
+  }
 
   const size_t H = hidden;
   p.wp_qkv = 0;
@@ -476,9 +519,9 @@ tsp_status tsp_plan_batched(int D, int64_t S, int batch, int hidden, int heads, 
     return o;
   };
   p.ws.status = take(256);
-  p.ws.qkv = take(Sz * 3 * p.Hd * 2);
-  p.ws.kn = take(Sz * p.Hd * 2);
-  p.ws.vn = take(Sz * p.Hd * 2);
+  p.ws.qkv = take(Sz * (size_t)(p.G_att > 3 ? p.G_att : 3) * p.Hd * 2);
+  p.ws.kn = take(Sz * (size_t)p.G_att * p.Hd * 2);
+  p.ws.vn = take(Sz * (size_t)p.G_att * p.Hd * 2);
   p.ws.o = take(Sz * H * 2);
   p.ws.h = take(Sz * H * 2);
   p.ws.h32 = take(Sz * H * 4);
@@ -515,6 +558,7 @@ tsp_status tsp_get_plan_info(tsp_plan_t plan, tsp_plan_info* info) {
   info->S = p.S;
   info->batch = p.B;
   info->tokens = p.N;
+  info->attention_group = p.G_att;
   info->hidden = p.H;
   info->heads = p.heads;
   info->head_dim = p.d;

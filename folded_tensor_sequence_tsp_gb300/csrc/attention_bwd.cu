@@ -897,10 +897,14 @@ tsp_status launch_attention_bwd(const AttentionBwdCall& c, cudaStream_t stream) 
   p.B = B;
   p.heads = c.heads;
   {
-    // pairs per group: their K and V (2 * S * d bf16 each) within 48 MB of the L2
-    const long long fit = (48LL << 20) / (4LL * c.S * c.d);
+    // pairs per group: their K and V (2 * S * d bf16 each) within 48 MB of the L2,
+    // the pairs split evenly over the fewest groups (no short last group, whose
+    // longest blocks would start late)
+    const long long fit0 = (48LL << 20) / (4LL * c.S * c.d);
+    const long long fit = fit0 < 1 ? 1 : fit0;
     const long long pairs = (long long)c.heads * B;
-    p.group = (int)(fit < 1 ? 1 : (fit > pairs ? pairs : fit));
+    const long long n_groups = (pairs + fit - 1) / fit;
+    p.group = (int)((pairs + n_groups - 1) / n_groups);
   }
   p.natural = (c.C % 128 == 0) ? 1 : 0;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);

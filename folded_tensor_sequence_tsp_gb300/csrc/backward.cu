@@ -340,14 +340,8 @@ tsp_status tsp_layer_fwd_train(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* o = saved;
   float* lse = at<float>(saved, saved_lse_offset(p));
-  void* q = at<void>(ws, p.ws.qkv);
-  void* kn = at<void>(ws, p.ws.kn);
-  void* vn = at<void>(ws, p.ws.vn);
   // the layer forward's steps, with o and each row's lse landing in `saved`
-  for (int k = 0; k < p.D; ++k) {
-    TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, q, kn, vn, ws, s));
-    TSP_TRY(causal_attention(p, k, q, p.Hd, kn, vn, o, ws, s, lse + (int64_t)k * p.hpr * p.ld_stat));
-  }
+  TSP_TRY(attention_shards(p, xs, wpack, o, ws, s, lse));
   void* h = at<void>(ws, p.ws.h);
   void* h32 = at<void>(ws, p.ws.h32);
   TSP_TRY(o_projection(p, o, wpack, xs, h, h32, ws, s));

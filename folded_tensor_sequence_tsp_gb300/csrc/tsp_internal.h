@@ -19,8 +19,9 @@ struct DevStatus;
 // rows: every token of the micro-batch.
 struct WorkspaceLayout {
   size_t status;   // DevStatus
-  size_t qkv;      // [N][3H/D] Q|K|V of the current attention shard (sharded rows)
-  size_t kn, vn;   // [N][H/D] K and V of the current shard in natural token order
+  size_t qkv;      // [N][max(3, G_att) H/D] Q|K|V of the current attention shard, or the Q
+                   //   of the G_att shards of one attention launch (sharded rows)
+  size_t kn, vn;   // [N][G_att H/D] K and V of those shards in natural token order
   size_t o;        // [N][H]   attention output before the O projection (sharded rows)
   size_t h;        // [N][H]   h = x + Attn(x) (sharded rows), bf16: input of the MLP
   size_t h32;      // [N][H]   the same h in fp32: the residual of the MLP block
@@ -53,6 +54,7 @@ struct Plan {
   int Fd;   // F / D
   int Fp;   // padded shard width of the MLP
   int NF;   // D * Fp
+  int G_att;  // shards whose attention runs in one launch (divides D)
   int64_t ld_stat;  // row stride of the per-head row statistics (N rounded up to 128)
   size_t wp_qkv, wp_o, wp_w13, wp_w2, wp_elems;
   WorkspaceLayout ws;
@@ -199,6 +201,10 @@ tsp_status launch_wait_selftest(DevStatus* st, unsigned long long limit_ns, cuda
 // Steps of the forward (api.cu), shared with the backward orchestration.
 tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
                                    void* q, void* kn, void* vn, void* ws, cudaStream_t s);
+// Q/K/V projections and attention of every shard (G_att shards per attention launch),
+// o (and lse when not NULL: [heads][ld_stat]) written for every head.
+tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, void* o, void* ws,
+                            cudaStream_t s, float* lse);
 // lse (optional): [heads/D][ld_stat], the rows of shard k's heads.
 tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
                             const void* vn, void* o, void* ws, cudaStream_t s,

@@ -86,6 +86,10 @@ typedef struct tsp_plan_info {
   int64_t stat_stride;        /* row stride of per-head row statistics (lse, delta): tokens rounded up to 128 */
   int batch;                  /* B: sequences of the micro-batch (1 for tsp_plan)  */
   int64_t tokens;             /* N = B * S: rows of every activation buffer        */
+  int attention_group;        /* shards whose attention runs in one launch in the
+                                 *_fwd calls: the fewest (a divisor of D) that give
+                                 512 two-tile CTAs, so a short sequence still fills
+                                 the GPU; their Q/K/V share the workspace           */
 } tsp_plan_info;
 
 /*
