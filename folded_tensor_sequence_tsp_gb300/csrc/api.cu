@@ -146,11 +146,12 @@ tsp_status qkv_projection(const Plan& p, int k, const void* xs, const void* wpac
   return launch_gemm(c, s);
 }
 
-// Q/K/V projection of shard k with the K/V all-gather fused into the epilogue: Q
-// rows stay in sharded order in q [S][ld]; K and V rows land at their natural token
-// positions in kn, vn [S][ld] (ld >= H/D elements; the shard's H/D columns start at
-// each pointer).
-tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
+// Q/K/V projection of shards k .. k + n - 1 (one product: their packed rows are
+// consecutive) with the K/V all-gather fused into the epilogue: Q rows stay in
+// sharded order in q [S][ld]; K and V rows land at their natural token positions in
+// kn, vn [S][ld] (ld >= n H/D elements; shard k + j's H/D columns start at column
+// j H/D of each).
+tsp_status qkv_projection_gathered(const Plan& p, int k, int n, const void* xs, const void* wpack,
                                    void* q, void* kn, void* vn, int64_t ld, void* ws,
                                    cudaStream_t s) {
   GemmCall c{};
@@ -162,7 +163,7 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
   c.ldb = p.H;
   c.b_rows = 3LL * p.H;
   c.b_row0 = (int64_t)k * 3 * p.Hd;
-  c.N = 3LL * p.Hd;
+  c.N = 3LL * n * p.Hd;
   c.K = p.H;
   c.C = q;
   c.ldc = ld;
@@ -180,7 +181,7 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
 
 tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const void* wpack,
                                    void* q, void* kn, void* vn, void* ws, cudaStream_t s) {
-  return qkv_projection_gathered(p, k, xs, wpack, q, kn, vn, p.Hd, ws, s);
+  return qkv_projection_gathered(p, k, 1, xs, wpack, q, kn, vn, p.Hd, ws, s);
 }
 
 // Attention of the heads of shards k .. k + n - 1 in one launch: q holds their Q
@@ -230,9 +231,8 @@ tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, vo
   const int G = p.G_att;
   const int64_t ld = (int64_t)G * p.Hd;
   for (int k = 0; k < p.D; k += G) {  // broadcast iterations k .. k + G - 1
-    for (int j = 0; j < G; ++j)  // local projections, K/V all-gather in the epilogue
-      TSP_TRY(qkv_projection_gathered(p, k + j, xs, wpack, q + j * p.Hd, kn + j * p.Hd,
-                                      vn + j * p.Hd, ld, ws, s));
+    // local projections of the G shards (one product), K/V all-gather in the epilogue
+    TSP_TRY(qkv_projection_gathered(p, k, G, xs, wpack, q, kn, vn, ld, ws, s));
     TSP_TRY(causal_attention_shards(p, k, G, q, ld, kn, vn, ld, o, ws, s,
                                     lse ? lse + (int64_t)k * p.hpr * p.ld_stat : nullptr));
   }

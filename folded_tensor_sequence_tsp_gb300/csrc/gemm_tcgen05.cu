@@ -390,13 +390,16 @@ __global__ void __launch_bounds__(THREADS, 1)
               store_row32(p.C + row * p.ldc + c1, d1);
               store_row32(p.C + row * p.ldc + c3, d3);
             } else if constexpr (EPI == K_QKV_SPLIT) {
-              // a 32-column chunk never straddles sections (split_hd % 32 == 0)
+              // a 32-column chunk never straddles sections (split_hd % 32 == 0); the
+              // sections go Q, K, V for each of the N / (3 split_hd) shards in turn,
+              // and shard j's columns land at offset j * split_hd of each destination
               const int sec = col / p.split_hd;
-              const int lc = col - sec * p.split_hd;
-              if (sec == 0)
+              const int part = sec % 3;
+              const int lc = (sec / 3) * p.split_hd + (col - sec * p.split_hd);
+              if (part == 0)
                 store_row32(p.C + row * p.ldc + lc, f);
               else
-                store_row32((sec == 1 ? p.split_k : p.split_v) + nat * p.split_ld + lc, f);
+                store_row32((part == 1 ? p.split_k : p.split_v) + nat * p.split_ld + lc, f);
             } else {
               store_row32(p.C + row * p.ldc + col, f);
             }
@@ -459,8 +462,8 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   if (c.C32 && c.epi != EPI_STORE_F32 && (c.epi != EPI_RESIDUAL || c.residual_f32))
     return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 output needs a bf16 residual");
   if (c.epi == EPI_QKV_SPLIT &&
-      (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N != 3 * c.split_hd ||
-       c.ldc < c.split_hd || c.split_ld < c.split_hd || (c.split_ld % 8) || !aligned16(c.split_k) ||
+      (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N % (3 * c.split_hd) ||
+       c.ldc < c.N / 3 || c.split_ld < c.N / 3 || (c.split_ld % 8) || !aligned16(c.split_k) ||
        !aligned16(c.split_v) || c.zz_C <= 0 || c.zz_T != 2 * c.zz_C || c.zz_D <= 0 ||
        c.M != c.zz_T * c.zz_D * (c.zz_B > 0 ? c.zz_B : 1)))
     return fail(TSP_ERR_INVALID_ARG, "gemm: bad Q/K/V split arguments");

@@ -136,7 +136,8 @@ struct GemmCall {
   const void* R; int64_t ldr;  // residual (EPI_RESIDUAL): bf16, or fp32 if residual_f32
   int residual_f32;
   void* C32;                   // optional fp32 copy of the output (EPI_RESIDUAL, bf16 residual), row stride ldc
-  // EPI_QKV_SPLIT: the N = 3 split_hd columns are Q | K | V; Q rows go to C (ldc),
+  // EPI_QKV_SPLIT: the N = 3 n split_hd columns are Q | K | V of n shards in turn (shard j's
+  // columns land at offset j split_hd of each destination); Q rows go to C (ldc),
   // K and V rows to split_k / split_v (row stride split_ld) at the natural token
   // position of the sharded row (zigzag chunk zz_C, tokens per rank zz_T, zz_D ranks,
   // zz_B sequences: sharded row (r*zz_B + b)*zz_T + l -> natural row b*S + pos(r, l))
