@@ -284,7 +284,9 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     layer.check()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
-    launches_per_step = 2 * D + 3
+    # one Q/K/V product and one attention launch per group of attention_group shards,
+    # then the O, gate/up and down products
+    launches_per_step = 2 * (D // i.attention_group) + 3
 
     # ---- end to end through the host entry point (pinned buffers), right after the
     # headline steps so that both run in the same thermal and power state

@@ -189,3 +189,29 @@ def test_layer_forward_replays_from_a_cuda_graph(name):
         torch.cuda.synchronize()
         assert torch.equal(eager.view(torch.int16), replay.view(torch.int16))
     L.check_status()
+
+
+@pytest.mark.parametrize("name", ["tiny", "d3", "small"])
+def test_grouped_attention_launches_equal_per_shard_steps(name):
+    """tsp_layer_fwd runs the Q/K/V product and the attention of attention_group
+    shards per launch; the single-step entry points, one shard per call, give the
+    same bits (every head's products and sums are the same)."""
+    L = Layer(*SHAPES[name], seed=13)
+    i = L.info
+    assert i.attention_group > 1  # these shapes are short enough to group shards
+    xs = L.sharded_x()
+    out = L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
+    q = torch.empty((i.S, i.shard_hidden), dtype=torch.bfloat16, device="cuda")
+    kn, vn = torch.empty_like(q), torch.empty_like(q)
+    o, h, out2 = L.act(), L.act(), L.act()
+    h32 = torch.empty((i.S, i.hidden), dtype=torch.float32, device="cuda")
+    g = torch.empty((i.S, i.ffn_padded), dtype=torch.bfloat16, device="cuda")
+    for k in range(i.D):
+        tsp.tsp_qkv_projection_gathered(L.plan, k, xs, L.wpack, q, kn, vn, L.ws)
+        tsp.tsp_causal_attention_q(L.plan, k, q, kn, vn, o, L.ws)
+    tsp.tsp_o_projection(L.plan, o, L.wpack, xs, h, L.ws, out32=h32)
+    tsp.tsp_swiglu_gate_up(L.plan, h, L.wpack, g, L.ws)
+    tsp.tsp_swiglu_down(L.plan, g, L.wpack, None, out2, L.ws, residual32=h32)
+    L.check_status()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
