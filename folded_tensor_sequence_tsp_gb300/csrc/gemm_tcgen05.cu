@@ -74,6 +74,7 @@ struct GemmParams {
   int ring_kblocks;
   int ring_rank0;
   int group_m;  // tile order: group_m row blocks walk down each column block in turn
+  int wide;     // every epilogue pointer and row stride is 32-byte aligned: 32-byte accesses
   DevStatus* status;
   unsigned long long limit_ns;
 };
@@ -92,7 +93,41 @@ __device__ __forceinline__ void tile_coords(int tile, int numM, int numN, int gr
   nt = r / gm;
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&f)[32]) {
+// 32-byte global accesses: eight 32-bit words per thread, one whole L2 sector per
+// access, so a row segment takes half the instructions and half the L2 sector writes
+// of 16-byte accesses (two of which would each write half of the same sector). Every
+// address must be 32-byte aligned: the launcher enables them (GemmParams::wide) only
+// when every epilogue pointer and row stride is.
+__device__ __forceinline__ void st_v8(void* ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void ld_nc_v8(const void* ptr, uint32_t (&w)[8]) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(ptr));
+}
+__device__ __forceinline__ void ld_cs_v8(const void* ptr, uint32_t (&w)[8]) {
+  asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(ptr));
+}
+
+// 32 fp32 values -> 32 bf16 (RNE) at dst (64 bytes).
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&f)[32], bool wide) {
+  if (wide) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(f[16 * h + 2 * e], f[16 * h + 2 * e + 1]);
+      st_v8(dst + 16 * h, w);
+    }
+    return;
+  }
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
@@ -102,6 +137,76 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&f)
     w.z = pack_bf16x2(f[8 * v + 4], f[8 * v + 5]);
     w.w = pack_bf16x2(f[8 * v + 6], f[8 * v + 7]);
     d[v] = w;
+  }
+}
+
+// 32 fp32 values at dst (128 bytes).
+__device__ __forceinline__ void store_row32_f32(float* dst, const float (&f)[32], bool wide) {
+  if (wide) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(f[8 * h + e]);
+      st_v8(dst + 8 * h, w);
+    }
+    return;
+  }
+  float4* c4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+}
+
+// f += 32 bf16 values at src (64 bytes, read through the non-coherent path).
+__device__ __forceinline__ void add_row32_bf16(float (&f)[32], const __nv_bfloat16* src, bool wide) {
+  uint32_t u[16];
+  if (wide) {
+    uint32_t a[8], b[8];
+    ld_nc_v8(src, a);
+    ld_nc_v8(src + 16, b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      u[e] = a[e];
+      u[8 + e] = b[e];
+    }
+  } else {
+    const uint4* r4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint4 rv = __ldg(r4 + w);
+      u[4 * w + 0] = rv.x;
+      u[4 * w + 1] = rv.y;
+      u[4 * w + 2] = rv.z;
+      u[4 * w + 3] = rv.w;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    f[2 * e] += bf16_lo(u[e]);
+    f[2 * e + 1] += bf16_hi(u[e]);
+  }
+}
+
+// f += 32 fp32 values at src (128 bytes, streamed: read once).
+__device__ __forceinline__ void add_row32_f32(float (&f)[32], const float* src, bool wide) {
+  if (wide) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t a[8];
+      ld_cs_v8(src + 8 * h, a);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[8 * h + e] += __uint_as_float(a[e]);
+    }
+    return;
+  }
+  const float4* r4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const float4 rv = __ldcs(r4 + w);
+    f[4 * w + 0] += rv.x;
+    f[4 * w + 1] += rv.y;
+    f[4 * w + 2] += rv.z;
+    f[4 * w + 3] += rv.w;
   }
 }
 
@@ -300,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float u = __uint_as_float(uv[j]);
               f[j] = g / (1.0f + __expf(-g)) * u;
             }
-            store_row32(p.C + row * p.ldc + ocol, f);
+            store_row32(p.C + row * p.ldc + ocol, f, p.wide);
             if constexpr (EPI == K_SWIGLU_SAVE) {
               float a1[32], a3[32];
 #pragma unroll
@@ -308,8 +413,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 a1[j] = __uint_as_float(gv[j]);
                 a3[j] = __uint_as_float(uv[j]);
               }
-              store_row32(p.C2 + row * p.ldc2 + nt * BN + c, a1);
-              store_row32(p.C2 + row * p.ldc2 + nt * BN + BN / 2 + c, a3);
+              store_row32(p.C2 + row * p.ldc2 + nt * BN + c, a1, p.wide);
+              store_row32(p.C2 + row * p.ldc2 + nt * BN + BN / 2 + c, a3, p.wide);
             }
           }
         }
@@ -325,45 +430,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             float f[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-            if constexpr (EPI == K_RES_BF16 || EPI == K_RES_BF16_OUT32) {
-              const uint4* r4 = reinterpret_cast<const uint4*>(
-                  static_cast<const __nv_bfloat16*>(p.R) + row * p.ldr + col);
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const uint4 rv = __ldg(r4 + w);
-                f[8 * w + 0] += bf16_lo(rv.x);
-                f[8 * w + 1] += bf16_hi(rv.x);
-                f[8 * w + 2] += bf16_lo(rv.y);
-                f[8 * w + 3] += bf16_hi(rv.y);
-                f[8 * w + 4] += bf16_lo(rv.z);
-                f[8 * w + 5] += bf16_hi(rv.z);
-                f[8 * w + 6] += bf16_lo(rv.w);
-                f[8 * w + 7] += bf16_hi(rv.w);
-              }
-            }
-            if constexpr (EPI == K_RES_F32) {
-              const float4* r4 =
-                  reinterpret_cast<const float4*>(static_cast<const float*>(p.R) + row * p.ldr + col);
-#pragma unroll
-              for (int w = 0; w < 8; ++w) {
-                const float4 rv = __ldcs(r4 + w);
-                f[4 * w + 0] += rv.x;
-                f[4 * w + 1] += rv.y;
-                f[4 * w + 2] += rv.z;
-                f[4 * w + 3] += rv.w;
-              }
-            }
-            if constexpr (EPI == K_RES_BF16_OUT32) {
-              float4* c4 = reinterpret_cast<float4*>(p.C32 + row * p.ldc + col);
-#pragma unroll
-              for (int w = 0; w < 8; ++w)
-                c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
-            }
+            if constexpr (EPI == K_RES_BF16 || EPI == K_RES_BF16_OUT32)
+              add_row32_bf16(f, static_cast<const __nv_bfloat16*>(p.R) + row * p.ldr + col, p.wide);
+            if constexpr (EPI == K_RES_F32)
+              add_row32_f32(f, static_cast<const float*>(p.R) + row * p.ldr + col, p.wide);
+            if constexpr (EPI == K_RES_BF16_OUT32) store_row32_f32(p.C32 + row * p.ldc + col, f, p.wide);
             if constexpr (EPI == K_STORE_F32) {
-              float4* c4 = reinterpret_cast<float4*>(p.C32 + row * p.ldc + col);
-#pragma unroll
-              for (int w = 0; w < 8; ++w)
-                c4[w] = make_float4(f[4 * w + 0], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+              store_row32_f32(p.C32 + row * p.ldc + col, f, p.wide);
             } else if constexpr (EPI == K_SWIGLU_BWD) {
               // f = dG for padded ffn columns col..col+31 (one 128-column group g);
               // silu'(a) = s (1 + a (1 - s)), s = sigmoid(a)
@@ -387,8 +460,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                   d3[8 * w + e] = dg * a1 * sg;
                 }
               }
-              store_row32(p.C + row * p.ldc + c1, d1);
-              store_row32(p.C + row * p.ldc + c3, d3);
+              store_row32(p.C + row * p.ldc + c1, d1, p.wide);
+              store_row32(p.C + row * p.ldc + c3, d3, p.wide);
             } else if constexpr (EPI == K_QKV_SPLIT) {
               // a 32-column chunk never straddles sections (split_hd % 32 == 0); the
               // sections go Q, K, V for each of the N / (3 split_hd) shards in turn,
@@ -397,11 +470,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               const int part = sec % 3;
               const int lc = (sec / 3) * p.split_hd + (col - sec * p.split_hd);
               if (part == 0)
-                store_row32(p.C + row * p.ldc + lc, f);
+                store_row32(p.C + row * p.ldc + lc, f, p.wide);
               else
-                store_row32((part == 1 ? p.split_k : p.split_v) + nat * p.split_ld + lc, f);
+                store_row32((part == 1 ? p.split_k : p.split_v) + nat * p.split_ld + lc, f, p.wide);
             } else {
-              store_row32(p.C + row * p.ldc + col, f);
+              store_row32(p.C + row * p.ldc + col, f, p.wide);
             }
           }
         }
@@ -519,6 +592,19 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
     const long long row_block_bytes = (long long)BM * c.K * 2;
     long long g = b_bytes <= (48ll << 20) ? 1 : (32ll << 20) / row_block_bytes;
     p.group_m = (int)(g < 1 ? 1 : g);
+  }
+  {
+    // 32-byte epilogue accesses need every pointer and row stride the epilogue
+    // touches to be 32-byte aligned (columns move in steps of 32 elements)
+    auto al32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+    bool w = true;
+    if (c.C) w = w && al32(c.C) && (c.ldc * 2) % 32 == 0;
+    if (c.C32) w = w && al32(c.C32) && (c.ldc * 4) % 32 == 0;
+    if (c.C2) w = w && al32(c.C2) && (c.ldc2 * 2) % 32 == 0;
+    if (c.R) w = w && al32(c.R) && (c.ldr * (c.residual_f32 ? 4 : 2)) % 32 == 0;
+    if (c.epi == EPI_QKV_SPLIT)
+      w = w && al32(c.split_k) && al32(c.split_v) && (c.split_ld * 2) % 32 == 0;
+    p.wide = w ? 1 : 0;
   }
   p.status = c.status;
   p.limit_ns = wait_limit_ns();

@@ -265,3 +265,47 @@ def test_7b_projections_sampled_rows():
     G = oracle.widen_bf16(g_bits[rows]).reshape(len(rows), i.D, i.shard_ffn_padded)[:, :, :i.shard_ffn]
     assert_close(f64(out)[rows], G.reshape(len(rows), i.ffn) @ L.f("W2").T, "7b swiglu down")
     L.check_status()
+
+
+# ------------------------------------ 16-byte-aligned (not 32) caller buffers
+
+def _offset16(shape, dtype):
+    """A view of `shape` that starts 16 bytes into a fresh buffer: 16-byte aligned
+    but not 32-byte aligned."""
+    esize = torch.tensor([], dtype=dtype).element_size()
+    n = int(np.prod(shape))
+    base = torch.empty(n + 32 // esize, dtype=dtype, device="cuda")
+    v = base[16 // esize:16 // esize + n].view(shape)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+@pytest.mark.parametrize("name", ["small"])
+def test_epilogue_with_16_byte_aligned_buffers(name):
+    """The GEMM epilogues use 32-byte loads and stores when every buffer they touch is
+    32-byte aligned and 16-byte ones otherwise; both give the same bits."""
+    L = Layer(*SHAPES[name], seed=71)
+    i = L.info
+    o = dev(rand_bits((i.S, i.hidden), 72, std=0.5))
+    r = dev(rand_bits((i.S, i.hidden), 73))
+    out_a, out32_a = L.act(), torch.empty((i.S, i.hidden), dtype=torch.float32, device="cuda")
+    tsp.tsp_o_projection(L.plan, o, L.wpack, r, out_a, L.ws, out32=out32_a)
+    o_b, r_b = _offset16((i.S, i.hidden), torch.bfloat16), _offset16((i.S, i.hidden), torch.bfloat16)
+    o_b.copy_(o)
+    r_b.copy_(r)
+    out_b = _offset16((i.S, i.hidden), torch.bfloat16)
+    out32_b = _offset16((i.S, i.hidden), torch.float32)
+    tsp.tsp_o_projection(L.plan, o_b, L.wpack, r_b, out_b, L.ws, out32=out32_b)
+    # SwiGLU gate/up and the down projection with the fp32 residual
+    g_a = torch.empty((i.S, i.ffn_padded), dtype=torch.bfloat16, device="cuda")
+    g_b = _offset16((i.S, i.ffn_padded), torch.bfloat16)
+    tsp.tsp_swiglu_gate_up(L.plan, out_a, L.wpack, g_a, L.ws)
+    tsp.tsp_swiglu_gate_up(L.plan, out_b, L.wpack, g_b, L.ws)
+    d_a, d_b = L.act(), _offset16((i.S, i.hidden), torch.bfloat16)
+    tsp.tsp_swiglu_down(L.plan, g_a, L.wpack, None, d_a, L.ws, residual32=out32_a)
+    tsp.tsp_swiglu_down(L.plan, g_b, L.wpack, None, d_b, L.ws, residual32=out32_b)
+    L.check_status()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(out32_a, out32_b)
+    assert torch.equal(g_a.view(torch.int16), g_b.view(torch.int16))
+    assert torch.equal(d_a.view(torch.int16), d_b.view(torch.int16))
