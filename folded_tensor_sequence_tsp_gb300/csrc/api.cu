@@ -224,7 +224,7 @@ tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q,
 // in the workspace) when one shard alone would not fill the GPU with CTAs; each
 // head's result is the same bit for bit. lse (optional) as for causal_attention.
 tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, void* o, void* ws,
-                            cudaStream_t s, float* lse) {
+                            cudaStream_t s, float* lse, bool first_group_projected) {
   uint16_t* q = at<uint16_t>(ws, p.ws.qkv);
   uint16_t* kn = at<uint16_t>(ws, p.ws.kn);
   uint16_t* vn = at<uint16_t>(ws, p.ws.vn);
@@ -232,7 +232,9 @@ tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, vo
   const int64_t ld = (int64_t)G * p.Hd;
   for (int k = 0; k < p.D; k += G) {  // broadcast iterations k .. k + G - 1
     // local projections of the G shards (one product), K/V all-gather in the epilogue
-    TSP_TRY(qkv_projection_gathered(p, k, G, xs, wpack, q, kn, vn, ld, ws, s));
+    // (the first group's may already be in the workspace: tsp_layer_fwd_host)
+    if (k > 0 || !first_group_projected)
+      TSP_TRY(qkv_projection_gathered(p, k, G, xs, wpack, q, kn, vn, ld, ws, s));
     TSP_TRY(causal_attention_shards(p, k, G, q, ld, kn, vn, ld, o, ws, s,
                                     lse ? lse + (int64_t)k * p.hpr * p.ld_stat : nullptr));
   }
@@ -350,8 +352,42 @@ tsp_status swiglu_down_rank(const Plan& p, int r, const void* g, const void* wpa
   return launch_gemm(c, s);
 }
 
-// A non-blocking stream per device for the device-to-host copies of
-// tsp_layer_fwd_host, created on first use and kept for the life of the process.
+// The Q/K/V product of the first attention group (shards 0 .. G_att - 1) for rank r's
+// rows only (rows [r B T, (r+1) B T)), into the workspace buffers of attention_shards;
+// K/V rows land at their natural positions. Every output element takes the same K
+// loop as in the product over all rows.
+tsp_status qkv_first_group_rank(const Plan& p, int r, const void* xs, const void* wpack, void* ws,
+                                cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.T, r0 = (int64_t)r * rows;
+  const int64_t ld = (int64_t)p.G_att * p.Hd;
+  GemmCall c{};
+  c.epi = EPI_QKV_SPLIT;
+  c.A = static_cast<const uint16_t*>(xs) + r0 * p.H;
+  c.lda = p.H;
+  c.M = rows;
+  c.B = static_cast<const uint16_t*>(wpack) + p.wp_qkv;
+  c.ldb = p.H;
+  c.b_rows = 3LL * p.H;
+  c.b_row0 = 0;
+  c.N = 3LL * p.G_att * p.Hd;
+  c.K = p.H;
+  c.C = at<uint16_t>(ws, p.ws.qkv) + r0 * ld;
+  c.ldc = ld;
+  c.split_k = at<void>(ws, p.ws.kn);
+  c.split_v = at<void>(ws, p.ws.vn);
+  c.split_ld = ld;
+  c.split_hd = p.Hd;
+  c.zz_C = p.C;
+  c.zz_T = p.T;
+  c.zz_D = p.D;
+  c.zz_B = p.B;
+  c.zz_row0 = r0;
+  c.status = status_of(ws);
+  return launch_gemm(c, s);
+}
+
+// A non-blocking stream per device for the host-link copies of tsp_layer_fwd_host,
+// created on first use and kept for the life of the process.
 tsp_status copy_stream(cudaStream_t* out) {
   static std::mutex mu;
   static cudaStream_t streams[64] = {};
@@ -414,6 +450,47 @@ tsp_status mlp_block_to_host(const Plan& p, const void* hs, const void* wpack,
   }
   if (ready) cudaEventDestroy(ready);
   if (copied) cudaEventDestroy(copied);
+  return st;
+}
+
+// The way in of tsp_layer_fwd_host, overlapped: rank by rank, the copy engine moves
+// the rank's rows of x (two runs of C natural rows per sequence) from pinned host
+// memory to their sharded rows in xs on the copy stream, and `s` runs the first
+// attention group's Q/K/V product on those rows while the next ranks' rows arrive.
+tsp_status shard_in_to_first_group(const Plan& p, const tsp_bf16* x_host, void* xs,
+                                   const void* wpack, void* ws, cudaStream_t s) {
+  cudaStream_t s2 = nullptr;
+  TSP_TRY(copy_stream(&s2));
+  cudaEvent_t start = nullptr, ready = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+  // the copies overwrite xs only after the work enqueued on `s` before this call
+  if (e == cudaSuccess) e = cudaEventRecord(start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s2, start, 0);
+  tsp_status st = e == cudaSuccess ? TSP_OK : cuda_fail(e, "tsp_layer_fwd_host: copy-in events");
+  const size_t run_bytes = (size_t)p.C * p.H * 2;
+  uint16_t* dst = static_cast<uint16_t*>(xs);
+  for (int r = 0; st == TSP_OK && r < p.D; ++r) {
+    for (int b = 0; e == cudaSuccess && b < p.B; ++b) {
+      const int64_t row = ((int64_t)r * p.B + b) * p.T;  // first sharded row of (r, b)
+      const int64_t nat0 = (int64_t)b * p.S + (int64_t)r * p.C;
+      const int64_t nat1 = (int64_t)b * p.S + (int64_t)(2 * p.D - 1 - r) * p.C;
+      e = cudaMemcpyAsync(dst + row * p.H, x_host + nat0 * p.H, run_bytes, cudaMemcpyHostToDevice,
+                          s2);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dst + (row + p.C) * p.H, x_host + nat1 * p.H, run_bytes,
+                            cudaMemcpyHostToDevice, s2);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ready, s2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ready, 0);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "tsp_layer_fwd_host: copy in");
+      break;
+    }
+    st = qkv_first_group_rank(p, r, xs, wpack, ws, s);
+  }
+  if (start) cudaEventDestroy(start);
+  if (ready) cudaEventDestroy(ready);
   return st;
 }
 
@@ -672,23 +749,33 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
   // in one pass over the host link); other host memory goes through staging copies.
   const void* x_dev = mapped_host_alias(x_host);
   void* out_dev = const_cast<void*>(mapped_host_alias(out_host));
-  if (x_dev) {
+  // rank-by-rank overlap needs whole 128-row tiles per rank (then the bits are those of
+  // the products over all rows)
+  const bool by_rank = p.T % 128 == 0;
+  void* o = at<void>(ws, p.ws.o);
+  void* h = at<void>(ws, p.ws.h);
+  float* h32 = at<float>(ws, p.ws.h32);
+  bool projected = false;
+  if (x_dev && by_rank) {
+    // b = shard(x) by the copy engine, rank by rank, under the first Q/K/V product
+    TSP_TRY(shard_in_to_first_group(p, x_host, b, wpack, ws, s));
+    projected = true;
+  } else if (x_dev) {
     TSP_TRY(launch_zigzag_rows(p, x_dev, b, p.H, true, s));  // b = shard(x), read from host
   } else {
     cudaError_t e = cudaMemcpyAsync(a, x_host, bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "tsp_layer_fwd_host: copy in");
     TSP_TRY(launch_zigzag_rows(p, a, b, p.H, true, s));  // b = shard(x)
   }
-  if (out_dev && p.T % 128 == 0) {
-    // h = x + Attn(x); then the MLP, whose output rows go back to the pinned host
-    // buffer rank by rank while the next rank's down projection runs
-    void* h = at<void>(ws, p.ws.h);
-    float* h32 = at<float>(ws, p.ws.h32);
-    TSP_TRY(attention_block(p, b, wpack, b, h, h32, ws, s));
+  // h = x + Attn(x), in bf16 and fp32 (the steps of tsp_layer_fwd)
+  TSP_TRY(attention_shards(p, b, wpack, o, ws, s, nullptr, projected));
+  TSP_TRY(o_projection(p, o, wpack, b, h, h32, ws, s));
+  if (out_dev && by_rank) {
+    // the MLP, whose output rows go back to the pinned host buffer rank by rank while
+    // the next rank's down projection runs
     return mlp_block_to_host(p, h, wpack, h32, a, out_host, ws, s);
   }
-  TSP_TRY(tsp_layer_fwd(plan, static_cast<const tsp_bf16*>(b), wpack, static_cast<tsp_bf16*>(a),
-                        ws, stream));  // a = layer(b)
+  TSP_TRY(mlp_block(p, h, wpack, h32, 1, a, ws, s));  // a = layer(b)
   if (out_dev) {
     TSP_TRY(launch_zigzag_rows(p, a, out_dev, p.H, false, s));  // unshard into host memory
   } else {

@@ -68,6 +68,7 @@ struct GemmParams {
   int split_hd;
   long long zz_C, zz_T;
   int zz_D, zz_B;
+  long long zz_row0;  // sharded row of the launch's first row (a launch over part of the rows)
   __nv_bfloat16* C2;  // K_SWIGLU_SAVE: pre-activations out; K_SWIGLU_BWD: pre-activations in
   long long ldc2;
   int ring_rows;
@@ -381,7 +382,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       long long nat = 0;  // natural token position of this row (K_QKV_SPLIT)
       if constexpr (EPI == K_QKV_SPLIT) {
         // sharded row (rank*B + b)*T + l of a micro-batch -> natural row b*S + pos
-        const long long rb = row / p.zz_T, l = row - rb * p.zz_T;
+        const long long arow = row + p.zz_row0;
+        const long long rb = arow / p.zz_T, l = arow - rb * p.zz_T;
         const long long rank = rb / p.zz_B, b = rb - rank * p.zz_B;
         nat = b * (p.zz_T * p.zz_D) +
               (l < p.zz_C ? rank * p.zz_C + l : (2 * p.zz_D - 1 - rank) * p.zz_C + (l - p.zz_C));
@@ -538,7 +540,7 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
       (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N % (3 * c.split_hd) ||
        c.ldc < c.N / 3 || c.split_ld < c.N / 3 || (c.split_ld % 8) || !aligned16(c.split_k) ||
        !aligned16(c.split_v) || c.zz_C <= 0 || c.zz_T != 2 * c.zz_C || c.zz_D <= 0 ||
-       c.M != c.zz_T * c.zz_D * (c.zz_B > 0 ? c.zz_B : 1)))
+       c.zz_row0 < 0 || c.zz_row0 + c.M > c.zz_T * c.zz_D * (c.zz_B > 0 ? c.zz_B : 1)))
     return fail(TSP_ERR_INVALID_ARG, "gemm: bad Q/K/V split arguments");
   if (c.M > (1ll << 30) || c.N > (1ll << 30) || c.K > (1ll << 30) || c.b_rows > (1ll << 30))
     return fail(TSP_ERR_UNSUPPORTED, "gemm: dimension too large");
@@ -577,6 +579,7 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   p.zz_T = c.zz_T;
   p.zz_D = c.zz_D;
   p.zz_B = c.zz_B > 0 ? c.zz_B : 1;
+  p.zz_row0 = c.zz_row0;
   p.C2 = static_cast<__nv_bfloat16*>(c.C2);
   p.ldc2 = c.ldc2;
   p.ring_rows = (int)c.ring_rows;

@@ -143,6 +143,7 @@ struct GemmCall {
   // zz_B sequences: sharded row (r*zz_B + b)*zz_T + l -> natural row b*S + pos(r, l))
   void* split_k; void* split_v; int64_t split_ld; int64_t split_hd;
   int64_t zz_C, zz_T; int zz_D; int zz_B;
+  int64_t zz_row0;             // sharded row of A's first row (a product over part of the rows)
   int64_t ring_rows;           // rows per rank for the ring K order, 0 = natural order
   int64_t ring_kblocks;        // 64-wide K blocks per shard
   int ring_rank0;              // rank of the launch's first row (ring order)
@@ -205,7 +206,7 @@ tsp_status qkv_projection_gathered(const Plan& p, int k, const void* xs, const v
 // Q/K/V projections and attention of every shard (G_att shards per attention launch),
 // o (and lse when not NULL: [heads][ld_stat]) written for every head.
 tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, void* o, void* ws,
-                            cudaStream_t s, float* lse);
+                            cudaStream_t s, float* lse, bool first_group_projected = false);
 // lse (optional): [heads/D][ld_stat], the rows of shard k's heads.
 tsp_status causal_attention(const Plan& p, int k, const void* qkv, int64_t ld_q, const void* kn,
                             const void* vn, void* o, void* ws, cudaStream_t s,

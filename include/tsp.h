@@ -195,14 +195,17 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
 /*
  * tsp_layer_fwd_host - the whole layer from and to HOST memory in natural token
  * order: x_host [S][H] in, out_host [S][H] out. A page-locked input (pinned or
- * registered, i.e. mapped into the device address space) is read by the zigzag
- * shard kernel directly over the host link, so the copy and the permutation are
- * one pass. A page-locked output comes back rank by rank: the down projection runs
- * per rank on `stream`, and each rank's rows (two runs of C natural rows per
- * sequence) are copied to out_host by the copy engine on a library-owned
- * non-blocking stream of the device (created on first use, kept until exit) while
- * the next ranks compute; `stream` then waits for the last copy. This needs
- * S/D % 128 == 0; otherwise the unshard kernel writes the mapped output directly.
+ * registered, i.e. mapped into the device address space) comes in rank by rank:
+ * the copy engine moves each rank's rows (two runs of C natural rows per sequence)
+ * to their sharded rows on a library-owned non-blocking stream of the device
+ * (created on first use, kept until exit), while `stream` runs the first attention
+ * group's Q/K/V product on the ranks already in. A page-locked output comes back
+ * rank by rank: the down projection runs
+ * per rank on `stream`, and each rank's rows are copied to out_host by the copy
+ * engine on that stream while the next ranks compute; `stream` then waits for the
+ * last copy. Both need S/D % 128 == 0; otherwise the zigzag shard / unshard kernels
+ * read and write the mapped buffers directly, the copy and the permutation in one
+ * pass.
  * The result is the same bit for bit either way. Pageable buffers are staged
  * through cudaMemcpyAsync and the workspace. The call returns once the work is
  * enqueued: synchronise `stream` before reading out_host.
