@@ -43,8 +43,8 @@
 // sequence b see only its own keys.
 //
 // CTA order. The (sequence, head) pairs of the call are cut into groups whose K/V
-// fit together in a share of L2 (one 64K-token head alone; every head of a 16K
-// sequence together). Groups run one after the other, so their K/V stay in L2
+// fit together in a share of L2 (two 64K-token heads; every head of a 16K sequence
+// together). Groups run one after the other, so their K/V stay in L2
 // across their CTAs. Inside a group the CTAs go query block by query block, every
 // pair of the group at each block, and, when the zigzag chunk is a multiple of 256
 // tokens, in decreasing position: the longest blocks of every pair start first
@@ -540,10 +540,10 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.heads = c.heads;
   p.q_blocks = (int)((c.S + QB - 1) / QB);
   {
-    // pairs per group: their K and V (2 * S * d bf16 each) within 48 MB of the L2,
+    // pairs per group: their K and V (2 * S * d bf16 each) within 72 MB of the L2,
     // the pairs split evenly over the fewest groups (no short last group, whose
     // longest blocks would start late)
-    const long long fit0 = (48LL << 20) / (4LL * c.S * c.d);
+    const long long fit0 = (72LL << 20) / (4LL * c.S * c.d);
     const long long fit = fit0 < 1 ? 1 : fit0;
     const long long pairs = (long long)c.heads * B;
     const long long n_groups = (pairs + fit - 1) / fit;

@@ -49,7 +49,7 @@
 // an earlier-issued product reads.
 // A micro-batch of B sequences (rank-major [D][B][T] sharded rows, natural K/V rows
 // b*S + t) pairs every CTA with one (sequence, head); the CTA order is the forward
-// kernel's: (sequence, head) pairs in groups whose K/V fit in 48 MB of L2, and
+// kernel's, with a 48 MB share of L2: (sequence, head) pairs in groups whose K/V fit, and
 // inside a group the owned tiles go tile index by tile index across the pairs, the
 // longest first.
 #include <type_traits>
