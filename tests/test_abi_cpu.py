@@ -164,3 +164,37 @@ def test_batched_plan_sizes_and_limits(lib):
     p2 = tsp.tsp_plan_batched(4, 4096, 2, 1024, 16, 2816)
     assert tsp.tsp_saved_bytes(p2) >= 2 * 4096 * 1024 * 2 + 16 * 2 * 4096 * 4
     assert tsp.tsp_bwd_workspace_bytes(p2) > 2 * (tsp.tsp_bwd_workspace_bytes(one) - 256 * 40)
+
+
+def test_header_is_plain_c_and_the_binding_matches_its_structs(tmp_path):
+    """include/tsp.h compiles as C99 and C++, and the ctypes structures of the binding
+    have the C structures' size and field offsets (a mismatch would corrupt every
+    plan-info read)."""
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.dirname(B.HEADER)
+    fields = {"tsp_plan_info": [f for f, _ in B.PlanInfo._fields_],
+              "tsp_cost": [f for f, _ in B.Cost._fields_]}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "tsp.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'  printf("{st} size %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'  printf("{st} {f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    subprocess.run(["g++", "-fsyntax-only", "-x", "c++", "-I", inc, B.HEADER], check=True,
+                   capture_output=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        st, f, v = ln.split()
+        got[(st, f)] = int(v)
+    for st, cls in (("tsp_plan_info", B.PlanInfo), ("tsp_cost", B.Cost)):
+        assert got[(st, "size")] == ctypes.sizeof(cls), st
+        for f, _ in cls._fields_:
+            assert got[(st, f)] == getattr(cls, f).offset, (st, f)
