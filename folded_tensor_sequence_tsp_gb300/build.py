@@ -9,6 +9,8 @@ flags skips the build when nothing changed.
 from __future__ import annotations
 
 import concurrent.futures
+import contextlib
+import fcntl
 import hashlib
 import os
 import shutil
@@ -49,8 +51,26 @@ def _digest(files, extra) -> str:
     return h.hexdigest()
 
 
+@contextlib.contextmanager
+def _build_lock():
+    """One build at a time per checkout: processes that start together (one per GPU
+    under torchrun) wait here, and the later ones find the library up to date."""
+    os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, "lock"), "w") as fh:
+        fcntl.flock(fh, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(fh, fcntl.LOCK_UN)
+
+
 def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
     """Compile and link libtsp.so if needed; return its path."""
+    with _build_lock():
+        return _build_locked(verbose, force, extra_flags)
+
+
+def _build_locked(verbose: bool, force: bool, extra_flags) -> str:
     srcs = _sources()
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     deps.append(os.path.join(INCLUDE, "tsp.h"))
