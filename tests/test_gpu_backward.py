@@ -336,3 +336,41 @@ def test_7b_attention_step_backward_sampled():
     _, rk, _ = oracle.causal_attention_head_backward_rows(*args, q_block=2048, o_round=bf16_round)
     assert_close_grad(got_k, dk, "7b dk head 0", noise=rk - dk)
     assert_close_grad(got_v, dv, "7b dv head 0")
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_training_step_replays_from_a_cuda_graph(name):
+    """The training pair (tsp_layer_fwd_train + tsp_layer_bwd_saved) enqueues only
+    kernels on the caller's stream, so one training step can be captured into a CUDA
+    graph; replays give the eager output and gradients bit for bit."""
+    L = Layer(*ATT_SHAPES[name], seed=43)
+    ws = L.bwd_workspace()
+    _, g_dev = _dout(L, 44)
+    xs, dout = L.sharded_x(), L.shard(g_dev)
+    i = L.info
+    saved = torch.empty(tsp.tsp_saved_bytes(L.plan), dtype=torch.uint8, device="cuda")
+    out_e, dxs_e = L.act(), L.act()
+    dw_e = torch.empty(i.wpack_elems, dtype=torch.float32, device="cuda")
+    tsp.tsp_layer_fwd_train(L.plan, xs, L.wpack, out_e, saved, ws)
+    tsp.tsp_layer_bwd_saved(L.plan, xs, L.wpack, saved, dout, dxs_e, dw_e, ws)
+    torch.cuda.synchronize()
+    out_g, dxs_g = L.act(), L.act()
+    dw_g = torch.empty_like(dw_e)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            tsp.tsp_layer_fwd_train(L.plan, xs, L.wpack, out_g, saved, ws)
+            tsp.tsp_layer_bwd_saved(L.plan, xs, L.wpack, saved, dout, dxs_g, dw_g, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        out_g.zero_()
+        dxs_g.zero_()
+        dw_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_e.view(torch.int16), out_g.view(torch.int16))
+        assert torch.equal(dxs_e.view(torch.int16), dxs_g.view(torch.int16))
+        assert torch.equal(dw_e, dw_g)
+    L.check_status()
