@@ -352,14 +352,13 @@ tsp_status swiglu_down_rank(const Plan& p, int r, const void* g, const void* wpa
   return launch_gemm(c, s);
 }
 
-// The Q/K/V product of the first attention group (shards 0 .. G_att - 1) for rank r's
-// rows only (rows [r B T, (r+1) B T)), into the workspace buffers of attention_shards;
-// K/V rows land at their natural positions. Every output element takes the same K
-// loop as in the product over all rows.
-tsp_status qkv_first_group_rank(const Plan& p, int r, const void* xs, const void* wpack, void* ws,
-                                cudaStream_t s) {
+// The Q/K/V product of shards 0 .. n - 1 for rank r's rows only (rows [r B T, (r+1) B T)),
+// into q, kn, vn (row stride ld, shard j's columns at j H/D); K/V rows land at their
+// natural positions. Every output element takes the same K loop as in the product over
+// all rows.
+tsp_status qkv_rank(const Plan& p, int r, int n, const void* xs, const void* wpack, void* q,
+                    void* kn, void* vn, int64_t ld, void* ws, cudaStream_t s) {
   const int64_t rows = (int64_t)p.B * p.T, r0 = (int64_t)r * rows;
-  const int64_t ld = (int64_t)p.G_att * p.Hd;
   GemmCall c{};
   c.epi = EPI_QKV_SPLIT;
   c.A = static_cast<const uint16_t*>(xs) + r0 * p.H;
@@ -369,12 +368,12 @@ tsp_status qkv_first_group_rank(const Plan& p, int r, const void* xs, const void
   c.ldb = p.H;
   c.b_rows = 3LL * p.H;
   c.b_row0 = 0;
-  c.N = 3LL * p.G_att * p.Hd;
+  c.N = 3LL * n * p.Hd;
   c.K = p.H;
-  c.C = at<uint16_t>(ws, p.ws.qkv) + r0 * ld;
+  c.C = static_cast<uint16_t*>(q) + r0 * ld;
   c.ldc = ld;
-  c.split_k = at<void>(ws, p.ws.kn);
-  c.split_v = at<void>(ws, p.ws.vn);
+  c.split_k = kn;
+  c.split_v = vn;
   c.split_ld = ld;
   c.split_hd = p.Hd;
   c.zz_C = p.C;
@@ -455,10 +454,12 @@ tsp_status mlp_block_to_host(const Plan& p, const void* hs, const void* wpack,
 
 // The way in of tsp_layer_fwd_host, overlapped: rank by rank, the copy engine moves
 // the rank's rows of x (two runs of C natural rows per sequence) from pinned host
-// memory to their sharded rows in xs on the copy stream, and `s` runs the first
-// attention group's Q/K/V product on those rows while the next ranks' rows arrive.
-tsp_status shard_in_to_first_group(const Plan& p, const tsp_bf16* x_host, void* xs,
-                                   const void* wpack, void* ws, cudaStream_t s) {
+// memory to their sharded rows in xs on the copy stream, and `s` runs the Q/K/V
+// product of shards 0 .. n - 1 on those rows (into q, kn, vn with row stride ld) while
+// the next ranks' rows arrive.
+tsp_status shard_in_with_qkv(const Plan& p, const tsp_bf16* x_host, void* xs, const void* wpack,
+                             int n, void* q, void* kn, void* vn, int64_t ld, void* ws,
+                             cudaStream_t s) {
   cudaStream_t s2 = nullptr;
   TSP_TRY(copy_stream(&s2));
   cudaEvent_t start = nullptr, ready = nullptr;
@@ -487,7 +488,7 @@ tsp_status shard_in_to_first_group(const Plan& p, const tsp_bf16* x_host, void* 
       st = cuda_fail(e, "tsp_layer_fwd_host: copy in");
       break;
     }
-    st = qkv_first_group_rank(p, r, xs, wpack, ws, s);
+    st = qkv_rank(p, r, n, xs, wpack, q, kn, vn, ld, ws, s);
   }
   if (start) cudaEventDestroy(start);
   if (ready) cudaEventDestroy(ready);
@@ -756,9 +757,25 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
   void* h = at<void>(ws, p.ws.h);
   float* h32 = at<float>(ws, p.ws.h32);
   bool projected = false;
-  if (x_dev && by_rank) {
-    // b = shard(x) by the copy engine, rank by rank, under the first Q/K/V product
-    TSP_TRY(shard_in_to_first_group(p, x_host, b, wpack, ws, s));
+  // Q/K/V of every shard fit in buffers that are idle until the O projection (G and
+  // the fp32 h) when the padded ffn is at least twice the hidden width
+  const bool all_shards = x_dev && by_rank && (int64_t)p.NF >= 2LL * p.H;
+  if (all_shards) {
+    // b = shard(x) by the copy engine, rank by rank, under the Q/K/V products of every
+    // shard; then the attention of every group from those buffers
+    uint16_t* qa = at<uint16_t>(ws, p.ws.g);
+    uint16_t* ka = qa + (size_t)p.N * p.H;
+    uint16_t* va = at<uint16_t>(ws, p.ws.h32);
+    TSP_TRY(shard_in_with_qkv(p, x_host, b, wpack, p.D, qa, ka, va, p.H, ws, s));
+    for (int k = 0; k < p.D; k += p.G_att)
+      TSP_TRY(causal_attention_shards(p, k, p.G_att, qa + (size_t)k * p.Hd, p.H,
+                                      ka + (size_t)k * p.Hd, va + (size_t)k * p.Hd, p.H, o,
+                                      ws, s, nullptr));
+  } else if (x_dev && by_rank) {
+    // b = shard(x) by the copy engine, rank by rank, under the first group's Q/K/V
+    const int64_t ld = (int64_t)p.G_att * p.Hd;
+    TSP_TRY(shard_in_with_qkv(p, x_host, b, wpack, p.G_att, at<void>(ws, p.ws.qkv),
+                              at<void>(ws, p.ws.kn), at<void>(ws, p.ws.vn), ld, ws, s));
     projected = true;
   } else if (x_dev) {
     TSP_TRY(launch_zigzag_rows(p, x_dev, b, p.H, true, s));  // b = shard(x), read from host
@@ -768,7 +785,7 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
     TSP_TRY(launch_zigzag_rows(p, a, b, p.H, true, s));  // b = shard(x)
   }
   // h = x + Attn(x), in bf16 and fp32 (the steps of tsp_layer_fwd)
-  TSP_TRY(attention_shards(p, b, wpack, o, ws, s, nullptr, projected));
+  if (!all_shards) TSP_TRY(attention_shards(p, b, wpack, o, ws, s, nullptr, projected));
   TSP_TRY(o_projection(p, o, wpack, b, h, h32, ws, s));
   if (out_dev && by_rank) {
     // the MLP, whose output rows go back to the pinned host buffer rank by rank while

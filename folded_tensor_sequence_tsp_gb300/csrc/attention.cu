@@ -491,13 +491,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int HD>
 tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
+  // each map spans only the call's head columns (heads * d from its base pointer),
+  // with the buffer's row stride: the buffers may hold more columns on either side
   const uint64_t rows = (uint64_t)c.S * (uint64_t)p.B;
-  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, (uint64_t)c.ld_qkv, rows,
-                                    (uint64_t)c.ld_qkv * 2, 64, QT);
+  const uint64_t cols = (uint64_t)c.heads * (uint64_t)c.d;
+  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, cols, rows, (uint64_t)c.ld_qkv * 2, 64, QT);
   if (st != TSP_OK) return st;
-  st = make_tmap_2d_bf16(&tk, c.kn, (uint64_t)c.ld_kv, rows, (uint64_t)c.ld_kv * 2, 64, KT);
+  st = make_tmap_2d_bf16(&tk, c.kn, cols, rows, (uint64_t)c.ld_kv * 2, 64, KT);
   if (st != TSP_OK) return st;
-  st = make_tmap_2d_bf16(&tv, c.vn, (uint64_t)c.ld_kv, rows, (uint64_t)c.ld_kv * 2, 64, KT);
+  st = make_tmap_2d_bf16(&tv, c.vn, cols, rows, (uint64_t)c.ld_kv * 2, 64, KT);
   if (st != TSP_OK) return st;
   auto kernel = attention_tcgen05_kernel<HD>;
   const size_t smem = Geometry<HD>::SMEM;

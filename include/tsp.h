@@ -198,8 +198,10 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
  * registered, i.e. mapped into the device address space) comes in rank by rank:
  * the copy engine moves each rank's rows (two runs of C natural rows per sequence)
  * to their sharded rows on a library-owned non-blocking stream of the device
- * (created on first use, kept until exit), while `stream` runs the first attention
- * group's Q/K/V product on the ranks already in. A page-locked output comes back
+ * (created on first use, kept until exit), while `stream` runs the Q/K/V products on
+ * the ranks already in: of every shard when the padded ffn is at least 2 H (their
+ * Q/K/V then live in workspace buffers that are idle until the O projection), else
+ * of the first attention group. A page-locked output comes back
  * rank by rank: the down projection runs
  * per rank on `stream`, and each rank's rows are copied to out_host by the copy
  * engine on that stream while the next ranks compute; `stream` then waits for the

@@ -109,15 +109,20 @@ def test_output_is_the_same_for_every_D():
         assert_close(outs[D], outs[1], f"D={D} vs D=1", scale=scale, max_abs=atol)
 
 
-@pytest.mark.parametrize("name", ["d3", "ragged"])
+HOST_SHAPES = dict(SHAPES, narrow_ffn=(2, 256, 256, 4, 128))
+
+
+@pytest.mark.parametrize("name", ["d3", "narrow_ffn", "ragged"])
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 def test_host_entry_point_matches_device_path(pinned, name):
-    """A pinned input is read by the shard kernel directly; a pinned output comes back
-    rank by rank through the copy engine while the next ranks' down projections run
-    (d3: S/D = 384 rows per rank) or is written by the unshard kernel directly (ragged:
-    S/D = 100, not a multiple of the 128-row tile); pageable buffers are staged
-    through copies. Every path gives the device path's bits."""
-    L = Layer(*SHAPES[name], seed=8)
+    """Pinned buffers move rank by rank when S/D is a multiple of the 128-row tile: the
+    input through the copy engine under the Q/K/V products (of every shard when the
+    padded ffn is at least 2 H, d3; of the first attention group otherwise,
+    narrow_ffn), the output through the copy engine while the next ranks' down
+    projections run. With S/D = 100 (ragged) the zigzag kernels read and write the
+    mapped buffers directly; pageable buffers are staged through copies. Every path
+    gives the device path's bits."""
+    L = Layer(*HOST_SHAPES[name], seed=8)
     xs = L.sharded_x()
     out = L.act()
     tsp.tsp_layer_fwd(L.plan, xs, L.wpack, out, L.ws)
