@@ -490,6 +490,11 @@ tsp_status shard_in_with_qkv(const Plan& p, const tsp_bf16* x_host, void* xs, co
     }
     st = qkv_rank(p, r, n, xs, wpack, q, kn, vn, ld, ws, s);
   }
+  if (st != TSP_OK && ready) {
+    // on a failure part way, `stream` still waits for the copies already enqueued, so
+    // none of them writes xs after the call has returned its error
+    if (cudaEventRecord(ready, s2) == cudaSuccess) cudaStreamWaitEvent(s, ready, 0);
+  }
   if (start) cudaEventDestroy(start);
   if (ready) cudaEventDestroy(ready);
   return st;
