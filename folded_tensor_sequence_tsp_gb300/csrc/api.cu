@@ -750,9 +750,11 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
   const size_t bytes = (size_t)p.N * p.H * 2;
   void* a = at<void>(ws, p.ws.stage_in);
   void* b = at<void>(ws, p.ws.stage_out);
-  // Page-locked host memory that the runtime maps into the device address space is
-  // read and written by the zigzag kernels themselves (the copy and the permutation
-  // in one pass over the host link); other host memory goes through staging copies.
+  // Page-locked host memory (mapped into the device address space) moves rank by rank
+  // through the copy engine, overlapped with the products, when every rank's rows are
+  // whole 128-row tiles; otherwise the zigzag kernels read and write it directly (the
+  // copy and the permutation in one pass over the host link). Other host memory goes
+  // through staging copies.
   const void* x_dev = mapped_host_alias(x_host);
   void* out_dev = const_cast<void*>(mapped_host_alias(out_host));
   // rank-by-rank overlap needs whole 128-row tiles per rank (then the bits are those of
