@@ -198,3 +198,46 @@ def test_header_is_plain_c_and_the_binding_matches_its_structs(tmp_path):
         assert got[(st, "size")] == ctypes.sizeof(cls), st
         for f, _ in cls._fields_:
             assert got[(st, f)] == getattr(cls, f).offset, (st, f)
+
+
+def test_library_links_and_plans_from_c(tmp_path, lib):
+    """A plain C program includes tsp.h, links libtsp.so and makes the host-only calls
+    (plan, plan info, sizes, cost model, error message) without a GPU."""
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "tsp.h"
+int main(void) {
+  tsp_plan_t plan = 0;
+  if (tsp_plan(8, 65536, 4096, 32, 11008, &plan) != TSP_OK) return 1;
+  tsp_plan_info info;
+  if (tsp_get_plan_info(plan, &info) != TSP_OK) return 2;
+  printf("%d %lld %zu %zu %d\n", info.D, (long long)info.T, tsp_workspace_bytes(plan),
+         tsp_packed_weight_bytes(plan), info.attention_group);
+  tsp_plan_destroy(plan);
+  tsp_plan_t bad = 0;
+  if (tsp_plan(3, 256, 256, 4, 688, &bad) != TSP_ERR_UNSUPPORTED || bad) return 3;
+  printf("%s\n", tsp_last_error());
+  tsp_cost c;
+  if (tsp_cost_model(TSP_SCHEME_TSP, 8, 0, 65536, 4096, 32, 11008, &c) != TSP_OK) return 4;
+  printf("%d %.0f\n", c.devices, c.weight_elems);
+  return 0;
+}
+''')
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(B.library_path())
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(B.HEADER), str(src),
+                    "-L", libdir, "-ltsp", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    p = tsp.tsp_plan(8, 65536, 4096, 32, 11008)
+    D, T, ws, wp, G = out[0].split()
+    assert (int(D), int(T), int(ws), int(wp), int(G)) == (
+        8, 8192, tsp.tsp_workspace_bytes(p), tsp.tsp_packed_weight_bytes(p), p.info.attention_group)
+    assert out[1].startswith("tsp_plan")
+    devices, welems = out[2].split()
+    assert int(devices) == 8 and float(welems) == (4 * 4096 * 4096 + 3 * 4096 * 11008) / 8
