@@ -54,6 +54,7 @@ import numpy as np
 
 __all__ = [
     "widen_bf16",
+    "round_bf16",
     "zigzag_owner",
     "zigzag_forward_index",
     "zigzag_inverse_index",
@@ -93,6 +94,26 @@ def widen_bf16(bits: np.ndarray) -> np.ndarray:
     """bfloat16 bit patterns (uint16) -> float64 values (exact widening)."""
     b = np.ascontiguousarray(bits).astype(np.uint32) << np.uint32(16)
     return b.view(np.float32).astype(np.float64)
+
+
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+def round_bf16(a) -> np.ndarray:
+    """The bfloat16 value nearest to each element, ties to the even significand.
+
+    bfloat16 keeps 8 significant bits and float32's exponent range, so a value
+    whose leading bit has weight 2^e is rounded to a multiple of 2^(e-7); below
+    the normal range (e < -126) the spacing stays 2^-133. Rounded straight from
+    float64 (no intermediate float32). Used only for the stored-precision variant
+    of the layer (`store=round_bf16` below): the values a bf16-in / fp32-accumulate
+    implementation hands from one product to the next are bf16.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)                      # a = m 2^e, 1/2 <= |m| < 1: leading bit 2^(e-1)
+    step = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    r = np.round(a / step) * step           # np.round: halves go to the even integer
+    return np.where(np.abs(r) > BF16_MAX, np.copysign(np.inf, a), r)
 
 
 # --------------------------------------------------------------------------
@@ -156,11 +177,14 @@ def rank_positions(S: int, D: int) -> np.ndarray:
 # gathered K/V; FlashAttention computes exact softmax attention)
 # --------------------------------------------------------------------------
 
-def causal_attention_head(q, k, v, q_pos, k_pos) -> np.ndarray:
+def causal_attention_head(q, k, v, q_pos, k_pos, store=None) -> np.ndarray:
     """One head: out_i = sum_j p_ij v_j / sum_j p_ij over keys with k_pos[j] <= q_pos[i].
 
     p_ij = exp(s_ij - max_j s_ij), s_ij = q_i . k_j / sqrt(d). q: [nq, d],
-    k, v: [nk, d], positions int arrays. float64 throughout.
+    k, v: [nk, d], positions int arrays. float64 throughout. With `store` (e.g.
+    round_bf16) the weights p_ij pass through it before the product with v (the sum
+    in the denominator stays unrounded), as when P is handed to the P V product in
+    bf16.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -171,15 +195,16 @@ def causal_attention_head(q, k, v, q_pos, k_pos) -> np.ndarray:
     s = np.where(visible, s, -np.inf)
     m = s.max(axis=1, keepdims=True)
     p = np.exp(s - m)
-    return (p @ v) / p.sum(axis=1, keepdims=True)
+    return ((p if store is None else store(p)) @ v) / p.sum(axis=1, keepdims=True)
 
 
 def multihead_causal_attention(q, k, v, heads: int, q_pos=None, k_pos=None,
-                               q_block: int = 1024) -> np.ndarray:
+                               q_block: int = 1024, store=None) -> np.ndarray:
     """Split the H columns into `heads` heads of d = H/heads and attend per head.
 
     q: [nq, H], k, v: [nk, H]; positions default to 0..n-1. Queries are taken in
-    blocks of `q_block` rows only to bound the score matrix's memory.
+    blocks of `q_block` rows only to bound the score matrix's memory. `store` as in
+    causal_attention_head.
     """
     nq, H = q.shape
     nk = k.shape[0]
@@ -191,18 +216,23 @@ def multihead_causal_attention(q, k, v, heads: int, q_pos=None, k_pos=None,
         c = slice(j * d, (j + 1) * d)
         for lo in range(0, nq, q_block):
             r = slice(lo, min(nq, lo + q_block))
-            out[r, c] = causal_attention_head(q[r, c], k[:, c], v[:, c], q_pos[r], k_pos)
+            out[r, c] = causal_attention_head(q[r, c], k[:, c], v[:, c], q_pos[r], k_pos, store)
     return out
 
 
-def attention_block(x, Wq, Wk, Wv, Wo, heads: int, rows=None) -> np.ndarray:
+def attention_block(x, Wq, Wk, Wv, Wo, heads: int, rows=None, store=None) -> np.ndarray:
     """Causal multi-head self-attention of a plain (unsharded) layer, no residual.
 
     Attn(x) = concat_j softmax(Q_j K_j^T / sqrt(d) + causal) V_j  W_O^T with
     Q = x W_Q^T, K = x W_K^T, V = x W_V^T. All inputs float64 arrays.
     With `rows` (sorted positions) only those output rows are computed; K/V are
     projected for positions 0..max(rows), one head at a time.
+    With `store` (a function of an array, e.g. round_bf16), the values one product
+    hands to the next are passed through it: Q, K and V, the softmax weights P before
+    P V, and the per-head attention output before W_O. Without it everything stays
+    float64.
     """
+    st = (lambda a: a) if store is None else store
     S, H = x.shape
     d = H // heads
     if rows is None:
@@ -214,13 +244,13 @@ def attention_block(x, Wq, Wk, Wv, Wo, heads: int, rows=None) -> np.ndarray:
     o = np.empty((rows.size, H), dtype=np.float64)
     for j in range(heads):
         c = slice(j * d, (j + 1) * d)
-        qh = xq @ Wq[c].T
-        kh = xk @ Wk[c].T
-        vh = xk @ Wv[c].T
+        qh = st(xq @ Wq[c].T)
+        kh = st(xk @ Wk[c].T)
+        vh = st(xk @ Wv[c].T)
         for lo in range(0, rows.size, 1024):
             r = slice(lo, min(rows.size, lo + 1024))
-            o[r, c] = causal_attention_head(qh[r], kh, vh, rows[r], np.arange(kmax))
-    return o @ Wo.T
+            o[r, c] = causal_attention_head(qh[r], kh, vh, rows[r], np.arange(kmax), store)
+    return st(o) @ Wo.T
 
 
 # --------------------------------------------------------------------------
@@ -237,9 +267,13 @@ def swiglu_gate(h, W1, W3) -> np.ndarray:
     return silu(h @ W1.T) * (h @ W3.T)
 
 
-def swiglu_mlp(h, W1, W3, W2) -> np.ndarray:
-    """MLP(h) = (silu(h W1^T) * (h W3^T)) W2^T, no residual."""
-    return swiglu_gate(h, W1, W3) @ W2.T
+def swiglu_mlp(h, W1, W3, W2, store=None) -> np.ndarray:
+    """MLP(h) = (silu(h W1^T) * (h W3^T)) W2^T, no residual.
+
+    With `store`, the gated activation G is passed through it before W2 (the value
+    the first product hands to the second)."""
+    G = swiglu_gate(h, W1, W3)
+    return (G if store is None else store(G)) @ W2.T
 
 
 def qkv_projection_shard(x, Wq, Wk, Wv, k: int, D: int) -> np.ndarray:
@@ -257,17 +291,31 @@ def qkv_projection_shard(x, Wq, Wk, Wv, k: int, D: int) -> np.ndarray:
 # Whole layer, plain and TSP-sharded
 # --------------------------------------------------------------------------
 
-def layer_forward(x, W: dict, heads: int, rows=None) -> dict:
+def layer_forward(x, W: dict, heads: int, rows=None, store=None) -> dict:
     """Plain layer: h = x + Attn(x); out = h + MLP(h). float64 arrays in and out.
 
     W holds Wq, Wk, Wv, Wo, W1, W3, W2 (float64, [out, in]). With `rows` only those
     token rows are returned (attention still sees every earlier token).
     Returns {"attn", "h", "mlp", "out"} for the requested rows.
+
+    With `store` (e.g. round_bf16) the layer is evaluated at a stated storage
+    precision: every value handed from one product to the next goes through it
+    (Q, K, V, the attention output before W_O, the MLP's input h and the gated
+    activation G), while sums, the softmax and both residual adds stay float64.
+    This is the bf16-in / fp32-accumulate layer with exact accumulation. Without
+    `store` the layer is exact.
     """
-    attn = attention_block(x, W["Wq"], W["Wk"], W["Wv"], W["Wo"], heads, rows=rows)
+    if store is None:
+        attn = attention_block(x, W["Wq"], W["Wk"], W["Wv"], W["Wo"], heads, rows=rows)
+    else:
+        attn = attention_block(x, W["Wq"], W["Wk"], W["Wv"], W["Wo"], heads, rows=rows,
+                               store=store)
     xr = x if rows is None else x[np.asarray(rows)]
     h = xr + attn
-    mlp = swiglu_mlp(h, W["W1"], W["W3"], W["W2"])
+    if store is None:
+        mlp = swiglu_mlp(h, W["W1"], W["W3"], W["W2"])
+    else:
+        mlp = swiglu_mlp(store(h), W["W1"], W["W3"], W["W2"], store=store)
     return {"attn": attn, "h": h, "mlp": mlp, "out": h + mlp}
 
 
@@ -354,12 +402,13 @@ def unshard_tokens_batched(xs: np.ndarray, D: int) -> np.ndarray:
     return flat[zigzag_forward_index_batched(D * T, D, B)].reshape((B, D * T) + rest)
 
 
-def layer_forward_batched(x, W: dict, heads: int, rows=None) -> dict:
+def layer_forward_batched(x, W: dict, heads: int, rows=None, store=None) -> dict:
     """The plain layer on each sequence of a micro-batch x [B, S, H] on its own.
 
     Returns layer_forward's dict with a leading batch axis ([B, S or len(rows), H]).
+    `store` as in layer_forward.
     """
-    res = [layer_forward(x[b], W, heads, rows=rows) for b in range(x.shape[0])]
+    res = [layer_forward(x[b], W, heads, rows=rows, store=store) for b in range(x.shape[0])]
     return {key: np.stack([r[key] for r in res]) for key in res[0]}
 
 
@@ -420,7 +469,7 @@ def silu_grad(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round=None):
+def causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round=None, store=None):
     """Gradients (dq, dk, dv) of one head of causal_attention_head for output grad do.
 
     With P the softmax weights and O = P v: dv = P^T do, dP = do v^T,
@@ -429,6 +478,10 @@ def causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round=None):
     With `o_round` (a function of an array), Delta is rowsum(do * o_round(O)): the
     gradient obtained from a rounded copy of the output, such as the bf16 output a
     kernel stores and reads back.
+    With `store` (e.g. round_bf16), the two values the products take from the
+    element-wise step pass through it: P before dv = P^T do, and dS before dq and dk;
+    and the output whose rounded copy forms Delta is the stored forward's
+    (causal_attention_head with the same `store`: P rounded before P v).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -438,28 +491,33 @@ def causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round=None):
     s = (q @ k.T) / math.sqrt(d)
     visible = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]
     s = np.where(visible, s, -np.inf)
-    p = np.exp(s - s.max(axis=1, keepdims=True))
-    p /= p.sum(axis=1, keepdims=True)
-    dv = p.T @ do
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    l = e.sum(axis=1, keepdims=True)
+    p = e / l
+    dv = (p if store is None else store(p)).T @ do
     dp = do @ v.T
     if o_round is None:
         delta = (dp * p).sum(axis=1, keepdims=True)
     else:
-        delta = (do * o_round(p @ v)).sum(axis=1, keepdims=True)
+        o = ((e if store is None else store(e)) @ v) / l
+        delta = (do * o_round(o)).sum(axis=1, keepdims=True)
     ds = p * (dp - delta)
+    if store is not None:
+        ds = store(ds)
     dq = ds @ k / math.sqrt(d)
     dk = ds.T @ q / math.sqrt(d)
     return dq, dk, dv
 
 
 def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_rows,
-                                        q_block: int = 1024, o_round=None):
+                                        q_block: int = 1024, o_round=None, store=None):
     """dq of the query rows q_rows and (dk, dv) of the key rows k_rows of one head.
 
     The same quantities as causal_attention_head_backward, for sequences whose full
     score matrix does not fit: dq_i depends on query i's own softmax only; dk_j and
     dv_j sum over every query that sees key j, so all queries are visited, `q_block`
-    rows at a time, each with its softmax over all of its visible keys.
+    rows at a time, each with its softmax over all of its visible keys. `o_round` and
+    `store` as in causal_attention_head_backward.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -469,7 +527,7 @@ def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_row
     q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
     d = q.shape[1]
     dq = causal_attention_head_backward(q[q_rows], k, v, q_pos[q_rows], k_pos, do[q_rows],
-                                        o_round)[0]
+                                        o_round, store)[0]
     dk = np.zeros((k_rows.size, d))
     dv = np.zeros((k_rows.size, d))
     for lo in range(0, q.shape[0], q_block):
@@ -477,20 +535,24 @@ def causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do, q_rows, k_row
         s = (q[r] @ k.T) / math.sqrt(d)
         visible = k_pos[None, :] <= q_pos[r, None]
         s = np.where(visible, s, -np.inf)
-        p = np.exp(s - s.max(axis=1, keepdims=True))
-        p /= p.sum(axis=1, keepdims=True)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        l = e.sum(axis=1, keepdims=True)
+        p = e / l
         dp = do[r] @ v.T
         if o_round is None:
             delta = (dp * p).sum(axis=1, keepdims=True)
         else:
-            delta = (do[r] * o_round(p @ v)).sum(axis=1, keepdims=True)
+            o = ((e if store is None else store(e)) @ v) / l
+            delta = (do[r] * o_round(o)).sum(axis=1, keepdims=True)
         ds = p * (dp - delta)
+        if store is not None:
+            ds, p = store(ds), store(p)
         dk += ds[:, k_rows].T @ q[r] / math.sqrt(d)
         dv += p[:, k_rows].T @ do[r]
     return dq, dk, dv
 
 
-def swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None) -> dict:
+def swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None, store=None) -> dict:
     """Gradients of MLP(h) = G W2^T, G = silu(A1) * A3, A1 = h W1^T, A3 = h W3^T,
     for the output gradient dmlp (the block alone, no residual):
 
@@ -501,59 +563,80 @@ def swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None) -> dict:
     Returns {"dh", "dW1", "dW3", "dW2"}. With `rows`, dh holds those token rows only
     (each needs every ffn column of its own row); with `ffn_cols`, dW1 and dW3 hold
     those rows and dW2 those columns only (each needs every token).
+    With `store` (e.g. round_bf16), the values handed from one product to the next
+    pass through it: the kept pre-activations A1 and A3 (dA1 and dA3 are formed from
+    the stored ones), G before dW2, and dA1, dA3 before the products that take them.
     """
     h = np.asarray(h, dtype=np.float64)
     dmlp = np.asarray(dmlp, dtype=np.float64)
+    st = (lambda a: a) if store is None else store
     r = slice(None) if rows is None else np.asarray(rows)
     c = slice(None) if ffn_cols is None else np.asarray(ffn_cols)
     A1, A3 = h[r] @ W1.T, h[r] @ W3.T
+    A1s, A3s = st(A1), st(A3)
     dG = dmlp[r] @ W2
-    out = {"dh": (dG * A3 * silu_grad(A1)) @ W1 + (dG * silu(A1)) @ W3}
+    out = {"dh": st(dG * A3s * silu_grad(A1s)) @ W1 + st(dG * silu(A1s)) @ W3}
     A1, A3 = h @ W1[c].T, h @ W3[c].T
+    A1s, A3s = st(A1), st(A3)
     dG = dmlp @ W2[:, c]
-    out["dW2"] = dmlp.T @ (silu(A1) * A3)
-    out["dW1"] = (dG * A3 * silu_grad(A1)).T @ h
-    out["dW3"] = (dG * silu(A1)).T @ h
+    out["dW2"] = dmlp.T @ st(silu(A1) * A3)
+    out["dW1"] = st(dG * A3s * silu_grad(A1s)).T @ h
+    out["dW3"] = st(dG * silu(A1s)).T @ h
     return out
 
 
-def attention_block_backward(x, Wq, Wk, Wv, Wo, heads: int, dattn) -> dict:
+def attention_block_backward(x, Wq, Wk, Wv, Wo, heads: int, dattn, store=None) -> dict:
     """Gradients of attention_block (no residual) for the output gradient dattn.
 
     With Q = x Wq^T, K = x Wk^T, V = x Wv^T, O the per-head causal attention and
     Attn = O Wo^T: dWo = dattn^T O, dO = dattn Wo, the per-head attention backward
     gives dQ, dK, dV, then dWq = dQ^T x (likewise K, V) and
     dx = dQ Wq + dK Wk + dV Wv. Returns {"dx", "dWq", "dWk", "dWv", "dWo"}.
+    With `store` (e.g. round_bf16), the values handed between products pass through
+    it: Q, K, V and O (as attention_block stores them: P rounded before P V), dO,
+    the per-head P and dS (Delta formed from the stored O), and dQ, dK, dV.
     """
     S, H = x.shape
     d = H // heads
-    Q, K, V = x @ Wq.T, x @ Wk.T, x @ Wv.T
-    O = multihead_causal_attention(Q, K, V, heads)
+    st = (lambda a: a) if store is None else store
+    Q, K, V = st(x @ Wq.T), st(x @ Wk.T), st(x @ Wv.T)
+    O = st(multihead_causal_attention(Q, K, V, heads, store=store))
     g = {"dWo": dattn.T @ O}
-    dO = dattn @ Wo
+    dO = st(dattn @ Wo)
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
     pos = np.arange(S)
     for j in range(heads):
         c = slice(j * d, (j + 1) * d)
         dQ[:, c], dK[:, c], dV[:, c] = causal_attention_head_backward(
-            Q[:, c], K[:, c], V[:, c], pos, pos, dO[:, c])
+            Q[:, c], K[:, c], V[:, c], pos, pos, dO[:, c], o_round=store, store=store)
+    dQ, dK, dV = st(dQ), st(dK), st(dV)
     g["dWq"], g["dWk"], g["dWv"] = dQ.T @ x, dK.T @ x, dV.T @ x
     g["dx"] = dQ @ Wq + dK @ Wk + dV @ Wv
     return g
 
 
-def layer_backward(x, W: dict, heads: int, dout) -> dict:
+def layer_backward(x, W: dict, heads: int, dout, store=None) -> dict:
     """Gradients of out = h + MLP(h), h = x + Attn(x), for the output gradient dout.
 
     The residual paths add the identity: dh = dout + (MLP backward of dout) and
     dx = dh + (attention backward of dh). Returns {"dx", "dWq", "dWk", "dWv",
     "dWo", "dW1", "dW3", "dW2"} (float64, the shapes of x and of the weights).
+    With `store` (e.g. round_bf16), the forward values are those of
+    layer_forward(..., store=store), the MLP backward takes the stored h, the
+    attention backward the stored dh, and each block stores as its own backward
+    says; both residual sums stay float64.
     """
     Wq, Wk, Wv, Wo = W["Wq"], W["Wk"], W["Wv"], W["Wo"]
-    h = x + attention_block(x, Wq, Wk, Wv, Wo, heads)
-    m = swiglu_mlp_backward(h, W["W1"], W["W3"], W["W2"], dout)
-    dh = dout + m["dh"]
-    a = attention_block_backward(x, Wq, Wk, Wv, Wo, heads, dh)
+    if store is None:
+        h = x + attention_block(x, Wq, Wk, Wv, Wo, heads)
+        m = swiglu_mlp_backward(h, W["W1"], W["W3"], W["W2"], dout)
+        dh = dout + m["dh"]
+        a = attention_block_backward(x, Wq, Wk, Wv, Wo, heads, dh)
+    else:
+        h = x + attention_block(x, Wq, Wk, Wv, Wo, heads, store=store)
+        m = swiglu_mlp_backward(store(h), W["W1"], W["W3"], W["W2"], dout, store=store)
+        dh = dout + m["dh"]
+        a = attention_block_backward(x, Wq, Wk, Wv, Wo, heads, store(dh), store=store)
     g = {"dW1": m["dW1"], "dW3": m["dW3"], "dW2": m["dW2"]}
     for n in ("dWq", "dWk", "dWv", "dWo"):
         g[n] = a[n]
@@ -561,14 +644,15 @@ def layer_backward(x, W: dict, heads: int, dout) -> dict:
     return g
 
 
-def layer_backward_batched(x, W: dict, heads: int, dout) -> dict:
+def layer_backward_batched(x, W: dict, heads: int, dout, store=None) -> dict:
     """Gradients of the sum over a micro-batch x [B, S, H] for dout [B, S, H].
 
     The sequences are independent: each sequence's input gradient is its own
     layer_backward's, and a weight gradient is the sum of the sequences' weight
     gradients. Returns layer_backward's keys, "dx" with a leading batch axis.
+    `store` as in layer_backward.
     """
-    res = [layer_backward(x[b], W, heads, dout[b]) for b in range(x.shape[0])]
+    res = [layer_backward(x[b], W, heads, dout[b], store=store) for b in range(x.shape[0])]
     g = {k: sum(r[k] for r in res) for k in res[0] if k != "dx"}
     g["dx"] = np.stack([r["dx"] for r in res])
     return g

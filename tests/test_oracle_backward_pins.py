@@ -206,10 +206,58 @@ def check_attention_gradient_sums(o):
     assert np.abs(dv.sum(axis=0) - do.sum(axis=0)).max() < 1e-12
 
 
+def check_stored_backward(o):
+    """The stored-precision backward (store=...): with the identity it is the exact
+    backward; with a coarse grid (multiples of 1/16, so that each rounding point
+    matters) the head's and the MLP's gradients equal library computations that
+    round at the stated points: torch's softmax and autograd (scores -> dS,
+    silu(a1) * a3 -> dA1, dA3), rounded where the docstrings say."""
+    ident = lambda a: a
+    S, H, heads, F = 10, 8, 2, 6
+    x, dout = _rand((S, H), 40), _rand((S, H), 41)
+    W = _weights(H, F, 42)
+    ex, st = o.layer_backward(x, W, heads, dout), o.layer_backward(x, W, heads, dout, store=ident)
+    for k in ex:
+        assert np.abs(ex[k] - st[k]).max() < 1e-12, k
+    coarse = lambda a: np.round(np.asarray(a) * 16) / 16
+    # one head: P rounded before dv, dS before dq and dk (Delta from the exact O)
+    n, d = 9, 4
+    q, k, v, do = (_rand((n, d), s) for s in (43, 44, 45, 46))
+    pos = np.arange(n)
+    dq, dk, dv = o.causal_attention_head_backward(q, k, v, pos, pos, do, store=coarse)
+    ts = (torch.from_numpy(q) @ torch.from_numpy(k).T / math.sqrt(d)).requires_grad_()
+    mask = torch.ones(n, n, dtype=torch.bool).tril()
+    P = torch.softmax(ts.masked_fill(~mask, float("-inf")), dim=1)
+    (P @ torch.from_numpy(v)).backward(torch.from_numpy(do))
+    dS = coarse(ts.grad.numpy())
+    assert np.abs(dv - coarse(P.detach().numpy()).T @ do).max() < 1e-12
+    assert np.abs(dq - dS @ k / math.sqrt(d)).max() < 1e-12
+    assert np.abs(dk - dS.T @ q / math.sqrt(d)).max() < 1e-12
+    # MLP: A1, A3 kept rounded; dA1, dA3 from them, rounded; G rounded before dW2
+    h, dy = coarse(_rand((S, H), 47)), _rand((S, H), 48)
+    g = o.swiglu_mlp_backward(h, W["W1"], W["W3"], W["W2"], dy, store=coarse)
+    a1 = torch.from_numpy(coarse(h @ W["W1"].T)).requires_grad_()
+    a3 = torch.from_numpy(coarse(h @ W["W3"].T)).requires_grad_()
+    (torch.nn.functional.silu(a1) * a3).backward(torch.from_numpy(dy @ W["W2"]))
+    dA1, dA3 = coarse(a1.grad.numpy()), coarse(a3.grad.numpy())
+    G = coarse((torch.nn.functional.silu(torch.from_numpy(h @ W["W1"].T))
+                * torch.from_numpy(h @ W["W3"].T)).numpy())
+    assert np.abs(g["dh"] - (dA1 @ W["W1"] + dA3 @ W["W3"])).max() < 1e-12
+    assert np.abs(g["dW1"] - dA1.T @ h).max() < 1e-12
+    assert np.abs(g["dW3"] - dA3.T @ h).max() < 1e-12
+    assert np.abs(g["dW2"] - dy.T @ G).max() < 1e-12
+    # the sampled forms take the same rounding
+    qr, kr = np.array([0, 4, 8]), np.array([0, 3, 8])
+    sq, sk, sv = o.causal_attention_head_backward_rows(q, k, v, pos, pos, do, qr, kr, q_block=4,
+                                                       store=coarse)
+    assert np.abs(sq - dq[qr]).max() < 1e-12 and np.abs(sk - dk[kr]).max() < 1e-12
+    assert np.abs(sv - dv[kr]).max() < 1e-12
+
+
 PINS = [check_layer_backward_vs_autograd, check_attention_backward_finite_differences,
         check_closed_forms, check_tsp_backward_equals_plain, check_block_backwards_vs_autograd,
         check_sampled_backwards, check_attention_gradient_sums, check_rounded_output_delta,
-        check_batched_backward_vs_autograd]
+        check_batched_backward_vs_autograd, check_stored_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -224,7 +272,7 @@ def _mutant(**overrides):
     return ns
 
 
-def _attn_bwd_no_rowsum(q, k, v, q_pos, k_pos, do, o_round=None):
+def _attn_bwd_no_rowsum(q, k, v, q_pos, k_pos, do, o_round=None, store=None):
     d = q.shape[1]
     s = (q @ k.T) / math.sqrt(d)
     s = np.where(np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
@@ -234,33 +282,54 @@ def _attn_bwd_no_rowsum(q, k, v, q_pos, k_pos, do, o_round=None):
     return ds @ k / math.sqrt(d), ds.T @ q / math.sqrt(d), p.T @ do
 
 
-def _layer_bwd_wrong_dw2(x, W, heads, dout):
-    g = oracle.layer_backward(x, W, heads, dout)
+def _layer_bwd_wrong_dw2(x, W, heads, dout, store=None):
+    g = oracle.layer_backward(x, W, heads, dout, store=store)
     g["dW2"] = g["dW2"] * 2.0
     return g
 
 
-def _mlp_bwd_no_w3_path(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None):
-    g = oracle.swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows, ffn_cols)
+def _mlp_bwd_no_w3_path(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None, store=None):
+    g = oracle.swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows, ffn_cols, store=store)
     r = slice(None) if rows is None else rows
     g["dh"] = g["dh"] - ((dmlp[r] @ W2) * oracle.silu(h[r] @ W1.T)) @ W3
     return g
 
 
 def _attn_rows_unnormalised(q, k, v, q_pos, k_pos, do, q_rows, k_rows, q_block=1024,
-                            o_round=None):
+                            o_round=None, store=None):
     dq, dk, dv = oracle.causal_attention_head_backward_rows(q, k, v, q_pos, k_pos, do,
-                                                            q_rows, k_rows, q_block, o_round)
+                                                            q_rows, k_rows, q_block, o_round, store)
     return dq, dk, dv * 1.5
 
 
-def _batched_bwd_mean(x, W, heads, dout):
+def _batched_bwd_mean(x, W, heads, dout, store=None):
     """Mistake: weight gradients averaged over the micro-batch instead of summed."""
-    g = oracle.layer_backward_batched(x, W, heads, dout)
+    g = oracle.layer_backward_batched(x, W, heads, dout, store=store)
     return {k: (v if k == "dx" else v / x.shape[0]) for k, v in g.items()}
 
 
+def _attn_bwd_store_skips_p(q, k, v, q_pos, k_pos, do, o_round=None, store=None):
+    """Mistake: dv from the unrounded P (the stored form rounds P before dv)."""
+    dq, dk, _ = oracle.causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round, store)
+    _, _, dv = oracle.causal_attention_head_backward(q, k, v, q_pos, k_pos, do, o_round)
+    return dq, dk, dv
+
+
+def _mlp_bwd_store_late(h, W1, W3, W2, dmlp, rows=None, ffn_cols=None, store=None):
+    """Mistake: dA1, dA3 formed from the unrounded pre-activations."""
+    if store is None:
+        return oracle.swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows, ffn_cols)
+    g = oracle.swiglu_mlp_backward(h, W1, W3, W2, dmlp, rows, ffn_cols)
+    r = slice(None) if rows is None else rows
+    A1, A3 = h[r] @ W1.T, h[r] @ W3.T
+    dG = dmlp[r] @ W2
+    g["dh"] = store(dG * A3 * oracle.silu_grad(A1)) @ W1 + store(dG * oracle.silu(A1)) @ W3
+    return g
+
+
 MUTANTS = {
+    "stored backward: dv from the unrounded P": dict(causal_attention_head_backward=_attn_bwd_store_skips_p),
+    "stored backward: MLP pre-activations unrounded": dict(swiglu_mlp_backward=_mlp_bwd_store_late),
     "micro-batch weight gradients averaged": dict(layer_backward_batched=_batched_bwd_mean),
     "MLP dh without the W3 path": dict(swiglu_mlp_backward=_mlp_bwd_no_w3_path),
     "sampled attention dv scaled": dict(causal_attention_head_backward_rows=_attn_rows_unnormalised),

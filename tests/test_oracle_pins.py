@@ -302,12 +302,102 @@ def check_batched_sequences_independent(o):
     assert not np.allclose(a["out"][1], c["out"][1])
 
 
+def check_qkv_projection_shard(o):
+    # The local projections of broadcast iteration k are x times the rows of heads
+    # group k of W_Q, W_K and W_V ([TSP] s2, attention layers: a packed shard per
+    # iteration). Pinned to torch's linear on the whole matrices, read per head:
+    # the Q | K | V blocks of shard k are heads k*h/D .. (k+1)*h/D - 1 of the full
+    # projections, in that order, and the shards together cover every head once.
+    S, heads, d = 11, 8, 4
+    H = heads * d
+    x = _rand((S, H), 90)
+    Wq, Wk, Wv = (_rand((H, H), s, 0.3) for s in (91, 92, 93))
+    tx = torch.from_numpy(x)
+    full = {n: torch.nn.functional.linear(tx, torch.from_numpy(w)).view(S, heads, d).numpy()
+            for n, w in (("q", Wq), ("k", Wk), ("v", Wv))}
+    for D in (1, 2, 4, 8):
+        hpr = heads // D
+        seen = np.zeros(heads, int)
+        for k in range(D):
+            got = o.qkv_projection_shard(x, Wq, Wk, Wv, k, D)
+            assert got.shape == (S, 3 * H // D)
+            blocks = got.reshape(S, 3, hpr, d)
+            for b, n in enumerate("qkv"):
+                want = full[n][:, k * hpr:(k + 1) * hpr]
+                assert np.abs(blocks[:, b] - want).max() < 1e-12, (D, k, n)
+            seen[k * hpr:(k + 1) * hpr] += 1
+        assert (seen == 1).all()
+
+
+def check_round_bf16(o):
+    # Against torch's float32 -> bfloat16 conversion (round to nearest even) on
+    # values float32 holds exactly, exact ties among them.
+    v = np.random.default_rng(94).standard_normal(20000).astype(np.float32) * 5
+    v[:8] = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 0.0, 2.0 ** -130,
+             -(2.0 ** -128) * 1.5, 255.5 * 2 ** -7, 3.0e38]
+    want = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.round_bf16(v.astype(np.float64)), want)
+    # float64 values that float32 cannot hold: the result is a bfloat16 value and no
+    # bfloat16 value is nearer (brute force over the two neighbours of its bit
+    # pattern); on a tie the pattern is even.
+    a = np.random.default_rng(95).standard_normal(20000) * np.exp2(
+        np.random.default_rng(96).integers(-20, 20, 20000))
+    r = o.round_bf16(a)
+    bits = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.int64)
+    assert np.array_equal(o.widen_bf16(bits.astype(np.uint16)), r)     # on the grid
+    for nb in (bits - 1, bits + 1):
+        other = o.widen_bf16((nb & 0xFFFF).astype(np.uint16))
+        da, db = np.abs(a - r), np.abs(a - other)
+        assert (da <= db).all()
+        assert (bits[da == db] % 2 == 0).all()
+
+
+def check_stored_layer_vs_torch(o):
+    # The stored-precision layer (store = round_bf16) against a torch composition
+    # that casts to bfloat16 at the same points: Q, K, V, the softmax weights before
+    # P V (exp(s - max), unnormalised; the normalising sum unrounded), the attention
+    # output before W_O, the MLP input and the gated activation.
+    S, H, heads, F = 24, 16, 4, 12
+    x = _rand((S, H), 97)
+    W = _rand_weights(H, F, 98)
+    got = o.layer_forward(x, W, heads, store=o.round_bf16)
+    th = {k: torch.from_numpy(v) for k, v in W.items()}
+    tx = torch.from_numpy(x)
+    b = lambda t: t.to(torch.bfloat16).to(torch.float64)
+    d = H // heads
+    sp = lambda a: a.view(S, heads, d).transpose(0, 1)
+    q, k, v = sp(b(tx @ th["Wq"].T)), sp(b(tx @ th["Wk"].T)), sp(b(tx @ th["Wv"].T))
+    sc = (q @ k.transpose(1, 2) / math.sqrt(d)).masked_fill(
+        ~torch.ones(S, S, dtype=torch.bool).tril(), float("-inf"))
+    e = torch.exp(sc - sc.amax(dim=-1, keepdim=True))
+    att = (b(e) @ v) / e.sum(dim=-1, keepdim=True)
+    attn = b(att.transpose(0, 1).reshape(S, H)) @ th["Wo"].T
+    h = tx + attn
+    hb = b(h)
+    g = b(torch.nn.functional.silu(hb @ th["W1"].T) * (hb @ th["W3"].T))
+    out = h + g @ th["W2"].T
+    assert np.abs(got["attn"] - attn.numpy()).max() < 1e-12
+    assert np.abs(got["h"] - h.numpy()).max() < 1e-12
+    assert np.abs(got["out"] - out.numpy()).max() < 1e-12
+    # the identity as `store` is the exact layer; rounding moves it by little
+    exact = o.layer_forward(x, W, heads)
+    same = o.layer_forward(x, W, heads, store=lambda a: a)
+    for key in exact:
+        assert np.array_equal(same[key], exact[key]), key
+    assert 0 < np.abs(got["out"] - exact["out"]).max() < 0.05 * np.abs(exact["out"]).max()
+    # sampled rows of the stored layer are the full stored layer's rows
+    rows = np.array([0, 5, 23])
+    part = o.layer_forward(x, W, heads, rows=rows, store=o.round_bf16)
+    assert np.abs(part["out"] - got["out"][rows]).max() < 1e-12
+
+
 PINS = [check_zigzag_golden, check_zigzag_bruteforce, check_zigzag_balance,
         check_shard_roundtrip, check_attention_hand_example, check_attention_vs_sdpa,
         check_attention_closed_forms, check_attention_positions, check_silu_and_mlp,
         check_layer_vs_torch, check_sampled_rows, check_tsp_equals_plain, check_rank_counts,
         check_zigzag_batched_golden, check_zigzag_batched_layout, check_tsp_batched_equals_plain,
-        check_batched_sequences_independent]
+        check_batched_sequences_independent, check_qkv_projection_shard, check_round_bf16,
+        check_stored_layer_vs_torch]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -346,6 +436,37 @@ def _one_long_sequence(x, W, heads, D):
     return {k: v.reshape(B, S, H) for k, v in r.items()}
 
 
+def _qkv_shifted(x, Wq, Wk, Wv, k, D):
+    """Mistake: the heads group of shard k starts one head late (wraps at the end)."""
+    heads = 8 if Wq.shape[0] % 8 == 0 else 1
+    d = Wq.shape[0] // heads
+    roll = lambda w: np.roll(w, -d, axis=0)
+    return oracle.qkv_projection_shard(x, roll(Wq), roll(Wk), roll(Wv), k, D)
+
+
+def _round_ties_away(a):
+    """Mistake: halves rounded away from zero instead of to even."""
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)
+    step = np.ldexp(1.0, np.maximum(e, -125) - 8)
+    return np.sign(a) * np.floor(np.abs(a) / step + 0.5) * step
+
+
+def _stored_layer_mutant(residual_rounded=False, round_g=True):
+    def f(x, W, heads, rows=None, store=None):
+        if store is None:
+            return oracle.layer_forward(x, W, heads, rows=rows)
+        attn = oracle.attention_block(x, W["Wq"], W["Wk"], W["Wv"], W["Wo"], heads, rows=rows,
+                                      store=store)
+        xr = x if rows is None else x[np.asarray(rows)]
+        h = xr + attn
+        hb = store(h)
+        mlp = oracle.swiglu_mlp(hb, W["W1"], W["W3"], W["W2"], store=store if round_g else None)
+        base = hb if residual_rounded else h
+        return {"attn": attn, "h": h, "mlp": mlp, "out": base + mlp}
+    return f
+
+
 def _run_pins(o):
     failed = 0
     for pin in PINS:
@@ -370,6 +491,16 @@ MUTANTS = {
     "micro-batch sequence-major": dict(zigzag_forward_index_batched=lambda S, D, B: (
         np.arange(B)[:, None] * S + oracle.zigzag_forward_index(S, D)[None, :]).reshape(-1)),
     "micro-batch as one sequence": dict(tsp_layer_forward_batched=_one_long_sequence),
+    "qkv blocks K|Q|V": dict(qkv_projection_shard=lambda x, Wq, Wk, Wv, k, D: (
+        oracle.qkv_projection_shard(x, Wk, Wq, Wv, k, D))),
+    "qkv heads group off by one head": dict(qkv_projection_shard=_qkv_shifted),
+    "qkv shard of W^T": dict(qkv_projection_shard=lambda x, Wq, Wk, Wv, k, D: (
+        oracle.qkv_projection_shard(x, Wq.T, Wk.T, Wv.T, k, D))),
+    "bf16 rounding truncates": dict(round_bf16=lambda a: oracle.widen_bf16(
+        (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16))),
+    "bf16 rounding ties away": dict(round_bf16=_round_ties_away),
+    "stored h in the residual": dict(layer_forward=_stored_layer_mutant(residual_rounded=True)),
+    "stored layer skips G": dict(layer_forward=_stored_layer_mutant(round_g=False)),
 }
 
 
