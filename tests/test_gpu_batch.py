@@ -17,8 +17,8 @@ import torch
 
 import oracle
 import tsp_inputs
-from gpu_util import (Layer, assert_close, assert_close_grad, bits, dev, f64, layer_row_scale,
-                      layer_tolerance, rand_bits)
+from gpu_util import (Layer, assert_close, assert_close_grad, bits, dev, f64, rand_bits,
+                      stored_layer, stored_mlp)
 
 tsp = pytest.importorskip("folded_tensor_sequence_tsp_gb300")
 pytestmark = pytest.mark.gpu
@@ -81,15 +81,13 @@ def test_batched_layer_matches_oracle(name):
     W = L.weights64()
     x = L.f("x")
     ref = oracle.layer_forward_batched(x, W, L.info.heads)
+    st = oracle.layer_forward_batched(x, W, L.info.heads, store=oracle.round_bf16)
     got_attn, got_mlp, got_out = (f64(_unshard(L, t)) for t in (attn, mlp, out))
     for b in range(batch):
-        assert_close(got_attn[b], ref["attn"][b], f"{name} seq {b} attn")
+        assert_close(got_attn[b], ref["attn"][b], f"batch {name} seq {b} attn", ref=st["attn"][b])
         want = oracle.swiglu_mlp(x[b], W["W1"], W["W3"], W["W2"])
-        G = oracle.swiglu_gate(x[b], W["W1"], W["W3"])
-        assert_close(got_mlp[b], want, f"{name} seq {b} mlp", scale=layer_row_scale(want, G))
-        s, atol = layer_tolerance(ref["out"][b], oracle.swiglu_gate(ref["h"][b], W["W1"], W["W3"]),
-                                  ref["h"][b], W)
-        assert_close(got_out[b], ref["out"][b], f"{name} seq {b} out", scale=s, max_abs=atol)
+        assert_close(got_mlp[b], want, f"batch {name} seq {b} mlp", ref=stored_mlp(x[b], W))
+        assert_close(got_out[b], ref["out"][b], f"batch {name} seq {b} out", ref=st["out"][b])
 
 
 @pytest.mark.parametrize("name", ["tiny-b3", "small-b2"])
@@ -148,9 +146,8 @@ def test_7b_16k_micro_batch_of_4_sampled_rows():
         rows = tsp_inputs.sample_rows(cfg.S, 64, cfg.seed + b)
         got = f64(nat[b][torch.from_numpy(rows).cuda()])
         ref = oracle.layer_forward(x[b], W, cfg.heads, rows=rows)
-        s, atol = layer_tolerance(ref["out"], oracle.swiglu_gate(ref["h"], W["W1"], W["W3"]),
-                                  ref["h"], W)
-        assert_close(got, ref["out"], f"7b-16k seq {b} out rows", scale=s, max_abs=atol)
+        st = stored_layer(x[b], W, cfg.heads, rows=rows)
+        assert_close(got, ref["out"], f"7b-16k x4 seq {b} out rows", ref=st["out"])
 
 
 # ---------------------------------------------------------------- backward
@@ -171,13 +168,14 @@ def test_batched_layer_backward_matches_oracle(name):
     tsp.tsp_layer_bwd(L.plan, L.sharded_x(), L.wpack, L.shard(g_dev), dxs, dwpack, ws)
     L.check_status()
     got = L.grads(dwpack)
-    ref = oracle.layer_backward_batched(L.f("x"), L.weights64(), L.info.heads,
-                                        oracle.widen_bf16(g_bits))
+    args = (L.f("x"), L.weights64(), L.info.heads, oracle.widen_bf16(g_bits))
+    ref = oracle.layer_backward_batched(*args)
+    st = oracle.layer_backward_batched(*args, store=oracle.round_bf16)
     dx = f64(_unshard(L, dxs))
     for b in range(batch):
-        assert_close_grad(dx[b], ref["dx"][b], f"{name} seq {b} dx")
+        assert_close_grad(dx[b], ref["dx"][b], f"batch bwd {name} seq {b} dx", ref=st["dx"][b])
     for k in ("dWq", "dWk", "dWv", "dWo", "dW1", "dW3", "dW2"):
-        assert_close_grad(got[k], ref[k], f"{name} {k}")
+        assert_close_grad(got[k], ref[k], f"batch bwd {name} {k}", ref=st[k], bf16_out=False)
 
 
 @pytest.mark.parametrize("name", ["tiny-b3", "small-b2"])
@@ -213,7 +211,7 @@ def test_batched_backward_equals_one_call_per_sequence(name):
         dsum += dw1
     want = dsum.double().cpu().numpy()
     have = dwpack.double().cpu().numpy()
-    assert_close_grad(have, want, f"{name} packed weight gradients")
+    assert_close_grad(have, want, f"batch bwd {name} packed weight gradients", bf16_out=False)
 
 
 def test_batched_training_pair_equals_layer_fwd_and_bwd():
