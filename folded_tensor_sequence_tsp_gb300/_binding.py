@@ -28,6 +28,8 @@ __all__ = [
     "tsp_last_error", "tsp_bwd_workspace_bytes", "tsp_mlp_bwd", "tsp_unpack_weight_grads",
     "tsp_attention_bwd", "tsp_layer_bwd", "tsp_causal_attention_lse", "tsp_causal_attention_bwd",
     "SCHEMES", "tsp_cost_model", "tsp_cost_model_batched", "tsp_cost_max_batch", "tsp_saved_bytes", "tsp_layer_fwd_train", "tsp_layer_bwd_saved",
+    "tsp_rank_shard_bytes", "tsp_pack_rank_shard", "tsp_rank_qkv", "tsp_rank_kv_gather",
+    "tsp_rank_attention", "tsp_rank_o_accumulate", "tsp_rank_mlp_step",
 ]
 
 TSP_OK, TSP_ERR_INVALID_ARG, TSP_ERR_UNSUPPORTED, TSP_ERR_CUDA, TSP_ERR_TIMEOUT = range(5)
@@ -118,6 +120,13 @@ _SIGS = {
     "tsp_saved_bytes": (ctypes.c_size_t, [_P]),
     "tsp_layer_fwd_train": (_I, [_P] * 7),
     "tsp_layer_bwd_saved": (_I, [_P] * 9),
+    "tsp_rank_shard_bytes": (_I, [_P, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]),
+    "tsp_pack_rank_shard": (_I, [_P, _I] + [_P] * 10),
+    "tsp_rank_qkv": (_I, [_P] * 7),
+    "tsp_rank_kv_gather": (_I, [_P] * 5),
+    "tsp_rank_attention": (_I, [_P, _I] + [_P] * 6),
+    "tsp_rank_o_accumulate": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "tsp_rank_mlp_step": (_I, [_P] * 9),
 }
 
 
@@ -531,3 +540,76 @@ def tsp_cost_max_batch(scheme: str, D: int, S: int, hidden: int, heads: int, ffn
                                              layers, float(mem_bytes), ctypes.byref(out)),
            "tsp_cost_max_batch")
     return int(out.value)
+
+
+# ------------------------------------------------------------ rank-local steps
+
+def tsp_rank_shard_bytes(plan: Plan):
+    """(attention part, MLP part) bytes of one rank's weight shard."""
+    a, m = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().tsp_rank_shard_bytes(plan.handle, ctypes.byref(a), ctypes.byref(m)),
+           "tsp_rank_shard_bytes")
+    return a.value, m.value
+
+
+def tsp_pack_rank_shard(plan, k, Wq, Wk, Wv, Wo, W1, W3, W2, attn_shard, mlp_shard, stream=None):
+    i = plan.info
+    H, F = i.hidden, i.ffn
+    a, m = tsp_rank_shard_bytes(plan)
+    _check(load_library().tsp_pack_rank_shard(
+        plan.handle, int(k), _dev(Wq, "Wq", H * H), _dev(Wk, "Wk", H * H), _dev(Wv, "Wv", H * H),
+        _dev(Wo, "Wo", H * H), _dev(W1, "W1", F * H), _dev(W3, "W3", F * H), _dev(W2, "W2", H * F),
+        _dev(attn_shard, "attn_shard", a // 2), _dev(mlp_shard, "mlp_shard", m // 2),
+        _stream(stream)), "tsp_pack_rank_shard")
+
+
+def tsp_rank_qkv(plan, xs_r, attn_shard, q_r, kv_r, ws, stream=None):
+    i = plan.info
+    T, Hd = i.T, i.shard_hidden
+    _check(load_library().tsp_rank_qkv(
+        plan.handle, _dev(xs_r, "xs_r", T * i.hidden),
+        _dev(attn_shard, "attn_shard", tsp_rank_shard_bytes(plan)[0] // 2),
+        _dev(q_r, "q_r", T * Hd), _dev(kv_r, "kv_r", 2 * T * Hd), _ws_status(ws),
+        _stream(stream)), "tsp_rank_qkv")
+
+
+def tsp_rank_kv_gather(plan, kv_all, kn, vn, stream=None):
+    i = plan.info
+    n = i.S * i.shard_hidden
+    _check(load_library().tsp_rank_kv_gather(
+        plan.handle, _dev(kv_all, "kv_all", 2 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _stream(stream)), "tsp_rank_kv_gather")
+
+
+def tsp_rank_attention(plan, r, q_r, kn, vn, o_r, ws, stream=None):
+    i = plan.info
+    n, nr = i.S * i.shard_hidden, i.T * i.shard_hidden
+    _check(load_library().tsp_rank_attention(
+        plan.handle, int(r), _dev(q_r, "q_r", nr), _dev(kn, "kn", n), _dev(vn, "vn", n),
+        _dev(o_r, "o_r", nr), _ws_status(ws), _stream(stream)), "tsp_rank_attention")
+
+
+def tsp_rank_o_accumulate(plan, o_r, attn_shard, residual, acc_r, h_r, ws, stream=None):
+    """acc_r = residual + o_r W_O,k^T (fp32), h_r = bf16(acc_r). residual: bf16 x_r or
+    fp32 (acc_r itself)."""
+    i = plan.info
+    n = i.T * i.hidden
+    f32 = residual is not None and residual.dtype == torch.float32
+    _check(load_library().tsp_rank_o_accumulate(
+        plan.handle, _dev(o_r, "o_r", i.T * i.shard_hidden),
+        _dev(attn_shard, "attn_shard", tsp_rank_shard_bytes(plan)[0] // 2),
+        _dev(residual, "residual", n, torch.float32 if f32 else torch.bfloat16), int(f32),
+        _dev(acc_r, "acc_r", n, torch.float32), _dev(h_r, "h_r", n), _ws_status(ws),
+        _stream(stream)), "tsp_rank_o_accumulate")
+
+
+def tsp_rank_mlp_step(plan, h_r, mlp_shard, residual32, acc_r, out_r, g_r, ws, stream=None):
+    i = plan.info
+    n = i.T * i.hidden
+    fq = (i.shard_ffn_padded + 127) // 128 * 128
+    _check(load_library().tsp_rank_mlp_step(
+        plan.handle, _dev(h_r, "h_r", n),
+        _dev(mlp_shard, "mlp_shard", tsp_rank_shard_bytes(plan)[1] // 2),
+        _dev(residual32, "residual32", n, torch.float32), _dev(acc_r, "acc_r", n, torch.float32),
+        _dev(out_r, "out_r", n), _dev(g_r, "g_r", i.T * fq), _ws_status(ws), _stream(stream)),
+        "tsp_rank_mlp_step")

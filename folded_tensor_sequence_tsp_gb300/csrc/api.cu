@@ -231,6 +231,7 @@ tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, vo
   const int G = p.G_att;
   const int64_t ld = (int64_t)G * p.Hd;
   for (int k = 0; k < p.D; k += G) {  // broadcast iterations k .. k + G - 1
+    NvtxRange range("tsp attention shards %d..%d", k, k + G - 1);
     // local projections of the G shards (one product), K/V all-gather in the epilogue
     // (the first group's may already be in the workspace: tsp_layer_fwd_host)
     if (k > 0 || !first_group_projected)
@@ -244,6 +245,7 @@ tsp_status attention_shards(const Plan& p, const void* xs, const void* wpack, vo
 // out = o W_O^T (+ residual, bf16); with out32 also the fp32 value of out.
 tsp_status o_projection(const Plan& p, const void* o, const void* wpack, const void* residual,
                         void* out, void* out32, void* ws, cudaStream_t s) {
+  NvtxRange range("tsp O projection (shards accumulated)");
   GemmCall c{};
   c.epi = residual ? EPI_RESIDUAL : EPI_STORE;
   c.A = o;
@@ -317,6 +319,7 @@ tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, con
 
 tsp_status mlp_block(const Plan& p, const void* hs, const void* wpack, const void* residual,
                      int residual_f32, void* out, void* ws, cudaStream_t s) {
+  NvtxRange range("tsp MLP ring (gate/up, down in ring order)");
   void* g = at<void>(ws, p.ws.g);
   TSP_TRY(swiglu_gate_up(p, hs, wpack, g, ws, s));
   return swiglu_down(p, g, wpack, residual, residual_f32, out, ws, s);

@@ -92,6 +92,11 @@ struct AttParams {
   int q_blocks;        // 256-row query blocks per (sequence, head)
   int group;           // (sequence, head) pairs whose CTAs interleave
   int natural_order;
+  // the call's query rows: sharded rows [q_row0, q_end) of the sequence's [D][T]
+  // layout (all S rows, or one rank's T rows); the Q, O and lse buffers hold them
+  // from their row 0 on (buffer row = sharded row - q_row0)
+  long long q_row0, q_end;
+  int q_local;         // 1: one rank's rows (longest-first = last local block first)
   float scale_log2;
   DevStatus* status;
   unsigned long long limit_ns;
@@ -149,12 +154,12 @@ __device__ __forceinline__ float exp_tile(const float (&sc)[KT], uint32_t p_tmem
 
 // Number of 128-key tiles the query rows [r0, r0 + QT) need (0 if none is a row).
 __device__ __forceinline__ int tiles_needed(long long r0, const AttParams& p) {
-  if (r0 >= p.S) return 0;
+  if (r0 >= p.q_end) return 0;
   long long mx = 0;
   if (p.natural_order) {
     mx = row_pos(r0 + QT - 1, p.C, p.T, p.D);
   } else {
-    const long long last = min(r0 + QT, p.S);
+    const long long last = min(r0 + QT, p.q_end);
     for (long long r = r0; r < last; ++r) mx = max(mx, row_pos(r, p.C, p.T, p.D));
   }
   return (int)(mx / KT) + 1;
@@ -201,9 +206,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair = g * p.group + (rem - blk * in_g);
   const int head = pair % p.heads;
   const int seq = pair / p.heads;
-  const long long row0 = p.natural_order
-                             ? zig_row((long long)(p.q_blocks - 1 - blk) * QB, p.C, p.T, p.D)
-                             : (long long)blk * QB;
+  const long long row0 =
+      p.q_local ? p.q_row0 + (p.natural_order ? p.q_end - p.q_row0 - (long long)(blk + 1) * QB
+                                              : (long long)blk * QB)
+      : p.natural_order ? zig_row((long long)(p.q_blocks - 1 - blk) * QB, p.C, p.T, p.D)
+                        : (long long)blk * QB;
   const int n_a = tiles_needed(row0, p);
   const int n_b = tiles_needed(row0 + QT, p);
   const int n_tiles = max(n_a, n_b);
@@ -224,8 +231,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     // a 128-row tile's rows are contiguous in the micro-batch layout too
-    out_row0[0] = batch_row(row0, seq, p);
-    out_row0[1] = batch_row(row0 + QT, seq, p);
+    out_row0[0] = batch_row(row0, seq, p) - p.q_row0;
+    out_row0[1] = batch_row(row0 + QT, seq, p) - p.q_row0;
     *out_head = head;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           tma_load_2d(sQ + t * G::TILE_BYTES + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b,
-                      (int)batch_row(row0 + t * QT, seq, p));
+                      (int)(batch_row(row0 + t * QT, seq, p) - p.q_row0));
         tma_load_2d(sK0 + b * BOX_BYTES, &tmK, q_full, col_q + 64 * b, kv_row0);
       }
       int last[STAGES];
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;         // TMEM lane quarter of this warp
     const int r_local = q * 32 + lane;
     const long long vrow = row0 + t * QT + r_local;  // row in the sequence's own layout
-    const bool row_ok = vrow < p.S;
+    const bool row_ok = vrow < p.q_end;
     // S < 2^30 (checked at launch): positions fit in int
     const int pos = row_ok ? (int)row_pos(vrow, p.C, p.T, p.D) : -1;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
@@ -495,7 +502,8 @@ tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t st
   // with the buffer's row stride: the buffers may hold more columns on either side
   const uint64_t rows = (uint64_t)c.S * (uint64_t)p.B;
   const uint64_t cols = (uint64_t)c.heads * (uint64_t)c.d;
-  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, cols, rows, (uint64_t)c.ld_qkv * 2, 64, QT);
+  const uint64_t q_rows = p.q_local ? (uint64_t)(p.q_end - p.q_row0) : rows;
+  tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, cols, q_rows, (uint64_t)c.ld_qkv * 2, 64, QT);
   if (st != TSP_OK) return st;
   st = make_tmap_2d_bf16(&tk, c.kn, cols, rows, (uint64_t)c.ld_kv * 2, 64, KT);
   if (st != TSP_OK) return st;
@@ -540,7 +548,15 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.D = c.D;
   p.B = B;
   p.heads = c.heads;
-  p.q_blocks = (int)((c.S + QB - 1) / QB);
+  // the call's query rows: every rank's, or rank-local rows [q_row0, q_row0 + q_rows)
+  const bool local = c.q_rows > 0;
+  if (local && (B > 1 || c.q_row0 < 0 || c.q_row0 + c.q_rows > c.S))
+    return fail(TSP_ERR_INVALID_ARG, "attention: query rows outside the sequence, or a "
+                                     "row range with a micro-batch");
+  p.q_local = local ? 1 : 0;
+  p.q_row0 = local ? c.q_row0 : 0;
+  p.q_end = local ? c.q_row0 + c.q_rows : c.S;
+  p.q_blocks = (int)((p.q_end - p.q_row0 + QB - 1) / QB);
   {
     // pairs per group: their K and V (2 * S * d bf16 each) within 72 MB of the L2,
     // the pairs split evenly over the fewest groups (no short last group, whose
@@ -551,7 +567,9 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
     const long long n_groups = (pairs + fit - 1) / fit;
     p.group = (int)((pairs + n_groups - 1) / n_groups);
   }
-  p.natural_order = (c.C % QB == 0) ? 1 : 0;
+  // last-row position = tile maximum; for a rank's rows also whole 256-row blocks
+  p.natural_order = (c.C % QB == 0 && (!local || (c.q_row0 % QB == 0 && c.q_rows % QB == 0)))
+                        ? 1 : 0;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)c.d);
   p.status = c.status;
   p.limit_ns = wait_limit_ns();

@@ -122,6 +122,7 @@ tsp_status weight_grad(const Plan& p, const void* A, int64_t M, const void* B, i
 tsp_status mlp_backward(const Plan& p, const void* hs, const void* wpack, const void* dmlp,
                         const void* residual, void* dhs, void* dhs32, float* dwpack, void* ws,
                         cudaStream_t s) {
+  NvtxRange range("tsp MLP backward (ring in reverse)");
   void* g = at<void>(ws, p.ws.g);
   void* a13 = at<void>(ws, p.ws.a13);
   TSP_TRY(swiglu_gate_up_save(p, hs, wpack, g, a13, ws, s));
@@ -219,6 +220,7 @@ tsp_status attention_recompute(const Plan& p, const void* xs, const void* wpack,
   uint16_t* va = at<uint16_t>(ws, p.ws.va);
   const int64_t shard = p.N * p.Hd;
   for (int k = 0; k < p.D; ++k) {
+    NvtxRange range("tsp attention recompute shard %d of %d", k, p.D);
     TSP_TRY(qkv_projection_gathered(p, k, xs, wpack, qa + k * shard, ka + k * shard,
                                     va + k * shard, ws, s));
     if (o)
@@ -253,10 +255,12 @@ tsp_status attention_backward(const Plan& p, const void* xs, const void* wpack, 
   TSP_TRY(weight_grad(p, dattn, p.H, o, p.H, dwpack + p.wp_o, p.H, ws, s));  // dWo = dattn^T o
   TSP_TRY(launch_attention_delta(o, dob, p.H, p.heads, p.d, p.N, delta, p.ld_stat, s));
   const int64_t shard = p.N * p.Hd;
-  for (int k = 0; k < p.D; ++k)  // broadcast iteration k, in reverse
+  for (int k = 0; k < p.D; ++k) {  // broadcast iteration k, in reverse
+    NvtxRange range("tsp attention backward shard %d of %d", k, p.D);
     TSP_TRY(attention_shard_backward(p, k, qa + k * shard, ka + k * shard, va + k * shard, dob,
                                      lse + (int64_t)k * p.hpr * p.ld_stat,
                                      delta + (int64_t)k * p.hpr * p.ld_stat, dqkv, ws, s));
+  }
   TSP_TRY(qkv_dgrad(p, dqkv, wpack, residual32, dxs, ws, s));
   return weight_grad(p, dqkv, 3LL * p.H, xs, p.H, dwpack + p.wp_qkv, p.H, ws, s);  // dW_QKV
 }

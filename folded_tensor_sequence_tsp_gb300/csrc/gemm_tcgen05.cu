@@ -50,6 +50,8 @@ enum Kind {
   K_STORE_F32 = 6,      // C32 = acc (fp32): weight gradients
   K_SWIGLU_SAVE = 7,    // as K_SWIGLU, and the pre-activations (A1|A3 tiles) to C2
   K_SWIGLU_BWD = 8,     // acc = dG; with A1/A3 from C2: dA1|dA3 to C in C2's packed order
+  K_RES_F32_OUT32 = 9,  // C = bf16(acc + R), C32 = acc + R (fp32), R fp32 (may be C32:
+                        // each element is read, then written, by one thread)
 };
 
 struct GemmParams {
@@ -434,9 +436,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
             if constexpr (EPI == K_RES_BF16 || EPI == K_RES_BF16_OUT32)
               add_row32_bf16(f, static_cast<const __nv_bfloat16*>(p.R) + row * p.ldr + col, p.wide);
-            if constexpr (EPI == K_RES_F32)
+            if constexpr (EPI == K_RES_F32 || EPI == K_RES_F32_OUT32)
               add_row32_f32(f, static_cast<const float*>(p.R) + row * p.ldr + col, p.wide);
-            if constexpr (EPI == K_RES_BF16_OUT32) store_row32_f32(p.C32 + row * p.ldc + col, f, p.wide);
+            if constexpr (EPI == K_RES_BF16_OUT32 || EPI == K_RES_F32_OUT32)
+              store_row32_f32(p.C32 + row * p.ldc + col, f, p.wide);
             if constexpr (EPI == K_STORE_F32) {
               store_row32_f32(p.C32 + row * p.ldc + col, f, p.wide);
             } else if constexpr (EPI == K_SWIGLU_BWD) {
@@ -534,8 +537,10 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
   if ((c.epi == EPI_SWIGLU_SAVE || c.epi == EPI_SWIGLU_BWD) &&
       (!c.C2 || !aligned16(c.C2) || (c.ldc2 % 8) || c.N % 128))
     return fail(TSP_ERR_INVALID_ARG, "gemm: SwiGLU pre-activation buffer missing or misaligned");
-  if (c.C32 && c.epi != EPI_STORE_F32 && (c.epi != EPI_RESIDUAL || c.residual_f32))
-    return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 output needs a bf16 residual");
+  if (c.C32 && c.epi != EPI_STORE_F32 && c.epi != EPI_RESIDUAL)
+    return fail(TSP_ERR_INVALID_ARG, "gemm: an fp32 copy of the output needs the residual epilogue");
+  if (c.C32 && c.residual_f32 && (c.a_mn || c.b_mn))
+    return fail(TSP_ERR_INVALID_ARG, "gemm: fp32 residual with an fp32 output: K-major operands only");
   if (c.epi == EPI_QKV_SPLIT &&
       (!c.split_k || !c.split_v || c.split_hd <= 0 || c.split_hd % 32 || c.N % (3 * c.split_hd) ||
        c.ldc < c.N / 3 || c.split_ld < c.N / 3 || (c.split_ld % 8) || !aligned16(c.split_k) ||
@@ -622,6 +627,8 @@ tsp_status launch_gemm(const GemmCall& c, cudaStream_t stream) {
       case EPI_SWIGLU_SAVE: return launch_epi<K_SWIGLU_SAVE, false, false>(ta, tb, p, grid, stream);
       case EPI_QKV_SPLIT: return launch_epi<K_QKV_SPLIT, false, false>(ta, tb, p, grid, stream);
       case EPI_RESIDUAL:
+        if (c.residual_f32 && c.C32)
+          return launch_epi<K_RES_F32_OUT32, false, false>(ta, tb, p, grid, stream);
         if (c.residual_f32) return launch_epi<K_RES_F32, false, false>(ta, tb, p, grid, stream);
         if (c.C32) return launch_epi<K_RES_BF16_OUT32, false, false>(ta, tb, p, grid, stream);
         return launch_epi<K_RES_BF16, false, false>(ta, tb, p, grid, stream);

@@ -3,7 +3,9 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
+#include <stdio.h>
 #include <stdint.h>
 
 #include <initializer_list>
@@ -135,7 +137,8 @@ struct GemmCall {
   void* C; int64_t ldc;
   const void* R; int64_t ldr;  // residual (EPI_RESIDUAL): bf16, or fp32 if residual_f32
   int residual_f32;
-  void* C32;                   // optional fp32 copy of the output (EPI_RESIDUAL, bf16 residual), row stride ldc
+  void* C32;                   // optional fp32 copy of the output (EPI_RESIDUAL), row stride ldc;
+                               // with an fp32 residual it may be the residual itself (in place)
   // EPI_QKV_SPLIT: the N = 3 n split_hd columns are Q | K | V of n shards in turn (shard j's
   // columns land at offset j split_hd of each destination); Q rows go to C (ldc),
   // K and V rows to split_k / split_v (row stride split_ld) at the natural token
@@ -162,6 +165,9 @@ struct AttentionCall {
   int heads;  // heads in this call
   int d;
   DevStatus* status;
+  // q_rows > 0: only the sharded query rows [q_row0, q_row0 + q_rows) of the (single)
+  // sequence, e.g. one rank's T rows; qkv, o and lse then hold those rows from row 0
+  int64_t q_row0, q_rows;
 };
 tsp_status launch_attention(const AttentionCall& call, cudaStream_t stream);
 
@@ -192,6 +198,8 @@ tsp_status launch_zigzag_index(const Plan& p, int32_t* fwd, int32_t* inv, cudaSt
 tsp_status launch_zigzag_rows(const Plan& p, const void* src, void* dst, int64_t width,
                               bool to_sharded, cudaStream_t s);
 tsp_status launch_kv_gather(const Plan& p, const void* qkv, void* kn, void* vn, cudaStream_t s);
+// the same from K|V rows ([D][B][T][2 H/D], K then V per row) to natural order
+tsp_status launch_kv_gather_kv(const Plan& p, const void* kv, void* kn, void* vn, cudaStream_t s);
 tsp_status launch_pack_weights(const Plan& p, const void* Wq, const void* Wk, const void* Wv,
                                const void* Wo, const void* W1, const void* W3, const void* W2,
                                void* wpack, cudaStream_t s);
@@ -218,6 +226,23 @@ tsp_status attention_block(const Plan& p, const void* xs, const void* wpack, con
 // G = SwiGLU(hs) then out = G W2^T (+ residual, fp32 when residual_f32) in ring order.
 tsp_status mlp_block(const Plan& p, const void* hs, const void* wpack, const void* residual,
                      int residual_f32, void* out, void* ws, cudaStream_t s);
+
+// An NVTX range around the host-side enqueue of one step of the schedules (a
+// broadcast iteration's projection and attention, the O projection, the MLP ring),
+// so that a trace tool shows which shard step issued which kernels. NVTX3 is
+// header-only: without a tool attached a range costs a few nanoseconds.
+class NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  NvtxRange(const char* fmt, int a, int b) {
+    char buf[96];
+    snprintf(buf, sizeof buf, fmt, a, b);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace tsp
 

@@ -76,25 +76,29 @@ __global__ void __launch_bounds__(256) zigzag_rows_kernel(const uint4* __restric
 }
 
 // kn[t] = qkv[zig(t)][Hd : 2Hd], vn[t] = qkv[zig(t)][2Hd : 3Hd]; one warp per token.
+// Source rows hold K at vector column k_off and V at v_off, src_vec vectors apart
+// (Q|K|V rows of a shard's projection: 3 vec_hd, vec_hd, 2 vec_hd; the K|V rows a
+// rank contributes to the all-gather: 2 vec_hd, 0, vec_hd).
 __global__ void __launch_bounds__(256) kv_gather_kernel(const uint4* __restrict__ qkv,
                                                         uint4* __restrict__ kn,
                                                         uint4* __restrict__ vn, long long S,
-                                                        int vec_hd, Zig z) {
+                                                        int vec_hd, Zig z, int src_vec,
+                                                        int k_off, int v_off) {
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long t = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); t < S;
        t += warps) {
-    const uint4* src = qkv + z.row_of(t) * (3LL * vec_hd);
+    const uint4* src = qkv + z.row_of(t) * (long long)src_vec;
     uint4* dk = kn + t * vec_hd;
     uint4* dv = vn + t * vec_hd;
     for (int v = lane; v < vec_hd; v += 64) {
       const bool second = v + 32 < vec_hd;
-      const uint4 k0 = __ldcs(src + vec_hd + v);
-      const uint4 v0 = __ldcs(src + 2 * vec_hd + v);
+      const uint4 k0 = __ldcs(src + k_off + v);
+      const uint4 v0 = __ldcs(src + v_off + v);
       uint4 k1, v1;
       if (second) {
-        k1 = __ldcs(src + vec_hd + v + 32);
-        v1 = __ldcs(src + 2 * vec_hd + v + 32);
+        k1 = __ldcs(src + k_off + v + 32);
+        v1 = __ldcs(src + v_off + v + 32);
       }
       dk[v] = k0;
       dv[v] = v0;
@@ -249,7 +253,16 @@ tsp_status launch_kv_gather(const Plan& p, const void* qkv, void* kn, void* vn, 
   const int vec_hd = p.Hd * 2 / 16;
   kv_gather_kernel<<<grid_for((p.N + 7) / 8, 16), 256, 0, s>>>(
       static_cast<const uint4*>(qkv), static_cast<uint4*>(kn), static_cast<uint4*>(vn), p.N,
-      vec_hd, z);
+      vec_hd, z, 3 * vec_hd, vec_hd, 2 * vec_hd);
+  return check_launch("kv gather launch");
+}
+
+tsp_status launch_kv_gather_kv(const Plan& p, const void* kv, void* kn, void* vn, cudaStream_t s) {
+  Zig z{p.C, p.T, p.D, p.B};
+  const int vec_hd = p.Hd * 2 / 16;
+  kv_gather_kernel<<<grid_for((p.N + 7) / 8, 16), 256, 0, s>>>(
+      static_cast<const uint4*>(kv), static_cast<uint4*>(kn), static_cast<uint4*>(vn), p.N,
+      vec_hd, z, 2 * vec_hd, 0, vec_hd);
   return check_launch("kv gather launch");
 }
 

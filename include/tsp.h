@@ -211,6 +211,11 @@ tsp_status tsp_layer_fwd(tsp_plan_t plan, const tsp_bf16* xs, const tsp_bf16* wp
  * The result is the same bit for bit either way. Pageable buffers are staged
  * through cudaMemcpyAsync and the workspace. The call returns once the work is
  * enqueued: synchronise `stream` before reading out_host.
+ * The library-owned copy stream is one per device, shared by every caller and
+ * thread: concurrent tsp_layer_fwd_host calls on different caller streams
+ * serialise their host-link copies on it, and a call made while another thread
+ * captures a CUDA graph that touches that stream disturbs the capture. Capture
+ * tsp_layer_fwd (device buffers) rather than this call.
  */
 tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp_bf16* wpack,
                               tsp_bf16* out_host, void* ws, void* stream);
@@ -227,13 +232,19 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
  * library, which every GPU that loads the library holds until the process exits.
  * Limit: tokens (B x S) x ffn_padded x 2 bytes <= 32 MiB - 256 (e.g. S = 4096 with hidden 1024
  * and ffn 2816); larger shapes return TSP_ERR_UNSUPPORTED with a message.
- * The call allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
- * The first call on a device looks the array's device address up
- * (cudaGetSymbolAddress, with that device current); make that first call before any
- * stream capture. Every call shares the array: calls that overlap on the GPU (other
- * streams, other threads) race on it and must be serialised by the caller. A device
- * wait that gives up leaves mlp undefined; this variant has no status query (use
- * tsp_mlp_fwd with a workspace and tsp_device_status when that report is needed).
+ * The call allocates nothing (no cudaMalloc/cudaFree, no allocating library call)
+ * once the array is in place on the device. Set-up: the first call on a device (in
+ * each CUDA context) looks the array's device address up with cudaGetSymbolAddress,
+ * with that device current. CUDA loads a library's device code lazily by default,
+ * so that first lookup is also when the driver reserves the 32 MiB on the device:
+ * make the first call at start-up, where reserving device memory is still allowed,
+ * and before any stream capture. Later calls in the same context reserve nothing
+ * (the free device memory does not change). Every call shares the array and the
+ * array keeps the last call's contents (the call clears the status word itself;
+ * G is overwritten in full): calls that overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller. A device wait that
+ * gives up leaves mlp undefined; this variant has no status query (use tsp_mlp_fwd
+ * with a workspace and tsp_device_status when that report is needed).
  */
 tsp_status tsp_mlp_fwd_noalloc(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf16* wpack,
                                tsp_bf16* mlp, void* stream);
@@ -319,6 +330,99 @@ tsp_status tsp_swiglu_gate_up(tsp_plan_t plan, const tsp_bf16* hs, const tsp_bf1
 tsp_status tsp_swiglu_down(tsp_plan_t plan, const tsp_bf16* g, const tsp_bf16* wpack,
                            const tsp_bf16* residual, const float* residual32, tsp_bf16* out,
                            void* ws, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Rank-local steps: the layer forward as one of D devices computes it ([TSP] s2,
+ * Methodology: "Attention layers" and "Gated MLP layers"), for running the D
+ * ranks on D devices (or several ranks on one). Rank r holds its T = S/D tokens
+ * xs_r [T][H] (zigzag chunks r and 2D-1-r, in that order) and weight shard r. The
+ * exchanges between the calls are the caller's (a collective library across
+ * devices; buffer copies between ranks on one device):
+ *   attention, broadcast iteration k = 0..D-1:
+ *     the owner of shard k broadcasts its attention part;
+ *     tsp_rank_qkv            (every rank, its own tokens)
+ *     all-gather of every rank's kv_r [T][2H/D] into kv_all [D][T][2H/D] (rank order)
+ *     tsp_rank_kv_gather      (K, V in natural token order)
+ *     tsp_rank_attention      (the rank's queries against the full K/V)
+ *     tsp_rank_o_accumulate   (acc_r += o_r W_O,k^T; residual x_r at k = 0)
+ *   MLP, ring step t = 0..D-1: rank r holds MLP part of shard (r + t) mod D;
+ *     tsp_rank_mlp_step       (acc_r += SwiGLU_k(h_r) W2_k^T; residual h32_r at t = 0)
+ *     then every rank sends its MLP part to rank r - 1 and receives from r + 1.
+ * No all-reduce anywhere: each rank accumulates its own rows. The result equals
+ * tsp_layer_fwd's rows of rank r up to fp32 summation order (each shard's partial
+ * product is added to an fp32 accumulator in HBM instead of one K loop in tensor
+ * memory). Plans of one sequence only (batch 1): TSP_ERR_UNSUPPORTED otherwise.
+ * `ws` provides the status word only (256 bytes, as for the single steps). All
+ * buffers are the caller's, 16-byte aligned; calls are asynchronous on `stream`.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * tsp_rank_shard_bytes - bytes of the two parts of one rank's weight shard k:
+ *   attention part (broadcast): Wqkv_k [3H/D][H] (Q, K, V rows of heads group k:
+ *     heads k*h/D .. (k+1)*h/D - 1), then W_O,k [H][H/D] (those heads' columns of W_O);
+ *   MLP part (ring): W13_k [Fq/128][256][H] (per 128 padded ffn columns of slice
+ *     k*F/D .., 128 W1 rows then the matching 128 W3 rows), then W2_k [H][Fp]
+ *     (the slice's columns of W2). Fp = shard_ffn_padded, Fq = Fp rounded up to
+ *     128; padded rows and columns are zero (silu(0) * 0 = 0 keeps it exact).
+ */
+tsp_status tsp_rank_shard_bytes(tsp_plan_t plan, size_t* attn_bytes, size_t* mlp_bytes);
+
+/*
+ * tsp_pack_rank_shard - lay out shard k from the natural weights (nn.Linear
+ * layout [out][in], as tsp_pack_weights) into attn_shard and mlp_shard. Only shard
+ * k's rows and columns are read.
+ */
+tsp_status tsp_pack_rank_shard(tsp_plan_t plan, int k, const tsp_bf16* Wq, const tsp_bf16* Wk,
+                               const tsp_bf16* Wv, const tsp_bf16* Wo, const tsp_bf16* W1,
+                               const tsp_bf16* W3, const tsp_bf16* W2, tsp_bf16* attn_shard,
+                               tsp_bf16* mlp_shard, void* stream);
+
+/*
+ * tsp_rank_qkv - local projections of one rank with attention shard k ([TSP] s2):
+ * q_r [T][H/D] = xs_r Wq_k^T; kv_r [T][2H/D] = (xs_r Wk_k^T | xs_r Wv_k^T) per row,
+ * the rank's contribution to the K/V all-gather. bf16 out, fp32 accumulation.
+ */
+tsp_status tsp_rank_qkv(tsp_plan_t plan, const tsp_bf16* xs_r, const tsp_bf16* attn_shard,
+                        tsp_bf16* q_r, tsp_bf16* kv_r, void* ws, void* stream);
+
+/*
+ * tsp_rank_kv_gather - K/V "all-gathered along the sequence" ([TSP] s2): kv_all
+ * [D][T][2H/D] (every rank's kv_r in rank order) -> kn, vn [S][H/D] in natural
+ * token order (the zigzag inverse). Bit-exact copy.
+ */
+tsp_status tsp_rank_kv_gather(tsp_plan_t plan, const tsp_bf16* kv_all, tsp_bf16* kn,
+                              tsp_bf16* vn, void* stream);
+
+/*
+ * tsp_rank_attention - causal attention of rank r's queries (global positions of
+ * its zigzag chunks) against the full K/V: o_r [T][H/D] for the h/D heads of the
+ * current shard (head j at columns j*d). Scale 1/sqrt(d), key t visible iff
+ * t <= position. q_r as tsp_rank_qkv wrote it.
+ */
+tsp_status tsp_rank_attention(tsp_plan_t plan, int r, const tsp_bf16* q_r, const tsp_bf16* kn,
+                              const tsp_bf16* vn, tsp_bf16* o_r, void* ws, void* stream);
+
+/*
+ * tsp_rank_o_accumulate - local accumulation of the O projection ([TSP] s2, read
+ * like the MLP's): acc_r [T][H] fp32 = residual + o_r W_O,k^T, and h_r = bf16(acc_r).
+ * residual: x_r (bf16, residual_f32 = 0) at the first broadcast iteration, then
+ * acc_r itself (fp32, residual_f32 = 1; in place). After the last iteration acc_r
+ * is h = x + Attn(x) in fp32 and h_r its bf16 value (the MLP input).
+ */
+tsp_status tsp_rank_o_accumulate(tsp_plan_t plan, const tsp_bf16* o_r, const tsp_bf16* attn_shard,
+                                 const void* residual, int residual_f32, float* acc_r,
+                                 tsp_bf16* h_r, void* ws, void* stream);
+
+/*
+ * tsp_rank_mlp_step - one ring step of the gated MLP ([TSP] s2, local accumulation,
+ * no all-reduce): g_r [T][Fq] bf16 = silu(h_r W1_k^T) * (h_r W3_k^T) (scratch), then
+ * acc_r [T][H] fp32 = residual32 + g_r W2_k^T and out_r = bf16(acc_r). residual32:
+ * the fp32 h of tsp_rank_o_accumulate at step 0, then acc_r itself (in place).
+ * After the last step out_r is the layer output of rank r's rows.
+ */
+tsp_status tsp_rank_mlp_step(tsp_plan_t plan, const tsp_bf16* h_r, const tsp_bf16* mlp_shard,
+                             const float* residual32, float* acc_r, tsp_bf16* out_r,
+                             tsp_bf16* g_r, void* ws, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Backward pass. [TSP] (title, s1) is about training but the page describes the

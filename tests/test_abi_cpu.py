@@ -241,3 +241,43 @@ int main(void) {
     assert out[1].startswith("tsp_plan")
     devices, welems = out[2].split()
     assert int(devices) == 8 and float(welems) == (4 * 4096 * 4096 + 3 * 4096 * 11008) / 8
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 256, 4, 688), (2, 200, 128, 2, 96),
+                                   (3, 1152, 384, 6, 600), (4, 4096, 1024, 16, 2816)],
+                         ids=["tiny", "ragged", "d3", "small"])
+def test_rank_calls_pass_their_host_checks(lib, shape):
+    """Without a GPU the rank-local calls get as far as the tensor-map encoding (the
+    first driver call) and no further: every host-side argument check of the call and
+    of the kernels it launches accepts the shapes the schedule uses. The pointers are
+    aligned placeholders that nothing dereferences here; the test never runs where a
+    CUDA device is present."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("placeholder pointers must never reach a GPU")
+    p = tsp.tsp_plan(*shape)
+    h = p.handle
+    P = lambda i: ctypes.c_void_p(1 << (24 + i))   # distinct 16 MiB-aligned placeholders
+    ws = P(0)
+    calls = {
+        "tsp_rank_qkv": lambda: lib.tsp_rank_qkv(h, P(1), P(2), P(3), P(4), ws, None),
+        "tsp_rank_attention": lambda: lib.tsp_rank_attention(h, shape[0] - 1, P(1), P(2), P(3),
+                                                             P(4), ws, None),
+        "tsp_rank_o_accumulate bf16": lambda: lib.tsp_rank_o_accumulate(h, P(1), P(2), P(3), 0,
+                                                                        P(4), P(5), ws, None),
+        "tsp_rank_o_accumulate fp32": lambda: lib.tsp_rank_o_accumulate(h, P(1), P(2), P(4), 1,
+                                                                        P(4), P(5), ws, None),
+        "tsp_rank_mlp_step": lambda: lib.tsp_rank_mlp_step(h, P(1), P(2), P(4), P(4), P(5), P(6),
+                                                           ws, None),
+    }
+    for name, call in calls.items():
+        st = call()
+        msg = B.tsp_last_error()
+        assert st == B.TSP_ERR_CUDA and "cuTensorMapEncodeTiled" in msg, (name, st, msg)
+    assert lib.tsp_rank_attention(h, shape[0], P(1), P(2), P(3), P(4), ws, None) \
+        == B.TSP_ERR_INVALID_ARG
+    a, m = tsp.tsp_rank_shard_bytes(p)
+    i = p.info
+    Fq = (i.shard_ffn_padded + 127) // 128 * 128
+    assert a == 2 * 4 * i.hidden * i.shard_hidden
+    assert m == 2 * (2 * Fq * i.hidden + i.hidden * i.shard_ffn_padded)
