@@ -21,30 +21,73 @@ constexpr size_t kNoallocStatusBytes = 256;
 
 }  // namespace
 
-// Every GPU that loads this library holds this array until the process exits.
+// Every GPU on which this array is first used holds it until the process exits.
+// CUDA loads a library's device code lazily by default (CUDA_MODULE_LOADING=LAZY):
+// the driver reserves this array on a device when the first tsp_mlp_fwd_noalloc
+// call there looks its address up, not when the library is loaded. With eager
+// loading it is reserved on every device the process initialises.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 namespace {
 
-std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[64] = {};  // device address of g_noalloc_scratch, per device
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device. The first call on a
-// device looks it up (cudaGetSymbolAddress, with that device current); later calls
-// reuse it.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, fetched through
+// the runtime's driver entry point), or 0 when it cannot be had. A context made
+// after cudaDeviceReset, or another context on the same device, has another id.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+struct ScratchAddr {
+  unsigned long long ctx_id;  // context the address belongs to
+  void* addr;                 // device address of g_noalloc_scratch in that context
+};
+
+std::mutex g_noalloc_mutex;
+ScratchAddr g_noalloc_addr[64] = {};  // per device
+
+// Device address of the scratch array in the current device's current context. The
+// first call in a context looks it up (cudaGetSymbolAddress, with that device
+// current); later calls in the same context reuse it. A new context (after
+// cudaDeviceReset, or a context the caller made) is looked up again, so no call
+// passes an address of a context that no longer exists.
 tsp_status noalloc_scratch(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return tsp::cuda_fail(e, "tsp_mlp_fwd_noalloc: cudaGetDevice");
   if (dev < 0 || dev >= 64) return tsp::fail(TSP_ERR_UNSUPPORTED, "tsp_mlp_fwd_noalloc: device index >= 64");
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_addr[dev]) {
+  ScratchAddr& c = g_noalloc_addr[dev];
+  if (!c.addr || ctx == 0 || c.ctx_id != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return tsp::cuda_fail(e, "tsp_mlp_fwd_noalloc: cudaGetSymbolAddress");
-    g_noalloc_addr[dev] = p;
+    // the runtime made its context current if there was none: key by that one
+    c.ctx_id = ctx ? ctx : current_context_id();
+    c.addr = p;
   }
-  *out = g_noalloc_addr[dev];
+  *out = c.addr;
   return TSP_OK;
 }
 
