@@ -16,8 +16,11 @@ Reported:
               the same kernels through the single-step entry points
   e2e         the same metric through tsp_layer_fwd_host with pinned host buffers
               (host->device copy of x and device->host copy of out every step)
-  cpu_baseline the float64 oracle on the host cores, timed on a causal prefix of
-              the same workload and scaled by FLOPs to the full workload
+  cpu_baseline the float64 oracle on the host cores: the whole layer for short
+              workloads; for long ones the projection of one attention shard over
+              the whole sequence, the attention of 256 sampled query rows and their
+              MLP, with the full-layer time extrapolated from those three rates
+              (the reference arm times the same sample)
   backward    tsp_layer_bwd on the same workload (a synthetic output gradient):
               ms per step, tokens/s and algorithmic TFLOP/s
               (16SH^2 + 12SHF + 5HS(S+1)), the attention backward of one shard, and
@@ -50,12 +53,13 @@ import tsp_inputs  # noqa: E402
 METRIC = "TSP layer fwd tokens/s and TFLOP/s (frac of bf16 TC peak) on 1 GB300"
 DEFAULT_WORKLOAD = "7b-64k"
 
-# DRAM bytes (read + write) per launch from one ncu capture of the kernel as it is
-# now (profiles/ holds the summaries: 7B shape, 64K tokens, per launch); a kernel
-# missing here has no capture of its current version.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, from one ncu
+# capture of the kernel as it is now, at the 7B shape and 64K tokens. These are stored
+# figures, not measured by this run (the line says so); a kernel missing here has no
+# capture of its current version and reports null.
 NCU_TRAFFIC_BYTES = {
-    "attention": 298_205_952 + 50_858_496,      # profiles/attention_7b-64k.md
-    "gemm_gate_up": 3_581_881_000 + 1_464_714_000,  # profiles/gemm_gate_up_7b-64k.md
+    "attention": 298_205_952 + 50_858_496,
+    "gemm_gate_up": 3_581_881_000 + 1_464_714_000,
 }
 
 
@@ -183,31 +187,68 @@ def gpu_smi_id(local_rank):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(cfg, bits, n_tokens, repeats=1):
-    """Time the float64 oracle on the first n_tokens of the workload (a causal prefix).
+SAMPLE_ROWS = 256       # sampled query rows of a long workload (always the first and last)
+FULL_LAYER_MAX_S = 4096  # workloads up to this length: the whole layer is timed
 
-    Returns (seconds per repeat, tokens/s extrapolated to the full workload by
-    algorithmic FLOPs, description).
+
+def oracle_sample_desc(cfg):
+    """What one CPU-baseline sample of the workload is (the same text for both legs)."""
+    if cfg.S <= FULL_LAYER_MAX_S:
+        return (f"float64 NumPy oracle, the whole layer of {cfg.name} ({cfg.S} tokens) per "
+                "sample: tokens/s measured directly")
+    return (f"float64 NumPy oracle on {cfg.name}, one sample = the Q/K/V projection of "
+            f"attention shard 0 over all {cfg.S} tokens, the causal attention of "
+            f"{SAMPLE_ROWS} sampled query rows (first and last included) against the full "
+            f"gathered K/V of that shard's {cfg.heads // cfg.D} heads, and the SwiGLU MLP of "
+            f"those rows. Full-layer time EXTRAPOLATED from the three measured rates: "
+            "projections 8SH^2 at the projection rate, attention 2HS(S+1) at the sampled "
+            "attention rate, MLP 6SHF at the MLP rate")
+
+
+def oracle_sample(cfg, bits, repeats=1):
+    """Time the float64 oracle on one sample of the workload (oracle_sample_desc).
+
+    Returns (seconds of oracle work per sample, tokens/s of the full workload - measured
+    for short workloads, extrapolated from component rates for long ones, and the
+    measured rates in GFLOP/s).
     """
     import oracle  # the oracle is timed here only as the CPU baseline / reference arm
-    n = int(min(n_tokens, cfg.S))
+    S, H, F, D, heads = cfg.S, cfg.hidden, cfg.ffn, cfg.D, cfg.heads
     xb = bits["x"] if bits["x"].ndim == 2 else bits["x"][0]  # first sequence of a micro-batch
-    x = oracle.widen_bf16(xb[:n])
+    x = oracle.widen_bf16(xb)
     W = {k: oracle.widen_bf16(bits[k]) for k in ("Wq", "Wk", "Wv", "Wo", "W1", "W3", "W2")}
-    times = []
+    if S <= FULL_LAYER_MAX_S:
+        times = []
+        for _ in range(repeats):
+            t0 = time.perf_counter()
+            oracle.layer_forward(x, W, heads)
+            times.append(time.perf_counter() - t0)
+        t = statistics.median(times)
+        return t, S / t, {"layer_gflops": round(algorithmic_flops(S, H, F) / t / 1e9, 2)}
+    Hd, hpr, d = H // D, heads // D, H // heads
+    rows = tsp_inputs.sample_rows(S, SAMPLE_ROWS, cfg.seed)
+    tp, ta, tm = [], [], []
     for _ in range(repeats):
         t0 = time.perf_counter()
-        oracle.layer_forward(x, W, cfg.heads)
-        times.append(time.perf_counter() - t0)
-    t = statistics.median(times)
-    f_sample = algorithmic_flops(n, cfg.hidden, cfg.ffn)
-    f_full = algorithmic_flops(cfg.S, cfg.hidden, cfg.ffn)
-    rate = f_sample / t
-    tokens_per_s = cfg.S * rate / f_full
-    desc = (f"float64 NumPy oracle, full layer on the causal prefix of {n} tokens of {cfg.name} "
-            f"({t:.2f} s, {rate / 1e9:.1f} GFLOP/s), scaled by algorithmic FLOPs to the "
-            f"{cfg.S}-token workload")
-    return t, tokens_per_s, desc
+        qkv = oracle.qkv_projection_shard(x, W["Wq"], W["Wk"], W["Wv"], 0, D)
+        t1 = time.perf_counter()
+        oracle.multihead_causal_attention(qkv[rows, :Hd], qkv[:, Hd:2 * Hd], qkv[:, 2 * Hd:],
+                                          hpr, q_pos=rows, k_pos=np.arange(S))
+        t2 = time.perf_counter()
+        oracle.swiglu_mlp(x[rows], W["W1"], W["W3"], W["W2"])
+        t3 = time.perf_counter()
+        tp.append(t1 - t0)
+        ta.append(t2 - t1)
+        tm.append(t3 - t2)
+    tp, ta, tm = statistics.median(tp), statistics.median(ta), statistics.median(tm)
+    r_proj = 2.0 * S * H * 3 * Hd / tp
+    r_att = float(sum(4.0 * d * hpr * (int(p) + 1) for p in rows)) / ta
+    r_mlp = 6.0 * len(rows) * H * F / tm
+    t_full = 8.0 * S * H * H / r_proj + 2.0 * H * S * (S + 1) / r_att + 6.0 * S * H * F / r_mlp
+    rates = {"projection_gflops": round(r_proj / 1e9, 2), "attention_gflops": round(r_att / 1e9, 2),
+             "mlp_gflops": round(r_mlp / 1e9, 2),
+             "extrapolated_layer_s": round(t_full, 1)}
+    return tp + ta + tm, S / t_full, rates
 
 
 def cpu_cores():
@@ -394,7 +435,11 @@ def run_ours(args, world, rank, local):
     roofline = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved"],
                 "peak": peaks["bf16_tflops_sustained"] if kd["bound"] == "tensor" else peaks["hbm_gbs"],
                 "unit": "TFLOP/s" if kd["bound"] == "tensor" else "GB/s",
-                "frac": kd["frac"], "traffic": NCU_TRAFFIC_BYTES.get(dom),
+                "frac": kd["frac"],
+                "traffic": NCU_TRAFFIC_BYTES.get(dom) if cfg.name == "7b-64k" and Bm == 1 else None,
+                "traffic_source": ("stored ncu capture of this kernel at 7b-64k "
+                                   "(dram__bytes_read.sum + dram__bytes_write.sum per launch), "
+                                   "not measured in this run"),
                 "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kd['bound'] == 'tensor' else 'hbm_gbs'})"}
     gather_gbs = 8.0 * N * i.shard_hidden / (gather_ms * 1e-3) / 1e9
     kernels["kv_gather_standalone"] = {
@@ -530,9 +575,10 @@ def run_ours(args, world, rank, local):
         result["backward"] = backward
     result["cost_model"] = cost_model_summary(tsp, cfg)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t, v, desc = oracle_sample(cfg, bits, args.cpu_sample_tokens)
+        t, v, rates = oracle_sample(cfg, bits, repeats=args.cpu_repeats)
         result["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),
-                                  "kind": "oracle", "sample": desc}
+                                  "kind": "oracle", "sample": oracle_sample_desc(cfg),
+                                  "sample_s": round(t, 2), "rates": rates}
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -542,16 +588,16 @@ def run_ours(args, world, rank, local):
 # --------------------------------------------------------- reference arm
 
 def run_reference(args, world, rank, local):
+    """The oracle on the host cores, the same sample as `cpu_baseline` per step."""
     if rank != 0:
         return
     cfg = tsp_inputs.config_by_name(args.workload)
     bits = tsp_inputs.layer_inputs(cfg)
     for _ in range(args.warmup):
-        oracle_sample(cfg, bits, args.ref_sample_tokens)
-    times, vals = [], []
-    desc = ""
+        oracle_sample(cfg, bits)
+    times, vals, rates = [], [], {}
     for _ in range(args.steps):
-        t, v, desc = oracle_sample(cfg, bits, args.ref_sample_tokens)
+        t, v, rates = oracle_sample(cfg, bits)
         times.append(t)
         vals.append(v)
     v = statistics.mean(vals)
@@ -564,11 +610,98 @@ def run_reference(args, world, rank, local):
                    "D": cfg.D, "S": cfg.S, "hidden": cfg.hidden, "heads": cfg.heads,
                    "head_dim": cfg.head_dim, "ffn": cfg.ffn, "batch": args.batch},
         "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(),
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": oracle_sample_desc(cfg),
+                         "sample_s": round(statistics.mean(times), 2), "rates": rates},
         "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(result), flush=True)
+
+
+# ------------------------------------------------------- one step, N times
+
+STEPS = ["qkv", "qkv_gathered", "gather", "attention", "o_proj", "gate_up", "down", "shard",
+         "attention_bwd"]
+
+
+def run_step(args):
+    """--step NAME: run one step of the hot path `--launches` times (after one untimed
+    launch) and print the average CUDA-event time per launch, for a profiler to capture.
+
+    Steps: qkv (Q/K/V projection of shard 0), qkv_gathered (the same with the K/V
+    all-gather in its epilogue, as the layer runs it), gather (K/V all-gather),
+    attention (causal attention of shard 0), o_proj (O projection with the fp32
+    residual copy), gate_up (SwiGLU gate/up), down (SwiGLU down with the fp32
+    residual), shard (zigzag rows), attention_bwd (Delta, key-side and query-side
+    attention backward of shard 0, after one forward with the log-sum-exp). Inputs are
+    seeded synthetic bf16 values with the workload's shapes; only the buffers the step
+    touches are allocated, so a 64K-token step fits in a few GB of device memory. A
+    time printed under a profiler is not a measurement.
+    """
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import folded_tensor_sequence_tsp_gb300 as B
+
+    def bf16(shape, seed, std=1.0):
+        b = tsp_inputs.normal_bf16_bits(shape, std, seed, 77)
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+
+    cfg = tsp_inputs.config_by_name(args.workload)
+    plan = B.tsp_plan(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn)
+    i = plan.info
+    S, H, Hd = i.S, i.hidden, i.shard_hidden
+    st = args.step
+    ws = None
+    if st not in ("gather", "shard"):  # single steps use only the status word
+        ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    wpack = bf16((i.wpack_elems,), 1, 0.02) if st in ("qkv", "qkv_gathered", "o_proj", "gate_up",
+                                                      "down") else None
+    empty = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device="cuda")
+    if st == "qkv":
+        xs, qkv = bf16((S, H), 2), empty((S, 3 * Hd))
+        run = lambda: B.tsp_qkv_projection(plan, 0, xs, wpack, qkv, ws)
+    elif st == "qkv_gathered":
+        xs, q, kn, vn = bf16((S, H), 2), empty((S, Hd)), empty((S, Hd)), empty((S, Hd))
+        run = lambda: B.tsp_qkv_projection_gathered(plan, 0, xs, wpack, q, kn, vn, ws)
+    elif st == "gather":
+        qkv, kn, vn = bf16((S, 3 * Hd), 3), empty((S, Hd)), empty((S, Hd))
+        run = lambda: B.tsp_kv_allgather(plan, qkv, kn, vn)
+    elif st == "attention":
+        qkv, kn, vn, o = bf16((S, 3 * Hd), 4), bf16((S, Hd), 5), bf16((S, Hd), 6), empty((S, H))
+        run = lambda: B.tsp_causal_attention(plan, 0, qkv, kn, vn, o, ws)
+    elif st == "o_proj":
+        o, xs, h, h32 = bf16((S, H), 7, 0.5), bf16((S, H), 8), empty((S, H)), empty((S, H), torch.float32)
+        run = lambda: B.tsp_o_projection(plan, o, wpack, xs, h, ws, out32=h32)
+    elif st == "gate_up":
+        h, g = bf16((S, H), 9), empty((S, i.ffn_padded))
+        run = lambda: B.tsp_swiglu_gate_up(plan, h, wpack, g, ws)
+    elif st == "down":
+        g, out = bf16((S, i.ffn_padded), 10, 0.5), empty((S, H))
+        h32 = torch.randn((S, H), dtype=torch.float32, device="cuda")
+        run = lambda: B.tsp_swiglu_down(plan, g, wpack, None, out, ws, residual32=h32)
+    elif st == "attention_bwd":
+        q, kn, vn, dout = bf16((S, Hd), 12), bf16((S, Hd), 13), bf16((S, Hd), 14), bf16((S, H), 15)
+        o = empty((S, H))
+        lse = empty(((cfg.heads // cfg.D) * i.stat_stride,), torch.float32)
+        delta, dqkv = torch.empty_like(lse), empty((S, 3 * H))
+        B.tsp_causal_attention_lse(plan, 0, q, kn, vn, o, lse, ws)
+        run = lambda: B.tsp_causal_attention_bwd(plan, 0, q, kn, vn, o, dout, lse, delta, dqkv, ws)
+    else:
+        x = bf16((S, H), 11)
+        xs = torch.empty_like(x)
+        run = lambda: B.tsp_shard(plan, x, xs)
+    run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.launches):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    if ws is not None and B.tsp_device_status(ws) != B.TSP_OK:
+        raise B.TSPError(B.tsp_device_status(ws), B.tsp_last_error())
+    print(f"{st} {cfg.name}: {a.elapsed_time(b) / args.launches:.4f} ms per launch", flush=True)
 
 
 def main():
@@ -585,12 +718,19 @@ def main():
     ap.add_argument("--batch", type=int, default=1,
                     help="sequences of the micro-batch (e.g. --workload 7b-16k --batch 4 is "
                          "4 x 16K tokens)")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
-    ap.add_argument("--ref-sample-tokens", type=int, default=1024)
+    ap.add_argument("--step", choices=STEPS,
+                    help="time one step of the hot path --launches times instead (for profiling; "
+                         "prints one line, not the benchmark's JSON)")
+    ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--cpu-repeats", type=int, default=2,
+                    help="samples of the oracle for cpu_baseline (median taken)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps do not meet the timing rules", file=sys.stderr)
     world, rank, local = dist_env()
+    if args.step:
+        run_step(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     else:

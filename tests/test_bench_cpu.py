@@ -19,8 +19,7 @@ def _run(*args):
 
 
 def test_reference_arm_prints_the_contract_line():
-    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "0",
-             "--ref-sample-tokens", "128")
+    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "0")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "cpu_baseline", "e2e"):
@@ -34,5 +33,25 @@ def test_reference_arm_prints_the_contract_line():
 
 def test_reference_arm_names_a_micro_batch():
     d = _run("--impl", "reference", "--workload", "tiny", "--batch", "2", "--steps", "1",
-             "--warmup", "0", "--ref-sample-tokens", "64")
+             "--warmup", "0")
     assert d["config"]["workload"] == "tiny-b2" and d["config"]["batch"] == 2
+
+
+def test_long_workload_sample_extrapolates_from_component_rates():
+    """Past 4096 tokens one sample times the oracle's projection of one attention
+    shard over the whole sequence, the attention of 256 sampled rows and their MLP;
+    the full-layer time is the sum of the layer's three FLOP classes at those rates."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import tsp_inputs
+    cfg = tsp_inputs.LayerConfig("long-narrow", 2, 8192, 256, 4, 688, 7)
+    bits = tsp_inputs.layer_inputs(cfg)
+    t, tokens_per_s, rates = bench.oracle_sample(cfg, bits)
+    assert t > 0 and tokens_per_s > 0
+    S, H, F = cfg.S, cfg.hidden, cfg.ffn
+    t_full = (8.0 * S * H * H / (rates["projection_gflops"] * 1e9)
+              + 2.0 * H * S * (S + 1) / (rates["attention_gflops"] * 1e9)
+              + 6.0 * S * H * F / (rates["mlp_gflops"] * 1e9))
+    assert abs(t_full - rates["extrapolated_layer_s"]) <= 0.05 * t_full + 0.1
+    assert abs(S / t_full - tokens_per_s) <= 0.05 * tokens_per_s
+    assert "EXTRAPOLATED" in bench.oracle_sample_desc(cfg)
