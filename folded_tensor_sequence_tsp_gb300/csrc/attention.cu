@@ -132,21 +132,21 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float exp_tile(const float (&sc)[KT], uint32_t p_tmem, float scale,
                                           float neg_ref) {
   const uint64_t scale2 = f2_pack(scale, scale), nref2 = f2_pack(neg_ref, neg_ref);
-  uint64_t sum2[4] = {0, 0, 0, 0};
+  uint64_t sum2[2] = {0, 0};
 #pragma unroll
-  for (int c = 0; c < KT; c += 32) {
-    uint32_t r[16];
+  for (int c = 0; c < KT; c += 16) {
+    uint32_t r[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
+    for (int e = 0; e < 8; ++e) {
       float x0, x1;
       f2_unpack(f2_fma(f2_pack(sc[c + 2 * e], sc[c + 2 * e + 1]), scale2, nref2), x0, x1);
       const float p0 = ex2(x0), p1 = ex2(x1);
-      sum2[e & 3] = f2_add(sum2[e & 3], f2_pack(p0, p1));
+      sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
       r[e] = pack_bf16x2(p0, p1);
     }
-    tmem_st16(p_tmem + (uint32_t)(c / 2), r);
+    tmem_st8(p_tmem + (uint32_t)(c / 2), r);
   }
-  const uint64_t s01 = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
+  const uint64_t s01 = f2_add(sum2[0], sum2[1]);
   float a, b;
   f2_unpack(s01, a, b);
   return a + b;
@@ -380,9 +380,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_ref = -INFINITY;  // reference maximum (scaled, log2 units)
     float l = 0.f;
     bool ok = true;
-    // every lane waits; the warp goes on only if all lanes saw the phase complete
+    // every lane waits; the warp goes on only if all lanes saw the phase complete (the
+    // bound is rebuilt from the kernel parameters at each wait: nothing of it stays in
+    // registers across the key loop)
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
-      const bool mine = mbar_wait(bar, parity, wb, SITE_ATT_SOFTMAX);
+      const WaitBound wbs{p.status, p.limit_ns, abort_flag};
+      const bool mine = mbar_wait(bar, parity, wbs, SITE_ATT_SOFTMAX);
       return __all_sync(0xffffffffu, mine) != 0;
     };
     for (int j = 0; j < my_tiles; ++j) {
@@ -437,8 +440,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
       l *= factor;
+      // P = exp2(s*scale - m) in bf16 over the first 64 columns of S (masked keys: 0)
+      l += exp_tile(sc, s_tmem, p.scale_log2, neg_ref);
+      // rescale O (written by the products up to P(j-1) V_{j-1}, complete since S(j)
+      // is) before P(j) is handed over; after the exponentials, so that the scores are
+      // no longer live: 16 columns at a time
       if (j > 0 && __any_sync(0xffffffffu, rescale && factor != 1.f)) {
-        // 16 columns at a time: the 128 scores stay live in registers meanwhile
 #pragma unroll 1
         for (int c = 0; c < HD; c += 16) {
           uint32_t r[16];
@@ -449,8 +456,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st16(o_tmem + c, r);
         }
       }
-      // P = exp2(s*scale - m) in bf16 over the first 64 columns of S (masked keys: 0)
-      l += exp_tile(sc, s_tmem, p.scale_log2, neg_ref);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
