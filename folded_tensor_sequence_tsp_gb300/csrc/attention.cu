@@ -325,19 +325,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_ts_w(d, a + (uint32_t)(kk * 8), b_lo + (uint32_t)(kk * (2048 >> 4)), v_hi, idesc_o,
                    kk > 0 ? 1u : first);
       };
-      bool ok = mbar_wait(q_full, 0, wb, SITE_ATT_MMA);
+      bool ok = mbar_wait_poll(q_full, 0, wb, SITE_ATT_MMA);
       if (ok) {
         tc_fence_after();
         if (n_a > 0) issue_s(0, 0);
         if (n_b > 0) issue_s(1, 0);
-        ok = mbar_wait(&kv_full[0], 0, wb, SITE_ATT_MMA);
+        ok = mbar_wait_poll(&kv_full[0], 0, wb, SITE_ATT_MMA);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         // stage j % 2 (V_j, K_{j+1}) has landed
         for (int t = 0; t < 2; ++t) {
           const int nt = t ? n_b : n_a;
           if (j < nt) {
-            if (!mbar_wait(&p_full[t], (uint32_t)(j & 1), wb, SITE_ATT_MMA)) {
+            if (!mbar_wait_poll(&p_full[t], (uint32_t)(j & 1), wb, SITE_ATT_MMA)) {
               ok = false;
               break;
             }
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           // while tile A's products run, wait for the next stage
           if (t == 0 && j + 1 < n_tiles &&
-              !mbar_wait(&kv_full[(j + 1) % STAGES], (uint32_t)(((j + 1) / STAGES) & 1), wb,
+              !mbar_wait_poll(&kv_full[(j + 1) % STAGES], (uint32_t)(((j + 1) / STAGES) & 1), wb,
                          SITE_ATT_MMA)) {
             ok = false;
             break;

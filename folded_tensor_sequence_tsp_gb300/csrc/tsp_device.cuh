@@ -90,6 +90,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 static __device__ __noinline__ void record_timeout(const WaitBound& wb, unsigned int site) {
   if (atomicCAS(&wb.status->code, 0u, kStatusTimeout) == 0u) {
     wb.status->site = site;
@@ -110,6 +122,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    if (wb.abort_flag && *wb.abort_flag) return false;
+    if (global_ns() - t0 > wb.limit_ns) {
+      record_timeout(wb, site);
+      return false;
+    }
+  }
+}
+
+// mbar_wait for a single thread on the critical path that has nothing else to do:
+// it polls the phase without being suspended, so it resumes as soon as the phase
+// completes. Same bound and abort rules as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, const WaitBound& wb,
+                                               unsigned int site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
     if (wb.abort_flag && *wb.abort_flag) return false;
     if (global_ns() - t0 > wb.limit_ns) {
       record_timeout(wb, site);
