@@ -202,7 +202,9 @@ def layer_forward_ranks(D: int, T: int, hd: int, ranks, xs: dict, attn_shards: d
     xs[r]: rank r's zigzag tokens [T][H]; attn_shards[r], mlp_shards[r]: the two parts
     of weight shard r (tsp_rank_shard_bytes layout for CudaRankCompute); hd = H/D.
     Returns {r: rank r's layer output [T][H]}. The MLP part circulates in a second
-    buffer so that the caller's shards are left as they were.
+    buffer so that the caller's shards are left as they were. Transfers overlap the
+    compute: the broadcast of attention shard k + 1 is in flight during iteration k,
+    and the ring shift for MLP step t + 1 during step t.
     """
     ranks = list(ranks)
     like = next(iter(xs.values()))
@@ -210,10 +212,20 @@ def layer_forward_ranks(D: int, T: int, hd: int, ranks, xs: dict, attn_shards: d
     kv = {r: torch.empty((T, 2 * hd), dtype=compute.act_dtype, device=like.device) for r in ranks}
     kv_all = {r: torch.empty((D, T, 2 * hd), dtype=compute.act_dtype, device=like.device)
               for r in ranks}
-    recv = {r: torch.empty_like(attn_shards[r]) for r in ranks}
+    # two receive buffers: the broadcast of shard k + 1 is in flight while iteration k
+    # computes (a rank's own shard is sent from where it lies)
+    recv = [{r: torch.empty_like(attn_shards[r]) for r in ranks} for _ in range(2)]
+
+    def start_broadcast(k):
+        bufs = {r: attn_shards[r] if r == k else recv[k % 2][r] for r in ranks}
+        return bufs, exchange.broadcast(bufs, src=k)
+
+    nxt_b = start_broadcast(0)
     for k in range(D):  # broadcast iteration k: shard k's attention part to every rank
-        cur = {r: attn_shards[r] if r == k else recv[r] for r in ranks}
-        exchange.broadcast(cur, src=k).wait()
+        cur, pending = nxt_b
+        pending.wait()
+        if k + 1 < D:
+            nxt_b = start_broadcast(k + 1)
         for r in ranks:
             compute.attention_project(state[r], k, cur[r], kv[r])
         exchange.all_gather(kv_all, kv).wait()
