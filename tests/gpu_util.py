@@ -40,8 +40,8 @@ REL_FRO = 1e-2
 MAX_ABS = 3e-2
 
 # (name, elements, rel_fro, max|got-exact|, elements above atol vs exact, atol,
-#  largest delta_i, max over elements of |got-ref| - bound)  -- one per check,
-# printed by the session summary
+#  largest delta_i, max over elements of |got-ref| - bound, rows, rows whose
+#  delta_i exceeds atol)  -- one per check, printed by the session summary
 RECORDS = []
 
 
@@ -102,8 +102,10 @@ def assert_close(got, exact, name="", ref=None, atol=MAX_ABS, bf16_out=True,
         margin = float(ex[k])
         where = (f" at {tuple(int(i) for i in k)}: ref={ref[k]:.5f} exact={exact[k]:.5f} "
                  f"got={got[k]:.5f} bound={float(np.broadcast_to(bound, ex.shape)[k]):.4f}")
+    rows = got.shape[0] if got.ndim else 1
+    wide = int((np.asarray(delta) > atol).sum()) if np.ndim(delta) else int(delta > atol)
     RECORDS.append((name, int(got.size), rel, mx, n_over, float(atol),
-                    float(np.max(delta)), margin))
+                    float(np.max(delta)), margin, rows, wide))
     assert rel <= rel_fro and margin <= 0.0, (
         f"{name}: rel_fro={rel:.3e} (<= {rel_fro:g}) max_abs vs exact={mx:.3e} "
         f"({n_over} of {got.size} above {atol:.3g}); worst excess over the bound "
