@@ -76,6 +76,10 @@ def test_plan_sizes(lib, cfg):
     ((4, 256, 192, 3, 688), B.TSP_ERR_UNSUPPORTED),       # heads % D
     ((2, 256, 256, 4, 687), B.TSP_ERR_UNSUPPORTED),       # ffn % D
     ((2, 2, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),         # S < 2D
+    ((2, 0, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),         # empty sequence
+    ((2, -4, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),        # negative length
+    ((2, 256, 0, 4, 688), B.TSP_ERR_UNSUPPORTED),         # no hidden width
+    ((2, 256, 256, 4, 0), B.TSP_ERR_UNSUPPORTED),         # no ffn
     ((2, 1 << 27, 256, 4, 688), B.TSP_ERR_UNSUPPORTED),   # S too large
     ((65, 130, 64 * 65, 65, 65), B.TSP_ERR_UNSUPPORTED),  # D > 64
 ])
