@@ -229,7 +229,7 @@ tsp_status tsp_layer_fwd_host(tsp_plan_t plan, const tsp_bf16* x_host, const tsp
  * forbid allocation after start-up. They still pass hs, wpack and mlp ([D][T][H]
  * as for tsp_mlp_fwd) but no workspace: the gated activation G and the status word
  * of the bounded device waits live in one static device array of 32 MiB inside the
- * library, which every GPU that loads the library holds until the process exits.
+ * library, which a device holds from the first call there until the process exits.
  * Limit: tokens (B x S) x ffn_padded x 2 bytes <= 32 MiB - 256 (e.g. S = 4096 with hidden 1024
  * and ffn 2816); larger shapes return TSP_ERR_UNSUPPORTED with a message.
  * The call allocates nothing (no cudaMalloc/cudaFree, no allocating library call)
