@@ -205,3 +205,40 @@ def test_two_processes_exchange_through_gloo():
     st = stored_layer(x, L.weights64(), heads)["out"]
     assert_close(oracle.unshard_tokens(oracle.widen_bf16(got), D), ref, "ranks gloo 2 processes",
                  ref=st)
+
+
+@pytest.mark.slow
+def test_rank_steps_at_the_7b_shape():
+    """At the 7B shape and 16K tokens (the benchmark's launch sizes for one rank): the
+    rank-local Q/K/V projection, K/V gather and attention of the first and the last
+    rank give the all-rank steps' rows bit for bit, for the first and the last shard."""
+    cfg = tsp_inputs.config_by_name("7b-16k")
+    L = Layer(cfg.D, cfg.S, cfg.hidden, cfg.heads, cfg.ffn, seed=cfg.seed)
+    i = L.info
+    D, T, S, Hd = i.D, i.T, i.S, i.shard_hidden
+    sh = _shards(L)
+    xs = L.sharded_x()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    q_all, kn, vn = (torch.empty((S, Hd), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    o_all = L.act()
+    kv_all = torch.empty((D, T, 2 * Hd), dtype=torch.bfloat16, device="cuda")
+    for k in (0, D - 1):
+        tsp.tsp_qkv_projection_gathered(L.plan, k, xs, L.wpack, q_all, kn, vn, L.ws)
+        tsp.tsp_causal_attention_q(L.plan, k, q_all, kn, vn, o_all, L.ws)
+        qs = {}
+        for r in range(D):
+            q_r = torch.empty((T, Hd), dtype=torch.bfloat16, device="cuda")
+            tsp.tsp_rank_qkv(L.plan, xs[r * T:(r + 1) * T], sh[k][0], q_r, kv_all[r], ws)
+            qs[r] = q_r
+        kn_r, vn_r = torch.empty_like(kn), torch.empty_like(vn)
+        tsp.tsp_rank_kv_gather(L.plan, kv_all, kn_r, vn_r)
+        assert torch.equal(kn_r.view(torch.int16), kn.view(torch.int16)), k
+        assert torch.equal(vn_r.view(torch.int16), vn.view(torch.int16)), k
+        for r in (0, D - 1):
+            assert torch.equal(qs[r].view(torch.int16), q_all[r * T:(r + 1) * T].view(torch.int16))
+            o_r = torch.full((T, Hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+            tsp.tsp_rank_attention(L.plan, r, qs[r], kn_r, vn_r, o_r, ws)
+            want = o_all[r * T:(r + 1) * T, k * Hd:(k + 1) * Hd].contiguous()
+            assert torch.equal(o_r.view(torch.int16), want.view(torch.int16)), (k, r)
+    assert tsp.tsp_device_status(ws) == tsp.TSP_OK
+    L.check_status()
