@@ -563,19 +563,25 @@ def tsp_pack_rank_shard(plan, k, Wq, Wk, Wv, Wo, W1, W3, W2, attn_shard, mlp_sha
         _stream(stream)), "tsp_pack_rank_shard")
 
 
+def _rank_rows(plan):
+    """Rows one rank holds: its T tokens of every sequence of the micro-batch."""
+    i = plan.info
+    return i.batch * i.T
+
+
 def tsp_rank_qkv(plan, xs_r, attn_shard, q_r, kv_r, ws, stream=None):
     i = plan.info
-    T, Hd = i.T, i.shard_hidden
+    n, Hd = _rank_rows(plan), i.shard_hidden
     _check(load_library().tsp_rank_qkv(
-        plan.handle, _dev(xs_r, "xs_r", T * i.hidden),
+        plan.handle, _dev(xs_r, "xs_r", n * i.hidden),
         _dev(attn_shard, "attn_shard", tsp_rank_shard_bytes(plan)[0] // 2),
-        _dev(q_r, "q_r", T * Hd), _dev(kv_r, "kv_r", 2 * T * Hd), _ws_status(ws),
+        _dev(q_r, "q_r", n * Hd), _dev(kv_r, "kv_r", 2 * n * Hd), _ws_status(ws),
         _stream(stream)), "tsp_rank_qkv")
 
 
 def tsp_rank_kv_gather(plan, kv_all, kn, vn, stream=None):
     i = plan.info
-    n = i.S * i.shard_hidden
+    n = i.tokens * i.shard_hidden
     _check(load_library().tsp_rank_kv_gather(
         plan.handle, _dev(kv_all, "kv_all", 2 * n), _dev(kn, "kn", n), _dev(vn, "vn", n),
         _stream(stream)), "tsp_rank_kv_gather")
@@ -583,7 +589,7 @@ def tsp_rank_kv_gather(plan, kv_all, kn, vn, stream=None):
 
 def tsp_rank_attention(plan, r, q_r, kn, vn, o_r, ws, stream=None):
     i = plan.info
-    n, nr = i.S * i.shard_hidden, i.T * i.shard_hidden
+    n, nr = i.tokens * i.shard_hidden, _rank_rows(plan) * i.shard_hidden
     _check(load_library().tsp_rank_attention(
         plan.handle, int(r), _dev(q_r, "q_r", nr), _dev(kn, "kn", n), _dev(vn, "vn", n),
         _dev(o_r, "o_r", nr), _ws_status(ws), _stream(stream)), "tsp_rank_attention")
@@ -593,10 +599,11 @@ def tsp_rank_o_accumulate(plan, o_r, attn_shard, residual, acc_r, h_r, ws, strea
     """acc_r = residual + o_r W_O,k^T (fp32), h_r = bf16(acc_r). residual: bf16 x_r or
     fp32 (acc_r itself)."""
     i = plan.info
-    n = i.T * i.hidden
+    rows = _rank_rows(plan)
+    n = rows * i.hidden
     f32 = residual is not None and residual.dtype == torch.float32
     _check(load_library().tsp_rank_o_accumulate(
-        plan.handle, _dev(o_r, "o_r", i.T * i.shard_hidden),
+        plan.handle, _dev(o_r, "o_r", rows * i.shard_hidden),
         _dev(attn_shard, "attn_shard", tsp_rank_shard_bytes(plan)[0] // 2),
         _dev(residual, "residual", n, torch.float32 if f32 else torch.bfloat16), int(f32),
         _dev(acc_r, "acc_r", n, torch.float32), _dev(h_r, "h_r", n), _ws_status(ws),
@@ -605,11 +612,12 @@ def tsp_rank_o_accumulate(plan, o_r, attn_shard, residual, acc_r, h_r, ws, strea
 
 def tsp_rank_mlp_step(plan, h_r, mlp_shard, residual32, acc_r, out_r, g_r, ws, stream=None):
     i = plan.info
-    n = i.T * i.hidden
+    rows = _rank_rows(plan)
+    n = rows * i.hidden
     fq = (i.shard_ffn_padded + 127) // 128 * 128
     _check(load_library().tsp_rank_mlp_step(
         plan.handle, _dev(h_r, "h_r", n),
         _dev(mlp_shard, "mlp_shard", tsp_rank_shard_bytes(plan)[1] // 2),
         _dev(residual32, "residual32", n, torch.float32), _dev(acc_r, "acc_r", n, torch.float32),
-        _dev(out_r, "out_r", n), _dev(g_r, "g_r", i.T * fq), _ws_status(ws), _stream(stream)),
+        _dev(out_r, "out_r", n), _dev(g_r, "g_r", rows * fq), _ws_status(ws), _stream(stream)),
         "tsp_rank_mlp_step")

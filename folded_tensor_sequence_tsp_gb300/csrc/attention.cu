@@ -96,6 +96,7 @@ struct AttParams {
   // layout (all S rows, or one rank's T rows); the Q, O and lse buffers hold them
   // from their row 0 on (buffer row = sharded row - q_row0)
   long long q_row0, q_end;
+  long long q_buf0;    // micro-batch-layout row of the call's first row (r B T for rank r)
   int q_local;         // 1: one rank's rows (longest-first = last local block first)
   float scale_log2;
   DevStatus* status;
@@ -231,8 +232,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     // a 128-row tile's rows are contiguous in the micro-batch layout too
-    out_row0[0] = batch_row(row0, seq, p) - p.q_row0;
-    out_row0[1] = batch_row(row0 + QT, seq, p) - p.q_row0;
+    out_row0[0] = batch_row(row0, seq, p) - p.q_buf0;
+    out_row0[1] = batch_row(row0 + QT, seq, p) - p.q_buf0;
     *out_head = head;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t)
           tma_load_2d(sQ + t * G::TILE_BYTES + b * BOX_BYTES, &tmQ, q_full, col_q + 64 * b,
-                      (int)(batch_row(row0 + t * QT, seq, p) - p.q_row0));
+                      (int)(batch_row(row0 + t * QT, seq, p) - p.q_buf0));
         tma_load_2d(sK0 + b * BOX_BYTES, &tmK, q_full, col_q + 64 * b, kv_row0);
       }
       int last[STAGES];
@@ -507,7 +508,7 @@ tsp_status launch_hd(const AttentionCall& c, const AttParams& p, cudaStream_t st
   // with the buffer's row stride: the buffers may hold more columns on either side
   const uint64_t rows = (uint64_t)c.S * (uint64_t)p.B;
   const uint64_t cols = (uint64_t)c.heads * (uint64_t)c.d;
-  const uint64_t q_rows = p.q_local ? (uint64_t)(p.q_end - p.q_row0) : rows;
+  const uint64_t q_rows = p.q_local ? (uint64_t)(p.q_end - p.q_row0) * (uint64_t)p.B : rows;
   tsp_status st = make_tmap_2d_bf16(&tq, c.qkv, cols, q_rows, (uint64_t)c.ld_qkv * 2, 64, QT);
   if (st != TSP_OK) return st;
   st = make_tmap_2d_bf16(&tk, c.kn, cols, rows, (uint64_t)c.ld_kv * 2, 64, KT);
@@ -555,12 +556,16 @@ tsp_status launch_attention(const AttentionCall& c, cudaStream_t stream) {
   p.heads = c.heads;
   // the call's query rows: every rank's, or rank-local rows [q_row0, q_row0 + q_rows)
   const bool local = c.q_rows > 0;
-  if (local && (B > 1 || c.q_row0 < 0 || c.q_row0 + c.q_rows > c.S))
-    return fail(TSP_ERR_INVALID_ARG, "attention: query rows outside the sequence, or a "
-                                     "row range with a micro-batch");
+  // with a micro-batch the range must be one rank's whole block (its rows of every
+  // sequence are contiguous in the [D][B][T] layout)
+  if (local && (c.q_row0 < 0 || c.q_row0 + c.q_rows > c.S ||
+                (B > 1 && (c.q_row0 % c.T || c.q_rows != c.T))))
+    return fail(TSP_ERR_INVALID_ARG, "attention: query rows outside the sequence, or not one "
+                                     "rank's rows of a micro-batch");
   p.q_local = local ? 1 : 0;
   p.q_row0 = local ? c.q_row0 : 0;
   p.q_end = local ? c.q_row0 + c.q_rows : c.S;
+  p.q_buf0 = local ? c.q_row0 * B : 0;  // q_row0 = r T: rank r's block starts at r B T
   p.q_blocks = (int)((p.q_end - p.q_row0 + QB - 1) / QB);
   {
     // pairs per group: their K and V (2 * S * d bf16 each) within 72 MB of the L2,

@@ -90,8 +90,10 @@ __global__ void rank_pack_kernel(RankPackArgs a) {
 
 tsp_status rank_check(tsp_plan_t plan, const char* what) {
   TSP_TRY(tsp_check_plan(plan));
-  if (plan->p.B != 1)
-    return fail(TSP_ERR_UNSUPPORTED, std::string(what) + ": rank-local calls take a plan of one sequence");
+  // a rank's rows of every sequence of a micro-batch ([B][T]) go through the 128-row
+  // tiles together, as in the all-rank path
+  if (plan->p.B > 1 && plan->p.T % 128)
+    return fail(TSP_ERR_UNSUPPORTED, std::string(what) + ": a micro-batch needs S/D % 128 == 0");
   return TSP_OK;
 }
 
@@ -160,7 +162,7 @@ tsp_status tsp_rank_qkv(tsp_plan_t plan, const tsp_bf16* xs_r, const tsp_bf16* a
   c.epi = EPI_QKV_SPLIT;
   c.A = xs_r;
   c.lda = p.H;
-  c.M = p.T;
+  c.M = (int64_t)p.B * p.T;  // the rank's rows of every sequence
   c.B = attn_shard;
   c.ldb = p.H;
   c.b_rows = 3LL * p.Hd;
@@ -178,7 +180,7 @@ tsp_status tsp_rank_qkv(tsp_plan_t plan, const tsp_bf16* xs_r, const tsp_bf16* a
   c.zz_C = p.T / 2;
   c.zz_T = p.T;
   c.zz_D = 1;
-  c.zz_B = 1;
+  c.zz_B = p.B;
   c.status = status_of(ws);
   return launch_gemm(c, static_cast<cudaStream_t>(stream));
 }
@@ -210,11 +212,11 @@ tsp_status tsp_rank_attention(tsp_plan_t plan, int r, const tsp_bf16* q_r, const
   a.T = p.T;
   a.C = p.C;
   a.D = p.D;
-  a.B = 1;
+  a.B = p.B;
   a.heads = p.hpr;
   a.d = p.d;
   a.status = status_of(ws);
-  a.q_row0 = (int64_t)r * p.T;  // rank r's rows of the rank-major layout
+  a.q_row0 = (int64_t)r * p.T;  // rank r's rows of each sequence's rank-major layout
   a.q_rows = p.T;
   return launch_attention(a, static_cast<cudaStream_t>(stream));
 }
@@ -230,7 +232,7 @@ tsp_status tsp_rank_o_accumulate(tsp_plan_t plan, const tsp_bf16* o_r, const tsp
   c.epi = EPI_RESIDUAL;
   c.A = o_r;
   c.lda = p.Hd;
-  c.M = p.T;
+  c.M = (int64_t)p.B * p.T;
   c.B = static_cast<const uint16_t*>(static_cast<const void*>(attn_shard)) + shard_layout(p).o_off;
   c.ldb = p.Hd;
   c.b_rows = p.H;
@@ -261,7 +263,7 @@ tsp_status tsp_rank_mlp_step(tsp_plan_t plan, const tsp_bf16* h_r, const tsp_bf1
   up.epi = EPI_SWIGLU;
   up.A = h_r;
   up.lda = p.H;
-  up.M = p.T;
+  up.M = (int64_t)p.B * p.T;
   up.B = w;
   up.ldb = p.H;
   up.b_rows = 2 * l.Fq;
@@ -276,7 +278,7 @@ tsp_status tsp_rank_mlp_step(tsp_plan_t plan, const tsp_bf16* h_r, const tsp_bf1
   down.epi = EPI_RESIDUAL;
   down.A = g_r;
   down.lda = l.Fq;
-  down.M = p.T;
+  down.M = (int64_t)p.B * p.T;
   down.B = w + l.w2_off;
   down.ldb = p.Fp;
   down.b_rows = p.H;

@@ -154,7 +154,9 @@ class CudaRankCompute:
     def __init__(self, plan):
         self.plan = plan
         i = plan.info
-        self.D, self.S, self.T, self.H, self.Hd = i.D, i.S, i.T, i.hidden, i.shard_hidden
+        # rows of one rank (its T tokens of every sequence of the micro-batch) and of
+        # the natural-order K/V (every token of every sequence)
+        self.D, self.S, self.T, self.H, self.Hd = i.D, i.tokens, i.batch * i.T, i.hidden, i.shard_hidden
         self.Fq = (i.shard_ffn_padded + 127) // 128 * 128
         self.device = torch.device("cuda", torch.cuda.current_device())
         self.ws = torch.zeros(256, dtype=torch.uint8, device=self.device)
@@ -199,8 +201,9 @@ def layer_forward_ranks(D: int, T: int, hd: int, ranks, xs: dict, attn_shards: d
     """One layer forward of the ranks `ranks` (the ranks this process drives: all D
     for a LocalExchange, its own rank for a TorchDistExchange).
 
-    xs[r]: rank r's zigzag tokens [T][H]; attn_shards[r], mlp_shards[r]: the two parts
-    of weight shard r (tsp_rank_shard_bytes layout for CudaRankCompute); hd = H/D.
+    xs[r]: rank r's zigzag tokens [T][H] (T: its rows, B S/D for a micro-batch of B
+    sequences, [B][S/D][H]); attn_shards[r], mlp_shards[r]: the two parts of weight
+    shard r (tsp_rank_shard_bytes layout for CudaRankCompute); hd = H/D.
     Returns {r: rank r's layer output [T][H]}. The MLP part circulates in a second
     buffer so that the caller's shards are left as they were. Transfers overlap the
     compute: the broadcast of attention shard k + 1 is in flight during iteration k,

@@ -351,7 +351,10 @@ tsp_status tsp_swiglu_down(tsp_plan_t plan, const tsp_bf16* g, const tsp_bf16* w
  * No all-reduce anywhere: each rank accumulates its own rows. The result equals
  * tsp_layer_fwd's rows of rank r up to fp32 summation order (each shard's partial
  * product is added to an fp32 accumulator in HBM instead of one K loop in tensor
- * memory). Plans of one sequence only (batch 1): TSP_ERR_UNSUPPORTED otherwise.
+ * memory). A micro-batch plan (tsp_plan_batched, B sequences) is supported when
+ * S/D % 128 == 0 (TSP_ERR_UNSUPPORTED otherwise): rank r then holds its T tokens of
+ * every sequence, [B][T] rows wherever [T] is written below, kv_all is
+ * [D][B][T][2H/D] and kn, vn are [B][S][H/D].
  * `ws` provides the status word only (256 bytes, as for the single steps). All
  * buffers are the caller's, 16-byte aligned; calls are asynchronous on `stream`.
  * ------------------------------------------------------------------------- */

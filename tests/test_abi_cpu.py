@@ -285,3 +285,20 @@ def test_rank_calls_pass_their_host_checks(lib, shape):
     Fq = (i.shard_ffn_padded + 127) // 128 * 128
     assert a == 2 * 4 * i.hidden * i.shard_hidden
     assert m == 2 * (2 * Fq * i.hidden + i.hidden * i.shard_ffn_padded)
+
+
+def test_rank_calls_pass_their_host_checks_with_a_micro_batch(lib):
+    """The same for a micro-batch of two sequences (a micro-batch plan has S/D a
+    multiple of 128, so each rank's rows of every sequence are whole 128-row tiles)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("placeholder pointers must never reach a GPU")
+    p = tsp.tsp_plan_batched(2, 256, 2, 256, 4, 688)
+    h = p.handle
+    P = lambda i: ctypes.c_void_p(1 << (24 + i))
+    ws = P(0)
+    for st in (lib.tsp_rank_qkv(h, P(1), P(2), P(3), P(4), ws, None),
+               lib.tsp_rank_attention(h, 1, P(1), P(2), P(3), P(4), ws, None),
+               lib.tsp_rank_o_accumulate(h, P(1), P(2), P(4), 1, P(4), P(5), ws, None),
+               lib.tsp_rank_mlp_step(h, P(1), P(2), P(4), P(4), P(5), P(6), ws, None)):
+        assert st == B.TSP_ERR_CUDA and "cuTensorMapEncodeTiled" in B.tsp_last_error()

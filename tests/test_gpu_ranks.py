@@ -125,11 +125,39 @@ def test_rank_schedule_reproduces_the_layer(name):
     assert_close(nat(got), nat(layer), f"ranks {name} vs tsp_layer_fwd")
 
 
-def test_rank_calls_reject_a_micro_batch_plan():
-    plan = tsp.tsp_plan_batched(2, 256, 2, 256, 4, 688)
-    with pytest.raises(tsp.TSPError) as e:
-        tsp.tsp_rank_shard_bytes(plan)
-    assert e.value.status == tsp.TSP_ERR_UNSUPPORTED
+@pytest.mark.parametrize("shape,batch", [((2, 256, 256, 4, 688), 3), ((4, 4096, 1024, 16, 2816), 2)],
+                         ids=["tiny-b3", "small-b2"])
+def test_rank_schedule_micro_batch(shape, batch):
+    """A micro-batch through the rank-local path (rank r holds its rows of every
+    sequence): each sequence's output against the oracle, and all of it against
+    tsp_layer_fwd of the same batched plan."""
+    from folded_tensor_sequence_tsp_gb300 import ranks as R
+    L = Layer(*shape, seed=55, batch=batch)
+    i = L.info
+    D, H = i.D, i.hidden
+    rows = batch * i.T
+    sh = _shards(L)
+    xs = L.sharded_x().view(-1, H)
+    comp = R.CudaRankCompute(L.plan)
+    out = R.layer_forward_ranks(D, rows, i.shard_hidden, range(D),
+                                {r: xs[r * rows:(r + 1) * rows] for r in range(D)},
+                                {r: sh[r][0] for r in range(D)}, {r: sh[r][1] for r in range(D)},
+                                R.LocalExchange(D), comp)
+    torch.cuda.synchronize()
+    comp.check()
+    got = torch.cat([out[r] for r in range(D)]).view(L.d["x"].shape)
+    layer = L.act()
+    tsp.tsp_layer_fwd(L.plan, xs, L.wpack, layer, L.ws)
+    L.check_status()
+    nat = lambda t: f64(L.unshard(t.reshape(L.d["x"].shape).contiguous()))
+    x = L.f("x")
+    W = L.weights64()
+    ref = oracle.layer_forward_batched(x, W, i.heads)["out"]
+    st = oracle.layer_forward_batched(x, W, i.heads, store=oracle.round_bf16)["out"]
+    g = nat(got)
+    for b in range(batch):
+        assert_close(g[b], ref[b], f"ranks batch {shape[0]}x{shape[1]} seq {b}", ref=st[b])
+    assert_close(g.reshape(-1, H), nat(layer).reshape(-1, H), f"ranks batch {batch} vs tsp_layer_fwd")
 
 
 def _free_port():
