@@ -21,30 +21,33 @@
 //             key tiles they see, computing S = Q K^T, dP = dO V^T and
 //             dQ += dS K. Its Q and dO rows sit in tensor memory as the A operand
 //             of the first two products.
-// The query side runs every product on a full 128-wide tile (N = 128 or N = d): a
+// Both sides run every product on a full 128-wide tile (N = 128 or N = d): a
 // tcgen05.mma with M = 128 and K = 16 occupies the tensor pipe for about as long
 // with N = 64 as with N = 128 on this part, so a narrower product runs at half
-// rate. Its element-wise work is split into two phases that depend on different
-// products, and the MMA lane orders its work (S(j+1), dQ(j), dP(j+1), ...) so that
-// one phase runs under the products of the other:
+// rate. Each side's element-wise work is split into two phases that depend on
+// different products, and the MMA lane orders its work so that one phase runs
+// under the products of the other.
+// Query side (S(j+1), dQ(j), dP(j+1), ...):
 //   phase a  (after the scores, which it then releases): P = exp2(s scale_log2 - lse);
 //   phase b  (after dP):  dS = P (dP - Delta), stored as bf16 over dP.
-// Warps 2..5 and 6..9 (two warpgroups, one accumulator row per thread) take key
-// columns [0, 64) and [64, 128) of every tile.
-// The key side streams each 128-row query tile as two 64-column halves (score and
-// dP^T products with N = 64): warps 2..5 take half 0 and warps 6..9 half 1, so one
-// half's element-wise work overlaps the other half's products. It keeps these
-// narrower products because its element-wise chain (two exponential-bound phases
-// and two tensor-memory round trips per tile) and its two-deep Q/dO ring, which is
-// what fits in shared memory beside the owned K and V, leave the tensor pipe idle
-// for longer than the halved products cost.
-//   warp 0  TMA producer (key side: 2 stages of Q, dO, lse, Delta; query side:
-//           3 stages of K, V)
+// Key side (dV(j), S^T(j+1), dK(j), dP^T(j+1), ...): two 128-column regions swap
+// roles from tile to tile. Tile j's scores land in one; its element-wise warps
+// turn them into P^T (bf16, kept in fp32 registers too) in place, then load dP^T(j)
+// from the other region, which the MMA lane refills with S^T(j+1) at once, and
+// store dS^T(j) beside P^T(j). dV(j) and dK(j) read P^T(j) and dS^T(j) as the A
+// operand; dP^T(j+1) then overwrites tile j's region (products execute in issue
+// order). The exponentials of tile j+1 run under dV(j), dK(j) and dP^T(j+1), and
+// dS^T under S^T(j+1).
+// Warps 2..5 and 6..9 (two warpgroups, one accumulator row per thread) take
+// columns [0, 64) and [64, 128) of every streamed tile.
+//   warp 0  TMA producer (key side: 3 stages of Q and lse, 2 of dO and Delta;
+//           query side: 3 stages of K, V)
 //   warp 1  TMEM allocation (512 columns) and the single MMA-issuing lane
-// TMEM columns: key side: dV [0, d), dK [d, 2d), half h: scores [256 + 128h, +64),
-// dP^T [320 + 128h, +64), with bf16 P^T / dS^T over the first 32 columns of each.
-// Query side: dQ [0, d), bf16 Q [d, 3d/2), bf16 dO [3d/2, 2d), scores [256, 384),
-// dP [384, 512) with bf16 dS over [384 + 64g, +32) for warpgroup g.
+// TMEM columns: key side: dV [0, d), dK [d, 2d), the two regions [256, 384) and
+// [384, 512), warpgroup g's bf16 P^T over [64g, +32) of the scores' region and its
+// dS^T over [64g + 32, +32). Query side: dQ [0, d), bf16 Q [d, 3d/2), bf16 dO
+// [3d/2, 2d), scores [256, 384), dP [384, 512) with bf16 dS over [384 + 64g, +32)
+// for warpgroup g.
 // MMAs issued by one thread execute in order, so a product may write columns that
 // an earlier-issued product reads.
 // A micro-batch of B sequences (rank-major [D][B][T] sharded rows, natural K/V rows
@@ -68,13 +71,11 @@ constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_SC = 256;  // query side: scores S, 128 columns
 constexpr uint32_t TM_DP = 384;  // query side: dP, 128 columns
-// key side: each streamed tile in two 64-column halves h, scores at
-// [256 + 128h, +64) and dP^T at [320 + 128h, +64)
-constexpr int HALF = 64;
-constexpr int STAGES = 2;
-constexpr uint32_t HALF_ROWS_BYTES = HALF * 128;  // 64 rows of a box
-__device__ __forceinline__ uint32_t tm_sc(int h) { return 256u + 128u * (uint32_t)h; }
-__device__ __forceinline__ uint32_t tm_dp(int h) { return 320u + 128u * (uint32_t)h; }
+// key side: two 128-column regions at 256 and 384 that swap roles from one streamed
+// tile to the next: tile j's scores (then its packed P^T and dS^T) in tm_s(j), its
+// dP^T in tm_g(j) = tm_s(j + 1)
+__device__ __forceinline__ uint32_t tm_s(int j) { return (j & 1) ? 384u : 256u; }
+__device__ __forceinline__ uint32_t tm_g(int j) { return (j & 1) ? 256u : 384u; }
 
 struct BwdParams {
   __nv_bfloat16* dq;
@@ -142,12 +143,19 @@ template <int HD>
 struct KeyGeom {
   static constexpr int BOXES = HD / 64;
   static constexpr uint32_t TILE = 128 * HD * 2;
-  // K, V, then per stage Q, dO, lse[128], Delta[128]
-  static constexpr uint32_t STAGE = 2 * TILE + 1024;
-  static constexpr size_t USED = 1024 + 2 * (size_t)TILE + STAGES * (size_t)STAGE + 256;
+  // Q tiles (with lse) and dO tiles (with Delta) in separate rings: a Q tile is read
+  // last by dK, a full tile after its scores, so it gets the deeper ring
+  static constexpr int QS = 3;
+  static constexpr int OS = 2;
+  // lse [QS][128], Delta [OS][128] and the barriers first; K, V, the Q ring and the
+  // dO ring from the next 1024-byte boundary
+  static constexpr uint32_t SMALL = (QS + OS) * 512 + 256;
+  static constexpr uint32_t TILES_OFF = (SMALL + 1023) / 1024 * 1024;
+  static constexpr size_t USED = TILES_OFF + (size_t)(2 + QS + OS) * TILE;
   // all 512 TMEM columns: one CTA per SM
   static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
 };
+static_assert(KeyGeom<128>::USED <= 227 * 1024, "key-side shared memory");
 
 template <int HD>
 struct QueryGeom {
@@ -185,27 +193,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                              const __grid_constant__ CUtensorMap tmV, const BwdParams p,
                              int q_col0, int do_col0) {
   using G = KeyGeom<HD>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sK = smem;
-  uint8_t* sV = sK + G::TILE;
-  uint8_t* sStage = sV + G::TILE;  // stage s: Q, dO, lse, Delta
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + STAGES * G::STAGE);
-  uint64_t* kv_full = bars;               // [1]
-  uint64_t* in_full = kv_full + 1;        // [STAGES]
-  uint64_t* in_empty = in_full + STAGES;  // [STAGES]
-  uint64_t* s_full = in_empty + STAGES;   // [2] per half
-  uint64_t* p_full = s_full + 2;          // [2] per half (4 warps)
-  uint64_t* acc_done = p_full + 2;        // [1]
-  uint64_t* drain = acc_done + 1;         // [1]
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  float* sLse = reinterpret_cast<float*>(smem_raw);  // [QS][128]
+  float* sDel = sLse + G::QS * 128;                  // [OS][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sDel + G::OS * 128);
+  uint64_t* kv_full = bars;              // [1]
+  uint64_t* q_full = kv_full + 1;        // [QS]
+  uint64_t* q_empty = q_full + G::QS;    // [QS]
+  uint64_t* o_full = q_empty + G::QS;    // [OS]
+  uint64_t* o_empty = o_full + G::OS;    // [OS]
+  uint64_t* s_full = o_empty + G::OS;    // scores of the current tile written
+  uint64_t* g_full = s_full + 1;         // dP^T of the current tile written
+  uint64_t* p_ready = g_full + 1;        // packed P^T stored (8 warps)
+  uint64_t* g_taken = p_ready + 1;       // dP^T loaded into registers (8 warps)
+  uint64_t* ds_ready = g_taken + 1;      // packed dS^T stored (8 warps)
+  uint64_t* acc_done = ds_ready + 1;
+  uint64_t* drain = acc_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  auto sQ = [&](int st) { return sStage + st * G::STAGE; };
-  auto sDO = [&](int st) { return sStage + st * G::STAGE + G::TILE; };
-  auto sLse = [&](int st) { return reinterpret_cast<float*>(sStage + st * G::STAGE + 2 * G::TILE); };
-  auto sDel = [&](int st) { return sLse(st) + 128; };
+  // the tiles start at the first 1024-byte boundary after the small buffers
+  const uint32_t base = smem_addr(smem_raw);
+  const uint32_t tiles_off = ((base + G::SMALL + 1023u) & ~1023u) - base;
+  if (tiles_off > G::TILES_OFF) {  // the allocation has no room for this base (uniform)
+    if (threadIdx.x == 0) record_error(p.status, kStatusUnsupported, SITE_SMEM_LAYOUT);
+    return;
+  }
+  uint8_t* sK = smem_raw + tiles_off;
+  uint8_t* sV = sK + G::TILE;
+  uint8_t* sQ0 = sV + G::TILE;               // [QS] Q tiles
+  uint8_t* sO0 = sQ0 + G::QS * G::TILE;      // [OS] dO tiles
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CtaPos cp = cta_pos(p);
@@ -222,14 +238,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&in_full[s], 1);
-      mbar_init(&in_empty[s], 1);
+    for (int s = 0; s < G::QS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], 4);
+    for (int s = 0; s < G::OS; ++s) {
+      mbar_init(&o_full[s], 1);
+      mbar_init(&o_empty[s], 1);
     }
+    mbar_init(s_full, 1);
+    mbar_init(g_full, 1);
+    mbar_init(p_ready, 8);
+    mbar_init(g_taken, 8);
+    mbar_init(ds_ready, 8);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -260,96 +281,132 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_2d(sK + b * BOX_BYTES, &tmK, kv_full, head * HD + 64 * b, kv_row0 + (int)k0);
         tma_load_2d(sV + b * BOX_BYTES, &tmV, kv_full, head * HD + 64 * b, kv_row0 + (int)k0);
       }
-      int last[STAGES] = {-1, -1};
+      int q_last[G::QS], o_last[G::OS];
+      for (int s = 0; s < G::QS; ++s) q_last[s] = -1;
+      for (int s = 0; s < G::OS; ++s) o_last[s] = -1;
       for (int idx = 0; idx < n_inner; ++idx) {
-        const int st = idx % STAGES;
-        const uint32_t ph = (uint32_t)((idx / STAGES) & 1);
-        if (!mbar_wait(&in_empty[st], ph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
         // the tile's rows in the micro-batch layout (contiguous: a 128-row tile never
         // spans two ranks' blocks when B > 1)
         const long long r0 = batch_row(row0_of(idx), seq, p);
-        mbar_arrive_expect_tx(&in_full[st], 2 * G::TILE + 1024);
+        const int qs = idx % G::QS, os = idx % G::OS;
+        const uint32_t qph = (uint32_t)((idx / G::QS) & 1), oph = (uint32_t)((idx / G::OS) & 1);
+        if (!mbar_wait(&q_empty[qs], qph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
+        mbar_arrive_expect_tx(&q_full[qs], G::TILE + 512);
 #pragma unroll
-        for (int b = 0; b < G::BOXES; ++b) {
-          tma_load_2d(sQ(st) + b * BOX_BYTES, &tmQ, &in_full[st], q_col0 + head * HD + 64 * b,
-                      (int)r0);
-          tma_load_2d(sDO(st) + b * BOX_BYTES, &tmDO, &in_full[st], do_col0 + head * HD + 64 * b,
-                      (int)r0);
-        }
-        bulk_load(sLse(st), lse_h + r0, 512, &in_full[st]);
-        bulk_load(sDel(st), del_h + r0, 512, &in_full[st]);
-        last[st] = (int)ph;
+        for (int b = 0; b < G::BOXES; ++b)
+          tma_load_2d(sQ0 + qs * G::TILE + b * BOX_BYTES, &tmQ, &q_full[qs],
+                      q_col0 + head * HD + 64 * b, (int)r0);
+        bulk_load(sLse + qs * 128, lse_h + r0, 512, &q_full[qs]);
+        q_last[qs] = (int)qph;
+        if (!mbar_wait(&o_empty[os], oph ^ 1u, wb, SITE_BWD_PRODUCER)) break;
+        mbar_arrive_expect_tx(&o_full[os], G::TILE + 512);
+#pragma unroll
+        for (int b = 0; b < G::BOXES; ++b)
+          tma_load_2d(sO0 + os * G::TILE + b * BOX_BYTES, &tmDO, &o_full[os],
+                      do_col0 + head * HD + 64 * b, (int)r0);
+        bulk_load(sDel + os * 128, del_h + r0, 512, &o_full[os]);
+        o_last[os] = (int)oph;
       }
       WaitBound wd{p.status, p.limit_ns, nullptr};
       mbar_wait(kv_full, 0, wd, SITE_DRAIN);
-      for (int s = 0; s < STAGES; ++s)
-        if (last[s] >= 0) mbar_wait(&in_full[s], (uint32_t)last[s], wd, SITE_DRAIN);
+      for (int s = 0; s < G::QS; ++s)
+        if (q_last[s] >= 0) mbar_wait(&q_full[s], (uint32_t)q_last[s], wd, SITE_DRAIN);
+      for (int s = 0; s < G::OS; ++s)
+        if (o_last[s] >= 0) mbar_wait(&o_full[s], (uint32_t)o_last[s], wd, SITE_DRAIN);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc_s = make_idesc_bf16(BT, HALF, false);
+      const uint32_t idesc_s = make_idesc_bf16(BT, IT, false);
       const uint32_t idesc_acc = make_idesc_bf16(BT, HD, true);
       const uint64_t dk0 = make_sdesc_sw128(smem_addr(sK), 16, 1024);
       const uint64_t dv0 = make_sdesc_sw128(smem_addr(sV), 16, 1024);
-      const uint64_t dst0 = make_sdesc_sw128(smem_addr(sStage), 16, 1024);            // K-major
-      const uint64_t dst0_mn = make_sdesc_sw128(smem_addr(sStage), BOX_BYTES, 1024);  // MN-major
+      const uint64_t dq0 = make_sdesc_sw128(smem_addr(sQ0), 16, 1024);            // K-major
+      const uint64_t dq0_mn = make_sdesc_sw128(smem_addr(sQ0), BOX_BYTES, 1024);  // MN-major
+      const uint64_t do0 = make_sdesc_sw128(smem_addr(sO0), 16, 1024);
+      const uint64_t do0_mn = make_sdesc_sw128(smem_addr(sO0), BOX_BYTES, 1024);
       const uint32_t k_lo = (uint32_t)dk0, k_hi = (uint32_t)(dk0 >> 32);
       const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
-      const uint32_t st_lo = (uint32_t)dst0, st_hi = (uint32_t)(dst0 >> 32);
-      const uint32_t mn_lo = (uint32_t)dst0_mn, mn_hi = (uint32_t)(dst0_mn >> 32);
-      // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (64 query columns of stage st)
-      auto issue_sdp = [&](int h, int st) {
-        const uint32_t q_lo = st_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
-        const uint32_t o_lo = q_lo + G::TILE / 16;
+      const uint32_t kq_hi = (uint32_t)(dq0 >> 32), mn_hi = (uint32_t)(dq0_mn >> 32);
+      // S^T(j) = K Q(j)^T and dP^T(j) = V dO(j)^T, one full-width product each
+      auto issue_s = [&](int j) {
+        const uint32_t q_lo = (uint32_t)dq0 + (uint32_t)(j % G::QS) * (G::TILE / 16);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss_w(tmem + tm_sc(h), k_lo + kmajor_step(kk), k_hi, q_lo + kmajor_step(kk), st_hi,
+          mma_ss_w(tmem + tm_s(j), k_lo + kmajor_step(kk), k_hi, q_lo + kmajor_step(kk), kq_hi,
                    idesc_s, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+      };
+      auto issue_g = [&](int j) {
+        const uint32_t o_lo = (uint32_t)do0 + (uint32_t)(j % G::OS) * (G::TILE / 16);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss_w(tmem + tm_dp(h), v_lo + kmajor_step(kk), v_hi, o_lo + kmajor_step(kk), st_hi,
+          mma_ss_w(tmem + tm_g(j), v_lo + kmajor_step(kk), v_hi, o_lo + kmajor_step(kk), kq_hi,
                    idesc_s, kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[h]);
+        mma_commit(g_full);
       };
-      // dV += P^T_h dO_h, dK += dS^T_h Q_h (B MN-major: 16 query rows = 2048 B)
-      auto issue_acc = [&](int h, int st, bool first) {
-        const uint32_t q_lo = mn_lo + ((uint32_t)st * G::STAGE + (uint32_t)h * HALF_ROWS_BYTES) / 16;
-        const uint32_t o_lo = q_lo + G::TILE / 16;
+      // dV += P^T(j) dO(j) and dK += dS^T(j) Q(j): A from tensor memory, B MN-major
+      // (16 query rows = 2048 B per K step)
+      auto issue_dv = [&](int j) {
+        const uint32_t o_lo = (uint32_t)do0_mn + (uint32_t)(j % G::OS) * (G::TILE / 16);
 #pragma unroll
-        for (int kk = 0; kk < HALF / 16; ++kk)
-          mma_ts_w(tmem + 0, tmem + tm_sc(h) + (uint32_t)(kk * 8), o_lo + (uint32_t)(kk * 128),
-                   mn_hi, idesc_acc, (first && kk == 0) ? 0u : 1u);
-#pragma unroll
-        for (int kk = 0; kk < HALF / 16; ++kk)
-          mma_ts_w(tmem + HD, tmem + tm_dp(h) + (uint32_t)(kk * 8), q_lo + (uint32_t)(kk * 128),
-                   mn_hi, idesc_acc, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < IT / 16; ++kk)
+          mma_ts_w(tmem + 0, tmem + packed_step(tm_s(j), kk), o_lo + (uint32_t)(kk * 128), mn_hi,
+                   idesc_acc, (j == 0 && kk == 0) ? 0u : 1u);
       };
-      bool ok = mbar_wait(kv_full, 0, wb, SITE_BWD_MMA) && mbar_wait(&in_full[0], 0, wb, SITE_BWD_MMA);
+      auto issue_dk = [&](int j) {
+        const uint32_t q_lo = (uint32_t)dq0_mn + (uint32_t)(j % G::QS) * (G::TILE / 16);
+#pragma unroll
+        for (int kk = 0; kk < IT / 16; ++kk)
+          mma_ts_w(tmem + HD, tmem + packed_step(tm_s(j) + 32, kk), q_lo + (uint32_t)(kk * 128),
+                   mn_hi, idesc_acc, (j == 0 && kk == 0) ? 0u : 1u);
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return mbar_wait_poll(bar, parity, wb, SITE_BWD_MMA);
+      };
+      bool ok = wait(kv_full, 0) && wait(&q_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_sdp(0, 0);
-        issue_sdp(1, 0);
+        issue_s(0);
       }
-      for (int idx = 0; ok && idx < n_inner; ++idx) {
-        const int st = idx % STAGES;
-        for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(&p_full[h], (uint32_t)(idx & 1), wb, SITE_BWD_MMA)) {
+      ok = ok && wait(&o_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_g(0);
+      }
+      // per tile j: dV(j) once P^T(j) is stored; S^T(j+1) into the dP^T(j) region once
+      // the element-wise warps hold dP^T(j); dK(j) once dS^T(j) is stored; dP^T(j+1)
+      // into the region of tile j, after dV(j) and dK(j) have read it (in issue order)
+      for (int j = 0; ok && j < n_inner; ++j) {
+        const uint32_t ph = (uint32_t)(j & 1);
+        const bool more = j + 1 < n_inner;
+        if (!wait(p_ready, ph)) break;
+        tc_fence_after();
+        issue_dv(j);
+        if (more) {
+          if (!wait(g_taken, ph) ||
+              !wait(&q_full[(j + 1) % G::QS], (uint32_t)(((j + 1) / G::QS) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_acc(h, st, idx == 0 && h == 0);
-          if (h == 1) mma_commit(&in_empty[st]);
-          if (idx + 1 < n_inner) {
-            if (h == 0 && !mbar_wait(&in_full[(idx + 1) % STAGES],
-                                     (uint32_t)(((idx + 1) / STAGES) & 1), wb, SITE_BWD_MMA)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_sdp(h, (idx + 1) % STAGES);
+          issue_s(j + 1);
+        }
+        if (!wait(ds_ready, ph)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dk(j);
+        mma_commit(&q_empty[j % G::QS]);
+        mma_commit(&o_empty[j % G::OS]);
+        if (more) {
+          if (!wait(&o_full[(j + 1) % G::OS], (uint32_t)(((j + 1) / G::OS) & 1))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          issue_g(j + 1);
         }
       }
       if (ok) mma_commit(acc_done);
@@ -359,93 +416,124 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- element-wise
-    const int h = (warp - 2) >> 2;  // half of every streamed tile this warpgroup takes
+    const int g = (warp - 2) >> 2;  // query columns [64g, 64g + 64) of every tile
     const int qq = warp & 3;        // TMEM lane quarter
     const int r_local = qq * 32 + lane;
     const long long kp = k0 + r_local;  // key position of this thread's row
     const uint32_t lane_base = tmem + ((uint32_t)(qq * 32) << 16);
-    const uint32_t s_t = lane_base + tm_sc(h), d_t = lane_base + tm_dp(h);
+    const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
       const bool mine = mbar_wait(bar, parity, wb, SITE_BWD_ELEMENTWISE);
       return __all_sync(0xffffffffu, mine) != 0;
     };
-    for (int idx = 0; idx < n_inner; ++idx) {
-      const int st = idx % STAGES;
-      if (!warp_wait(&s_full[h], (uint32_t)(idx & 1)) ||
-          !warp_wait(&in_full[st], (uint32_t)((idx / STAGES) & 1))) {
+    for (int j = 0; j < n_inner; ++j) {
+      const uint32_t ph = (uint32_t)(j & 1);
+      const int qs = j % G::QS, os = j % G::OS;
+      if (!warp_wait(s_full, ph) || !warp_wait(&q_full[qs], (uint32_t)((j / G::QS) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // the half's 64 scores and 64 dP values of this key row: one TMEM round trip
-      uint32_t s0[32], s1[32], g0[32], g1[32];
-      tmem_ld32(s_t, s0);
-      tmem_ld32(s_t + 32, s1);
-      tmem_ld32(d_t, g0);
-      tmem_ld32(d_t + 32, g1);
-      const float4* sl4 = reinterpret_cast<const float4*>(sLse(st) + h * HALF);
-      const float4* sd4 = reinterpret_cast<const float4*>(sDel(st) + h * HALF);
-      const long long r0 = row0_of(idx);
+      const uint32_t s_t = lane_base + tm_s(j) + (uint32_t)(GCOLS * g);
+      const uint32_t g_t = lane_base + tm_g(j) + (uint32_t)(GCOLS * g);
+      uint32_t sv[2][32];
+      tmem_ld32(s_t, sv[0]);
+      tmem_ld32(s_t + 32, sv[1]);
+      const float4* sl4 = reinterpret_cast<const float4*>(sLse + qs * 128 + g * GCOLS);
+      const long long r0 = row0_of(j);
       // natural tiles are contiguous positions; a tile needs masks only where it
       // meets the diagonal (or always, in the general zigzag layout)
-      const long long qbase = p.natural ? (long long)(kt + idx) * IT + h * HALF : 0;
+      const long long qbase = p.natural ? (long long)(kt + j) * IT + g * GCOLS : 0;
       const bool masked = !p.natural || qbase < k0 + BT - 1;
       tmem_ld_wait();
-      uint32_t pp[32], dd[32];
-      // P^T = exp2(s * scale_log2 - lse[q]), dS^T = P^T (dP^T - Delta[q]) for 32 columns
-      auto chunk = [&](const uint32_t (&sv)[32], const uint32_t (&gv)[32], int c0, auto mask_tag) {
+      // P^T = exp2(s * scale_log2 - lse[q]), kept in fp32 for dS^T and stored as bf16
+      float pf[64];
+      uint32_t pp[32];
+      auto p_chunk = [&](const uint32_t (&s)[32], int c0, auto mask_tag) {
         constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = sl4[(c0 + e) >> 2], d4 = sd4[(c0 + e) >> 2];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          const float4 l4 = sl4[(c0 + e) >> 2];
+          const uint64_t nl[2] = {f2_pack(-l4.x, -l4.y), f2_pack(-l4.z, -l4.w)};
 #pragma unroll
           for (int u = 0; u < 4; u += 2) {
-            float p0 = ex2(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lv[u]));
-            float p1 = ex2(fmaf(__uint_as_float(sv[e + u + 1]), p.scale_log2, -lv[u + 1]));
-            uint64_t ds = f2_mul(f2_pack(p0, p1),
-                                 f2_sub(f2_pack(__uint_as_float(gv[e + u]), __uint_as_float(gv[e + u + 1])),
-                                        f2_pack(dl[u], dl[u + 1])));
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[e + u]), __uint_as_float(s[e + u + 1])),
+                             scale2, nl[u >> 1]),
+                      x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
             if constexpr (MASK) {
               bool vis[2];
 #pragma unroll
               for (int w = 0; w < 2; ++w) {
-                const int col = h * HALF + c0 + e + u + w;
+                const int col = g * GCOLS + c0 + e + u + w;
                 if (p.natural) {
-                  vis[w] = kp <= (long long)(kt + idx) * IT + col;
+                  vis[w] = kp <= (long long)(kt + j) * IT + col;
                 } else {
                   const long long r = r0 + col;
                   vis[w] = r < p.S && kp <= row_pos(r, p.C, p.T, p.D);
                 }
               }
-              float d0, d1;
-              f2_unpack(ds, d0, d1);
               p0 = vis[0] ? p0 : 0.f;
               p1 = vis[1] ? p1 : 0.f;
-              ds = f2_pack(vis[0] ? d0 : 0.f, vis[1] ? d1 : 0.f);
             }
-            float d0, d1;
-            f2_unpack(ds, d0, d1);
+            pf[c0 + e + u] = p0;
+            pf[c0 + e + u + 1] = p1;
             pp[(c0 + e + u) >> 1] = pack_bf16x2(p0, p1);
-            dd[(c0 + e + u) >> 1] = pack_bf16x2(d0, d1);
           }
         }
       };
       if (masked) {
-        chunk(s0, g0, 0, std::true_type{});
-        chunk(s1, g1, 32, std::true_type{});
+        p_chunk(sv[0], 0, std::true_type{});
+        p_chunk(sv[1], 32, std::true_type{});
       } else {
-        chunk(s0, g0, 0, std::false_type{});
-        chunk(s1, g1, 32, std::false_type{});
+        p_chunk(sv[0], 0, std::false_type{});
+        p_chunk(sv[1], 32, std::false_type{});
       }
       tmem_st32(s_t, pp);
-      tmem_st32(d_t, dd);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[h]);
+      if (lane == 0) mbar_arrive(p_ready);
+      if (!warp_wait(g_full, ph) || !warp_wait(&o_full[os], (uint32_t)((j / G::OS) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t gv[2][32];
+      tmem_ld32(g_t, gv[0]);
+      tmem_ld32(g_t + 32, gv[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(g_taken);
+      // dS^T = P^T (dP^T - Delta[q]) (zero where P^T is masked to zero)
+      const float4* sd4 = reinterpret_cast<const float4*>(sDel + os * 128 + g * GCOLS);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = sd4[(32 * c + e) >> 2];
+          const uint64_t dl[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(pf[32 * c + e + u], pf[32 * c + e + u + 1]),
+                             f2_sub(f2_pack(__uint_as_float(gv[c][e + u]),
+                                            __uint_as_float(gv[c][e + u + 1])),
+                                    dl[u >> 1])),
+                      d0, d1);
+            dd[(e + u) >> 1] = pack_bf16x2(d0, d1);
+          }
+        }
+        tmem_st16(s_t + 32 + 16 * c, dd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_ready);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && warp_wait(acc_done, 0u)) {
@@ -455,7 +543,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __nv_bfloat16* dvp = p.dv + orow * p.ld_dqkv + head * HD;
       __nv_bfloat16* dkp = p.dk + orow * p.ld_dqkv + head * HD;
 #pragma unroll
-      for (int c = h * (HD / 2); c < (h + 1) * (HD / 2); c += 32) {
+      for (int c = g * (HD / 2); c < (g + 1) * (HD / 2); c += 32) {
         uint32_t a[32], b[32];
         tmem_ld32(lane_base + (uint32_t)c, a);
         tmem_ld32(lane_base + (uint32_t)(HD + c), b);

@@ -33,9 +33,11 @@ enum Site : unsigned int {
   SITE_BWD_PRODUCER = 9,
   SITE_BWD_MMA = 10,
   SITE_BWD_ELEMENTWISE = 11,
+  SITE_SMEM_LAYOUT = 12,  // the dynamic shared memory base left no room for the layout
 };
 
-constexpr unsigned int kStatusTimeout = 4;  // == TSP_ERR_TIMEOUT
+constexpr unsigned int kStatusUnsupported = 2;  // == TSP_ERR_UNSUPPORTED
+constexpr unsigned int kStatusTimeout = 4;      // == TSP_ERR_TIMEOUT
 
 struct WaitBound {
   DevStatus* status;
@@ -109,6 +111,16 @@ static __device__ __noinline__ void record_timeout(const WaitBound& wb, unsigned
     wb.status->thread = threadIdx.x;
   }
   if (wb.abort_flag) *wb.abort_flag = 1;
+}
+
+// Records a failure other than a wait that gave up (first error wins).
+static __device__ __noinline__ void record_error(DevStatus* status, unsigned int code,
+                                                 unsigned int site) {
+  if (atomicCAS(&status->code, 0u, code) == 0u) {
+    status->site = site;
+    status->block = blockIdx.x;
+    status->thread = threadIdx.x;
+  }
 }
 
 // Wait until the phase of `bar` with parity `parity` has completed. Gives up after
