@@ -32,8 +32,8 @@ class OracleRankCompute:
 
     act_dtype = torch.float64
 
-    def __init__(self, D, S, H, heads, F):
-        self.D, self.S, self.H, self.heads, self.F = D, S, H, heads, F
+    def __init__(self, D, S, H, heads, F, B=1):
+        self.D, self.S, self.H, self.heads, self.F, self.B = D, S, H, heads, F, B
         self.T, self.Hd, self.Fd = S // D, H // D, F // D
 
     def shards(self, W, k):
@@ -59,12 +59,18 @@ class OracleRankCompute:
         kv_r.copy_(torch.from_numpy(np.concatenate([st["x"] @ Wk.T, st["x"] @ Wv.T], axis=1)))
 
     def attention_finish(self, st, k, attn_shard, kv_all):
+        # a micro-batch: rank rows [B][T], gathered K|V [D][B][T][2H/D]; one sequence's
+        # queries see only that sequence's keys
         _, _, _, Wo = self._attn(attn_shard)
-        kv = kv_all.numpy()
-        K = oracle.unshard_tokens(kv[:, :, :self.Hd], self.D)
-        V = oracle.unshard_tokens(kv[:, :, self.Hd:], self.D)
-        o = oracle.multihead_causal_attention(st["q"], K, V, self.heads // self.D,
-                                              q_pos=st["pos"], k_pos=np.arange(self.S))
+        B, T = self.B, self.T
+        kv = kv_all.numpy().reshape(self.D, B, T, 2 * self.Hd)
+        o = np.empty((B * T, self.Hd))
+        for b in range(B):
+            K = oracle.unshard_tokens(kv[:, b, :, :self.Hd], self.D)
+            V = oracle.unshard_tokens(kv[:, b, :, self.Hd:], self.D)
+            o[b * T:(b + 1) * T] = oracle.multihead_causal_attention(
+                st["q"][b * T:(b + 1) * T], K, V, self.heads // self.D, q_pos=st["pos"],
+                k_pos=np.arange(self.S))
         st["acc"] = (st["x"] if k == 0 else st["acc"]) + o @ Wo.T
         if k == self.D - 1:
             st["h"] = st["acc"].copy()
@@ -105,6 +111,42 @@ def test_schedule_with_local_exchange_is_the_plain_layer(D):
     x, W, got = _run_local(D, S, H, heads, F, 70 + D)
     want = oracle.layer_forward(x, W, heads)["out"]
     assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+
+
+def _batch_problem(D, S, H, heads, F, B, seed):
+    """B sequences of one layer (same weights): x [B][S][H] float64 and the weights."""
+    xs, W = [], None
+    for b in range(B):
+        x, Wb = _problem(D, S, H, heads, F, seed + 101 * b)
+        xs.append(x)
+        W = W or Wb
+    return np.stack(xs), W
+
+
+def _rank_rows(x, D, r):
+    """Rank r's rows of a micro-batch: its zigzag tokens of every sequence, [B*T][H]."""
+    return np.concatenate([oracle.shard_tokens(x[b], D)[r] for b in range(x.shape[0])])
+
+
+@pytest.mark.parametrize("D,B", [(2, 2), (3, 3)])
+def test_micro_batch_schedule_with_local_exchange(D, B):
+    """A micro-batch through the same schedule: rank r holds its T tokens of every
+    sequence, K|V are gathered as [D][B][T][2H/D], and every sequence's rows equal the
+    plain layer of that sequence alone."""
+    S, heads, F = 24 * D, 2 * D, 24 * D
+    H = 8 * heads
+    x, W = _batch_problem(D, S, H, heads, F, B, 300 + D)
+    comp = OracleRankCompute(D, S, H, heads, F, B)
+    sh = {r: comp.shards(W, r) for r in range(D)}
+    out = R.layer_forward_ranks(D, B * (S // D), H // D, range(D),
+                                {r: torch.from_numpy(_rank_rows(x, D, r)) for r in range(D)},
+                                {r: sh[r][0] for r in range(D)}, {r: sh[r][1] for r in range(D)},
+                                R.LocalExchange(D), comp)
+    T = S // D
+    for b in range(B):
+        got = oracle.unshard_tokens(np.stack([out[r].numpy()[b * T:(b + 1) * T] for r in range(D)]), D)
+        want = oracle.layer_forward(x[b], W, heads)["out"]
+        assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max()), b
 
 
 def test_a_ring_that_skips_a_rank_is_caught(monkeypatch):
@@ -170,6 +212,57 @@ def test_two_gloo_ranks_run_the_layer():
         H, F, T = 256, 688, 128
         assert recv["broadcast"] == 8 * (4 * H * H // 2)
         assert recv["all_gather"] == 8 * 2 * (T * 2 * H // 2)
+        assert recv["ring"] == 8 * (3 * H * F // 2)
+
+
+def _gloo_batch_rank(rank, world, port, shape, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        D, S, H, heads, F, B, seed = shape
+        x, W = _batch_problem(D, S, H, heads, F, B, seed)
+        comp = OracleRankCompute(D, S, H, heads, F, B)
+        att, mlp = comp.shards(W, rank)
+        xs_r = torch.from_numpy(np.ascontiguousarray(_rank_rows(x, D, rank)))
+        ex = R.TorchDistExchange()
+        out = R.layer_forward_ranks(D, B * (S // D), H // D, [rank], {rank: xs_r}, {rank: att},
+                                    {rank: mlp}, ex, comp)[rank].numpy()
+        pos = oracle.rank_positions(S, D)[rank]
+        T = S // D
+        err = 0.0
+        for b in range(B):
+            want = oracle.layer_forward(x[b], W, heads, rows=np.sort(pos))["out"]
+            want = want[np.argsort(np.argsort(pos))]
+            err = max(err, float(np.abs(out[b * T:(b + 1) * T] - want).max()) /
+                      max(1.0, float(np.abs(want).max())))
+        results[rank] = (err, dict(ex.recv_bytes))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_run_a_micro_batch():
+    """Two processes through gloo with a micro-batch of 3 sequences: each rank's rows of
+    each sequence equal that sequence's plain layer; the K/V all-gather carries B times
+    one sequence's bytes, the weight messages are unchanged."""
+    D, S, H, heads, F, B = 2, 64, 32, 4, 64, 3
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        procs = [ctx.Process(target=_gloo_batch_rank, args=(r, 2, port, (D, S, H, heads, F, B, 505),
+                                                            results)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(300)
+            assert p.exitcode == 0
+        res = dict(results)
+    T = S // D
+    for r in (0, 1):
+        err, recv = res[r]
+        assert err <= 1e-12, (r, err)
+        assert recv["broadcast"] == 8 * (4 * H * H // 2)
+        assert recv["all_gather"] == 8 * 2 * (B * T * 2 * H // 2)
         assert recv["ring"] == 8 * (3 * H * F // 2)
 
 
