@@ -699,8 +699,9 @@ def run_step(args):
         run()
     b.record()
     torch.cuda.synchronize()
-    if ws is not None and B.tsp_device_status(ws) != B.TSP_OK:
-        raise B.TSPError(B.tsp_device_status(ws), B.tsp_last_error())
+    status = B.tsp_device_status(ws) if ws is not None else B.TSP_OK
+    if status != B.TSP_OK:  # the call reads and clears the status word: read it once
+        raise B.TSPError(status, B.tsp_last_error())
     print(f"{st} {cfg.name}: {a.elapsed_time(b) / args.launches:.4f} ms per launch", flush=True)
 
 

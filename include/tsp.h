@@ -615,7 +615,9 @@ tsp_status tsp_cost_max_batch(int scheme, int D, int tp, int64_t S, int hidden, 
 /*
  * tsp_device_status - synchronise `stream`, then read and clear the workspace
  * status word. Returns TSP_OK, TSP_ERR_TIMEOUT (a bounded device wait gave up; the
- * outputs of the affected call are undefined) or TSP_ERR_CUDA.
+ * outputs of the affected call are undefined), TSP_ERR_UNSUPPORTED (a kernel whose
+ * shared-memory layout fills the 227 KB limit found its dynamic shared memory at a
+ * base that left no room, and returned without computing) or TSP_ERR_CUDA.
  */
 tsp_status tsp_device_status(void* ws, void* stream);
 
