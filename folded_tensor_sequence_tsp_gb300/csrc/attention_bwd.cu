@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                              const __grid_constant__ CUtensorMap tmV, const BwdParams p,
                              int q_col0, int do_col0) {
   using G = KeyGeom<HD>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // no alignment is assumed for the base: the tiles start at the first 1024-byte
+  // boundary after the small buffers, and the check below tests that they fit
+  extern __shared__ uint8_t smem_raw[];
   float* sLse = reinterpret_cast<float*>(smem_raw);  // [QS][128]
   float* sDel = sLse + G::QS * 128;                  // [OS][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sDel + G::OS * 128);
